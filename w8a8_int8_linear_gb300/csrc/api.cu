@@ -1,0 +1,296 @@
+// C ABI of the W8A8 INT8 Linear library (declared in include/w8a8.h):
+// argument checks, device checks, workspace carving and kernel launches.
+// Every check runs before anything is enqueued, so a rejected call leaves
+// all outputs untouched.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/w8a8.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int64_t kMaxK = 131072;  // 127 * 127 * K must stay below 2^31
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ok;
+    int num_sms;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+std::atomic<bool> g_dev_known[kMaxDevices];
+void* g_encode = nullptr;
+thread_local char t_detail[256] = "";
+thread_local cudaEvent_t t_gemm_start = nullptr;
+thread_local cudaEvent_t t_gemm_end = nullptr;
+
+void set_detail(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_detail, sizeof t_detail, fmt, ap);
+    va_end(ap);
+}
+
+w8a8_status cuda_fail(const char* what, cudaError_t e) {
+    set_detail("%s: %s", what, cudaGetErrorString(e));
+    return W8A8_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Current device must be compute capability 10.3.
+w8a8_status current_device(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("cudaGetDevice", ge);
+    }
+    if (dev < 0 || dev >= kMaxDevices) return W8A8_ERR_UNSUPPORTED_DEVICE;
+    if (!g_dev_known[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_dev_known[dev].load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+                cudaGetLastError();
+                set_detail("cudaDeviceGetAttribute failed on device %d", dev);
+                return W8A8_ERR_CUDA;
+            }
+            g_dev[dev].ok = (major == 10 && minor == 3);
+            g_dev[dev].num_sms = sms;
+            g_dev_known[dev].store(true, std::memory_order_release);
+        }
+    }
+    *out = g_dev[dev];
+    return out->ok ? W8A8_OK : W8A8_ERR_UNSUPPORTED_DEVICE;
+}
+
+void* encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn) {
+            g_encode = fn;
+        } else {
+            cudaGetLastError();
+            set_detail("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled): %s, query result %d",
+                       cudaGetErrorString(e), (int)q);
+        }
+    }
+    return g_encode;
+}
+
+w8a8_status from_cuda(cudaError_t e, const char* what = "kernel launch") {
+    return e == cudaSuccess ? W8A8_OK : cuda_fail(what, e);
+}
+
+w8a8_status check_k(int64_t K, bool block) {
+    if (K <= 0) return W8A8_ERR_INVALID_ARG;
+    if (K % 16 != 0 || K > kMaxK) return W8A8_ERR_SHAPE;
+    if (block && K % 128 != 0) return W8A8_ERR_SHAPE;
+    return W8A8_OK;
+}
+
+// Shared checks of the GEMM entry points.  need_sx/need_sw: scale pointers
+// used by this variant.
+w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw, const void* bias,
+                       const void* out, int64_t M, int64_t N, int64_t K, bool block, bool need_scales,
+                       const void* ws, size_t ws_bytes, DeviceInfo* dev, bool* nothing_to_do) {
+    *nothing_to_do = false;
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, block);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0 || N == 0) {
+        *nothing_to_do = true;
+        return W8A8_OK;
+    }
+    if (!Xq || !Wq || !out || (need_scales && (!sx || !sw))) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(out) || (sx && !aligned16(sx)) ||
+        (sw && !aligned16(sw)) || (bias && !aligned16(bias)))
+        return W8A8_ERR_ALIGNMENT;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w8a8_gemm_workspace_size(M, N, K))
+        return W8A8_ERR_WORKSPACE;
+    return current_device(dev);
+}
+
+w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                     const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* ws, const DeviceInfo& dev,
+                     cudaStream_t st) {
+    void* enc = encode_fn();
+    if (!enc) return W8A8_ERR_CUDA;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    void* Ab = w;
+    void* Bb = w + align256(static_cast<size_t>(M) * K * 2);
+    cudaError_t e = w8a8::launch_expand_s8_bf16(Xq, M * K, Ab, dev.num_sms, st);
+    if (e != cudaSuccess) return cuda_fail("expand Xq launch", e);
+    e = w8a8::launch_expand_s8_bf16(Wq, N * K, Bb, dev.num_sms, st);
+    if (e != cudaSuccess) return cuda_fail("expand Wq launch", e);
+    w8a8::GemmArgs a;
+    a.sx = sx;
+    a.sw = sw;
+    a.bias = bias;
+    a.out = out;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
+    e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    if (t_gemm_end && (e = cudaEventRecord(t_gemm_end, st)) != cudaSuccess) return cuda_fail("event", e);
+    return W8A8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w8a8_status_string(w8a8_status s) {
+    switch (s) {
+        case W8A8_OK: return "W8A8_OK";
+        case W8A8_ERR_INVALID_ARG: return "W8A8_ERR_INVALID_ARG: null pointer, bad mode or negative size";
+        case W8A8_ERR_ALIGNMENT: return "W8A8_ERR_ALIGNMENT: a pointer is not 16-byte aligned";
+        case W8A8_ERR_SHAPE: return "W8A8_ERR_SHAPE: K must be a positive multiple of 16 (128 for blocks), <= 131072";
+        case W8A8_ERR_UNSUPPORTED_DEVICE: return "W8A8_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
+        case W8A8_ERR_CUDA: return "W8A8_ERR_CUDA: a CUDA call failed";
+        case W8A8_ERR_TIMEOUT: return "W8A8_ERR_TIMEOUT: a device-side bounded wait ran out";
+        case W8A8_ERR_WORKSPACE: return "W8A8_ERR_WORKSPACE: workspace missing, unaligned or too small";
+    }
+    return "unknown w8a8_status";
+}
+
+w8a8_status w8a8_quantize_weight(const void* W, int64_t N, int64_t K, w8a8_scale_mode mode, int8_t* Wq,
+                                 float* sw, void* stream) {
+    if (mode != W8A8_SCALE_PER_ROW && mode != W8A8_SCALE_BLOCK) return W8A8_ERR_INVALID_ARG;
+    if (N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, mode == W8A8_SCALE_BLOCK);
+    if (s != W8A8_OK) return s;
+    if (N > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (N == 0) return W8A8_OK;
+    if (!W || !Wq || !sw) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(Wq) || !aligned16(sw)) return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(W, N, K, Wq, sw, st));
+    if ((N + 127) / 128 > 65535) return W8A8_ERR_SHAPE;
+    return from_cuda(w8a8::launch_quant_weight_block(W, N, K, Wq, sw, st));
+}
+
+w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8_scale_mode mode, int8_t* Xq, float* sx,
+                              void* stream) {
+    if (mode != W8A8_SCALE_PER_ROW && mode != W8A8_SCALE_BLOCK) return W8A8_ERR_INVALID_ARG;
+    if (M < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, mode == W8A8_SCALE_BLOCK);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0) return W8A8_OK;
+    if (!X || !Xq || !sx) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Xq) || !aligned16(sx)) return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(X, M, K, Xq, sx, st));
+    return from_cuda(w8a8::launch_quant_act_block(X, M, K, Xq, sx, dev.num_sms, st));
+}
+
+size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2);
+}
+
+w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    DeviceInfo dev;
+    bool none;
+    w8a8_status s =
+        check_gemm(Xq, sx, Wq, sw, bias, Y, M, N, K, false, true, workspace, workspace_bytes, &dev, &none);
+    if (s != W8A8_OK || none) return s;
+    return run_gemm(w8a8::kEpiPostscaleBf16, Xq, sx, Wq, sw, bias, Y, M, N, K, workspace, dev,
+                    static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_gemm_blockwise(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    DeviceInfo dev;
+    bool none;
+    w8a8_status s =
+        check_gemm(Xq, sx, Wq, sw, bias, Y, M, N, K, true, true, workspace, workspace_bytes, &dev, &none);
+    if (s != W8A8_OK || none) return s;
+    return run_gemm(w8a8::kEpiBlockwiseBf16, Xq, sx, Wq, sw, bias, Y, M, N, K, workspace, dev,
+                    static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_gemm_postscale_s32(const int8_t* Xq, const int8_t* Wq, int32_t* acc, int64_t M, int64_t N,
+                                    int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+    DeviceInfo dev;
+    bool none;
+    w8a8_status s = check_gemm(Xq, nullptr, Wq, nullptr, nullptr, acc, M, N, K, false, false, workspace,
+                               workspace_bytes, &dev, &none);
+    if (s != W8A8_OK || none) return s;
+    return run_gemm(w8a8::kEpiPostscaleS32, Xq, nullptr, Wq, nullptr, nullptr, acc, M, N, K, workspace, dev,
+                    static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_gemm_blockwise_f32(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                    float* acc, int64_t M, int64_t N, int64_t K, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    DeviceInfo dev;
+    bool none;
+    w8a8_status s = check_gemm(Xq, sx, Wq, sw, nullptr, acc, M, N, K, true, true, workspace, workspace_bytes,
+                               &dev, &none);
+    if (s != W8A8_OK || none) return s;
+    return run_gemm(w8a8::kEpiBlockwiseF32, Xq, sx, Wq, sw, nullptr, acc, M, N, K, workspace, dev,
+                    static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_get_device_error(int* code) {
+    if (!code) return W8A8_ERR_INVALID_ARG;
+    *code = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    unsigned int v = 0;
+    if (w8a8::gemm_read_device_error(&v) != cudaSuccess) return W8A8_ERR_CUDA;
+    *code = static_cast<int>(v);
+    if (v >= w8a8::kDeviceErrorTimeoutBase) return W8A8_ERR_TIMEOUT;
+    return v ? W8A8_ERR_CUDA : W8A8_OK;
+}
+
+const char* w8a8_last_error_detail(void) { return t_detail; }
+
+w8a8_status w8a8_set_gemm_timing_events(void* start, void* end) {
+    if ((start == nullptr) != (end == nullptr)) return W8A8_ERR_INVALID_ARG;
+    t_gemm_start = static_cast<cudaEvent_t>(start);
+    t_gemm_end = static_cast<cudaEvent_t>(end);
+    return W8A8_OK;
+}
+
+w8a8_status w8a8_measure_imma_peak(double* tops, void* stream) {
+    if (!tops) return W8A8_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    w8a8_status s = current_device(&dev);
+    if (s != W8A8_OK) return s;
+    return from_cuda(w8a8::measure_imma_peak(tops, dev.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

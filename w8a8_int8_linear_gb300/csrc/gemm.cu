@@ -1,0 +1,484 @@
+// Exact INT8 GEMM of the W8A8 Linear on the sm_103a tensor cores.
+//
+// "TurboDiffusion Integration Notes", section "Differences From
+// TurboDiffusion": the post-scale kernel keeps the integer accumulation
+// continuous across K and applies the activation and weight scales in the
+// epilogue; TurboDiffusion's original kernel is blockwise-scaled.  Both
+// modes are computed here.
+//
+// GB300 has no 8-bit integer tcgen05 MMA (kind::i8 does not assemble for
+// sm_103a), so the integer product runs on the bf16 pipe (kind::f16) with
+// fp32 accumulation in tensor memory, which is exact for this data:
+//   - every int8 value in [-127, 127] is exact in bf16, and every product
+//     (|p| <= 16129) is exact in fp32;
+//   - a chunk of at most 1024 K has a sum of absolute products of at most
+//     127*127*1024 = 16,516,096 < 2^24, so every partial sum, in any order
+//     and with any alignment of the addends, is an integer that fp32 holds
+//     exactly;
+//   - after each chunk the fp32 accumulator is read out of tensor memory
+//     and added into an int32 running sum held in registers.
+// The post-scale mode folds every 1024 K (16 stages of 64); the blockwise
+// mode folds at every 128-wide K block, where the fp32 value read out is the
+// block's exact integer partial P, and applies acc = acc + (P * sx) * sw.
+//
+// Kernel layout (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: bf16 A and B tiles, 128-byte swizzle, into a
+//               4-stage shared-memory ring;
+//   warp 1      tensor-memory allocator and MMA issuer (one elected lane):
+//               tcgen05.mma 128x256x16 into one of two 256-column fp32
+//               accumulators (512 TMEM columns), committing each smem stage
+//               back to the producer and each finished chunk to the
+//               epilogue;
+//   warps 2..9  epilogue: each warp reads its 32 TMEM lanes (rows) x 128
+//               columns, folds chunks into registers, and writes the output
+//               tile with the scales and bias applied.
+// Two accumulator buffers let the MMA of chunk c+1 run while chunk c is
+// folded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdio>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace w8a8 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // bf16 elements per stage row = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = BN;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr int POSTSCALE_CHUNK_STAGES = 16;  // 1024 K: 127*127*1024 < 2^24
+constexpr int BLOCK_CHUNK_STAGES = 2;       // one 128-wide scale block
+constexpr int GROUP_M = 16;                 // tile raster: bands of 16 row blocks
+constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
+
+enum WaitSite : int {
+    kSiteProducerEmpty = 1,
+    kSiteMmaAccEmpty = 2,
+    kSiteMmaFull = 3,
+    kSiteEpiAccFull = 4,
+    kSiteMmaDrain = 5,
+    kSiteProducerDrain = 6,
+};
+
+struct KParams {
+    const float* sx;
+    const float* sw;
+    const __nv_bfloat16* bias;
+    void* out;
+    int M, N, K;
+    int num_m, num_n, num_tiles;
+    int k_stages, chunk_stages, kb_count;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+    const int per_group = GROUP_M * num_n;
+    const int group = tile / per_group;
+    const int first_m = group * GROUP_M;
+    const int gm = min(num_m - first_m, GROUP_M);
+    const int local = tile - group * per_group;
+    mb = first_m + local % gm;
+    nb = local / gm;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int EPI>
+struct AccType {
+    using T = int32_t;
+};
+template <>
+struct AccType<kEpiBlockwiseBf16> {
+    using T = float;
+};
+template <>
+struct AccType<kEpiBlockwiseF32> {
+    using T = float;
+};
+
+// Write the 128 accumulated columns [col0, col0+128) of one row.
+template <int EPI>
+__device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[128], const KParams& p, int row,
+                                          int col0) {
+    if (row >= p.M) return;
+    const int N = p.N;
+    const bool vec = (N & 7) == 0;
+    const int64_t rowoff = static_cast<int64_t>(row) * N;
+    float sxr = 0.0f;
+    if constexpr (EPI == kEpiPostscaleBf16) sxr = p.sx[row];
+#pragma unroll
+    for (int j = 0; j < 128; j += 8) {
+        const int col = col0 + j;
+        if (col < N) {
+            const bool full = vec && (col + 8 <= N);
+            if constexpr (EPI == kEpiPostscaleS32 || EPI == kEpiBlockwiseF32) {
+                using T = typename AccType<EPI>::T;
+                T* out = static_cast<T*>(p.out) + rowoff + col;
+                if (full) {
+                    uint4 lo, hi;
+                    lo.x = *reinterpret_cast<const uint32_t*>(&acc[j + 0]);
+                    lo.y = *reinterpret_cast<const uint32_t*>(&acc[j + 1]);
+                    lo.z = *reinterpret_cast<const uint32_t*>(&acc[j + 2]);
+                    lo.w = *reinterpret_cast<const uint32_t*>(&acc[j + 3]);
+                    hi.x = *reinterpret_cast<const uint32_t*>(&acc[j + 4]);
+                    hi.y = *reinterpret_cast<const uint32_t*>(&acc[j + 5]);
+                    hi.z = *reinterpret_cast<const uint32_t*>(&acc[j + 6]);
+                    hi.w = *reinterpret_cast<const uint32_t*>(&acc[j + 7]);
+                    reinterpret_cast<uint4*>(out)[0] = lo;
+                    reinterpret_cast<uint4*>(out)[1] = hi;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (col + e < N) out[e] = acc[j + e];
+                }
+            } else {
+                float y[8];
+                float swc[8];
+                float bc[8];
+                if (full) {
+                    if constexpr (EPI == kEpiPostscaleBf16) {
+                        const float4 s0 = *reinterpret_cast<const float4*>(p.sw + col);
+                        const float4 s1 = *reinterpret_cast<const float4*>(p.sw + col + 4);
+                        swc[0] = s0.x; swc[1] = s0.y; swc[2] = s0.z; swc[3] = s0.w;
+                        swc[4] = s1.x; swc[5] = s1.y; swc[6] = s1.z; swc[7] = s1.w;
+                    }
+                    if (p.bias) {
+                        const uint4 b = *reinterpret_cast<const uint4*>(p.bias + col);
+                        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            bc[2 * e] = __uint_as_float(bw[e] << 16);
+                            bc[2 * e + 1] = __uint_as_float(bw[e] & 0xFFFF0000u);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const bool in = col + e < N;
+                        if constexpr (EPI == kEpiPostscaleBf16) swc[e] = in ? p.sw[col + e] : 0.0f;
+                        if (p.bias)
+                            bc[e] = in ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.bias)[col + e]) : 0.0f;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float v;
+                    if constexpr (EPI == kEpiPostscaleBf16)
+                        v = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e]), sxr), swc[e]);
+                    else
+                        v = acc[j + e];
+                    if (p.bias) v = __fadd_rn(v, bc[e]);
+                    y[e] = v;
+                }
+                uint16_t* out = static_cast<uint16_t*>(p.out) + rowoff + col;
+                if (full) {
+                    uint4 o;
+                    o.x = pack_bf16x2(y[0], y[1]);
+                    o.y = pack_bf16x2(y[2], y[3]);
+                    o.z = pack_bf16x2(y[4], y[5]);
+                    o.w = pack_bf16x2(y[6], y[7]);
+                    *reinterpret_cast<uint4*>(out) = o;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (col + e < N) {
+                            __nv_bfloat16 h = __float2bfloat16_rn(y[e]);
+                            out[e] = *reinterpret_cast<uint16_t*>(&h);
+                        }
+                }
+            }
+        }
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* mma_drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(mma_drain, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0;  // bit s: stage s was armed at least once
+            uint32_t armed_phase = 0;  // bit s: parity of the last armed phase
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.num_m, p.num_n, mb, nb);
+                for (int ks = 0; ks < p.k_stages; ++ks) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+                    tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], ks * BK, mb * BM);
+                    tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], ks * BK, nb * BN);
+                    armed |= 1u << stage;
+                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy this thread issued has landed before the CTA exits.
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, kSiteProducerDrain);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                for (int c = 0; ok && c < nchunks; ++c) {
+                    if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * ACC_COLS;
+                    const int s0 = c * p.chunk_stages;
+                    const int s1 = min(p.k_stages, s0 + p.chunk_stages);
+                    for (int ks = s0; ks < s1; ++ks) {
+                        if (!mbar_wait(&full[stage], phase, kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+                        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t da = smem_desc_kmajor_sw128(a_addr + k * 32);
+                            const uint64_t db = smem_desc_kmajor_sw128(b_addr + k * 32);
+                            mma_bf16_ss(d_tmem, da, db, IDESC, (ks > s0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&empty[stage]);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&acc_full[buf]);
+                    buf ^= 1;
+                    if (buf == 0) buf_phase ^= 1u;
+                }
+            }
+            // Every MMA this thread issued has completed before TMEM is freed.
+            mma_commit(mma_drain);
+            mbar_wait(mma_drain, 0, kSiteMmaDrain);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        using T = typename AccType<EPI>::T;
+        const int quarter = warp & 3;          // TMEM lanes this warp may access
+        const int half = (warp - 2) >> 2;      // which 128-column half of the tile
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.num_m, p.num_n, mb, nb);
+            const int row = mb * BM + quarter * 32 + lane;
+            const int col0 = nb * BN + half * 128;
+            T acc[128];
+#pragma unroll
+            for (int e = 0; e < 128; ++e) acc[e] = T(0);
+            for (int c = 0; c < nchunks; ++c) {
+                float sxv = 0.0f, swv = 0.0f;
+                if constexpr (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32) {
+                    if (row < p.M) sxv = p.sx[static_cast<int64_t>(row) * p.kb_count + c];
+                    if (col0 < p.N) swv = p.sw[static_cast<int64_t>(col0 >> 7) * p.kb_count + c];
+                }
+                if (!mbar_wait(&acc_full[buf], buf_phase, kSiteEpiAccFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(buf) * ACC_COLS + static_cast<uint32_t>(half * 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + j * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = __uint_as_float(r[e]);
+                        if constexpr (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32) {
+                            acc[j * 32 + e] = __fadd_rn(acc[j * 32 + e], __fmul_rn(__fmul_rn(v, sxv), swv));
+                        } else {
+                            acc[j * 32 + e] += __float2int_rz(v);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                buf ^= 1;
+                if (buf == 0) buf_phase ^= 1u;
+            }
+            if (!ok) break;
+            store_row<EPI>(acc, p, row, col0);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+CUresult make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, const void* base, int64_t inner,
+                  int64_t rows, uint32_t box_inner, uint32_t box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <int EPI>
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const KParams& p, int grid,
+                       cudaStream_t st) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    gemm_kernel<EPI><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const GemmArgs& a, int num_sms,
+                        void* encode_fn, cudaStream_t st, char* detail, size_t n) {
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encode_fn);
+    CUtensorMap tmA, tmB;
+    CUresult r = make_map(encode, &tmA, Ab, a.K, a.M, BK, BM);
+    if (r != CUDA_SUCCESS) {
+        snprintf(detail, n, "cuTensorMapEncodeTiled(A: %lld x %lld) returned %d", (long long)a.M, (long long)a.K,
+                 (int)r);
+        return cudaErrorInvalidValue;
+    }
+    r = make_map(encode, &tmB, Bb, a.K, a.N, BK, BN);
+    if (r != CUDA_SUCCESS) {
+        snprintf(detail, n, "cuTensorMapEncodeTiled(B: %lld x %lld) returned %d", (long long)a.N, (long long)a.K,
+                 (int)r);
+        return cudaErrorInvalidValue;
+    }
+    KParams p;
+    p.sx = a.sx;
+    p.sw = a.sw;
+    p.bias = static_cast<const __nv_bfloat16*>(a.bias);
+    p.out = a.out;
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.N);
+    p.K = static_cast<int>(a.K);
+    p.num_m = static_cast<int>((a.M + BM - 1) / BM);
+    p.num_n = static_cast<int>((a.N + BN - 1) / BN);
+    p.num_tiles = p.num_m * p.num_n;
+    p.k_stages = static_cast<int>((a.K + BK - 1) / BK);
+    const bool blockwise = epilogue == kEpiBlockwiseBf16 || epilogue == kEpiBlockwiseF32;
+    p.chunk_stages = blockwise ? BLOCK_CHUNK_STAGES : POSTSCALE_CHUNK_STAGES;
+    p.kb_count = static_cast<int>(a.K / 128);
+    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    cudaError_t e;
+    switch (epilogue) {
+        case kEpiPostscaleBf16: e = launch_one<kEpiPostscaleBf16>(tmA, tmB, p, grid, st); break;
+        case kEpiPostscaleS32: e = launch_one<kEpiPostscaleS32>(tmA, tmB, p, grid, st); break;
+        case kEpiBlockwiseBf16: e = launch_one<kEpiBlockwiseBf16>(tmA, tmB, p, grid, st); break;
+        case kEpiBlockwiseF32: e = launch_one<kEpiBlockwiseF32>(tmA, tmB, p, grid, st); break;
+        default: e = cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess)
+        snprintf(detail, n, "GEMM launch (grid %d, %d threads, %zu bytes smem): %s", grid, THREADS, SMEM_BYTES,
+                 cudaGetErrorString(e));
+    return e;
+}
+
+cudaError_t gemm_read_device_error(unsigned int* code) {
+    unsigned int v = 0, z = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_device_error, &z, sizeof z);
+    *code = v;
+    return e;
+}
+
+}  // namespace w8a8

@@ -1,0 +1,53 @@
+// Internal launchers shared by the C-ABI layer (api.cu) and the kernel
+// translation units.  Arguments are validated by the caller.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace w8a8 {
+
+// Per-row quantization of A[R,K] (bf16): one scale per row (per token for
+// activations, per output channel for weights).
+cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, cudaStream_t st);
+// 1x128-block activation quantization, sx[M][K/128].
+cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, float* sx, int num_sms,
+                                   cudaStream_t st);
+// 128x128-block weight quantization, sw[ceil(N/128)][K/128].
+cudaError_t launch_quant_weight_block(const void* W, int64_t N, int64_t K, int8_t* Wq, float* sw,
+                                      cudaStream_t st);
+// Exact int8 -> bf16 image of n values (n % 16 == 0).
+cudaError_t launch_expand_s8_bf16(const int8_t* src, int64_t n, void* dst, int num_sms, cudaStream_t st);
+
+enum GemmEpilogue : int {
+    kEpiPostscaleBf16 = 0,  // Y = bf16(((acc * sx) * sw) + bias)
+    kEpiPostscaleS32 = 1,   // acc int32
+    kEpiBlockwiseBf16 = 2,  // Y = bf16(acc_f32 + bias)
+    kEpiBlockwiseF32 = 3,   // acc fp32
+};
+
+struct GemmArgs {
+    const float* sx;
+    const float* sw;
+    const void* bias;  // bf16 [N] or nullptr
+    void* out;         // Y bf16 / acc int32 / acc fp32, [M,N]
+    int64_t M, N, K;
+};
+
+// Tensor-core GEMM on the bf16 images (Ab [M,K], Bb [N,K]) of the int8
+// operands.  `encode` is the driver's cuTensorMapEncodeTiled.
+// On failure, a one-line description is written to `detail` (size `n`).
+cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const GemmArgs& args, int num_sms,
+                        void* encode_fn, cudaStream_t st, char* detail, size_t n);
+
+// Device error codes at or above this value mean a bounded wait ran out.
+constexpr unsigned int kDeviceErrorTimeoutBase = 0x100;
+
+// Reads and clears the GEMM translation unit's device error word.
+cudaError_t gemm_read_device_error(unsigned int* code);
+
+// Throughput kernel of warp-level INT8 MMAs; returns tera-ops per second.
+cudaError_t measure_imma_peak(double* tops, int num_sms, cudaStream_t st);
+
+}  // namespace w8a8
