@@ -146,6 +146,32 @@ W8A8_API w8a8_status w8a8_gemm_blockwise(const int8_t* Xq, const float* sx, cons
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * Allocation-free variant of w8a8_gemm_postscale (the pages have no
+ * counterpart: this is a library convenience).  Same arguments, results and
+ * checks, minus the workspace: the scratch lives in a fixed 64 MiB device
+ * array inside the library, so the shape must satisfy
+ * w8a8_gemm_workspace_size(M,N,K) <= 64 MiB (for example M = N = K = 4096),
+ * else W8A8_ERR_WORKSPACE and nothing is launched.
+ *
+ * For callers that cannot allocate device memory at the call site, for
+ * example code running inside a host callback or a real-time loop where
+ * cudaMalloc's implicit synchronization is not allowed, or a plugin whose
+ * host framework owns the device allocator and offers it no hook.
+ *
+ * The array is created when the library is loaded on a device and held by
+ * every device that loads the library until the process exits.  The first
+ * call on each device looks up the array's device address (once, with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the one array and leaves its contents behind (nothing in it
+ * needs to start at zero): calls whose work overlaps on the GPU, on
+ * different streams or threads, race on it and must be serialized by the
+ * caller.  Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+W8A8_API w8a8_status w8a8_gemm_postscale_noalloc(const int8_t* Xq, const float* sx, const int8_t* Wq,
+                                                 const float* sw, const void* bias, void* Y, int64_t M, int64_t N,
+                                                 int64_t K, void* stream);
+
+/*
  * Test and debug exports of the same mainloops, stopping before the bf16
  * epilogue.
  *   w8a8_gemm_postscale_s32: acc [M,N] int32 = sum_k Xq[m,k] * Wq[n,k].

@@ -1,0 +1,73 @@
+"""The allocation-free post-scale GEMM entry point, through the C ABI.
+
+w8a8_gemm_postscale_noalloc serves callers that cannot allocate device memory
+where they call (a host callback or real-time loop that must not trigger
+cudaMalloc's synchronization, or a plugin whose framework owns the
+allocator): its scratch is a fixed 64 MiB device array inside the library.
+This file is collected last so that a failure here leaves every other test
+already run; it also passes when run alone in a fresh process."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_bf16_close, bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(M, N, K, seed, bias):
+    g = torch.Generator().manual_seed(seed)
+    X = (torch.randn((M, K), generator=g)).to(torch.bfloat16).to(DEV)
+    W = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).to(DEV)
+    b = (torch.randn((N,), generator=g) * 0.01).to(torch.bfloat16).to(DEV) if bias else None
+    return X, W, b
+
+
+def _call_noalloc(L, Xq, sx, Wq, sw, b, Y):
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    P = ctypes.c_void_p
+    return L.w8a8_gemm_postscale_noalloc(P(Xq.data_ptr()), P(sx.data_ptr()), P(Wq.data_ptr()), P(sw.data_ptr()),
+                                         None if b is None else P(b.data_ptr()), P(Y.data_ptr()), M, N, K,
+                                         P(torch.cuda.current_stream().cuda_stream))
+
+
+def test_noalloc_matches_workspace_entry_point_twice(w8a8):
+    L = w8a8.lib()
+    # two calls in a row, different shapes (the second at the 64 MiB limit),
+    # each against the workspace entry point on the same inputs
+    for (M, N, K, bias, seed) in [(300, 520, 1040, True, 1), (4096, 4096, 4096, False, 2)]:
+        X, W, b = _inputs(M, N, K, seed, bias)
+        Xq, sx = w8a8.quantize_act(X)
+        Wq, sw = w8a8.quantize_weight(W)
+        Y_ref = w8a8.gemm_postscale(Xq, sx, Wq, sw, b)
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+        assert _call_noalloc(L, Xq, sx, Wq, sw, b, Y) == 0
+        torch.cuda.synchronize()
+        assert_bf16_close(bits(Y), bits(Y_ref), 1)
+    assert w8a8.get_device_error() == (0, 0)
+
+
+def test_noalloc_repeat_same_shape_and_limit(w8a8):
+    L = w8a8.lib()
+    X, W, b = _inputs(129, 264, 4112, 3, True)
+    Xq, sx = w8a8.quantize_act(X)
+    Wq, sw = w8a8.quantize_weight(W)
+    Y_ref = w8a8.gemm_postscale(Xq, sx, Wq, sw, b)
+    for _ in range(2):
+        Y = torch.zeros((129, 264), dtype=torch.bfloat16, device=DEV)
+        assert _call_noalloc(L, Xq, sx, Wq, sw, b, Y) == 0
+        torch.cuda.synchronize()
+        assert_bf16_close(bits(Y), bits(Y_ref), 1)
+    # one row past the limit is rejected with W8A8_ERR_WORKSPACE, nothing launched
+    M, N, K = 4097, 4096, 4096
+    Xq = torch.zeros((M, K), dtype=torch.int8, device=DEV)
+    Wq = torch.zeros((N, K), dtype=torch.int8, device=DEV)
+    Y = torch.zeros((M, N), dtype=torch.bfloat16, device=DEV)
+    st = _call_noalloc(L, Xq, torch.ones(M, device=DEV), Wq, torch.ones(N, device=DEV), None, Y)
+    assert st == 7
+    assert "no-alloc scratch holds" in L.w8a8_last_error_detail().decode()
+    assert torch.all(Y == 0)

@@ -41,6 +41,7 @@ SIGNATURES = [
     ("w8a8_gemm_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w8a8_gemm_postscale", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_gemm_postscale_noalloc", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_get_device_error", _I32, [ctypes.POINTER(ctypes.c_int)]),
@@ -189,6 +190,28 @@ def gemm_blockwise(Xq, sx, Wq, sw, bias=None, out=None, workspace=None):
     _check("w8a8_gemm_blockwise",
            lib().w8a8_gemm_blockwise(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
                                      _ptr(ws), ws.numel(), _stream()))
+    return Y
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def gemm_postscale_noalloc(Xq, sx, Wq, sw, bias=None, out=None):
+    """Post-scale GEMM using the library's fixed 64 MiB device scratch instead
+    of a caller workspace (for callers that cannot allocate device memory at
+    the call site).  Calls overlapping on the GPU race on the shared scratch."""
+    _need(Xq, torch.int8, "Xq", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(sx, torch.float32, "sx")
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    _check("w8a8_gemm_postscale_noalloc",
+           lib().w8a8_gemm_postscale_noalloc(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
+                                             _stream()))
     return Y
 
 

@@ -157,6 +157,40 @@ w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* W
     return W8A8_OK;
 }
 
+// Scratch of the allocation-free GEMM entry point: a fixed device array,
+// loaded with the library on every device that uses it and held until the
+// process exits.  The name is a host-side stand-in; its device address comes
+// from cudaGetSymbolAddress, taken once per device with that device current.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_ptr[kMaxDevices];
+std::atomic<bool> g_noalloc_ready[kMaxDevices];
+
+w8a8_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("cudaGetDevice", e);
+    }
+    if (dev < 0 || dev >= kMaxDevices) return W8A8_ERR_UNSUPPORTED_DEVICE;
+    if (!g_noalloc_ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_noalloc_ready[dev].load(std::memory_order_relaxed)) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || p == nullptr) {
+                cudaGetLastError();
+                return cuda_fail("cudaGetSymbolAddress(no-alloc scratch)", e);
+            }
+            g_noalloc_ptr[dev] = p;
+            g_noalloc_ready[dev].store(true, std::memory_order_release);
+        }
+    }
+    *out = g_noalloc_ptr[dev];
+    return W8A8_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -236,6 +270,28 @@ w8a8_status w8a8_gemm_blockwise(const int8_t* Xq, const float* sx, const int8_t*
         check_gemm(Xq, sx, Wq, sw, bias, Y, M, N, K, true, true, workspace, workspace_bytes, &dev, &none);
     if (s != W8A8_OK || none) return s;
     return run_gemm(w8a8::kEpiBlockwiseBf16, Xq, sx, Wq, sw, bias, Y, M, N, K, workspace, dev,
+                    static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_gemm_postscale_noalloc(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
+                                        const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream) {
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, false);
+    if (s != W8A8_OK) return s;
+    if (M == 0 || N == 0) return W8A8_OK;
+    if (w8a8_gemm_workspace_size(M, N, K) > kNoAllocScratchBytes) {
+        set_detail("shape %lld x %lld x %lld needs %zu bytes of scratch; the fixed no-alloc scratch holds %zu",
+                   (long long)M, (long long)N, (long long)K, w8a8_gemm_workspace_size(M, N, K),
+                   kNoAllocScratchBytes);
+        return W8A8_ERR_WORKSPACE;
+    }
+    void* scratch = nullptr;
+    if ((s = noalloc_scratch(&scratch)) != W8A8_OK) return s;
+    DeviceInfo dev;
+    bool none;
+    s = check_gemm(Xq, sx, Wq, sw, bias, Y, M, N, K, false, true, scratch, kNoAllocScratchBytes, &dev, &none);
+    if (s != W8A8_OK || none) return s;
+    return run_gemm(w8a8::kEpiPostscaleBf16, Xq, sx, Wq, sw, bias, Y, M, N, K, scratch, dev,
                     static_cast<cudaStream_t>(stream));
 }
 
