@@ -162,19 +162,27 @@ def oracle_sample_run(work, rows, X_bits, W_bits, b_bits):
 
 
 def cpu_baseline(work, X, W, b, target_s=10.0):
+    """The oracle, as it stands, on blocks of 256 rows of the same X until
+    about `target_s` seconds of host time have been spent."""
     import oracle
     from w8a8_int8_linear_gb300.workloads import bf16_bits
-    rows_max = min(work.M, 1024)
+    rows_max = min(work.M, 4096)
     Xb = bf16_bits(X[:rows_max])
     Wq_o = oracle.quantize_weight(bf16_bits(W), oracle.PER_ROW)
     bb = None if b is None else bf16_bits(b)
-    dt, ops = oracle_sample_run(work, 8, Xb, Wq_o, bb)  # calibration
-    rate = ops / max(dt, 1e-9)
-    rows = int(max(8, min(rows_max, target_s * rate / (2.0 * work.N * work.K))))
-    dt, ops = oracle_sample_run(work, rows, Xb, Wq_o, bb)
-    return dict(value=ops / dt / 1e12, unit="TOPS", cores=oracle.num_threads(), kind="oracle",
-                sample=f"{rows} of {work.M} rows of X (per-token quant + int32 GEMM + epilogue vs all "
-                       f"{work.N} outputs, weights pre-quantized), {dt:.1f} s")
+    blk = min(256, rows_max)
+    total_t, total_ops, rows_done, r0 = 0.0, 0.0, 0, 0
+    while total_t < target_s:
+        if r0 + blk > rows_max:
+            r0 = 0
+        dt, ops = oracle_sample_run(work, blk, Xb[r0:r0 + blk], Wq_o, bb)
+        total_t += dt
+        total_ops += ops
+        rows_done += blk
+        r0 += blk
+    return dict(value=total_ops / total_t / 1e12, unit="TOPS", cores=oracle.num_threads(), kind="oracle",
+                sample=f"{rows_done} rows of X in blocks of {blk} (per-token quant + int32 GEMM + epilogue vs all "
+                       f"{work.N} outputs, weights pre-quantized), {total_t:.1f} s of host time")
 
 
 # ----------------------------------------------------------------- main arm
@@ -237,12 +245,15 @@ def run_w8a8(args):
     clk = ClockSampler(gpu_uuid)
     clk.start()
     clk.active = True
-    # bring clocks up (a bounded number of untimed steps), then the W warm-up steps
-    t_end = time.time() + 1.0
-    for _ in range(100):
+    # bring clocks up: ~1.5 s of back-to-back untimed steps (bounded by count),
+    # sampled by the clock reader together with the timed region
+    t_end = time.time() + 1.5
+    for i in range(20000):
         step()
-        if time.time() > t_end:
-            break
+        if i % 16 == 15:
+            torch.cuda.synchronize()
+            if time.time() > t_end:
+                break
     torch.cuda.synchronize()
     for _ in range(max(args.warmup, 3)):
         flush.zero_()

@@ -48,20 +48,21 @@
 namespace w8a8 {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // bf16 elements per stage row = 128 bytes = one swizzle row
-constexpr int STAGES = 4;
+constexpr int BM = 128;      // rows of A per CTA; a CTA pair covers TILE_M rows
+constexpr int TILE_M = 2 * BM;
+constexpr int BN = 256;      // output columns per tile; each CTA of the pair loads BN/2 rows of B
+constexpr int BK = 64;       // bf16 elements per stage row = 128 bytes = one swizzle row
+constexpr int STAGES = 6;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
 constexpr int POSTSCALE_CHUNK_STAGES = 16;  // 1024 K: 127*127*1024 < 2^24
 constexpr int BLOCK_CHUNK_STAGES = 2;       // one 128-wide scale block
-constexpr int GROUP_M = 16;                 // tile raster: bands of 16 row blocks
+constexpr int GROUP_M = 8;                  // tile raster: bands of 8 row tiles (2048 rows)
 constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
 
 enum WaitSite : int {
@@ -226,15 +227,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
+    const bool leader = rank == 0;
+    const int cluster = static_cast<int>(cluster_id_x());
+    const int nclusters = static_cast<int>(nclusters_x());
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&full[s], 1);   // leader only: its arrive + both CTAs' bytes
+            mbar_init(&empty[s], 1);  // both: the leader's multicast commit
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], EPI_WARPS);
+            mbar_init(&acc_full[b], 1);               // both: multicast commit
+            mbar_init(&acc_empty[b], 2 * EPI_WARPS);  // leader only: every epilogue warp of the pair
         }
         mbar_init(mma_drain, 1);
         fence_mbarrier_init();
@@ -244,33 +249,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the peer's barriers are initialized before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer (both CTAs)
         if (elect_one_sync()) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t armed = 0;  // bit s: stage s was armed at least once
-            uint32_t armed_phase = 0;  // bit s: parity of the last armed phase
+            uint32_t armed = 0, armed_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
                 int mb, nb;
                 tile_coords(tile, p.num_m, p.num_n, mb, nb);
+                const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
+                const int b_row = nb * BN + static_cast<int>(rank) * (BN / 2);
                 for (int ks = 0; ks < p.k_stages; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], ks * BK, mb * BM);
-                    tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], ks * BK, nb * BN);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+                    const uint32_t bar = map_to_rank(smem_u32(&full[stage]), 0);
+                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, ks * BK, a_row);
+                    tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, ks * BK, b_row);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -279,20 +288,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            // Every copy this thread issued has landed before the CTA exits.
+            // The MMAs that read each stage's last fill have completed (so its
+            // copies landed) before this CTA's shared memory is released.
             for (int s = 0; s < STAGES; ++s)
-                if (armed & (1u << s)) mbar_wait(&full[s], (armed_phase >> s) & 1u, kSiteProducerDrain);
+                if (armed & (1u << s)) mbar_wait(&empty[s], (armed_phase >> s) & 1u, kSiteProducerDrain);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (elect_one_sync()) {
+        // ------------------------------------------------------------ MMA issuer (leader only)
+        if (leader && elect_one_sync()) {
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
-            const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
                 for (int c = 0; ok && c < nchunks; ++c) {
                     if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteMmaAccEmpty)) {
                         ok = false;
@@ -314,37 +323,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int k = 0; k < BK / 16; ++k) {
                             const uint64_t da = smem_desc_kmajor_sw128(a_addr + k * 32);
                             const uint64_t db = smem_desc_kmajor_sw128(b_addr + k * 32);
-                            mma_bf16_ss(d_tmem, da, db, IDESC, (ks > s0 || k > 0) ? 1u : 0u);
+                            mma_bf16_ss_pair(d_tmem, da, db, IDESC, (ks > s0 || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(&empty[stage]);
+                        mma_commit_pair_multicast(&empty[stage], 0x3);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&acc_full[buf]);
+                    mma_commit_pair_multicast(&acc_full[buf], 0x3);
                     buf ^= 1;
                     if (buf == 0) buf_phase ^= 1u;
                 }
             }
-            // Every MMA this thread issued has completed before TMEM is freed.
-            mma_commit(mma_drain);
+            // Every MMA issued has completed before TMEM is freed.
+            mma_commit_pair(mma_drain);
             mbar_wait(mma_drain, 0, kSiteMmaDrain);
         }
     } else {
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------------------------------ epilogue (both CTAs)
         using T = typename AccType<EPI>::T;
-        const int quarter = warp & 3;          // TMEM lanes this warp may access
-        const int half = (warp - 2) >> 2;      // which 128-column half of the tile
+        const int quarter = warp & 3;      // TMEM lanes this warp may access
+        const int half = (warp - 2) >> 2;  // which 128-column half of the tile
+        const uint32_t leader_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
-        const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
             int mb, nb;
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
-            const int row = mb * BM + quarter * 32 + lane;
+            const int row = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
             const int col0 = nb * BN + half * 128;
             T acc[128];
 #pragma unroll
@@ -363,23 +372,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(buf) * ACC_COLS + static_cast<uint32_t>(half * 128);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + j * 32, r);
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(taddr + j * 16, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < 16; ++e) {
                         const float v = __uint_as_float(r[e]);
                         if constexpr (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32) {
-                            acc[j * 32 + e] = __fadd_rn(acc[j * 32 + e], __fmul_rn(__fmul_rn(v, sxv), swv));
+                            acc[j * 16 + e] = __fadd_rn(acc[j * 16 + e], __fmul_rn(__fmul_rn(v, sxv), swv));
                         } else {
-                            acc[j * 32 + e] += __float2int_rz(v);
+                            acc[j * 16 + e] += __float2int_rz(v);
                         }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + static_cast<uint32_t>(buf) * 8u);
                 buf ^= 1;
                 if (buf == 0) buf_phase ^= 1u;
             }
@@ -390,9 +399,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // neither CTA leaves while the pair may still touch its barriers or smem
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -407,27 +417,58 @@ CUresult make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, co
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+struct DeviceLaunchInfo {
+    bool configured[4];
+    int max_clusters;
+};
+DeviceLaunchInfo g_launch_info[64];
+
 template <int EPI>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const KParams& p, int grid,
-                       cudaStream_t st) {
-    static bool configured[64] = {};
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const KParams& p, int num_sms,
+                       cudaStream_t st, char* detail, size_t n) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    DeviceLaunchInfo& info = g_launch_info[dev];
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!info.configured[EPI]) {
         e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES));
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
+        if (info.max_clusters == 0) {
+            cfg.gridDim = dim3(2 * (num_sms / 2));
+            int nc = 0;
+            e = cudaOccupancyMaxActiveClusters(&nc, gemm_kernel<EPI>, &cfg);
+            if (e != cudaSuccess) return e;
+            if (nc < 1) {
+                snprintf(detail, n, "no CTA pair of the GEMM kernel fits on this device");
+                return cudaErrorInvalidConfiguration;
+            }
+            info.max_clusters = nc;
+        }
+        info.configured[EPI] = true;
     }
-    gemm_kernel<EPI><<<grid, THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    const int clusters = p.num_tiles < info.max_clusters ? p.num_tiles : info.max_clusters;
+    cfg.gridDim = dim3(2 * clusters);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, tmA, tmB, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const GemmArgs& a, int num_sms,
                         void* encode_fn, cudaStream_t st, char* detail, size_t n) {
+    if (n) detail[0] = 0;
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encode_fn);
     CUtensorMap tmA, tmB;
     CUresult r = make_map(encode, &tmA, Ab, a.K, a.M, BK, BM);
@@ -436,7 +477,7 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
                  (int)r);
         return cudaErrorInvalidValue;
     }
-    r = make_map(encode, &tmB, Bb, a.K, a.N, BK, BN);
+    r = make_map(encode, &tmB, Bb, a.K, a.N, BK, BN / 2);
     if (r != CUDA_SUCCESS) {
         snprintf(detail, n, "cuTensorMapEncodeTiled(B: %lld x %lld) returned %d", (long long)a.N, (long long)a.K,
                  (int)r);
@@ -450,24 +491,23 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
-    p.num_m = static_cast<int>((a.M + BM - 1) / BM);
+    p.num_m = static_cast<int>((a.M + TILE_M - 1) / TILE_M);
     p.num_n = static_cast<int>((a.N + BN - 1) / BN);
     p.num_tiles = p.num_m * p.num_n;
     p.k_stages = static_cast<int>((a.K + BK - 1) / BK);
     const bool blockwise = epilogue == kEpiBlockwiseBf16 || epilogue == kEpiBlockwiseF32;
     p.chunk_stages = blockwise ? BLOCK_CHUNK_STAGES : POSTSCALE_CHUNK_STAGES;
     p.kb_count = static_cast<int>(a.K / 128);
-    const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
     cudaError_t e;
     switch (epilogue) {
-        case kEpiPostscaleBf16: e = launch_one<kEpiPostscaleBf16>(tmA, tmB, p, grid, st); break;
-        case kEpiPostscaleS32: e = launch_one<kEpiPostscaleS32>(tmA, tmB, p, grid, st); break;
-        case kEpiBlockwiseBf16: e = launch_one<kEpiBlockwiseBf16>(tmA, tmB, p, grid, st); break;
-        case kEpiBlockwiseF32: e = launch_one<kEpiBlockwiseF32>(tmA, tmB, p, grid, st); break;
+        case kEpiPostscaleBf16: e = launch_one<kEpiPostscaleBf16>(tmA, tmB, p, num_sms, st, detail, n); break;
+        case kEpiPostscaleS32: e = launch_one<kEpiPostscaleS32>(tmA, tmB, p, num_sms, st, detail, n); break;
+        case kEpiBlockwiseBf16: e = launch_one<kEpiBlockwiseBf16>(tmA, tmB, p, num_sms, st, detail, n); break;
+        case kEpiBlockwiseF32: e = launch_one<kEpiBlockwiseF32>(tmA, tmB, p, num_sms, st, detail, n); break;
         default: e = cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess)
-        snprintf(detail, n, "GEMM launch (grid %d, %d threads, %zu bytes smem): %s", grid, THREADS, SMEM_BYTES,
+    if (e != cudaSuccess && detail[0] == 0)
+        snprintf(detail, n, "GEMM launch (%d threads, %zu bytes smem, clusters of 2): %s", THREADS, SMEM_BYTES,
                  cudaGetErrorString(e));
     return e;
 }
