@@ -47,7 +47,8 @@ def special_rows(K):
 
 
 # ----------------------------------------------------------------- quantization
-@pytest.mark.parametrize("M,K", [(1, 16), (7, 256), (300, 5120), (33, 13824), (5, 20480), (3, 131072)])
+@pytest.mark.parametrize("M,K", [(1, 16), (7, 256), (5, 1024), (9, 2048), (33, 4096), (300, 5120), (3, 6144),
+                                 (2, 8192), (33, 13824), (5, 20480), (3, 131072)])
 def test_quantize_act_per_token(w8a8, oracle, M, K):
     X = torch.cat([rand_bf16((M, K), seed=M + K, outliers=0.01, oscale=20.0), special_rows(K)])
     Xq, sx = w8a8.quantize_act(X.to(DEV), w8a8.PER_ROW)
@@ -56,7 +57,19 @@ def test_quantize_act_per_token(w8a8, oracle, M, K):
     assert np.array_equal(sx.cpu().numpy().view(np.uint32), os_.view(np.uint32))
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (9, 256), (1000, 1408), (17, 13824)])
+@pytest.mark.parametrize("M,K", [(6000, 2048), (1300, 8192), (3000, 5120)])
+def test_quantize_act_per_token_streamed_many_units(w8a8, oracle, M, K):
+    """Enough rows that every CTA of the streaming quantizer wraps its
+    shared-memory ring several times."""
+    X = rand_bf16((M, K), seed=M, outliers=0.01, oscale=20.0)
+    Xq, sx = w8a8.quantize_act(X.to(DEV), w8a8.PER_ROW)
+    oq, os_ = oracle.quantize_act(bits(X), oracle.PER_ROW)
+    assert np.array_equal(Xq.cpu().numpy(), oq)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert w8a8.get_device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (9, 256), (1000, 1408), (17, 13824), (4001, 4096)])
 def test_quantize_act_block(w8a8, oracle, M, K):
     X = torch.cat([torch.nn.functional.gelu(rand_bf16((M, K), seed=K).float()).to(torch.bfloat16),
                    special_rows(K)])

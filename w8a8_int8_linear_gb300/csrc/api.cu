@@ -222,7 +222,7 @@ w8a8_status w8a8_quantize_weight(const void* W, int64_t N, int64_t K, w8a8_scale
     DeviceInfo dev;
     if ((s = current_device(&dev)) != W8A8_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(W, N, K, Wq, sw, st));
+    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(W, N, K, Wq, sw, dev.num_sms, st));
     if ((N + 127) / 128 > 65535) return W8A8_ERR_SHAPE;
     return from_cuda(w8a8::launch_quant_weight_block(W, N, K, Wq, sw, st));
 }
@@ -240,7 +240,7 @@ w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8_scale_mo
     DeviceInfo dev;
     if ((s = current_device(&dev)) != W8A8_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(X, M, K, Xq, sx, st));
+    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(X, M, K, Xq, sx, dev.num_sms, st));
     return from_cuda(w8a8::launch_quant_act_block(X, M, K, Xq, sx, dev.num_sms, st));
 }
 
@@ -325,8 +325,10 @@ w8a8_status w8a8_get_device_error(int* code) {
         cudaGetLastError();
         return W8A8_ERR_CUDA;
     }
-    unsigned int v = 0;
+    unsigned int v = 0, vq = 0;
     if (w8a8::gemm_read_device_error(&v) != cudaSuccess) return W8A8_ERR_CUDA;
+    if (w8a8::quant_read_device_error(&vq) != cudaSuccess) return W8A8_ERR_CUDA;
+    if (v == 0) v = vq;
     *code = static_cast<int>(v);
     if (v >= w8a8::kDeviceErrorTimeoutBase) return W8A8_ERR_TIMEOUT;
     return v ? W8A8_ERR_CUDA : W8A8_OK;

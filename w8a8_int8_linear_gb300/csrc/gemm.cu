@@ -54,7 +54,14 @@ constexpr int BN = 256;      // output columns per tile; each CTA of the pair lo
 constexpr int BK = 64;       // bf16 elements per stage row = 128 bytes = one swizzle row
 constexpr int STAGES = 6;
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_WARP0 = 4;  // warps 0-3: producer, MMA issuer, two idle; warps 4-11: epilogue
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512),
+// warpgroup 0 drops to 56 and the two epilogue warpgroups rise to 224:
+// 128 x 56 + 256 x 224 = 64512.
+constexpr int REGS_LOW = 56;
+constexpr int REGS_HIGH = 224;
+static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= THREADS * 168, "register split exceeds the launch budget");
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
 constexpr uint32_t TMEM_COLS = 512;
@@ -258,8 +265,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
-
-    if (warp == 0) {
+    if (warp < EPI_WARP0) {
+      regs_dec<REGS_LOW>();
+      if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
         if (elect_one_sync()) {
             int stage = 0;
@@ -341,11 +349,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_commit_pair(mma_drain);
             mbar_wait(mma_drain, 0, kSiteMmaDrain);
         }
+      }
     } else {
+        regs_inc<REGS_HIGH>();
         // ------------------------------------------------------------ epilogue (both CTAs)
+        constexpr bool kBlock = (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32);
         using T = typename AccType<EPI>::T;
         const int quarter = warp & 3;      // TMEM lanes this warp may access
-        const int half = (warp - 2) >> 2;  // which 128-column half of the tile
+        const int half = (warp - EPI_WARP0) >> 2;  // which 128-column half of the tile
         const uint32_t leader_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
         int buf = 0;
         uint32_t buf_phase = 0;
@@ -355,12 +366,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
             const int row = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
             const int col0 = nb * BN + half * 128;
+            // post-scale: 128 int32 running sums; blockwise: 128 fp32 accumulators
             T acc[128];
 #pragma unroll
             for (int e = 0; e < 128; ++e) acc[e] = T(0);
             for (int c = 0; c < nchunks; ++c) {
                 float sxv = 0.0f, swv = 0.0f;
-                if constexpr (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32) {
+                if constexpr (kBlock) {
                     if (row < p.M) sxv = p.sx[static_cast<int64_t>(row) * p.kb_count + c];
                     if (col0 < p.N) swv = p.sw[static_cast<int64_t>(col0 >> 7) * p.kb_count + c];
                 }
@@ -371,20 +383,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(buf) * ACC_COLS + static_cast<uint32_t>(half * 128);
+                // 4 groups of 32 columns; the load of group j+1 is in flight
+                // while group j is folded.
+                uint32_t ra[32], rb[32];
+                tmem_ld_32x32b_x32(taddr, ra);
+                tmem_wait_ld_regs32(ra);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(taddr + j * 16, r);
-                    tmem_wait_ld();
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t(&cur)[32] = (j & 1) ? rb : ra;
+                    uint32_t(&nxt)[32] = (j & 1) ? ra : rb;
+                    if (j + 1 < 4) tmem_ld_32x32b_x32(taddr + (j + 1) * 32, nxt);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float v = __uint_as_float(r[e]);
-                        if constexpr (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32) {
-                            acc[j * 16 + e] = __fadd_rn(acc[j * 16 + e], __fmul_rn(__fmul_rn(v, sxv), swv));
+                    for (int e = 0; e < 32; ++e) {
+                        const float v = __uint_as_float(cur[e]);
+                        if constexpr (kBlock) {
+                            // t = (P * sx) * sw; acc = acc + t, each rounded on its own
+                            acc[j * 32 + e] = __fadd_rn(acc[j * 32 + e], __fmul_rn(__fmul_rn(v, sxv), swv));
                         } else {
-                            acc[j * 16 + e] += __float2int_rz(v);
+                            acc[j * 32 + e] += __float2int_rz(v);
                         }
                     }
+                    if (j + 1 < 4) tmem_wait_ld_regs32(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -10,7 +10,8 @@ namespace w8a8 {
 
 // Per-row quantization of A[R,K] (bf16): one scale per row (per token for
 // activations, per output channel for weights).
-cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, cudaStream_t st);
+cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, int num_sms,
+                              cudaStream_t st);
 // 1x128-block activation quantization, sx[M][K/128].
 cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, float* sx, int num_sms,
                                    cudaStream_t st);
@@ -44,8 +45,10 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
 // Device error codes at or above this value mean a bounded wait ran out.
 constexpr unsigned int kDeviceErrorTimeoutBase = 0x100;
 
-// Reads and clears the GEMM translation unit's device error word.
+// Read and clear the device error words of the GEMM and quantization
+// translation units.
 cudaError_t gemm_read_device_error(unsigned int* code);
+cudaError_t quant_read_device_error(unsigned int* code);
 
 // Throughput kernel of warp-level INT8 MMAs; returns tera-ops per second.
 cudaError_t measure_imma_peak(double* tops, int num_sms, cudaStream_t st);

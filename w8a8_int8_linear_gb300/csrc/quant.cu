@@ -6,23 +6,40 @@
 // Quantizer: s = absmax / 127 (IEEE fp32 division); q = clamp(rne(x / s),
 // -127, 127) with x / s an IEEE fp32 division; absmax 0 gives s = 0, q = 0.
 //
-// The per-element division is evaluated as t = x * (1/s), where 1/s is the
-// correctly rounded reciprocal.  Error bound: with u = 2^-24, t and the
-// correctly rounded quotient fl(x/s) both lie within 3u*|x/s| <= 3u*127.01
-// (< 2.3e-5) of each other, so they round to the same integer unless one of
-// them is within that distance of a half-integer.  Elements whose t lies
-// within 2^-14 (6.1e-5) of a half-integer take the exact path (IEEE division
-// and round-half-even); every other element provably gets the same q.
+// Scales without division.  absmax is a bf16 value, M * 2^k with an 8-bit
+// significand M in [128, 255].  Scaling by a power of two commutes with
+// rounding while the result stays normal, so fl(absmax / 127) =
+// fl(M / 127) * 2^k and fl(1 / s) = fl(1 / fl(M / 127)) * 2^-k.  Each CTA
+// builds the two 128-entry tables fl(M/127) and fl(1/fl(M/127)) with IEEE
+// division; a scale is then a table read plus an exponent add.  (An
+// exhaustive host check over every bf16 value confirms the identity for
+// exponent fields 7..254; the tables are used for 8..250 and every other
+// nonzero absmax takes IEEE division.)
 //
-// Rounding uses the 1.5 * 2^23 constant: for |t| < 2^22, fl(t + 1.5*2^23)
-// rounds t to the nearest integer with ties to even, and the low byte of its
-// bit pattern is that integer in two's complement.
+// Quantizing one value x with P = x * (1/s) (the exact product):
+//   big = fma(x, 1/s, 1.5*2^23): for |P| < 2^22 this rounds P to the nearest
+//         integer with ties to even, and the low byte of its bit pattern is
+//         that integer in two's complement;
+//   d   = fma(x, 1/s, -(big - 1.5*2^23)) = P - rne(P), rounded once.
+// Error bound: with u = 2^-24, |P - x/s| <= u|x/s| and the IEEE quotient
+// fl(x/s) is within u|x/s| of x/s, so P and fl(x/s) are within
+// 2u * 127.01 < 1.6e-5 of each other.  They round to different integers only
+// if a half-integer lies between them, and then |d| >= 0.5 - 1.6e-5 - 2^-25.
+// Any chunk holding a value with |d| > 0.5 - 2^-14 (6.1e-5) takes the exact
+// path (IEEE division, round half to even, clamp) for those values; every
+// other value provably gets round_half_even(fl(x/s)).
+//
+// No clamp is needed on the fast path: |x| <= absmax and s >= (absmax/127)
+// (1-u), so |P| <= 127 (1+u)^2 < 127.5 and rne(P) lies in [-127, 127].  That
+// bound needs a normal s; a group whose scale is subnormal takes the exact
+// path for every element, which clamps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace w8a8 {
 
@@ -33,14 +50,43 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 constexpr float kTieGuard = 6.103515625e-05f;  // 2^-14
 
 struct RowScale {
-    float s;    // stored scale
-    float inv;  // correctly rounded 1/s (0 when s == 0)
+    float s;     // stored scale
+    float inv;   // correctly rounded 1/s (0 when s == 0)
+    bool exact;  // subnormal, nonzero scale: every element takes the exact path
 };
 
-__device__ __forceinline__ RowScale make_scale(float amax) {
+constexpr float kMinNormal = 1.17549435e-38f;  // 2^-126
+
+struct ScaleTables {
+    float T[128];  // fl((128 + i) / 127)
+    float R[128];  // fl(1 / T[i])
+};
+
+// All threads of the CTA call this before any make_scale.
+__device__ __forceinline__ void build_scale_tables(ScaleTables& t) {
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const float v = __fdiv_rn(static_cast<float>(128 + i), kQMax);
+        t.T[i] = v;
+        t.R[i] = __frcp_rn(v);
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ RowScale make_scale(float amax, const ScaleTables& t) {
     RowScale r;
-    r.s = __fdiv_rn(amax, kQMax);
-    r.inv = (r.s > 0.0f) ? __frcp_rn(r.s) : 0.0f;
+    const uint32_t b = __float_as_uint(amax);  // a bf16 value: low 16 bits are zero
+    const int ef = static_cast<int>(b >> 23);
+    if (ef >= 8 && ef <= 250) {
+        const int f = static_cast<int>((b >> 16) & 0x7Fu);
+        const int k = ef - 134;
+        r.s = __uint_as_float(__float_as_uint(t.T[f]) + (k << 23));
+        r.inv = __uint_as_float(__float_as_uint(t.R[f]) - (k << 23));
+        r.exact = false;
+    } else {
+        r.s = __fdiv_rn(amax, kQMax);
+        r.inv = (r.s > 0.0f) ? __frcp_rn(r.s) : 0.0f;
+        r.exact = r.s > 0.0f && r.s < kMinNormal;
+    }
     return r;
 }
 
@@ -53,22 +99,6 @@ __device__ __noinline__ int quant_exact(float x, float s) {
     float r = rintf(__fdiv_rn(x, s));
     r = fminf(fmaxf(r, -kQMax), kQMax);
     return static_cast<int>(r);
-}
-
-// Quantize one value; returns the int8 code in the low byte.
-__device__ __forceinline__ uint32_t quant_one(float x, const RowScale& sc) {
-    const float t = __fmul_rn(x, sc.inv);
-    const float big = __fadd_rn(t, kRoundMagic);
-    const float r = __fsub_rn(big, kRoundMagic);
-    const float dist = fabsf(__fsub_rn(t, r));  // exact: |t - rne(t)| <= 0.5
-    // Near-ties take the exact path; so does a NaN distance, which arises only
-    // when 1/s overflowed (s below 2^-128) and must not be trusted.
-    if (!(dist <= 0.5f - kTieGuard)) return static_cast<uint32_t>(quant_exact(x, sc.s)) & 0xFFu;
-    // |t| <= 127.01, so r is within [-127, 127] except through rounding slop
-    // at the boundary; clamp on the biased value keeps the byte extraction valid.
-    const float lo = kRoundMagic - kQMax, hi = kRoundMagic + kQMax;
-    const float c = fminf(fmaxf(big, lo), hi);
-    return __float_as_uint(c) & 0xFFu;
 }
 
 // absmax of the 8 bf16 values in a 16-byte chunk, as a non-negative float.
@@ -86,18 +116,60 @@ __device__ __forceinline__ float chunk_absmax(const uint4& v) {
     return fmaxf(bf16_lo(xb), bf16_hi(xb));
 }
 
-__device__ __forceinline__ uint32_t quant_word(uint32_t w, const RowScale& sc) {
-    uint32_t q0 = quant_one(bf16_lo(w), sc);
-    uint32_t q1 = quant_one(bf16_hi(w), sc);
-    return q0 | (q1 << 8);
+// Exact-path code of one value, as a byte.
+__device__ __forceinline__ uint32_t quant_byte_exact(float x, float s) {
+    return static_cast<uint32_t>(quant_exact(x, s)) & 0xFFu;
 }
 
-// 8 bf16 -> 8 int8 packed into a uint2.
+// 8 bf16 -> 8 int8 packed into a uint2.  Two values per packed fp32
+// operation; a chunk holding a value within 2^-14 of a rounding boundary
+// re-derives those values on the exact path.
 __device__ __forceinline__ uint2 quant_chunk(const uint4& v, const RowScale& sc) {
-    uint2 o;
-    o.x = quant_word(v.x, sc) | (quant_word(v.y, sc) << 16);
-    o.y = quant_word(v.z, sc) | (quant_word(v.w, sc) << 16);
-    return o;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (sc.exact) {
+        uint32_t b[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            b[2 * i] = quant_byte_exact(bf16_lo(w[i]), sc.s);
+            b[2 * i + 1] = quant_byte_exact(bf16_hi(w[i]), sc.s);
+        }
+        return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                          b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+    }
+    const uint64_t inv2 = f2_pack(sc.inv, sc.inv);
+    const uint64_t magic2 = f2_pack(kRoundMagic, kRoundMagic);
+    uint32_t big[8];
+    float dmax = 0.0f;
+    float dist[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint64_t x2 = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+        const uint64_t bg = f2_fma(x2, inv2, magic2);     // rne(P) + 1.5*2^23
+        const uint64_t nr = f2_sub(magic2, bg);           // -rne(P), exact
+        const uint64_t d = f2_fma(x2, inv2, nr);          // P - rne(P), rounded once
+        float b0, b1, d0, d1;
+        f2_unpack(bg, b0, b1);
+        f2_unpack(d, d0, d1);
+        big[2 * i] = __float_as_uint(b0);
+        big[2 * i + 1] = __float_as_uint(b1);
+        dist[2 * i] = d0;
+        dist[2 * i + 1] = d1;
+        dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
+    }
+    if (!(dmax <= 0.5f - kTieGuard)) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (!(fabsf(dist[2 * i]) <= 0.5f - kTieGuard)) big[2 * i] = quant_byte_exact(bf16_lo(w[i]), sc.s);
+            if (!(fabsf(dist[2 * i + 1]) <= 0.5f - kTieGuard))
+                big[2 * i + 1] = quant_byte_exact(bf16_hi(w[i]), sc.s);
+        }
+    }
+    // low byte of each value, four to a word
+    const uint32_t lo01 = __byte_perm(big[0], big[1], 0x0040);
+    const uint32_t lo23 = __byte_perm(big[2], big[3], 0x0040);
+    const uint32_t lo45 = __byte_perm(big[4], big[5], 0x0040);
+    const uint32_t lo67 = __byte_perm(big[6], big[7], 0x0040);
+    return make_uint2(__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo45, lo67, 0x5410));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -124,6 +196,8 @@ template <int CPT>
 __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
                                                              uint2* __restrict__ Aq, float* __restrict__ s) {
     __shared__ float red[32];
+    __shared__ ScaleTables tab;
+    build_scale_tables(tab);
     const int64_t row = blockIdx.x;
     if (row >= R) return;
     const int64_t chunks = K >> 3;
@@ -139,7 +213,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
         }
     }
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax);
+    const RowScale sc = make_scale(amax, tab);
     if (threadIdx.x == 0) s[row] = sc.s;
     uint2* q = Aq + row * chunks;
 #pragma unroll
@@ -149,10 +223,59 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
     }
 }
 
+// One warp per row, two passes: the absmax pass streams the row with U
+// 16-byte loads per lane in flight, the quantize pass reads it again (from
+// L2, where the first pass left it) and writes the codes.  Few registers, so
+// many rows are in flight per SM.
+template <int U>
+__global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
+                                                               uint2* __restrict__ Aq, float* __restrict__ s) {
+    __shared__ ScaleTables tab;
+    build_scale_tables(tab);
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= R) return;
+    const int chunks = static_cast<int>(K >> 3);
+    const uint4* a = A + row * chunks;
+    float amax = 0.0f;
+    for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + lane + 32 * u;
+            if (c < chunks) v[u] = a[c];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + lane + 32 * u;
+            if (c < chunks) amax = fmaxf(amax, chunk_absmax(v[u]));
+        }
+    }
+    amax = warp_max(amax);
+    const RowScale sc = make_scale(amax, tab);
+    if (lane == 0) s[row] = sc.s;
+    uint2* q = Aq + row * chunks;
+    for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + lane + 32 * u;
+            if (c < chunks) v[u] = __ldcs(a + c);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + lane + 32 * u;
+            if (c < chunks) __stcs(q + c, quant_chunk(v[u], sc));
+        }
+    }
+}
+
 // Rows too long to keep in registers: absmax pass, then a second read.
 __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
                                                                uint2* __restrict__ Aq, float* __restrict__ s) {
     __shared__ float red[32];
+    __shared__ ScaleTables tab;
+    build_scale_tables(tab);
     const int64_t row = blockIdx.x;
     if (row >= R) return;
     const int64_t chunks = K >> 3;
@@ -160,38 +283,51 @@ __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __re
     float amax = 0.0f;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) amax = fmaxf(amax, chunk_absmax(a[c]));
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax);
+    const RowScale sc = make_scale(amax, tab);
     if (threadIdx.x == 0) s[row] = sc.s;
     uint2* q = Aq + row * chunks;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) __stcs(q + c, quant_chunk(__ldcs(a + c), sc));
 }
 
-// 1x128 activation blocks: 16 lanes own one block (8 bf16 each).  Each warp
-// handles two blocks per step and UNROLL steps per iteration of a grid-stride
-// loop, with all loads of an iteration issued before any arithmetic.
+// 1x128 activation blocks: 4 lanes own one block (4 chunks of 8 bf16 each),
+// so a warp handles 8 blocks per step.  For chunk i of its block, lane l reads
+// 16 bytes at offset 16 * ((l & 3) + 4 i) of block (l >> 2): each load
+// instruction of the warp covers 8 runs of 64 contiguous bytes.  A grid-stride
+// loop with UNROLL steps per iteration keeps 64 * UNROLL bytes per lane in
+// flight.
 template <int UNROLL>
 __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __restrict__ X, int64_t n_blocks,
                                                               uint2* __restrict__ Xq, float* __restrict__ sx) {
+    __shared__ ScaleTables tab;
+    build_scale_tables(tab);
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, sub = lane & 15;
+    const int sub = lane & 3, bl = lane >> 2;
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t warps_total = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t base = warp_global * 2 * UNROLL; base < n_blocks; base += warps_total * 2 * UNROLL) {
-        uint4 v[UNROLL];
+    for (int64_t base = warp_global * 8 * UNROLL; base < n_blocks; base += warps_total * 8 * UNROLL) {
+        uint4 v[UNROLL][4];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
-            if (blk < n_blocks) v[u] = __ldcs(X + blk * 16 + sub);
+            const int64_t blk = base + 8 * u + bl;
+            if (blk < n_blocks) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[u][i] = __ldcs(X + blk * 16 + sub + 4 * i);
+            }
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
-            float m = (blk < n_blocks) ? chunk_absmax(v[u]) : 0.0f;
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            const RowScale sc = make_scale(m);
+            const int64_t blk = base + 8 * u + bl;
+            float m = 0.0f;
             if (blk < n_blocks) {
-                __stcs(Xq + blk * 16 + sub, quant_chunk(v[u], sc));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m = fmaxf(m, chunk_absmax(v[u][i]));
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const RowScale sc = make_scale(m, tab);
+            if (blk < n_blocks) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) __stcs(Xq + blk * 16 + sub + 4 * i, quant_chunk(v[u][i], sc));
                 if (sub == 0) sx[blk] = sc.s;
             }
         }
@@ -202,6 +338,8 @@ __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __res
 __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __restrict__ W, int64_t N, int64_t K,
                                                                  uint2* __restrict__ Wq, float* __restrict__ sw) {
     __shared__ float red[32];
+    __shared__ ScaleTables tab;
+    build_scale_tables(tab);
     const int64_t kb = blockIdx.x, nb = blockIdx.y;
     const int64_t kbs = K >> 7;
     const int64_t chunks_per_row = K >> 3;
@@ -218,7 +356,7 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __
         }
     }
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax);
+    const RowScale sc = make_scale(amax, tab);
     if (threadIdx.x == 0) sw[nb * kbs + kb] = sc.s;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -261,13 +399,22 @@ __global__ void __launch_bounds__(256) expand_s8_bf16_kernel(const uint4* __rest
 
 }  // namespace
 
-cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, cudaStream_t st) {
+cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, int num_sms,
+                              cudaStream_t st) {
+    (void)num_sms;
     const int64_t chunks = K >> 3;
     const uint4* a = static_cast<const uint4*>(A);
     uint2* q = reinterpret_cast<uint2*>(Aq);
     const dim3 grid(static_cast<unsigned>(R));
-    if (chunks <= 256)
-        quant_rows_reg_kernel<1><<<grid, chunks <= 128 ? 128 : 256, 0, st>>>(a, R, K, q, s);
+    if (chunks > 512) {
+        // long rows: one warp per row, two passes, many rows in flight per SM
+        quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, s);
+        return cudaGetLastError();
+    }
+    if (chunks <= 128)
+        quant_rows_reg_kernel<1><<<grid, 128, 0, st>>>(a, R, K, q, s);
+    else if (chunks <= 256)
+        quant_rows_reg_kernel<1><<<grid, 256, 0, st>>>(a, R, K, q, s);
     else if (chunks <= 512)
         quant_rows_reg_kernel<2><<<grid, 256, 0, st>>>(a, R, K, q, s);
     else if (chunks <= 1024)
@@ -282,8 +429,8 @@ cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, f
 cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, float* sx, int num_sms,
                                    cudaStream_t st) {
     const int64_t n_blocks = M * (K >> 7);
-    constexpr int kUnroll = 4;
-    const int64_t warps_needed = (n_blocks + 2 * kUnroll - 1) / (2 * kUnroll);
+    constexpr int kUnroll = 2;
+    const int64_t warps_needed = (n_blocks + 8 * kUnroll - 1) / (8 * kUnroll);
     int64_t grid = (warps_needed + 7) / 8;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (grid > cap) grid = cap;
@@ -310,6 +457,15 @@ cudaError_t launch_expand_s8_bf16(const int8_t* src, int64_t n, void* dst, int n
     expand_s8_bf16_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(reinterpret_cast<const uint4*>(src), n16,
                                                                        static_cast<uint4*>(dst));
     return cudaGetLastError();
+}
+
+cudaError_t quant_read_device_error(unsigned int* code) {
+    unsigned int v = 0, z = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_device_error, &z, sizeof z);
+    *code = v;
+    return e;
 }
 
 }  // namespace w8a8
