@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(leader_acc_empty0 + static_cast<uint32_t>(buf) * 8u);
+                if (lane == 0) mbar_arrive_cluster_relaxed(leader_acc_empty0 + static_cast<uint32_t>(buf) * 8u);
                 buf ^= 1;
                 if (buf == 0) buf_phase ^= 1u;
             }
