@@ -97,6 +97,8 @@ def test_quantize_weight_modes(w8a8, oracle, N, K):
     (257, 600, 2048, False),   # two folds of 1024 K
     (129, 264, 4112, True),    # five folds, last one 16 K
     (77, 3072, 5120, False),
+    (2048, 4096, 1024, True),  # selects 224-column tiles (2 full waves of CTA pairs)
+    (2432, 1792, 768, False),  # selects 256-column tiles
 ])
 def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=1 + M, outliers=0.01, oscale=20.0)

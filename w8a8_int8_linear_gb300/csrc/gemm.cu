@@ -21,17 +21,21 @@
 // mode folds at every 128-wide K block, where the fp32 value read out is the
 // block's exact integer partial P, and applies acc = acc + (P * sx) * sw.
 //
-// Kernel layout (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: bf16 A and B tiles, 128-byte swizzle, into a
-//               4-stage shared-memory ring;
-//   warp 1      tensor-memory allocator and MMA issuer (one elected lane):
-//               tcgen05.mma 128x256x16 into one of two 256-column fp32
-//               accumulators (512 TMEM columns), committing each smem stage
-//               back to the producer and each finished chunk to the
-//               epilogue;
-//   warps 2..9  epilogue: each warp reads its 32 TMEM lanes (rows) x 128
-//               columns, folds chunks into registers, and writes the output
-//               tile with the scales and bias applied.
+// Kernel layout: clusters of two CTAs (one per SM), persistent over output
+// tiles of 256 rows x BN columns (BN = 256, 224 or 192, chosen per shape).
+// The pair shares each tile: CTA r loads rows [128r, 128r+128) of the A tile
+// and rows [r*BN/2, (r+1)*BN/2) of the B tile into its own shared memory.
+//   warp 0       TMA producer (both CTAs): bf16 A and B stages, 128-byte
+//                swizzle, 6-deep ring; completion is counted on the leader's
+//                barrier;
+//   warp 1       TMEM allocator (both CTAs) and, in the leader only, the MMA
+//                issuer: tcgen05.mma.cta_group::2 (M = 256, N = BN) into one
+//                of two BN-column fp32 accumulators in each CTA's TMEM,
+//                commits multicast to both CTAs;
+//   warps 4..11  epilogue (both CTAs): each warp reads its 32 TMEM lanes
+//                (rows) x BN/2 columns, folds chunks into registers, writes
+//                the output with scales and bias, and releases the buffer
+//                with a remote arrive on the leader's barrier.
 // Two accumulator buffers let the MMA of chunk c+1 run while chunk c is
 // folded.
 #include <cuda.h>
@@ -48,11 +52,11 @@
 namespace w8a8 {
 namespace {
 
-constexpr int BM = 128;      // rows of A per CTA; a CTA pair covers TILE_M rows
+constexpr int BM = 128;  // rows of A per CTA; a CTA pair covers TILE_M rows
 constexpr int TILE_M = 2 * BM;
-constexpr int BN = 256;      // output columns per tile; each CTA of the pair loads BN/2 rows of B
-constexpr int BK = 64;       // bf16 elements per stage row = 128 bytes = one swizzle row
-constexpr int STAGES = 6;
+constexpr int BK = 64;   // bf16 elements per stage row = 128 bytes = one swizzle row
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t RING_BUDGET = 192 * 1024;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;  // warps 0-3: producer, MMA issuer, two idle; warps 4-11: epilogue
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
@@ -62,15 +66,25 @@ constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int REGS_LOW = 56;
 constexpr int REGS_HIGH = 224;
 static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= THREADS * 168, "register split exceeds the launch budget");
-constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COLS = BN;
-constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
 constexpr int POSTSCALE_CHUNK_STAGES = 16;  // 1024 K: 127*127*1024 < 2^24
 constexpr int BLOCK_CHUNK_STAGES = 2;       // one 128-wide scale block
 constexpr int GROUP_M = 8;                  // tile raster: bands of 8 row tiles (2048 rows)
-constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
+
+// Per-tile-width constants.
+template <int BN_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr int HALF = BN / 2;  // B rows per CTA = output columns per epilogue warp
+    static_assert(HALF % 16 == 0 && BN <= 256, "tile width");
+    static constexpr uint32_t B_BYTES = HALF * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : int(RING_BUDGET / STAGE_BYTES);
+    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
+    static constexpr int LDW = (HALF % 32 == 0) ? 32 : 16;  // TMEM load width (columns)
+    static constexpr int GROUPS = HALF / LDW;
+};
 
 enum WaitSite : int {
     kSiteProducerEmpty = 1,
@@ -123,9 +137,22 @@ struct AccType<kEpiBlockwiseF32> {
     using T = float;
 };
 
-// Write the 128 accumulated columns [col0, col0+128) of one row.
-template <int EPI>
-__device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[128], const KParams& p, int row,
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]);
+template <>
+__device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, uint32_t (&r)[16]) {
+    tmem_ld_32x32b_x16(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, uint32_t (&r)[32]) {
+    tmem_ld_32x32b_x32(taddr, r);
+}
+__device__ __forceinline__ void tmem_wait_cols(uint32_t (&r)[16]) { tmem_wait_ld_regs(r); }
+__device__ __forceinline__ void tmem_wait_cols(uint32_t (&r)[32]) { tmem_wait_ld_regs32(r); }
+
+// Write the COLS accumulated columns [col0, col0+COLS) of one row.
+template <int EPI, int COLS>
+__device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[COLS], const KParams& p, int row,
                                           int col0) {
     if (row >= p.M) return;
     const int N = p.N;
@@ -134,7 +161,7 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
     float sxr = 0.0f;
     if constexpr (EPI == kEpiPostscaleBf16) sxr = p.sx[row];
 #pragma unroll
-    for (int j = 0; j < 128; j += 8) {
+    for (int j = 0; j < COLS; j += 8) {
         const int col = col0 + j;
         if (col < N) {
             const bool full = vec && (col + 8 <= N);
@@ -218,14 +245,17 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
     }
 }
 
-template <int EPI>
+template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+    using C = Cfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int HALF = C::HALF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -278,16 +308,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int mb, nb;
                 tile_coords(tile, p.num_m, p.num_n, mb, nb);
                 const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
-                const int b_row = nb * BN + static_cast<int>(rank) * (BN / 2);
+                const int b_row = nb * BN + static_cast<int>(rank) * HALF;
                 for (int ks = 0; ks < p.k_stages; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
                     const uint32_t bar = map_to_rank(smem_u32(&full[stage]), 0);
                     tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, ks * BK, a_row);
-                    tma_load_2d_pair(sB + stage * B_BYTES, &tmB, bar, ks * BK, b_row);
+                    tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar, ks * BK, b_row);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -316,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * ACC_COLS;
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                     const int s0 = c * p.chunk_stages;
                     const int s1 = min(p.k_stages, s0 + p.chunk_stages);
                     for (int ks = s0; ks < s1; ++ks) {
@@ -326,12 +356,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+                        const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
                             const uint64_t da = smem_desc_kmajor_sw128(a_addr + k * 32);
                             const uint64_t db = smem_desc_kmajor_sw128(b_addr + k * 32);
-                            mma_bf16_ss_pair(d_tmem, da, db, IDESC, (ks > s0 || k > 0) ? 1u : 0u);
+                            mma_bf16_ss_pair(d_tmem, da, db, C::IDESC, (ks > s0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit_pair_multicast(&empty[stage], 0x3);
                         if (++stage == STAGES) {
@@ -354,9 +384,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         regs_inc<REGS_HIGH>();
         // ------------------------------------------------------------ epilogue (both CTAs)
         constexpr bool kBlock = (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32);
+        static_assert(!kBlock || HALF == 128, "blockwise needs each warp's columns inside one 128-wide block");
         using T = typename AccType<EPI>::T;
-        const int quarter = warp & 3;      // TMEM lanes this warp may access
-        const int half = (warp - EPI_WARP0) >> 2;  // which 128-column half of the tile
+        constexpr int LDW = C::LDW;
+        constexpr int GROUPS = C::GROUPS;
+        const int quarter = warp & 3;                  // TMEM lanes this warp may access
+        const int half = (warp - EPI_WARP0) >> 2;      // which column half of the tile
         const uint32_t leader_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
         int buf = 0;
         uint32_t buf_phase = 0;
@@ -365,11 +398,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             int mb, nb;
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
             const int row = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
-            const int col0 = nb * BN + half * 128;
-            // post-scale: 128 int32 running sums; blockwise: 128 fp32 accumulators
-            T acc[128];
+            const int col0 = nb * BN + half * HALF;
+            // post-scale: int32 running sums; blockwise: fp32 accumulators
+            T acc[HALF];
 #pragma unroll
-            for (int e = 0; e < 128; ++e) acc[e] = T(0);
+            for (int e = 0; e < HALF; ++e) acc[e] = T(0);
             for (int c = 0; c < nchunks; ++c) {
                 float sxv = 0.0f, swv = 0.0f;
                 if constexpr (kBlock) {
@@ -382,28 +415,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(buf) * ACC_COLS + static_cast<uint32_t>(half * 128);
-                // 4 groups of 32 columns; the load of group j+1 is in flight
-                // while group j is folded.
-                uint32_t ra[32], rb[32];
-                tmem_ld_32x32b_x32(taddr, ra);
-                tmem_wait_ld_regs32(ra);
+                                       static_cast<uint32_t>(buf * BN + half * HALF);
+                // GROUPS groups of LDW columns; the load of group j+1 is in
+                // flight while group j is folded.
+                uint32_t ra[LDW], rb[LDW];
+                tmem_ld_cols<LDW>(taddr, ra);
+                tmem_wait_cols(ra);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t(&cur)[32] = (j & 1) ? rb : ra;
-                    uint32_t(&nxt)[32] = (j & 1) ? ra : rb;
-                    if (j + 1 < 4) tmem_ld_32x32b_x32(taddr + (j + 1) * 32, nxt);
+                for (int j = 0; j < GROUPS; ++j) {
+                    uint32_t(&cur)[LDW] = (j & 1) ? rb : ra;
+                    uint32_t(&nxt)[LDW] = (j & 1) ? ra : rb;
+                    if (j + 1 < GROUPS) tmem_ld_cols<LDW>(taddr + (j + 1) * LDW, nxt);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < LDW; ++e) {
                         const float v = __uint_as_float(cur[e]);
                         if constexpr (kBlock) {
                             // t = (P * sx) * sw; acc = acc + t, each rounded on its own
-                            acc[j * 32 + e] = __fadd_rn(acc[j * 32 + e], __fmul_rn(__fmul_rn(v, sxv), swv));
+                            acc[j * LDW + e] = __fadd_rn(acc[j * LDW + e], __fmul_rn(__fmul_rn(v, sxv), swv));
                         } else {
-                            acc[j * 32 + e] += __float2int_rz(v);
+                            acc[j * LDW + e] += __float2int_rz(v);
                         }
                     }
-                    if (j + 1 < 4) tmem_wait_ld_regs32(nxt);
+                    if (j + 1 < GROUPS) tmem_wait_cols(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -412,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (buf == 0) buf_phase ^= 1u;
             }
             if (!ok) break;
-            store_row<EPI>(acc, p, row, col0);
+            store_row<EPI, HALF>(acc, p, row, col0);
         }
     }
 
@@ -436,15 +469,39 @@ CUresult make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, co
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Per device: whether each kernel instance has its shared-memory attribute set,
+// and how many CTA pairs of the GEMM kernel fit at once.
 struct DeviceLaunchInfo {
-    bool configured[4];
+    bool configured[8];
     int max_clusters;
 };
 DeviceLaunchInfo g_launch_info[64];
 
-template <int EPI>
-cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const KParams& p, int num_sms,
-                       cudaStream_t st, char* detail, size_t n) {
+template <int EPI, int BN>
+constexpr int instance_id() {
+    return (EPI == kEpiPostscaleBf16 ? 0 : EPI == kEpiPostscaleS32 ? 3 : EPI == kEpiBlockwiseBf16 ? 6 : 7) +
+           (BN == 256 ? 0 : BN == 224 ? 1 : 2);
+}
+
+template <int EPI, int BN>
+cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
+                       int num_sms, cudaStream_t st, char* detail, size_t n) {
+    using C = Cfg<BN>;
+    CUtensorMap tmA, tmB;
+    CUresult r = make_map(encode, &tmA, Ab, p.K, p.M, BK, BM);
+    if (r != CUDA_SUCCESS) {
+        snprintf(detail, n, "cuTensorMapEncodeTiled(A: %d x %d) returned %d", p.M, p.K, (int)r);
+        return cudaErrorInvalidValue;
+    }
+    r = make_map(encode, &tmB, Bb, p.K, p.N, BK, C::HALF);
+    if (r != CUDA_SUCCESS) {
+        snprintf(detail, n, "cuTensorMapEncodeTiled(B: %d x %d) returned %d", p.N, p.K, (int)r);
+        return cudaErrorInvalidValue;
+    }
+    p.num_m = (p.M + TILE_M - 1) / TILE_M;
+    p.num_n = (p.N + BN - 1) / BN;
+    p.num_tiles = p.num_m * p.num_n;
+
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -457,18 +514,19 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const KPa
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!info.configured[EPI]) {
-        e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(SMEM_BYTES));
+    constexpr int id = instance_id<EPI, BN>();
+    if (!info.configured[id]) {
+        e = cudaFuncSetAttribute(gemm_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(C::SMEM));
         if (e != cudaSuccess) return e;
         if (info.max_clusters == 0) {
             cfg.gridDim = dim3(2 * (num_sms / 2));
             int nc = 0;
-            e = cudaOccupancyMaxActiveClusters(&nc, gemm_kernel<EPI>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&nc, gemm_kernel<EPI, BN>, &cfg);
             if (e != cudaSuccess) return e;
             if (nc < 1) {
                 snprintf(detail, n, "no CTA pair of the GEMM kernel fits on this device");
@@ -476,11 +534,41 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const KPa
             }
             info.max_clusters = nc;
         }
-        info.configured[EPI] = true;
+        info.configured[id] = true;
     }
     const int clusters = p.num_tiles < info.max_clusters ? p.num_tiles : info.max_clusters;
     cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, tmA, tmB, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, BN>, tmA, tmB, p);
+}
+
+// Tile width for the post-scale GEMM: the candidate minimizing
+// waves x (BN + 16), i.e. whole waves of CTA pairs times the per-tile MMA
+// time plus a fixed per-tile cost.
+int choose_bn(int64_t M, int64_t N, int clusters) {
+    const int cand[3] = {256, 224, 192};
+    const int64_t mt = (M + TILE_M - 1) / TILE_M;
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int bn : cand) {
+        const int64_t tiles = mt * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + clusters - 1) / clusters;
+        const int64_t cost = waves * (bn + 16);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+template <int EPI>
+cudaError_t launch_bn(int bn, const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                      const KParams& p, int num_sms, cudaStream_t st, char* detail, size_t n) {
+    switch (bn) {
+        case 224: return launch_one<EPI, 224>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        case 192: return launch_one<EPI, 192>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        default: return launch_one<EPI, 256>(Ab, Bb, encode, p, num_sms, st, detail, n);
+    }
 }
 
 }  // namespace
@@ -489,19 +577,6 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
                         void* encode_fn, cudaStream_t st, char* detail, size_t n) {
     if (n) detail[0] = 0;
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encode_fn);
-    CUtensorMap tmA, tmB;
-    CUresult r = make_map(encode, &tmA, Ab, a.K, a.M, BK, BM);
-    if (r != CUDA_SUCCESS) {
-        snprintf(detail, n, "cuTensorMapEncodeTiled(A: %lld x %lld) returned %d", (long long)a.M, (long long)a.K,
-                 (int)r);
-        return cudaErrorInvalidValue;
-    }
-    r = make_map(encode, &tmB, Bb, a.K, a.N, BK, BN / 2);
-    if (r != CUDA_SUCCESS) {
-        snprintf(detail, n, "cuTensorMapEncodeTiled(B: %lld x %lld) returned %d", (long long)a.N, (long long)a.K,
-                 (int)r);
-        return cudaErrorInvalidValue;
-    }
     KParams p;
     p.sx = a.sx;
     p.sw = a.sw;
@@ -510,23 +585,23 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
-    p.num_m = static_cast<int>((a.M + TILE_M - 1) / TILE_M);
-    p.num_n = static_cast<int>((a.N + BN - 1) / BN);
-    p.num_tiles = p.num_m * p.num_n;
     p.k_stages = static_cast<int>((a.K + BK - 1) / BK);
     const bool blockwise = epilogue == kEpiBlockwiseBf16 || epilogue == kEpiBlockwiseF32;
     p.chunk_stages = blockwise ? BLOCK_CHUNK_STAGES : POSTSCALE_CHUNK_STAGES;
     p.kb_count = static_cast<int>(a.K / 128);
+    const int bn = blockwise ? 256 : choose_bn(a.M, a.N, num_sms / 2);
     cudaError_t e;
     switch (epilogue) {
-        case kEpiPostscaleBf16: e = launch_one<kEpiPostscaleBf16>(tmA, tmB, p, num_sms, st, detail, n); break;
-        case kEpiPostscaleS32: e = launch_one<kEpiPostscaleS32>(tmA, tmB, p, num_sms, st, detail, n); break;
-        case kEpiBlockwiseBf16: e = launch_one<kEpiBlockwiseBf16>(tmA, tmB, p, num_sms, st, detail, n); break;
-        case kEpiBlockwiseF32: e = launch_one<kEpiBlockwiseF32>(tmA, tmB, p, num_sms, st, detail, n); break;
+        case kEpiPostscaleBf16: e = launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n); break;
+        case kEpiPostscaleS32: e = launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n); break;
+        case kEpiBlockwiseBf16:
+            e = launch_one<kEpiBlockwiseBf16, 256>(Ab, Bb, encode, p, num_sms, st, detail, n);
+            break;
+        case kEpiBlockwiseF32: e = launch_one<kEpiBlockwiseF32, 256>(Ab, Bb, encode, p, num_sms, st, detail, n); break;
         default: e = cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess && detail[0] == 0)
-        snprintf(detail, n, "GEMM launch (%d threads, %zu bytes smem, clusters of 2): %s", THREADS, SMEM_BYTES,
+    if (e != cudaSuccess && n && detail[0] == 0)
+        snprintf(detail, n, "GEMM launch (%d threads, clusters of 2, tile width %d): %s", THREADS, bn,
                  cudaGetErrorString(e));
     return e;
 }
