@@ -146,6 +146,45 @@ W8A8_API w8a8_status w8a8_gemm_blockwise(const int8_t* Xq, const float* sx, cons
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * Exact bf16 image of INT8 weight codes: Wimg[n,k] = (bf16) Wq[n,k], every
+ * value in [-127, 127] exact.  The tensor-core GEMM consumes this image (GB300
+ * has no 8-bit integer tcgen05 MMA), so packing it once, next to the weight
+ * quantization at model initialization ("Reused Components", W8A8 Linear),
+ * takes the per-call expansion out of the fused Linear below.  It occupies the
+ * same 2 bytes per weight as the bf16 weight copy the pages keep.
+ *   Wq [N,K] int8 in, Wimg [N,K] bf16 out.  K % 16 == 0.
+ */
+W8A8_API w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, void* Wimg, void* stream);
+
+/* Device workspace bytes of the fused Linear entry points (the bf16 image of
+ * the quantized activations, M * K * 2 bytes rounded up to 256). */
+W8A8_API size_t w8a8_linear_workspace_size(int64_t M, int64_t K);
+
+/*
+ * Fused W8A8 Linear, post-scale: dynamic per-token quantization of X ("Reused
+ * Components": activations quantized before each Linear) followed by the
+ * post-scale GEMM ("Differences From TurboDiffusion"), against a packed
+ * weight image.  Results are identical to w8a8_quantize_act (PER_ROW) +
+ * w8a8_gemm_postscale on the same inputs.
+ *   X [M,K] bf16, Wimg [N,K] bf16 image from w8a8_pack_weight, sw [N] fp32,
+ *   bias [N] bf16 or NULL, Y [M,N] bf16 out, sx [M] fp32 out (the per-token
+ *   scales), Xq [M,K] int8 out or NULL (codes are written only if given),
+ *   workspace of w8a8_linear_workspace_size(M,K) bytes, 256-byte aligned.
+ */
+W8A8_API w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, const float* sw, const void* bias,
+                                           void* Y, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Fused W8A8 Linear, blockwise: 1x128 activation quantization followed by the
+ * blockwise GEMM, against a packed weight image.  K % 128 == 0.  sx is
+ * [M][K/128] out, sw is [ceil(N/128)][K/128]; other arguments as above.
+ */
+W8A8_API w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, const float* sw, const void* bias,
+                                           void* Y, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free variant of w8a8_gemm_postscale (the pages have no
  * counterpart: this is a library convenience).  Same arguments, results and
  * checks, minus the workspace: the scratch lives in a fixed 64 MiB device

@@ -32,9 +32,13 @@ def run_case(w8a8, oracle, work, rows_max=96, cols_max=96):
     Xq, sx = w8a8.quantize_act(X, mode)
     if mode == w8a8.PER_ROW:
         Y = w8a8.gemm_postscale(Xq, sx, Wq, sw, b)
+        Yf, sxf, _ = w8a8.linear_postscale(X, w8a8.pack_weight(Wq), sw, b)
     else:
         Y = w8a8.gemm_blockwise(Xq, sx, Wq, sw, b)
+        Yf, sxf, _ = w8a8.linear_blockwise(X, w8a8.pack_weight(Wq), sw, b)
     torch.cuda.synchronize()
+    # the fused Linear (the benchmark's step) gives the same bytes everywhere
+    assert torch.equal(Yf, Y) and torch.equal(sxf, sx)
     assert w8a8.get_device_error() == (0, 0)
     rows = sample(work.M, 128, rng, rows_max)
     cols = sample(work.N, 256, rng, cols_max)

@@ -214,3 +214,59 @@ def test_blockwise_adversary(w8a8, oracle):
     ref = oracle.gemm_blockwise_f32(Xq.numpy(), sx.numpy(), Wq.numpy(), sw.numpy())
     acc = w8a8.gemm_blockwise_f32(Xq.to(DEV), sx.to(DEV), Wq.to(DEV), sw.to(DEV)).cpu().numpy()
     assert np.array_equal(acc.view(np.uint32), ref.view(np.uint32))
+
+
+# ----------------------------------------------------------------- fused Linear entry points
+def test_pack_weight_is_exact_image(w8a8):
+    g = torch.Generator().manual_seed(31)
+    Wq = torch.randint(-127, 128, (300, 1040), generator=g, dtype=torch.int8)
+    Wimg = w8a8.pack_weight(Wq.to(DEV))
+    assert torch.equal(Wimg.cpu().float(), Wq.float())
+    assert np.array_equal(bits(Wimg), bits(Wq.to(torch.bfloat16)))
+
+
+@pytest.mark.parametrize("M,N,K,bias", [(64, 128, 256, True), (300, 520, 1040, True), (2048, 4096, 1024, False),
+                                        (77, 3072, 5120, True)])
+def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
+    X = rand_bf16((M, K), seed=40 + M, outliers=0.01, oscale=20.0)
+    W = rand_bf16((N, K), seed=41 + N, scale=0.02)
+    b = rand_bf16((N,), seed=42, scale=0.01) if bias else None
+    ref = oracle.linear_postscale(bits(X), bits(W), None if b is None else bits(b))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV))
+    Wimg = w8a8.pack_weight(Wq)
+    Y, sx, Xq = w8a8.linear_postscale(X.to(DEV), Wimg, sw, None if b is None else b.to(DEV), codes=True)
+    assert np.array_equal(Xq.cpu().numpy(), ref["Xq"])
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), ref["sx"].view(np.uint32))
+    d = assert_bf16_close(bits(Y), ref["Y"], 1)
+    assert d.max() == 0
+    # without codes requested: same output
+    Y2, _, none = w8a8.linear_postscale(X.to(DEV), Wimg, sw, None if b is None else b.to(DEV))
+    assert none is None and torch.equal(Y2, Y)
+    assert w8a8.get_device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("M,N,K,bias", [(64, 256, 256, False), (300, 456, 1408, True), (1, 130, 13824, False)])
+def test_linear_blockwise_fused(w8a8, oracle, M, N, K, bias):
+    X = torch.nn.functional.gelu(rand_bf16((M, K), seed=50 + M).float()).to(torch.bfloat16)
+    W = rand_bf16((N, K), seed=51 + N, scale=0.01)
+    b = rand_bf16((N,), seed=52, scale=0.01) if bias else None
+    ref = oracle.linear_blockwise(bits(X), bits(W), None if b is None else bits(b))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV), w8a8.BLOCK)
+    Y, sx, Xq = w8a8.linear_blockwise(X.to(DEV), w8a8.pack_weight(Wq), sw, None if b is None else b.to(DEV),
+                                      codes=True)
+    assert np.array_equal(Xq.cpu().numpy(), ref["Xq"])
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), ref["sx"].view(np.uint32))
+    d = assert_bf16_close(bits(Y), ref["Y"], 1)
+    assert d.max() == 0
+
+
+def test_linear_fused_rejects_bad_arguments(w8a8):
+    X = torch.zeros((4, 64), dtype=torch.bfloat16, device=DEV)
+    Wimg = torch.zeros((8, 64), dtype=torch.bfloat16, device=DEV)
+    sw = torch.ones(8, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="WORKSPACE"):
+        w8a8.linear_postscale(X, Wimg, sw, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):
+        w8a8.linear_blockwise(X, Wimg, torch.ones((1, 1), device=DEV))
+    Y, sx, _ = w8a8.linear_postscale(torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV), Wimg, sw)
+    assert Y.shape == (0, 8)

@@ -41,6 +41,10 @@ SIGNATURES = [
     ("w8a8_gemm_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w8a8_gemm_postscale", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_pack_weight", _I32, [_P, _I64, _I64, _P, _P]),
+    ("w8a8_linear_workspace_size", _SZ, [_I64, _I64]),
+    ("w8a8_linear_postscale", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    ("w8a8_linear_blockwise", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_gemm_postscale_noalloc", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -244,16 +248,54 @@ def gemm_blockwise_f32(Xq, sx, Wq, sw, workspace=None):
     return acc
 
 
-def linear_postscale(X, Wq, sw, bias=None, out=None, workspace=None):
-    """Dynamic per-token activation quantization followed by the post-scale GEMM."""
-    Xq, sx = quantize_act(X, PER_ROW)
-    return gemm_postscale(Xq, sx, Wq, sw, bias, out=out, workspace=workspace)
+def pack_weight(Wq):
+    """Exact bf16 image [N,K] of INT8 weight codes, made once at init; the
+    fused Linear entry points take it in place of Wq."""
+    _need(Wq, torch.int8, "Wq", 2)
+    N, K = Wq.shape
+    Wimg = torch.empty((N, K), dtype=torch.bfloat16, device=Wq.device)
+    _check("w8a8_pack_weight", lib().w8a8_pack_weight(_ptr(Wq), N, K, _ptr(Wimg), _stream()))
+    return Wimg
 
 
-def linear_blockwise(X, Wq, sw, bias=None, out=None, workspace=None):
-    """Dynamic 1x128 activation quantization followed by the blockwise GEMM."""
-    Xq, sx = quantize_act(X, BLOCK)
-    return gemm_blockwise(Xq, sx, Wq, sw, bias, out=out, workspace=workspace)
+def linear_workspace_size(M, K):
+    return int(lib().w8a8_linear_workspace_size(M, K))
+
+
+def _linear(fn, mode, X, Wimg, sw, bias, out, workspace, sx_out, codes):
+    _need(X, torch.bfloat16, "X", 2)
+    _need(Wimg, torch.bfloat16, "Wimg", 2)
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = X.shape
+    N = Wimg.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if sx_out is None:
+        sx_out = torch.empty((M,) if mode == PER_ROW else (M, K // BLOCK_SIZE), dtype=torch.float32, device=X.device)
+    Xq = None
+    if codes is True:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    elif isinstance(codes, torch.Tensor):
+        Xq = codes
+    ws = workspace
+    if ws is None:
+        ws = torch.empty(max(linear_workspace_size(M, K), 256), dtype=torch.uint8, device=X.device)
+    _check(fn, getattr(lib(), fn)(_ptr(X), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K, _ptr(sx_out), _ptr(Xq),
+                                  _ptr(ws), ws.numel(), _stream()))
+    return Y, sx_out, Xq
+
+
+def linear_postscale(X, Wimg, sw, bias=None, out=None, workspace=None, sx_out=None, codes=False):
+    """Fused W8A8 Linear, post-scale: per-token quantization of X, then the
+    exact INT8 GEMM against the packed weight image, scales and bias in the
+    epilogue.  Returns (Y, sx, Xq or None); codes=True also returns Xq."""
+    return _linear("w8a8_linear_postscale", PER_ROW, X, Wimg, sw, bias, out, workspace, sx_out, codes)
+
+
+def linear_blockwise(X, Wimg, sw, bias=None, out=None, workspace=None, sx_out=None, codes=False):
+    """Fused W8A8 Linear, blockwise (1x128 activation, 128x128 weight scales)."""
+    return _linear("w8a8_linear_blockwise", BLOCK, X, Wimg, sw, bias, out, workspace, sx_out, codes)
 
 
 def get_device_error():

@@ -127,6 +127,55 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
     return current_device(dev);
 }
 
+// GEMM on bf16 operand images, with the timing hook around the launch.
+w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float* sx, const float* sw,
+                            const void* bias, void* out, int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
+                            cudaStream_t st) {
+    void* enc = encode_fn();
+    if (!enc) return W8A8_ERR_CUDA;
+    w8a8::GemmArgs a;
+    a.sx = sx;
+    a.sw = sw;
+    a.bias = bias;
+    a.out = out;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    cudaError_t e;
+    if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
+    e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W8A8_ERR_CUDA;
+    }
+    if (t_gemm_end && (e = cudaEventRecord(t_gemm_end, st)) != cudaSuccess) return cuda_fail("event", e);
+    return W8A8_OK;
+}
+
+// Checks and launches of the fused Linear entry points.
+w8a8_status run_linear(bool block, const void* X, const void* Wimg, const float* sw, const void* bias, void* Y,
+                       int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq, void* ws, size_t ws_bytes,
+                       cudaStream_t st) {
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, block);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0 || N == 0) return W8A8_OK;
+    if (!X || !Wimg || !sw || !Y || !sx) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wimg) || !aligned16(sw) || !aligned16(Y) || !aligned16(sx) ||
+        (Xq && !aligned16(Xq)) || (bias && !aligned16(bias)))
+        return W8A8_ERR_ALIGNMENT;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w8a8_linear_workspace_size(M, K))
+        return W8A8_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    cudaError_t e = block ? w8a8::launch_quant_act_block(X, M, K, Xq, ws, sx, dev.num_sms, st)
+                          : w8a8::launch_quant_rows(X, M, K, Xq, ws, sx, dev.num_sms, st);
+    if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
+    return run_gemm_images(block ? w8a8::kEpiBlockwiseBf16 : w8a8::kEpiPostscaleBf16, ws, Wimg, sx, sw, bias, Y, M,
+                           N, K, dev, st);
+}
+
 w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
                      const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* ws, const DeviceInfo& dev,
                      cudaStream_t st) {
@@ -139,22 +188,7 @@ w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* W
     if (e != cudaSuccess) return cuda_fail("expand Xq launch", e);
     e = w8a8::launch_expand_s8_bf16(Wq, N * K, Bb, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("expand Wq launch", e);
-    w8a8::GemmArgs a;
-    a.sx = sx;
-    a.sw = sw;
-    a.bias = bias;
-    a.out = out;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
-    e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return W8A8_ERR_CUDA;
-    }
-    if (t_gemm_end && (e = cudaEventRecord(t_gemm_end, st)) != cudaSuccess) return cuda_fail("event", e);
-    return W8A8_OK;
+    return run_gemm_images(epi, Ab, Bb, sx, sw, bias, out, M, N, K, dev, st);
 }
 
 // Scratch of the allocation-free GEMM entry point: a fixed device array,
@@ -222,7 +256,7 @@ w8a8_status w8a8_quantize_weight(const void* W, int64_t N, int64_t K, w8a8_scale
     DeviceInfo dev;
     if ((s = current_device(&dev)) != W8A8_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(W, N, K, Wq, sw, dev.num_sms, st));
+    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(W, N, K, Wq, nullptr, sw, dev.num_sms, st));
     if ((N + 127) / 128 > 65535) return W8A8_ERR_SHAPE;
     return from_cuda(w8a8::launch_quant_weight_block(W, N, K, Wq, sw, st));
 }
@@ -240,8 +274,39 @@ w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8_scale_mo
     DeviceInfo dev;
     if ((s = current_device(&dev)) != W8A8_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(X, M, K, Xq, sx, dev.num_sms, st));
-    return from_cuda(w8a8::launch_quant_act_block(X, M, K, Xq, sx, dev.num_sms, st));
+    if (mode == W8A8_SCALE_PER_ROW) return from_cuda(w8a8::launch_quant_rows(X, M, K, Xq, nullptr, sx, dev.num_sms, st));
+    return from_cuda(w8a8::launch_quant_act_block(X, M, K, Xq, nullptr, sx, dev.num_sms, st));
+}
+
+w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, void* Wimg, void* stream) {
+    if (N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, false);
+    if (s != W8A8_OK) return s;
+    if (N == 0) return W8A8_OK;
+    if (!Wq || !Wimg) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(Wq) || !aligned16(Wimg)) return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    return from_cuda(w8a8::launch_expand_s8_bf16(Wq, N * K, Wimg, dev.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w8a8_linear_workspace_size(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0) return 0;
+    return align256(static_cast<size_t>(M) * K * 2);
+}
+
+w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, const float* sw, const void* bias, void* Y,
+                                  int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    return run_linear(false, X, Wimg, sw, bias, Y, M, N, K, sx, Xq, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, const float* sw, const void* bias, void* Y,
+                                  int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    return run_linear(true, X, Wimg, sw, bias, Y, M, N, K, sx, Xq, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
 }
 
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {

@@ -9,12 +9,13 @@
 namespace w8a8 {
 
 // Per-row quantization of A[R,K] (bf16): one scale per row (per token for
-// activations, per output channel for weights).
-cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, int num_sms,
+// activations, per output channel for weights).  Writes the int8 codes to Aq
+// and/or their exact bf16 image to img (either may be null, not both).
+cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, void* img, float* s, int num_sms,
                               cudaStream_t st);
-// 1x128-block activation quantization, sx[M][K/128].
-cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, float* sx, int num_sms,
-                                   cudaStream_t st);
+// 1x128-block activation quantization, sx[M][K/128]; outputs as above.
+cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, void* img, float* sx,
+                                   int num_sms, cudaStream_t st);
 // 128x128-block weight quantization, sw[ceil(N/128)][K/128].
 cudaError_t launch_quant_weight_block(const void* W, int64_t N, int64_t K, int8_t* Wq, float* sw,
                                       cudaStream_t st);

@@ -172,6 +172,32 @@ __device__ __forceinline__ uint2 quant_chunk(const uint4& v, const RowScale& sc)
     return make_uint2(__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo45, lo67, 0x5410));
 }
 
+// int8 -> bf16, exact.  For a byte b holding x in two's complement,
+// bits 0x4B000000 | (b ^ 0x80) encode 2^23 + x + 128, and subtracting
+// 2^23 + 128 gives x exactly; bf16 holds every integer in [-128, 127].
+__device__ __forceinline__ uint32_t s8x2_to_bf16x2(uint32_t w, int first) {
+    const float k = 8388736.0f;  // 2^23 + 128
+    const uint32_t flipped = w ^ 0x80808080u;
+    const float f0 = __fsub_rn(__uint_as_float(0x4B000000u | ((flipped >> (8 * first)) & 0xFFu)), k);
+    const float f1 = __fsub_rn(__uint_as_float(0x4B000000u | ((flipped >> (8 * first + 8)) & 0xFFu)), k);
+    __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Write one chunk of 8 codes: as int8 to q[i] (when q is given) and as the
+// exact bf16 image of the codes to img[i] (when img is given).
+__device__ __forceinline__ void put_codes(uint2* __restrict__ q, uint4* __restrict__ img, int64_t i, uint2 c) {
+    if (q) __stcs(q + i, c);
+    if (img) {
+        uint4 o;
+        o.x = s8x2_to_bf16x2(c.x, 0);
+        o.y = s8x2_to_bf16x2(c.x, 2);
+        o.z = s8x2_to_bf16x2(c.y, 0);
+        o.w = s8x2_to_bf16x2(c.y, 2);
+        img[i] = o;
+    }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -194,7 +220,8 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 // per thread) between the absmax pass and the quantize pass.
 template <int CPT>
 __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
-                                                             uint2* __restrict__ Aq, float* __restrict__ s) {
+                                                             uint2* __restrict__ Aq, uint4* __restrict__ img,
+                                                             float* __restrict__ s) {
     __shared__ float red[32];
     __shared__ ScaleTables tab;
     build_scale_tables(tab);
@@ -215,11 +242,10 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
     amax = block_max(amax, red);
     const RowScale sc = make_scale(amax, tab);
     if (threadIdx.x == 0) s[row] = sc.s;
-    uint2* q = Aq + row * chunks;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
         const int64_t c = threadIdx.x + static_cast<int64_t>(i) * blockDim.x;
-        if (c < chunks) __stcs(q + c, quant_chunk(v[i], sc));
+        if (c < chunks) put_codes(Aq, img, row * chunks + c, quant_chunk(v[i], sc));
     }
 }
 
@@ -229,7 +255,8 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
 // many rows are in flight per SM.
 template <int U>
 __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
-                                                               uint2* __restrict__ Aq, float* __restrict__ s) {
+                                                                  uint2* __restrict__ Aq, uint4* __restrict__ img,
+                                                                  float* __restrict__ s) {
     __shared__ ScaleTables tab;
     build_scale_tables(tab);
     const int lane = threadIdx.x & 31;
@@ -254,7 +281,6 @@ __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* _
     amax = warp_max(amax);
     const RowScale sc = make_scale(amax, tab);
     if (lane == 0) s[row] = sc.s;
-    uint2* q = Aq + row * chunks;
     for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
         uint4 v[U];
 #pragma unroll
@@ -265,14 +291,15 @@ __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* _
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = c0 + lane + 32 * u;
-            if (c < chunks) __stcs(q + c, quant_chunk(v[u], sc));
+            if (c < chunks) put_codes(Aq, img, row * chunks + c, quant_chunk(v[u], sc));
         }
     }
 }
 
 // Rows too long to keep in registers: absmax pass, then a second read.
 __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
-                                                               uint2* __restrict__ Aq, float* __restrict__ s) {
+                                                               uint2* __restrict__ Aq, uint4* __restrict__ img,
+                                                               float* __restrict__ s) {
     __shared__ float red[32];
     __shared__ ScaleTables tab;
     build_scale_tables(tab);
@@ -285,8 +312,8 @@ __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __re
     amax = block_max(amax, red);
     const RowScale sc = make_scale(amax, tab);
     if (threadIdx.x == 0) s[row] = sc.s;
-    uint2* q = Aq + row * chunks;
-    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) __stcs(q + c, quant_chunk(__ldcs(a + c), sc));
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
+        put_codes(Aq, img, row * chunks + c, quant_chunk(__ldcs(a + c), sc));
 }
 
 // 1x128 activation blocks: 4 lanes own one block (4 chunks of 8 bf16 each),
@@ -297,7 +324,8 @@ __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __re
 // flight.
 template <int UNROLL>
 __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __restrict__ X, int64_t n_blocks,
-                                                              uint2* __restrict__ Xq, float* __restrict__ sx) {
+                                                              uint2* __restrict__ Xq, uint4* __restrict__ img,
+                                                              float* __restrict__ sx) {
     __shared__ ScaleTables tab;
     build_scale_tables(tab);
     const int lane = threadIdx.x & 31;
@@ -327,7 +355,7 @@ __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __res
             const RowScale sc = make_scale(m, tab);
             if (blk < n_blocks) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) __stcs(Xq + blk * 16 + sub + 4 * i, quant_chunk(v[u][i], sc));
+                for (int i = 0; i < 4; ++i) put_codes(Xq, img, blk * 16 + sub + 4 * i, quant_chunk(v[u][i], sc));
                 if (sub == 0) sx[blk] = sc.s;
             }
         }
@@ -366,18 +394,6 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __
     }
 }
 
-// int8 -> bf16, exact.  For a byte b holding x in two's complement,
-// bits 0x4B000000 | (b ^ 0x80) encode 2^23 + x + 128, and subtracting
-// 2^23 + 128 gives x exactly; bf16 holds every integer in [-128, 127].
-__device__ __forceinline__ uint32_t s8x2_to_bf16x2(uint32_t w, int first) {
-    const float k = 8388736.0f;  // 2^23 + 128
-    const uint32_t flipped = w ^ 0x80808080u;
-    const float f0 = __fsub_rn(__uint_as_float(0x4B000000u | ((flipped >> (8 * first)) & 0xFFu)), k);
-    const float f1 = __fsub_rn(__uint_as_float(0x4B000000u | ((flipped >> (8 * first + 8)) & 0xFFu)), k);
-    __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
 __global__ void __launch_bounds__(256) expand_s8_bf16_kernel(const uint4* __restrict__ src, int64_t n16,
                                                              uint4* __restrict__ dst) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -399,35 +415,36 @@ __global__ void __launch_bounds__(256) expand_s8_bf16_kernel(const uint4* __rest
 
 }  // namespace
 
-cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, float* s, int num_sms,
+cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, void* img, float* s, int num_sms,
                               cudaStream_t st) {
     (void)num_sms;
     const int64_t chunks = K >> 3;
     const uint4* a = static_cast<const uint4*>(A);
     uint2* q = reinterpret_cast<uint2*>(Aq);
+    uint4* im = static_cast<uint4*>(img);
     const dim3 grid(static_cast<unsigned>(R));
     if (chunks > 512) {
         // long rows: one warp per row, two passes, many rows in flight per SM
-        quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, s);
+        quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, im, s);
         return cudaGetLastError();
     }
     if (chunks <= 128)
-        quant_rows_reg_kernel<1><<<grid, 128, 0, st>>>(a, R, K, q, s);
+        quant_rows_reg_kernel<1><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 256)
-        quant_rows_reg_kernel<1><<<grid, 256, 0, st>>>(a, R, K, q, s);
+        quant_rows_reg_kernel<1><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 512)
-        quant_rows_reg_kernel<2><<<grid, 256, 0, st>>>(a, R, K, q, s);
+        quant_rows_reg_kernel<2><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 1024)
-        quant_rows_reg_kernel<4><<<grid, 256, 0, st>>>(a, R, K, q, s);
+        quant_rows_reg_kernel<4><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 2048)
-        quant_rows_reg_kernel<8><<<grid, 256, 0, st>>>(a, R, K, q, s);
+        quant_rows_reg_kernel<8><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     else
-        quant_rows_2pass_kernel<<<grid, 256, 0, st>>>(a, R, K, q, s);
+        quant_rows_2pass_kernel<<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, float* sx, int num_sms,
-                                   cudaStream_t st) {
+cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* Xq, void* img, float* sx,
+                                   int num_sms, cudaStream_t st) {
     const int64_t n_blocks = M * (K >> 7);
     constexpr int kUnroll = 2;
     const int64_t warps_needed = (n_blocks + 8 * kUnroll - 1) / (8 * kUnroll);
@@ -436,7 +453,7 @@ cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* 
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     quant_act_block_kernel<kUnroll><<<static_cast<unsigned>(grid), 256, 0, st>>>(
-        static_cast<const uint4*>(X), n_blocks, reinterpret_cast<uint2*>(Xq), sx);
+        static_cast<const uint4*>(X), n_blocks, reinterpret_cast<uint2*>(Xq), static_cast<uint4*>(img), sx);
     return cudaGetLastError();
 }
 
