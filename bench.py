@@ -44,6 +44,38 @@ def parse():
     return ap.parse_args()
 
 
+GEMM_SOURCES = ["gemm.cu", "ptx.cuh", "kernels.h", "w8a8_device_error.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic_square_postscale_4096.txt")
+
+
+def gemm_source_hash():
+    """sha256 (first 16 hex digits) of the GEMM kernel's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "w8a8_int8_linear_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu capture, or None when
+    the capture is for another workload or the kernel changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_FILE):
+        if "=" in line and not line.lstrip().startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("workload") != workload or kv.get("gemm_source_sha256_16") != gemm_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_read"]) + float(kv["dram_bytes_write"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -223,7 +255,9 @@ def run_w8a8(args):
         linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
 
     if args.profile_once:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         for _ in range(args.warmup + args.steps):
+            flush.zero_()  # as in the timed loop: L2 holds nothing of the step's inputs
             step()
         torch.cuda.synchronize()
         st, code = w.get_device_error()
@@ -371,9 +405,12 @@ def run_w8a8(args):
         "impl": "w8a8",
         "roofline": {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f16, exact int8 products)",
                      "achieved": round(gemm_tflops, 2), "peak": peak_bf16, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / peak_bf16, 4), "traffic": None,
+                     "frac": round(gemm_tflops / peak_bf16, 4), "traffic": recorded_traffic(work.name),
+                     "traffic_source": "profiles/gemm_traffic_square_postscale_4096.txt (ncu dram bytes per "
+                                       "launch; null if the GEMM sources changed since the capture)",
                      "peak_source": f"bf16 dense burst, {peaks['source']}",
-                     "algorithmic": f"2*M*N*K = {ops:.4g} ops per launch",
+                     "algorithmic": f"2*M*N*K = {ops:.4g} ops per launch; operand images + Y = "
+                                    f"{(2 * M * K + 2 * N * K + 2 * M * N) / 1e6:.1f} MB",
                      "gemm_ms": round(ms_gemm, 5)},
         "int8_peak": {"measured_imma_tops": round(imma_tops, 1),
                       "frac_of_imma_peak": round(gemm_tflops / imma_tops, 3) if imma_tops else None,

@@ -56,7 +56,8 @@ constexpr int BM = 128;  // rows of A per CTA; a CTA pair covers TILE_M rows
 constexpr int TILE_M = 2 * BM;
 constexpr int BK = 64;   // bf16 elements per stage row = 128 bytes = one swizzle row
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t RING_BUDGET = 192 * 1024;
+constexpr uint32_t MAX_DYN_SMEM = 232448;  // 227 KB opt-in shared memory per block
+constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - 256 - 512;  // minus alignment slack, barriers, margin
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;  // warps 0-3: producer, MMA issuer, two idle; warps 4-11: epilogue
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
