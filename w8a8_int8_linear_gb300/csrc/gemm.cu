@@ -57,7 +57,11 @@ constexpr int TILE_M = 2 * BM;
 constexpr int BK = 64;   // bf16 elements per stage row = 128 bytes = one swizzle row
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t MAX_DYN_SMEM = 232448;  // 227 KB opt-in shared memory per block
-constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - 256 - 512;  // minus alignment slack, barriers, margin
+// Output staging for the TMA-store epilogue: per epilogue warp, two 1 KB
+// buffers of 32 rows x 16 bf16 columns (32-byte swizzle).
+constexpr uint32_t STAGE_OUT_BYTES = 32 * 16 * 2;
+constexpr uint32_t STAGING_BYTES = 8 * 2 * STAGE_OUT_BYTES;
+constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - 256 - 512 - STAGING_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;  // warps 0-3: producer, MMA issuer, two idle; warps 4-11: epilogue
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
@@ -81,7 +85,7 @@ struct Cfg {
     static constexpr uint32_t B_BYTES = HALF * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : int(RING_BUDGET / STAGE_BYTES);
-    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + 256;
     static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
     static constexpr int LDW = (HALF % 32 == 0) ? 32 : 16;  // TMEM load width (columns)
     static constexpr int GROUPS = HALF / LDW;
@@ -104,6 +108,7 @@ struct KParams {
     int M, N, K;
     int num_m, num_n, num_tiles;
     int k_stages, chunk_stages, kb_count;
+    int tma_store;  // bf16 output written through shared memory and TMA (needs N % 8 == 0)
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
@@ -151,7 +156,9 @@ __device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, uint32_t (&r)[3
 __device__ __forceinline__ void tmem_wait_cols(uint32_t (&r)[16]) { tmem_wait_ld_regs(r); }
 __device__ __forceinline__ void tmem_wait_cols(uint32_t (&r)[32]) { tmem_wait_ld_regs32(r); }
 
-// Write the COLS accumulated columns [col0, col0+COLS) of one row.
+// Write the COLS accumulated columns [col0, col0+COLS) of one row.  The
+// per-column scales and bias are read through the read-only path (they never
+// alias Y), so their loads need not wait behind this row's stores.
 template <int EPI, int COLS>
 __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[COLS], const KParams& p, int row,
                                           int col0) {
@@ -160,7 +167,8 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
     const bool vec = (N & 7) == 0;
     const int64_t rowoff = static_cast<int64_t>(row) * N;
     float sxr = 0.0f;
-    if constexpr (EPI == kEpiPostscaleBf16) sxr = p.sx[row];
+    if constexpr (EPI == kEpiPostscaleBf16) sxr = __ldg(p.sx + row);
+    const uint16_t* bias16 = reinterpret_cast<const uint16_t*>(p.bias);
 #pragma unroll
     for (int j = 0; j < COLS; j += 8) {
         const int col = col0 + j;
@@ -192,13 +200,13 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
                 float bc[8];
                 if (full) {
                     if constexpr (EPI == kEpiPostscaleBf16) {
-                        const float4 s0 = *reinterpret_cast<const float4*>(p.sw + col);
-                        const float4 s1 = *reinterpret_cast<const float4*>(p.sw + col + 4);
+                        const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.sw + col));
+                        const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.sw + col + 4));
                         swc[0] = s0.x; swc[1] = s0.y; swc[2] = s0.z; swc[3] = s0.w;
                         swc[4] = s1.x; swc[5] = s1.y; swc[6] = s1.z; swc[7] = s1.w;
                     }
                     if (p.bias) {
-                        const uint4 b = *reinterpret_cast<const uint4*>(p.bias + col);
+                        const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col));
                         const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -210,9 +218,8 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const bool in = col + e < N;
-                        if constexpr (EPI == kEpiPostscaleBf16) swc[e] = in ? p.sw[col + e] : 0.0f;
-                        if (p.bias)
-                            bc[e] = in ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.bias)[col + e]) : 0.0f;
+                        if constexpr (EPI == kEpiPostscaleBf16) swc[e] = in ? __ldg(p.sw + col + e) : 0.0f;
+                        if (p.bias) bc[e] = in ? bf16_bits_to_f32(__ldg(bias16 + col + e)) : 0.0f;
                     }
                 }
 #pragma unroll
@@ -246,9 +253,93 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
     }
 }
 
+// bf16 output of one warp's 32 rows x COLS columns through shared memory and
+// TMA stores: 16-column groups, each written by the 32 lanes (one row each)
+// into a 1 KB staging buffer with the 32-byte swizzle (16-byte chunk index
+// XOR bit 2 of the row, which spreads each quarter-warp over 8 bank groups),
+// then stored by one lane as a 16 x 32 box.  Two buffers per warp alternate;
+// a buffer is rewritten only after the store issued from it two groups ago
+// has read it.  Out-of-range rows and columns are clipped by the TMA unit.
+template <int EPI, int COLS>
+__device__ __forceinline__ void store_rows_tma(const typename AccType<EPI>::T (&acc)[COLS], const KParams& p,
+                                               const CUtensorMap* tmY, int row, int row_base, int col0,
+                                               uint8_t* stg, int& sbuf, int lane) {
+    float sxr = 0.0f;
+    if constexpr (EPI == kEpiPostscaleBf16) sxr = (row < p.M) ? __ldg(p.sx + row) : 0.0f;
+    const uint16_t* bias16 = reinterpret_cast<const uint16_t*>(p.bias);
+#pragma unroll
+    for (int g = 0; g < COLS; g += 16) {
+        const int col = col0 + g;
+        if (col >= p.N) break;
+        float swc[16], bc[16];
+        const bool full = col + 16 <= p.N;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            if constexpr (EPI == kEpiPostscaleBf16) {
+                if (full) {
+                    const float4 s4 = __ldg(reinterpret_cast<const float4*>(p.sw + col + e));
+                    swc[e] = s4.x; swc[e + 1] = s4.y; swc[e + 2] = s4.z; swc[e + 3] = s4.w;
+                } else {
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) swc[e + f] = (col + e + f < p.N) ? __ldg(p.sw + col + e + f) : 0.0f;
+                }
+            }
+        }
+        if (p.bias) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 8) {
+                if (full) {
+                    const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col + e));
+                    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        bc[e + 2 * f] = __uint_as_float(bw[f] << 16);
+                        bc[e + 2 * f + 1] = __uint_as_float(bw[f] & 0xFFFF0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int f = 0; f < 8; ++f)
+                        bc[e + f] = (col + e + f < p.N) ? bf16_bits_to_f32(__ldg(bias16 + col + e + f)) : 0.0f;
+                }
+            }
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            float v0, v1;
+            if constexpr (EPI == kEpiPostscaleBf16) {
+                v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sxr), swc[e]);
+                v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e + 1]), sxr), swc[e + 1]);
+            } else {
+                v0 = acc[g + e];
+                v1 = acc[g + e + 1];
+            }
+            if (p.bias) {
+                v0 = __fadd_rn(v0, bc[e]);
+                v1 = __fadd_rn(v1, bc[e + 1]);
+            }
+            o[e >> 1] = pack_bf16x2(v0, v1);
+        }
+        uint8_t* buf = stg + sbuf * STAGE_OUT_BYTES;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
+        __syncwarp();
+        const int sw = (lane >> 2) & 1;
+        *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (0 ^ sw)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (1 ^ sw)) = make_uint4(o[4], o[5], o[6], o[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmY, buf, col, row_base);
+            bulk_commit_group();
+        }
+        sbuf ^= 1;
+    }
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmY, const KParams p) {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES;
     constexpr int HALF = C::HALF;
@@ -256,7 +347,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_BYTES);
+    uint8_t* staging = sB + STAGES * C::B_BYTES;  // 1 KB aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -392,13 +484,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;                  // TMEM lanes this warp may access
         const int half = (warp - EPI_WARP0) >> 2;      // which column half of the tile
         const uint32_t leader_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
+        constexpr bool kBf16Out = (EPI == kEpiPostscaleBf16 || EPI == kEpiBlockwiseBf16);
+        uint8_t* stg = staging + (warp - EPI_WARP0) * 2 * STAGE_OUT_BYTES;
+        int sbuf = 0;
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
         for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
             int mb, nb;
             tile_coords(tile, p.num_m, p.num_n, mb, nb);
-            const int row = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
+            const int row_base = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
+            const int row = row_base + lane;
             const int col0 = nb * BN + half * HALF;
             // post-scale: int32 running sums; blockwise: fp32 accumulators
             T acc[HALF];
@@ -446,8 +542,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (buf == 0) buf_phase ^= 1u;
             }
             if (!ok) break;
-            store_row<EPI, HALF>(acc, p, row, col0);
+            if (kBf16Out && p.tma_store)
+                store_rows_tma<EPI, HALF>(acc, p, &tmY, row, row_base, col0, stg, sbuf, lane);
+            else
+                store_row<EPI, HALF>(acc, p, row, col0);
         }
+        if (lane == 0) bulk_wait_group_all();  // this warp's output stores have completed
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -499,6 +600,22 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
         snprintf(detail, n, "cuTensorMapEncodeTiled(B: %d x %d) returned %d", p.N, p.K, (int)r);
         return cudaErrorInvalidValue;
     }
+    CUtensorMap tmY = tmB;  // placeholder when the output is not written through TMA
+    constexpr bool kBf16Out = (EPI == kEpiPostscaleBf16 || EPI == kEpiBlockwiseBf16);
+    p.tma_store = (kBf16Out && (p.N % 8) == 0) ? 1 : 0;
+    if (p.tma_store) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 2};
+        cuuint32_t box[2] = {16, 32};
+        cuuint32_t estr[2] = {1, 1};
+        r = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            snprintf(detail, n, "cuTensorMapEncodeTiled(Y: %d x %d) returned %d", p.M, p.N, (int)r);
+            return cudaErrorInvalidValue;
+        }
+    }
     p.num_m = (p.M + TILE_M - 1) / TILE_M;
     p.num_n = (p.N + BN - 1) / BN;
     p.num_tiles = p.num_m * p.num_n;
@@ -539,7 +656,7 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     }
     const int clusters = p.num_tiles < info.max_clusters ? p.num_tiles : info.max_clusters;
     cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, BN>, tmA, tmB, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, BN>, tmA, tmB, tmY, p);
 }
 
 // Tile width for the post-scale GEMM: the candidate minimizing
