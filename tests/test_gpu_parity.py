@@ -69,6 +69,25 @@ def test_quantize_act_per_token_streamed_many_units(w8a8, oracle, M, K):
     assert w8a8.get_device_error() == (0, 0)
 
 
+def test_scales_cover_every_absmax_mantissa(w8a8, oracle):
+    """Rows whose absmax takes all 128 bf16 significands at several binary
+    exponents (including ones that fall back to IEEE division), so every
+    entry of the quantizer's scale tables is compared with the oracle."""
+    rows = []
+    for e in (-130, -126, -100, -20, -3, 0, 5, 40, 120, 126):
+        for i in range(128):
+            r = torch.zeros(256)
+            r[7] = (128 + i) / 128.0 * 2.0 ** e
+            r[100] = -(64 + i / 2) / 128.0 * 2.0 ** e
+            rows.append(r)
+    X = torch.stack(rows).to(torch.bfloat16)
+    for mode in (w8a8.PER_ROW, w8a8.BLOCK):
+        Xq, sx = w8a8.quantize_act(X.to(DEV), mode)
+        oq, os_ = oracle.quantize_act(bits(X), mode)
+        assert np.array_equal(Xq.cpu().numpy(), oq)
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
 @pytest.mark.parametrize("M,K", [(1, 128), (9, 256), (1000, 1408), (17, 13824), (4001, 4096)])
 def test_quantize_act_block(w8a8, oracle, M, K):
     X = torch.cat([torch.nn.functional.gelu(rand_bf16((M, K), seed=K).float()).to(torch.bfloat16),

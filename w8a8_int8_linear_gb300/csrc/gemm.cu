@@ -386,6 +386,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     cluster_sync();  // the peer's barriers are initialized before anyone signals them
     tc_fence_after();
+    // Everything above overlaps the tail of the kernel that wrote the
+    // operands and scales (programmatic dependent launch); nothing below
+    // reads global memory before that kernel has completed.
+    grid_dependency_wait();
     const uint32_t tmem_base = *tmem_slot;
     const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
     if (warp < EPI_WARP0) {
@@ -626,16 +630,18 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     DeviceLaunchInfo& info = g_launch_info[dev];
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
     constexpr int id = instance_id<EPI, BN>();
     if (!info.configured[id]) {
         e = cudaFuncSetAttribute(gemm_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -656,6 +662,7 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     }
     const int clusters = p.num_tiles < info.max_clusters ? p.num_tiles : info.max_clusters;
     cfg.gridDim = dim3(2 * clusters);
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, BN>, tmA, tmB, tmY, p);
 }
 

@@ -35,6 +35,11 @@ __device__ __forceinline__ bool elect_one_sync() {
     return pred != 0;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel on the
+// stream has completed and its memory is visible (a no-op when this kernel
+// was launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

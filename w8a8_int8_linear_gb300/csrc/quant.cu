@@ -9,9 +9,9 @@
 // Scales without division.  absmax is a bf16 value, M * 2^k with an 8-bit
 // significand M in [128, 255].  Scaling by a power of two commutes with
 // rounding while the result stays normal, so fl(absmax / 127) =
-// fl(M / 127) * 2^k and fl(1 / s) = fl(1 / fl(M / 127)) * 2^-k.  Each CTA
-// builds the two 128-entry tables fl(M/127) and fl(1/fl(M/127)) with IEEE
-// division; a scale is then a table read plus an exponent add.  (An
+// fl(M / 127) * 2^k and fl(1 / s) = fl(1 / fl(M / 127)) * 2^-k.  The two
+// 128-entry tables fl(M/127) and fl(1/fl(M/127)) are compile-time constants
+// in device memory; a scale is then a table read plus an exponent add.  (An
 // exhaustive host check over every bf16 value confirms the identity for
 // exponent fields 7..254; the tables are used for 8..250 and every other
 // nonzero absmax takes IEEE division.)
@@ -57,30 +57,35 @@ struct RowScale {
 
 constexpr float kMinNormal = 1.17549435e-38f;  // 2^-126
 
+// fl(M / 127) and fl(1 / fl(M / 127)) for M = 128 + i, i in [0, 128): built
+// at compile time (the host compiler folds IEEE single-precision division
+// with round to nearest) and placed in device global memory, where the
+// per-row or per-block lookups hit L1.
 struct ScaleTables {
-    float T[128];  // fl((128 + i) / 127)
-    float R[128];  // fl(1 / T[i])
+    float T[128];
+    float R[128];
 };
 
-// All threads of the CTA call this before any make_scale.
-__device__ __forceinline__ void build_scale_tables(ScaleTables& t) {
-    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
-        const float v = __fdiv_rn(static_cast<float>(128 + i), kQMax);
-        t.T[i] = v;
-        t.R[i] = __frcp_rn(v);
+constexpr ScaleTables make_scale_tables() {
+    ScaleTables t{};
+    for (int i = 0; i < 128; ++i) {
+        t.T[i] = static_cast<float>(128 + i) / 127.0f;
+        t.R[i] = 1.0f / t.T[i];
     }
-    __syncthreads();
+    return t;
 }
 
-__device__ __forceinline__ RowScale make_scale(float amax, const ScaleTables& t) {
+__device__ const ScaleTables kScaleTables = make_scale_tables();
+
+__device__ __forceinline__ RowScale make_scale(float amax, const ScaleTables& t = kScaleTables) {
     RowScale r;
     const uint32_t b = __float_as_uint(amax);  // a bf16 value: low 16 bits are zero
     const int ef = static_cast<int>(b >> 23);
     if (ef >= 8 && ef <= 250) {
         const int f = static_cast<int>((b >> 16) & 0x7Fu);
         const int k = ef - 134;
-        r.s = __uint_as_float(__float_as_uint(t.T[f]) + (k << 23));
-        r.inv = __uint_as_float(__float_as_uint(t.R[f]) - (k << 23));
+        r.s = __uint_as_float(__float_as_uint(__ldg(&t.T[f])) + (k << 23));
+        r.inv = __uint_as_float(__float_as_uint(__ldg(&t.R[f])) - (k << 23));
         r.exact = false;
     } else {
         r.s = __fdiv_rn(amax, kQMax);
@@ -223,8 +228,6 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
                                                              uint2* __restrict__ Aq, uint4* __restrict__ img,
                                                              float* __restrict__ s) {
     __shared__ float red[32];
-    __shared__ ScaleTables tab;
-    build_scale_tables(tab);
     const int64_t row = blockIdx.x;
     if (row >= R) return;
     const int64_t chunks = K >> 3;
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
         }
     }
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax, tab);
+    const RowScale sc = make_scale(amax);
     if (threadIdx.x == 0) s[row] = sc.s;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
@@ -257,8 +260,6 @@ template <int U>
 __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
                                                                   uint2* __restrict__ Aq, uint4* __restrict__ img,
                                                                   float* __restrict__ s) {
-    __shared__ ScaleTables tab;
-    build_scale_tables(tab);
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= R) return;
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* _
         }
     }
     amax = warp_max(amax);
-    const RowScale sc = make_scale(amax, tab);
+    const RowScale sc = make_scale(amax);
     if (lane == 0) s[row] = sc.s;
     for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
         uint4 v[U];
@@ -301,8 +302,6 @@ __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __re
                                                                uint2* __restrict__ Aq, uint4* __restrict__ img,
                                                                float* __restrict__ s) {
     __shared__ float red[32];
-    __shared__ ScaleTables tab;
-    build_scale_tables(tab);
     const int64_t row = blockIdx.x;
     if (row >= R) return;
     const int64_t chunks = K >> 3;
@@ -310,7 +309,7 @@ __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __re
     float amax = 0.0f;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) amax = fmaxf(amax, chunk_absmax(a[c]));
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax, tab);
+    const RowScale sc = make_scale(amax);
     if (threadIdx.x == 0) s[row] = sc.s;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
         put_codes(Aq, img, row * chunks + c, quant_chunk(__ldcs(a + c), sc));
@@ -326,8 +325,6 @@ template <int UNROLL>
 __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __restrict__ X, int64_t n_blocks,
                                                               uint2* __restrict__ Xq, uint4* __restrict__ img,
                                                               float* __restrict__ sx) {
-    __shared__ ScaleTables tab;
-    build_scale_tables(tab);
     const int lane = threadIdx.x & 31;
     const int sub = lane & 3, bl = lane >> 2;
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -352,7 +349,7 @@ __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __res
             }
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const RowScale sc = make_scale(m, tab);
+            const RowScale sc = make_scale(m);
             if (blk < n_blocks) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) put_codes(Xq, img, blk * 16 + sub + 4 * i, quant_chunk(v[u][i], sc));
@@ -366,8 +363,6 @@ __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __res
 __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __restrict__ W, int64_t N, int64_t K,
                                                                  uint2* __restrict__ Wq, float* __restrict__ sw) {
     __shared__ float red[32];
-    __shared__ ScaleTables tab;
-    build_scale_tables(tab);
     const int64_t kb = blockIdx.x, nb = blockIdx.y;
     const int64_t kbs = K >> 7;
     const int64_t chunks_per_row = K >> 3;
@@ -384,7 +379,7 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __
         }
     }
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax, tab);
+    const RowScale sc = make_scale(amax);
     if (threadIdx.x == 0) sw[nb * kbs + kb] = sc.s;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -423,21 +418,16 @@ cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, v
     uint2* q = reinterpret_cast<uint2*>(Aq);
     uint4* im = static_cast<uint4*>(img);
     const dim3 grid(static_cast<unsigned>(R));
-    if (chunks > 512) {
-        // long rows: one warp per row, two passes, many rows in flight per SM
-        quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, im, s);
-        return cudaGetLastError();
-    }
+    // one 128-thread CTA per row for rows of up to 512 chunks (K <= 4096),
+    // two-pass warp-per-row beyond
     if (chunks <= 128)
         quant_rows_reg_kernel<1><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 256)
-        quant_rows_reg_kernel<1><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
+        quant_rows_reg_kernel<2><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 512)
-        quant_rows_reg_kernel<2><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
-    else if (chunks <= 1024)
-        quant_rows_reg_kernel<4><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
-    else if (chunks <= 2048)
-        quant_rows_reg_kernel<8><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
+        quant_rows_reg_kernel<4><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
+    else if (chunks <= 16384)
+        quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, im, s);
     else
         quant_rows_2pass_kernel<<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     return cudaGetLastError();
