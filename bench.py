@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (rows of X)")
+    ap.add_argument("--report-configs", action="store_true",
+                    help="time every workload (tiny, square, FFN up, FFN down, ragged sweep) and print a table")
     ap.add_argument("--profile-once", action="store_true",
                     help="only the W warm-up and K plain steps, no flush or side measurements (for ncu)")
     return ap.parse_args()
@@ -473,10 +475,117 @@ def run_reference(args):
     }))
 
 
+def report_configs(args):
+    """Per-workload table: step time (quant + GEMM through the fused Linear),
+    TOPS, GEMM TFLOP/s and its fraction of the bf16 peak, multiple of the
+    measured INT8 (mma.sync) peak, quant GB/s, torch bf16 matmul, and the
+    oracle's host throughput on a bounded sample."""
+    import torch
+    import oracle
+    import w8a8_int8_linear_gb300 as w
+    from w8a8_int8_linear_gb300 import workloads as wl
+    from w8a8_int8_linear_gb300.workloads import bf16_bits
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    imma = w.measure_imma_peak()
+    works = [wl.TINY, wl.SQUARE, wl.FFN_UP, wl.FFN_DOWN] + [wl.ragged(M, N) for N in wl.RAGGED_N for M in wl.RAGGED_M]
+    Xw = torch.randn((8192, 8192), device=dev).to(torch.bfloat16)
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        for _ in range(10):
+            torch.matmul(Xw, Xw)
+        torch.cuda.synchronize()
+    del Xw
+    rows = []
+    for work in works:
+        blockwise = work.mode == "blockwise"
+        mode = w.BLOCK if blockwise else w.PER_ROW
+        X = wl.make_x(work, dev)
+        W = wl.make_w(work, dev)
+        b = wl.make_bias(work, dev)
+        Wq, sw = w.quantize_weight(W, mode)
+        Wimg = w.pack_weight(Wq)
+        M, N, K = work.M, work.N, work.K
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        sx = torch.empty((M, K // 128) if blockwise else (M,), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(w.linear_workspace_size(M, K), 256), dtype=torch.uint8, device=dev)
+        Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        linear = w.linear_blockwise if blockwise else w.linear_postscale
+        for _ in range(3):
+            linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(); gb.record()
+        steps, gemms, quants = [], [], []
+        for _ in range(10):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w.set_gemm_timing_events(ga, gb)
+            a.record()
+            linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
+            c.record()
+            w.set_gemm_timing_events(None, None)
+            torch.cuda.synchronize()
+            steps.append(a.elapsed_time(c))
+            gemms.append(ga.elapsed_time(gb))
+        for _ in range(5):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            w.quantize_act(X, mode, out=(Xq, sx))
+            c.record()
+            torch.cuda.synchronize()
+            quants.append(a.elapsed_time(c))
+        tms = []
+        for _ in range(5):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            torch.matmul(X, W.t())
+            c.record()
+            torch.cuda.synchronize()
+            tms.append(a.elapsed_time(c))
+        st, code = w.get_device_error()
+        assert st == 0 and code == 0, f"device error {code}"
+        # oracle on a bounded sample of rows (about a second of host time)
+        rows_s = max(1, min(M, int(2e9 / (2 * N * K)) or 1))
+        Xb = bf16_bits(X[:rows_s])
+        t0 = time.perf_counter()
+        if blockwise:
+            oracle.linear_blockwise(Xb, bf16_bits(W), None if b is None else bf16_bits(b))
+        else:
+            oracle.linear_postscale(Xb, bf16_bits(W), None if b is None else bf16_bits(b))
+        odt = time.perf_counter() - t0  # includes the oracle's weight quantization
+        ops = work.ops
+        step_ms = statistics.median(steps)
+        gemm_ms = statistics.median(gemms)
+        q_ms = statistics.median(quants)
+        q_bytes = M * K * 3 + sx.numel() * 4
+        r = dict(workload=work.name, M=M, N=N, K=K, mode=work.mode, step_ms=round(step_ms, 4),
+                 tops=round(ops / step_ms / 1e9, 1), gemm_tflops=round(ops / gemm_ms / 1e9, 1),
+                 gemm_frac_bf16_peak=round(ops / gemm_ms / 1e9 / peaks["bf16_tflops"], 3),
+                 x_int8_mma_peak=round(ops / gemm_ms / 1e9 / imma, 2), quant_gbs=round(q_bytes / q_ms / 1e6, 0),
+                 torch_bf16_tflops=round(ops / statistics.median(tms) / 1e9, 1),
+                 oracle_tops=round(2.0 * rows_s * N * K / odt / 1e12, 4), oracle_rows=rows_s)
+        rows.append(r)
+        print(json.dumps(r), flush=True)
+        del X, W, Wq, Wimg, Y, Xq, ws
+        torch.cuda.empty_cache()
+    print(f"| workload | step ms | TOPS | GEMM TFLOP/s | of bf16 peak ({peaks['source']}) | x INT8 peak "
+          f"({imma:.0f} TOPS) | quant GB/s | torch bf16 TFLOP/s | oracle TOPS ({oracle.num_threads()} cores) |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for r in rows:
+        print(f"| {r['workload']} | {r['step_ms']} | {r['tops']} | {r['gemm_tflops']} | {r['gemm_frac_bf16_peak']} | "
+              f"{r['x_int8_mma_peak']} | {r['quant_gbs']:.0f} | {r['torch_bf16_tflops']} | {r['oracle_tops']} |")
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.report_configs:
+        report_configs(args)
     else:
         run_w8a8(args)
 

@@ -289,3 +289,21 @@ def test_linear_fused_rejects_bad_arguments(w8a8):
         w8a8.linear_blockwise(X, Wimg, torch.ones((1, 1), device=DEV))
     Y, sx, _ = w8a8.linear_postscale(torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV), Wimg, sw)
     assert Y.shape == (0, 8)
+
+
+# ----------------------------------------------------------------- Int8Linear module
+@pytest.mark.parametrize("mode", ["postscale", "blockwise"])
+def test_int8linear_module(w8a8, oracle, mode):
+    from w8a8_int8_linear_gb300.module import Int8Linear
+    torch.manual_seed(0)
+    lin = torch.nn.Linear(384, 200, bias=True).to(DEV).to(torch.bfloat16)
+    m = Int8Linear.from_linear(lin, mode)
+    x = rand_bf16((3, 5, 384), seed=60).to(DEV)  # leading dims are flattened
+    y = m(x)
+    assert y.shape == (3, 5, 200) and y.dtype == torch.bfloat16
+    X = bits(x.reshape(15, 384))
+    W = bits(lin.weight)
+    b = bits(lin.bias)
+    ref = oracle.linear_postscale(X, W, b) if mode == "postscale" else oracle.linear_blockwise(X, W, b)
+    d = assert_bf16_close(bits(y.reshape(15, 200)), ref["Y"], 1)
+    assert d.max() == 0
