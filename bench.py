@@ -249,7 +249,7 @@ def run_w8a8(args):
     Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
     sx = torch.empty((M, K // 128) if blockwise else (M,), dtype=torch.float32, device=dev)
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(w.linear_workspace_size(M, K), dtype=torch.uint8, device=dev)
+    ws = torch.empty(w.linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     linear = w.linear_blockwise if blockwise else w.linear_postscale
 
@@ -510,7 +510,7 @@ def report_configs(args):
         M, N, K = work.M, work.N, work.K
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         sx = torch.empty((M, K // 128) if blockwise else (M,), dtype=torch.float32, device=dev)
-        ws = torch.empty(max(w.linear_workspace_size(M, K), 256), dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(w.linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
         Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
         linear = w.linear_blockwise if blockwise else w.linear_postscale
         for _ in range(3):

@@ -116,7 +116,9 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * Bytes of device workspace the GEMM entry points need for this shape.  The
  * tensor-core path runs the exact integer product on the bf16 tensor pipe
  * (GB300 has no 8-bit integer tcgen05 MMA); the workspace holds the bf16
- * images of Xq and Wq (every int8 value is exact in bf16).
+ * images of Xq and Wq (every int8 value is exact in bf16) and, for few-token
+ * post-scale shapes (M <= 256 with few 256-row weight tiles), the int32
+ * partial sums of the K splits.  The same size serves both scale modes.
  */
 W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -156,9 +158,10 @@ W8A8_API w8a8_status w8a8_gemm_blockwise(const int8_t* Xq, const float* sx, cons
  */
 W8A8_API w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, void* Wimg, void* stream);
 
-/* Device workspace bytes of the fused Linear entry points (the bf16 image of
- * the quantized activations, M * K * 2 bytes rounded up to 256). */
-W8A8_API size_t w8a8_linear_workspace_size(int64_t M, int64_t K);
+/* Device workspace bytes of the fused Linear entry points: the bf16 image of
+ * the quantized activations (M * K * 2 bytes, rounded up to 256) plus, for
+ * few-token post-scale shapes, the int32 partial sums of the K splits. */
+W8A8_API size_t w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
  * Fused W8A8 Linear, post-scale: dynamic per-token quantization of X ("Reused
@@ -169,7 +172,7 @@ W8A8_API size_t w8a8_linear_workspace_size(int64_t M, int64_t K);
  *   X [M,K] bf16, Wimg [N,K] bf16 image from w8a8_pack_weight, sw [N] fp32,
  *   bias [N] bf16 or NULL, Y [M,N] bf16 out, sx [M] fp32 out (the per-token
  *   scales), Xq [M,K] int8 out or NULL (codes are written only if given),
- *   workspace of w8a8_linear_workspace_size(M,K) bytes, 256-byte aligned.
+ *   workspace of w8a8_linear_workspace_size(M,N,K) bytes, 256-byte aligned.
  */
 W8A8_API w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, const float* sw, const void* bias,
                                            void* Y, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq,

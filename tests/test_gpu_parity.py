@@ -120,6 +120,31 @@ def test_quantize_weight_modes(w8a8, oracle, N, K):
     (2432, 1792, 768, False),  # selects 256-column tiles
 ])
 def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
+    check_postscale(w8a8, oracle, M, N, K, bias)
+
+
+# Few tokens (M <= 256): the weights take the 256-row side of the MMA and the
+# tokens its narrow side (32 / 64 / 128 / 256), and Y is written transposed.
+# With few 256-row weight tiles, K is split and the int32 partials summed in
+# a second kernel (S = number of splits).
+@pytest.mark.parametrize("M,N,K,bias", [
+    (1, 4096, 4096, True),     # one token: 32-token tiles, S = 4
+    (16, 24, 128, False),      # fewer output columns than one store box, S = 1
+    (32, 520, 1040, True),     # S = 4, the last split ends in a 16-wide K stage
+    (33, 1000, 2048, False),   # 64-token tiles, S = 8
+    (64, 776, 512, True),      # S = 2
+    (65, 304, 1408, True),     # 128-token tiles, S = 5
+    (128, 257, 256, False),    # N % 8 != 0: direct stores, S = 1
+    (200, 1536, 3072, True),   # 256-token tiles, S = 8
+    (256, 2048, 1024, False),  # the largest swapped M, S = 4
+    (77, 9728, 1024, True),    # 38 weight tiles: no split, TMA stores
+    (3, 10000, 256, False),    # 40 weight tiles, no split, ragged last tile
+])
+def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
+    check_postscale(w8a8, oracle, M, N, K, bias)
+
+
+def check_postscale(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=1 + M, outliers=0.01, oscale=20.0)
     W = rand_bf16((N, K), seed=2 + N, scale=0.02)
     b = rand_bf16((N,), seed=3, scale=0.01) if bias else None
@@ -136,10 +161,11 @@ def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
     assert w8a8.get_device_error() == (0, 0)
 
 
-def test_gemm_exactness_adversary(w8a8, oracle):
+@pytest.mark.parametrize("M", [130, 520])  # swapped operands / the regular tiles
+def test_gemm_exactness_adversary(w8a8, oracle, M):
     """All-+-127 operands at K = 13824: per-chunk partial sums reach
     127*127*1024 and the total 2.2e8, far past fp32's 2^24 integer range."""
-    M, N, K = 130, 260, 13824
+    N, K = 260, 13824
     g = torch.Generator().manual_seed(11)
     sgn_x = torch.randint(0, 2, (M, K), generator=g) * 2 - 1
     sgn_w = torch.randint(0, 2, (N, K), generator=g) * 2 - 1
@@ -155,7 +181,7 @@ def test_gemm_exactness_adversary(w8a8, oracle):
     assert acc[0, 0] == 16129 * K and acc[0, 1] == -16129 * K
     assert np.array_equal(acc, ref)
     # near 2^24 inside one chunk: values that a 24-bit accumulator would round
-    Xq2 = torch.full((128, 1024), 127, dtype=torch.int8)
+    Xq2 = torch.full((M, 1024), 127, dtype=torch.int8)
     Wq2 = torch.full((256, 1024), 127, dtype=torch.int8)
     Wq2[:, :7] = torch.arange(1, 8, dtype=torch.int8)  # odd offsets from the all-127 sum
     ref2 = oracle.gemm_s32(Xq2.numpy(), Wq2.numpy())
@@ -245,7 +271,7 @@ def test_pack_weight_is_exact_image(w8a8):
 
 
 @pytest.mark.parametrize("M,N,K,bias", [(64, 128, 256, True), (300, 520, 1040, True), (2048, 4096, 1024, False),
-                                        (77, 3072, 5120, True)])
+                                        (77, 3072, 5120, True), (5, 4096, 4096, False)])
 def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=40 + M, outliers=0.01, oscale=20.0)
     W = rand_bf16((N, K), seed=41 + N, scale=0.02)

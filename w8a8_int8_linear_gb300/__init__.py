@@ -42,7 +42,7 @@ SIGNATURES = [
     ("w8a8_gemm_postscale", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_pack_weight", _I32, [_P, _I64, _I64, _P, _P]),
-    ("w8a8_linear_workspace_size", _SZ, [_I64, _I64]),
+    ("w8a8_linear_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w8a8_linear_postscale", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_linear_blockwise", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_gemm_postscale_noalloc", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -258,8 +258,8 @@ def pack_weight(Wq):
     return Wimg
 
 
-def linear_workspace_size(M, K):
-    return int(lib().w8a8_linear_workspace_size(M, K))
+def linear_workspace_size(M, N, K):
+    return int(lib().w8a8_linear_workspace_size(M, N, K))
 
 
 def _linear(fn, mode, X, Wimg, sw, bias, out, workspace, sx_out, codes):
@@ -280,7 +280,7 @@ def _linear(fn, mode, X, Wimg, sw, bias, out, workspace, sx_out, codes):
         Xq = codes
     ws = workspace
     if ws is None:
-        ws = torch.empty(max(linear_workspace_size(M, K), 256), dtype=torch.uint8, device=X.device)
+        ws = torch.empty(max(linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=X.device)
     _check(fn, getattr(lib(), fn)(_ptr(X), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K, _ptr(sx_out), _ptr(Xq),
                                   _ptr(ws), ws.numel(), _stream()))
     return Y, sx_out, Xq

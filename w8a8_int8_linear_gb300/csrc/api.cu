@@ -129,8 +129,8 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
 
 // GEMM on bf16 operand images, with the timing hook around the launch.
 w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float* sx, const float* sw,
-                            const void* bias, void* out, int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
-                            cudaStream_t st) {
+                            const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* partial,
+                            const DeviceInfo& dev, cudaStream_t st) {
     void* enc = encode_fn();
     if (!enc) return W8A8_ERR_CUDA;
     w8a8::GemmArgs a;
@@ -141,6 +141,7 @@ w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float
     a.M = M;
     a.N = N;
     a.K = K;
+    a.partial = static_cast<int32_t*>(partial);
     cudaError_t e;
     if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
     e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
@@ -165,15 +166,16 @@ w8a8_status run_linear(bool block, const void* X, const void* Wimg, const float*
     if (!aligned16(X) || !aligned16(Wimg) || !aligned16(sw) || !aligned16(Y) || !aligned16(sx) ||
         (Xq && !aligned16(Xq)) || (bias && !aligned16(bias)))
         return W8A8_ERR_ALIGNMENT;
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w8a8_linear_workspace_size(M, K))
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w8a8_linear_workspace_size(M, N, K))
         return W8A8_ERR_WORKSPACE;
     DeviceInfo dev;
     if ((s = current_device(&dev)) != W8A8_OK) return s;
     cudaError_t e = block ? w8a8::launch_quant_act_block(X, M, K, Xq, ws, sx, dev.num_sms, st)
                           : w8a8::launch_quant_rows(X, M, K, Xq, ws, sx, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
+    void* partial = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K * 2);
     return run_gemm_images(block ? w8a8::kEpiBlockwiseBf16 : w8a8::kEpiPostscaleBf16, ws, Wimg, sx, sw, bias, Y, M,
-                           N, K, dev, st);
+                           N, K, partial, dev, st);
 }
 
 w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
@@ -184,11 +186,12 @@ w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* W
     uint8_t* w = static_cast<uint8_t*>(ws);
     void* Ab = w;
     void* Bb = w + align256(static_cast<size_t>(M) * K * 2);
+    void* partial = static_cast<uint8_t*>(Bb) + align256(static_cast<size_t>(N) * K * 2);
     cudaError_t e = w8a8::launch_expand_s8_bf16(Xq, M * K, Ab, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("expand Xq launch", e);
     e = w8a8::launch_expand_s8_bf16(Wq, N * K, Bb, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("expand Wq launch", e);
-    return run_gemm_images(epi, Ab, Bb, sx, sw, bias, out, M, N, K, dev, st);
+    return run_gemm_images(epi, Ab, Bb, sx, sw, bias, out, M, N, K, partial, dev, st);
 }
 
 // Scratch of the allocation-free GEMM entry point: a fixed device array,
@@ -290,9 +293,9 @@ w8a8_status w8a8_pack_weight(const int8_t* Wq, int64_t N, int64_t K, void* Wimg,
     return from_cuda(w8a8::launch_expand_s8_bf16(Wq, N * K, Wimg, dev.num_sms, static_cast<cudaStream_t>(stream)));
 }
 
-size_t w8a8_linear_workspace_size(int64_t M, int64_t K) {
-    if (M <= 0 || K <= 0) return 0;
-    return align256(static_cast<size_t>(M) * K * 2);
+size_t w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return align256(static_cast<size_t>(M) * K * 2) + align256(w8a8::splitk_partial_bytes(M, N, K));
 }
 
 w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, const float* sw, const void* bias, void* Y,
@@ -311,7 +314,8 @@ w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, const float* 
 
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2);
+    return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2) +
+           align256(w8a8::splitk_partial_bytes(M, N, K));
 }
 
 w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,

@@ -75,6 +75,10 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int POSTSCALE_CHUNK_STAGES = 16;  // 1024 K: 127*127*1024 < 2^24
 constexpr int BLOCK_CHUNK_STAGES = 2;       // one 128-wide scale block
 constexpr int GROUP_M = 8;                  // tile raster: bands of 8 row tiles (2048 rows)
+constexpr int kSwapMaxTokens = 256;         // post-scale GEMMs with M <= this swap operands
+constexpr int kSplitTargetUnits = 72;       // split K until about this many CTA-pair work units exist
+constexpr int kSplitMinStages = 4;          // at least 256 K per split
+constexpr int kSplitMax = 8;
 
 // Per-tile-width constants.
 template <int BN_>
@@ -109,6 +113,9 @@ struct KParams {
     int num_m, num_n, num_tiles;
     int k_stages, chunk_stages, kb_count;
     int tma_store;  // bf16 output written through shared memory and TMA (needs N % 8 == 0)
+    int k_split;    // work units per tile, each over split_stages K stages (1: no split)
+    int split_stages;
+    int32_t* partial;  // k_split > 1: int32 partial sums [k_split][N][M] in kernel dims
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
@@ -119,6 +126,21 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
     const int local = tile - group * per_group;
     mb = first_m + local % gm;
     nb = local / gm;
+}
+
+// One work unit: a tile and the K stages [ks0, ks1) it accumulates.
+struct Unit {
+    int mb, nb, split, ks0, ks1;
+};
+
+__device__ __forceinline__ Unit unit_coords(int u, const KParams& p) {
+    Unit w;
+    const int tile = u / p.k_split;
+    w.split = u - tile * p.k_split;
+    tile_coords(tile, p.num_m, p.num_n, w.mb, w.nb);
+    w.ks0 = w.split * p.split_stages;
+    w.ks1 = min(p.k_stages, w.ks0 + p.split_stages);
+    return w;
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
@@ -336,7 +358,83 @@ __device__ __forceinline__ void store_rows_tma(const typename AccType<EPI>::T (&
     }
 }
 
-template <int EPI, int BN>
+// Split K (swapped operands only): this unit's exact int32 partial sums, for
+// output column n = kernel row and COLS tokens, into slice `split` of the
+// partial buffer [k_split][tokens][N]; lanes write consecutive n.
+template <int COLS>
+__device__ __forceinline__ void store_partial(const int32_t (&acc)[COLS], const KParams& p, int n_base, int tok0,
+                                              int split, int lane) {
+    const int n = n_base + lane;
+    const int Nout = p.M, Mtok = p.N;
+    if (n >= Nout) return;
+    int32_t* dst = p.partial + (static_cast<int64_t>(split) * Mtok + tok0) * Nout + n;
+#pragma unroll
+    for (int e = 0; e < COLS; ++e)
+        if (tok0 + e < Mtok) dst[static_cast<int64_t>(e) * Nout] = acc[e];
+}
+
+// Swapped operands (few tokens): the kernel's rows are weight rows n and its
+// columns are tokens m, so this thread holds output column n for COLS tokens.
+// y = ((float(acc) * sx[m]) * sw[n]) + bias[n], the same operations in the
+// same order as the unswapped epilogue.  bf16 output goes through shared
+// memory as [16 tokens x 32 columns] boxes (one 2-byte value per lane per
+// token row) and a TMA store into Y[m][n]; the int32 export and rows of N not
+// a multiple of 8 use direct stores.
+template <int EPI, int COLS>
+__device__ __forceinline__ void store_swapped(const int32_t (&acc)[COLS], const KParams& p, const CUtensorMap* tmY,
+                                              int n_base, int tok0, uint8_t* stg, int& sbuf, int lane) {
+    const int n = n_base + lane;       // output column (kernel row)
+    const int Nout = p.M, Mtok = p.N;  // kernel dims: rows = weights, columns = tokens
+    if constexpr (EPI == kEpiPostscaleS32) {
+        if (n < Nout) {
+#pragma unroll
+            for (int e = 0; e < COLS; ++e)
+                if (tok0 + e < Mtok) static_cast<int32_t*>(p.out)[static_cast<int64_t>(tok0 + e) * Nout + n] = acc[e];
+        }
+        return;
+    } else {
+        const float swn = (n < Nout) ? __ldg(p.sw + n) : 0.0f;
+        const float bn = (p.bias && n < Nout) ? bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(p.bias) + n))
+                                              : 0.0f;
+#pragma unroll
+        for (int g = 0; g < COLS; g += 16) {
+            const int t0 = tok0 + g;
+            if (t0 >= Mtok) break;
+            float sxt[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sxt[e] = (t0 + e < Mtok) ? __ldg(p.sx + t0 + e) : 0.0f;
+            uint16_t y[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float v = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sxt[e]), swn);
+                if (p.bias) v = __fadd_rn(v, bn);
+                __nv_bfloat16 h = __float2bfloat16_rn(v);
+                y[e] = *reinterpret_cast<uint16_t*>(&h);
+            }
+            if (p.tma_store) {
+                uint8_t* buf = stg + sbuf * STAGE_OUT_BYTES;
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) *reinterpret_cast<uint16_t*>(buf + e * 64 + lane * 2) = y[e];
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmY, buf, n_base, t0);
+                    bulk_commit_group();
+                }
+                sbuf ^= 1;
+            } else if (n < Nout) {
+                uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (t0 + e < Mtok) out[static_cast<int64_t>(t0 + e) * Nout + n] = y[e];
+            }
+        }
+    }
+}
+
+template <int EPI, int BN, bool SWAP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const KParams p) {
@@ -391,7 +489,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // reads global memory before that kernel has completed.
     grid_dependency_wait();
     const uint32_t tmem_base = *tmem_slot;
-    const int nchunks = (p.k_stages + p.chunk_stages - 1) / p.chunk_stages;
     if (warp < EPI_WARP0) {
       regs_dec<REGS_LOW>();
       if (warp == 0) {
@@ -401,12 +498,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0;
             uint32_t armed = 0, armed_phase = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
-                int mb, nb;
-                tile_coords(tile, p.num_m, p.num_n, mb, nb);
-                const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
-                const int b_row = nb * BN + static_cast<int>(rank) * HALF;
-                for (int ks = 0; ks < p.k_stages; ++ks) {
+            for (int u = cluster; ok && u < p.num_tiles; u += nclusters) {
+                const Unit w = unit_coords(u, p);
+                const int a_row = w.mb * TILE_M + static_cast<int>(rank) * BM;
+                const int b_row = w.nb * BN + static_cast<int>(rank) * HALF;
+                for (int ks = w.ks0; ks < w.ks1; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -436,7 +532,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
+            for (int u = cluster; ok && u < p.num_tiles; u += nclusters) {
+                const Unit w = unit_coords(u, p);
+                const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
                 for (int c = 0; ok && c < nchunks; ++c) {
                     if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteMmaAccEmpty)) {
                         ok = false;
@@ -444,8 +542,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                    const int s0 = c * p.chunk_stages;
-                    const int s1 = min(p.k_stages, s0 + p.chunk_stages);
+                    const int s0 = w.ks0 + c * p.chunk_stages;
+                    const int s1 = min(w.ks1, s0 + p.chunk_stages);
                     for (int ks = s0; ks < s1; ++ks) {
                         if (!mbar_wait(&full[stage], phase, kSiteMmaFull)) {
                             ok = false;
@@ -482,6 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         constexpr bool kBlock = (EPI == kEpiBlockwiseBf16 || EPI == kEpiBlockwiseF32);
         static_assert(!kBlock || HALF == 128, "blockwise needs each warp's columns inside one 128-wide block");
+        static_assert(!(kBlock && SWAP), "swapped operands are for the post-scale GEMM only");
         using T = typename AccType<EPI>::T;
         constexpr int LDW = C::LDW;
         constexpr int GROUPS = C::GROUPS;
@@ -494,9 +593,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
-        for (int tile = cluster; ok && tile < p.num_tiles; tile += nclusters) {
-            int mb, nb;
-            tile_coords(tile, p.num_m, p.num_n, mb, nb);
+        for (int u = cluster; ok && u < p.num_tiles; u += nclusters) {
+            const Unit w = unit_coords(u, p);
+            const int mb = w.mb, nb = w.nb;
+            const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
             const int row_base = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
             const int row = row_base + lane;
             const int col0 = nb * BN + half * HALF;
@@ -560,10 +660,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (buf == 0) buf_phase ^= 1u;
             }
             if (!ok) break;
-            if (kBf16Out && p.tma_store)
+            if constexpr (SWAP) {
+                if constexpr (!kBlock) {
+                    if (p.k_split > 1)
+                        store_partial<HALF>(acc, p, row_base, col0, w.split, lane);
+                    else
+                        store_swapped<EPI, HALF>(acc, p, &tmY, row_base, col0, stg, sbuf, lane);
+                }
+            } else if (kBf16Out && p.tma_store) {
                 store_rows_tma<EPI, HALF>(acc, p, &tmY, row, row_base, col0, stg, sbuf, lane);
-            else
+            } else {
                 store_row<EPI, HALF>(acc, p, row, col0);
+            }
         }
         if (lane == 0) bulk_wait_group_all();  // this warp's output stores have completed
         __syncwarp();
@@ -575,6 +683,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+// Split K, last step: Y[m][n] from the sum of the k_split int32 partials of
+// output (m, n) -- integer additions, exact in any order -- then the
+// post-scale epilogue in the unsplit kernel's operation order.  Launched as a
+// programmatic dependent of the GEMM; one thread per output, lanes along n.
+template <int EPI>
+__global__ void __launch_bounds__(256) splitk_finalize_kernel(const int32_t* __restrict__ partial, int k_split,
+                                                              int M, int N, const float* __restrict__ sx,
+                                                              const float* __restrict__ sw,
+                                                              const __nv_bfloat16* __restrict__ bias,
+                                                              void* __restrict__ out) {
+    grid_dependency_wait();
+    const int64_t total = static_cast<int64_t>(M) * N;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        int32_t acc = 0;
+        for (int s = 0; s < k_split; ++s) acc += __ldcs(partial + s * total + i);
+        if constexpr (EPI == kEpiPostscaleS32) {
+            static_cast<int32_t*>(out)[i] = acc;
+        } else {
+            const int m = static_cast<int>(i / N);
+            const int n = static_cast<int>(i - static_cast<int64_t>(m) * N);
+            float v = __fmul_rn(__fmul_rn(__int2float_rn(acc), __ldg(sx + m)), __ldg(sw + n));
+            if (bias) v = __fadd_rn(v, bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(bias) + n)));
+            static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+        }
     }
 }
 
@@ -592,18 +728,22 @@ CUresult make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map, co
 // Per device: whether each kernel instance has its shared-memory attribute set,
 // and how many CTA pairs of the GEMM kernel fit at once.
 struct DeviceLaunchInfo {
-    bool configured[8];
+    bool configured[32];
     int max_clusters;
 };
 DeviceLaunchInfo g_launch_info[64];
 
-template <int EPI, int BN>
+template <int EPI, int BN, bool SWAP>
 constexpr int instance_id() {
-    return (EPI == kEpiPostscaleBf16 ? 0 : EPI == kEpiPostscaleS32 ? 3 : EPI == kEpiBlockwiseBf16 ? 6 : 7) +
-           (BN == 256 ? 0 : BN == 224 ? 1 : 2);
+    return (EPI == kEpiPostscaleBf16 ? 0 : EPI == kEpiPostscaleS32 ? 8 : EPI == kEpiBlockwiseBf16 ? 16 : 17) +
+           (SWAP ? 4 : 0) +
+           (BN == 256 ? 0 : BN == 224 ? 1 : BN == 192 ? 2 : BN == 128 ? 1 : BN == 64 ? 2 : 3);
 }
 
-template <int EPI, int BN>
+// Launch one kernel instance.  Ab / Bb are the operand images of the kernel's
+// rows and columns; p.M / p.N are the kernel's dimensions (with SWAP the rows
+// are weight rows and the columns tokens, and Y is written transposed).
+template <int EPI, int BN, bool SWAP>
 cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
                        int num_sms, cudaStream_t st, char* detail, size_t n) {
     using C = Cfg<BN>;
@@ -620,15 +760,17 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     }
     CUtensorMap tmY = tmB;  // placeholder when the output is not written through TMA
     constexpr bool kBf16Out = (EPI == kEpiPostscaleBf16 || EPI == kEpiBlockwiseBf16);
-    p.tma_store = (kBf16Out && (p.N % 8) == 0) ? 1 : 0;
+    const int y_cols = SWAP ? p.M : p.N;  // Y is [tokens, output columns]
+    const int y_rows = SWAP ? p.N : p.M;
+    p.tma_store = (kBf16Out && (y_cols % 8) == 0) ? 1 : 0;
     if (p.tma_store) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 2};
-        cuuint32_t box[2] = {16, 32};
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(y_cols), static_cast<cuuint64_t>(y_rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(y_cols) * 2};
+        cuuint32_t box[2] = {SWAP ? 32u : 16u, SWAP ? 16u : 32u};
         cuuint32_t estr[2] = {1, 1};
         r = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, SWAP ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_32B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) {
             snprintf(detail, n, "cuTensorMapEncodeTiled(Y: %d x %d) returned %d", p.M, p.N, (int)r);
             return cudaErrorInvalidValue;
@@ -636,7 +778,7 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     }
     p.num_m = (p.M + TILE_M - 1) / TILE_M;
     p.num_n = (p.N + BN - 1) / BN;
-    p.num_tiles = p.num_m * p.num_n;
+    p.num_tiles = p.num_m * p.num_n * p.k_split;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -656,15 +798,15 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
-    constexpr int id = instance_id<EPI, BN>();
+    constexpr int id = instance_id<EPI, BN, SWAP>();
     if (!info.configured[id]) {
-        e = cudaFuncSetAttribute(gemm_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemm_kernel<EPI, BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::SMEM));
         if (e != cudaSuccess) return e;
         if (info.max_clusters == 0) {
             cfg.gridDim = dim3(2 * (num_sms / 2));
             int nc = 0;
-            e = cudaOccupancyMaxActiveClusters(&nc, gemm_kernel<EPI, BN>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&nc, gemm_kernel<EPI, BN, SWAP>, &cfg);
             if (e != cudaSuccess) return e;
             if (nc < 1) {
                 snprintf(detail, n, "no CTA pair of the GEMM kernel fits on this device");
@@ -677,7 +819,7 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
     const int clusters = p.num_tiles < info.max_clusters ? p.num_tiles : info.max_clusters;
     cfg.gridDim = dim3(2 * clusters);
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, BN>, tmA, tmB, tmY, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, BN, SWAP>, tmA, tmB, tmY, p);
 }
 
 // Tile width for the post-scale GEMM: the candidate minimizing
@@ -704,13 +846,65 @@ template <int EPI>
 cudaError_t launch_bn(int bn, const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode,
                       const KParams& p, int num_sms, cudaStream_t st, char* detail, size_t n) {
     switch (bn) {
-        case 224: return launch_one<EPI, 224>(Ab, Bb, encode, p, num_sms, st, detail, n);
-        case 192: return launch_one<EPI, 192>(Ab, Bb, encode, p, num_sms, st, detail, n);
-        default: return launch_one<EPI, 256>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        case 224: return launch_one<EPI, 224, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        case 192: return launch_one<EPI, 192, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        default: return launch_one<EPI, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
     }
 }
 
+// Few tokens (M <= 256): weights take the 256-row side of the CTA-pair MMA and
+// the tokens its N side (the narrowest of 32 / 64 / 128 / 256 that holds them).
+template <int EPI>
+cudaError_t launch_swapped(const void* Ximg, const void* Wimg, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
+                           int num_sms, cudaStream_t st, char* detail, size_t n) {
+    const int tokens = p.M;
+    p.M = p.N;  // kernel rows: weight rows
+    p.N = tokens;
+    if (tokens <= 32) return launch_one<EPI, 32, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
+    if (tokens <= 64) return launch_one<EPI, 64, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
+    if (tokens <= 128) return launch_one<EPI, 128, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
+    return launch_one<EPI, 256, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
+}
+
+template <int EPI>
+cudaError_t launch_finalize(const KParams& p, const GemmArgs& a, int num_sms, cudaStream_t st) {
+    const int64_t total = a.M * a.N;
+    int64_t grid = (total + 255) / 256;
+    if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_finalize_kernel<EPI>, static_cast<const int32_t*>(p.partial), p.k_split,
+                              static_cast<int>(a.M), static_cast<int>(a.N), a.sx, a.sw,
+                              static_cast<const __nv_bfloat16*>(a.bias), a.out);
+}
+
 }  // namespace
+
+int splitk_plan(bool blockwise, int64_t M, int64_t N, int64_t K, int* split_stages) {
+    const int64_t k_stages = (K + BK - 1) / BK;
+    if (split_stages) *split_stages = static_cast<int>(k_stages);
+    if (blockwise || M <= 0 || M > kSwapMaxTokens || N <= 0 || K <= 0) return 1;
+    const int64_t tiles = (N + TILE_M - 1) / TILE_M;
+    int64_t s = kSplitTargetUnits / tiles;
+    if (s > k_stages / kSplitMinStages) s = k_stages / kSplitMinStages;
+    if (s > kSplitMax) s = kSplitMax;
+    if (s < 2) return 1;
+    const int64_t per = (k_stages + s - 1) / s;  // stages per split; no split is left empty
+    if (split_stages) *split_stages = static_cast<int>(per);
+    return static_cast<int>((k_stages + per - 1) / per);
+}
+
+size_t splitk_partial_bytes(int64_t M, int64_t N, int64_t K) {
+    const int s = splitk_plan(false, M, N, K, nullptr);
+    return s > 1 ? static_cast<size_t>(s) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4 : 0;
+}
 
 cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const GemmArgs& a, int num_sms,
                         void* encode_fn, cudaStream_t st, char* detail, size_t n) {
@@ -728,17 +922,45 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     const bool blockwise = epilogue == kEpiBlockwiseBf16 || epilogue == kEpiBlockwiseF32;
     p.chunk_stages = blockwise ? BLOCK_CHUNK_STAGES : POSTSCALE_CHUNK_STAGES;
     p.kb_count = static_cast<int>(a.K / 128);
+    const bool swap = !blockwise && a.M <= kSwapMaxTokens;
+    p.k_split = 1;
+    p.split_stages = p.k_stages;
+    p.partial = nullptr;
+    if (swap) {
+        int per = 0;
+        const int ks = splitk_plan(false, a.M, a.N, a.K, &per);
+        if (ks > 1) {
+            if (!a.partial) {
+                snprintf(detail, n, "split-K GEMM without a partial-sum buffer");
+                return cudaErrorInvalidValue;
+            }
+            p.k_split = ks;
+            p.split_stages = per;
+            p.partial = a.partial;
+        }
+    }
     const int bn = blockwise ? 256 : choose_bn(a.M, a.N, num_sms / 2);
     cudaError_t e;
     switch (epilogue) {
-        case kEpiPostscaleBf16: e = launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n); break;
-        case kEpiPostscaleS32: e = launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n); break;
-        case kEpiBlockwiseBf16:
-            e = launch_one<kEpiBlockwiseBf16, 256>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        case kEpiPostscaleBf16:
+            e = swap ? launch_swapped<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                     : launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
             break;
-        case kEpiBlockwiseF32: e = launch_one<kEpiBlockwiseF32, 256>(Ab, Bb, encode, p, num_sms, st, detail, n); break;
+        case kEpiPostscaleS32:
+            e = swap ? launch_swapped<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                     : launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
+            break;
+        case kEpiBlockwiseBf16:
+            e = launch_one<kEpiBlockwiseBf16, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
+            break;
+        case kEpiBlockwiseF32:
+            e = launch_one<kEpiBlockwiseF32, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
+            break;
         default: e = cudaErrorInvalidValue;
     }
+    if (e == cudaSuccess && p.k_split > 1)
+        e = epilogue == kEpiPostscaleS32 ? launch_finalize<kEpiPostscaleS32>(p, a, num_sms, st)
+                                         : launch_finalize<kEpiPostscaleBf16>(p, a, num_sms, st);
     if (e != cudaSuccess && n && detail[0] == 0)
         snprintf(detail, n, "GEMM launch (%d threads, clusters of 2, tile width %d): %s", THREADS, bn,
                  cudaGetErrorString(e));

@@ -35,7 +35,14 @@ struct GemmArgs {
     const void* bias;  // bf16 [N] or nullptr
     void* out;         // Y bf16 / acc int32 / acc fp32, [M,N]
     int64_t M, N, K;
+    int32_t* partial;  // split-K partial sums, splitk_partial_bytes(M,N,K) bytes (unused when that is 0)
 };
+
+// Split K for few-token post-scale GEMMs: the number of K splits (1: none)
+// and, through split_stages, the 64-wide K stages each split covers.
+int splitk_plan(bool blockwise, int64_t M, int64_t N, int64_t K, int* split_stages);
+// Bytes of int32 partial sums a post-scale GEMM of this shape needs (0 without split).
+size_t splitk_partial_bytes(int64_t M, int64_t N, int64_t K);
 
 // Tensor-core GEMM on the bf16 images (Ab [M,K], Bb [N,K]) of the int8
 // operands.  `encode` is the driver's cuTensorMapEncodeTiled.

@@ -60,7 +60,7 @@ constexpr float kMinNormal = 1.17549435e-38f;  // 2^-126
 // fl(M / 127) and fl(1 / fl(M / 127)) for M = 128 + i, i in [0, 128): built
 // at compile time (the host compiler folds IEEE single-precision division
 // with round to nearest) and placed in device global memory, where the
-// per-row or per-block lookups hit L1.
+// per-block lookups of the 1x128 and 128x128 kernels hit L1.
 struct ScaleTables {
     float T[128];
     float R[128];
@@ -76,6 +76,17 @@ constexpr ScaleTables make_scale_tables() {
 }
 
 __device__ const ScaleTables kScaleTables = make_scale_tables();
+
+// The scale of one row by IEEE division, once per row: the same values as
+// the table path below (s = fl(amax / 127); 1/s scales by powers of two
+// exactly), without a memory access in the row kernels' dependency chain.
+__device__ __forceinline__ RowScale make_scale_div(float amax) {
+    RowScale r;
+    r.s = __fdiv_rn(amax, kQMax);
+    r.inv = (r.s > 0.0f) ? __frcp_rn(r.s) : 0.0f;
+    r.exact = r.s > 0.0f && r.s < kMinNormal;
+    return r;
+}
 
 __device__ __forceinline__ RowScale make_scale(float amax, const ScaleTables& t = kScaleTables) {
     RowScale r;
@@ -243,7 +254,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
         }
     }
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax);
+    const RowScale sc = make_scale_div(amax);
     if (threadIdx.x == 0) s[row] = sc.s;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
@@ -280,7 +291,7 @@ __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* _
         }
     }
     amax = warp_max(amax);
-    const RowScale sc = make_scale(amax);
+    const RowScale sc = make_scale_div(amax);
     if (lane == 0) s[row] = sc.s;
     for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
         uint4 v[U];
@@ -309,7 +320,7 @@ __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __re
     float amax = 0.0f;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) amax = fmaxf(amax, chunk_absmax(a[c]));
     amax = block_max(amax, red);
-    const RowScale sc = make_scale(amax);
+    const RowScale sc = make_scale_div(amax);
     if (threadIdx.x == 0) s[row] = sc.s;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x)
         put_codes(Aq, img, row * chunks + c, quant_chunk(__ldcs(a + c), sc));
@@ -412,20 +423,26 @@ __global__ void __launch_bounds__(256) expand_s8_bf16_kernel(const uint4* __rest
 
 cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, void* img, float* s, int num_sms,
                               cudaStream_t st) {
-    (void)num_sms;
     const int64_t chunks = K >> 3;
     const uint4* a = static_cast<const uint4*>(A);
     uint2* q = reinterpret_cast<uint2*>(Aq);
     uint4* im = static_cast<uint4*>(img);
     const dim3 grid(static_cast<unsigned>(R));
-    // one 128-thread CTA per row for rows of up to 512 chunks (K <= 4096),
-    // two-pass warp-per-row beyond
+    // One 128-thread CTA per row for rows of up to 512 chunks (K <= 4096).
+    // Longer rows: few of them (about one wave) still get a CTA each, 256
+    // threads with the row in registers, so the row is read once with every
+    // load in flight; many long rows go two-pass warp-per-row.
+    const bool few = R <= static_cast<int64_t>(num_sms) * 8;
     if (chunks <= 128)
         quant_rows_reg_kernel<1><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 256)
         quant_rows_reg_kernel<2><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 512)
         quant_rows_reg_kernel<4><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
+    else if (few && chunks <= 1024)
+        quant_rows_reg_kernel<4><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
+    else if (few && chunks <= 2048)
+        quant_rows_reg_kernel<8><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
     else if (chunks <= 16384)
         quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, im, s);
     else

@@ -43,7 +43,7 @@ class Int8Linear(torch.nn.Module):
         return cls(w, b, mode)
 
     def _workspace(self, M, device):
-        need = max(linear_workspace_size(M, self.in_features), 256)
+        need = max(linear_workspace_size(M, self.out_features, self.in_features), 256)
         if self._ws is None or self._ws.numel() < need or self._ws.device != device:
             self._ws = torch.empty(need, dtype=torch.uint8, device=device)
         return self._ws
