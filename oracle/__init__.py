@@ -51,6 +51,10 @@ def lib():
         L.orc_bf16_from_f32.restype = None
         L.orc_f32_from_bf16.argtypes = [P, I64, P]
         L.orc_f32_from_bf16.restype = None
+        L.orc_gelu_f32.argtypes = [P, I64, P]
+        L.orc_gelu_f32.restype = None
+        L.orc_gelu_bf16.argtypes = [P, I64, P]
+        L.orc_gelu_bf16.restype = None
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         L.orc_set_num_threads.restype = None
@@ -178,6 +182,37 @@ def linear_blockwise(X, W, bias=None):
     acc = gemm_blockwise_f32(Xq, sx, Wq, sw)
     Y = epilogue_blockwise(acc, bias)
     return dict(Xq=Xq, sx=sx, Wq=Wq, sw=sw, acc=acc, Y=Y)
+
+
+def gelu_f32(x):
+    """GELU (erf form, erf by Abramowitz & Stegun 7.1.28) of fp32 values, in
+    the fixed binary32 operation order stated in w8a8_oracle.c."""
+    x = _c(x, np.float32)
+    g = np.empty_like(x)
+    lib().orc_gelu_f32(_p(x), x.size, _p(g))
+    return g
+
+
+def gelu_bf16(Y):
+    """bf16(gelu(Y)) for bf16 Y given as uint16 bit patterns."""
+    Y = _c(Y, np.uint16)
+    G = np.empty_like(Y)
+    lib().orc_gelu_bf16(_p(Y), Y.size, _p(G))
+    return G
+
+
+def ffn_up_gelu_quant(X, W, bias=None):
+    """FFN up-projection as the down-projection consumes it: the post-scale
+    W8A8 Linear Y = linear_postscale(X, W, bias), G = bf16(gelu(Y)), then
+    G quantized in 1x128 blocks.  N must be a multiple of 128.
+
+    Returns linear_postscale's dict plus G (bf16 bits), Gq int8 [M,N] and
+    sg fp32 [M, N/128]."""
+    r = linear_postscale(X, W, bias)
+    G = gelu_bf16(r["Y"])
+    Gq, sg = quantize_act(G, BLOCK)
+    r.update(G=G, Gq=Gq, sg=sg)
+    return r
 
 
 def linear_sampled(X, W, bias, rows, cols, mode=PER_ROW):

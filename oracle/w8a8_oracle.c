@@ -246,3 +246,55 @@ void orc_epilogue_blockwise(const float* acc, const uint16_t* bias, int64_t M, i
             Y[m * N + n] = orc_f32_to_bf16(y);
         }
 }
+
+/* ------------------------------------------------------------------------
+ * FFN up-projection activation: GELU, then 1x128 quantization of its output.
+ *
+ * The pages tune the post-scale kernel for "LTX FFN shapes" ("TurboDiffusion
+ * Integration Notes", section "Differences From TurboDiffusion") and name no
+ * activation.  Reading taken: the FFN's activation is GELU in its erf form,
+ * gelu(x) = x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2, applied to the
+ * bf16 output of the up-projection, rounded back to bf16, and that tensor is
+ * what the down-projection quantizes in 1x128 blocks.
+ *
+ * erf comes from Abramowitz & Stegun, Handbook of Mathematical Functions,
+ * formula 7.1.28: for z >= 0, erf(z) = 1 - p(z)^-16 with
+ * p(z) = 1 + a1 z + a2 z^2 + ... + a6 z^6 and |error| <= 3e-7.  So for
+ * z = |x| / sqrt 2, Phi(-|x|) = p(z)^-16 / 2 and Phi(|x|) = 1 - p(z)^-16 / 2.
+ * Evaluated in binary32, each operation rounded on its own, in exactly this
+ * order (so that any implementation following it gets the same bits):
+ *   z = |x| * 0.70710677;  t = a6; then for a5, a4, a3, a2, a1: t = t * z + a_i;
+ *   t = t * z + 1;  t2 = t*t; t4 = t2*t2; t8 = t4*t4; t16 = t8*t8;
+ *   e = 1 / t16;  h = 0.5 * e;  phi = (x >= 0) ? 1 - h : h;  g = x * phi.
+ * ------------------------------------------------------------------------ */
+static float orc_gelu(float x) {
+    const float a1 = 0.0705230784f, a2 = 0.0422820123f, a3 = 0.0092705272f;
+    const float a4 = 0.0001520143f, a5 = 0.0002765672f, a6 = 0.0000430638f;
+    const float z = fabsf(x) * 0.70710678118654752f;
+    float t = a6;
+    t = t * z; t = t + a5;
+    t = t * z; t = t + a4;
+    t = t * z; t = t + a3;
+    t = t * z; t = t + a2;
+    t = t * z; t = t + a1;
+    t = t * z; t = t + 1.0f;
+    float t2 = t * t;
+    float t4 = t2 * t2;
+    float t8 = t4 * t4;
+    float t16 = t8 * t8;
+    float e = 1.0f / t16;
+    float h = 0.5f * e;
+    float phi = (x >= 0.0f) ? 1.0f - h : h;
+    return x * phi;
+}
+
+/* g[i] = gelu(x[i]) in binary32 (for the accuracy checks of the formula). */
+void orc_gelu_f32(const float* x, int64_t n, float* g) {
+    for (int64_t i = 0; i < n; ++i) g[i] = orc_gelu(x[i]);
+}
+
+/* G = bf16(gelu(Y)) for bf16 Y (bit patterns in, bit patterns out). */
+void orc_gelu_bf16(const uint16_t* y, int64_t n, uint16_t* g) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) g[i] = orc_f32_to_bf16(orc_gelu(orc_bf16_to_f32(y[i])));
+}

@@ -359,3 +359,88 @@ def test_sampled_matches_full(oracle, mode):
     Y, acc = oracle.linear_sampled(X, W, b, rows, cols, md)
     assert np.array_equal(Y, full["Y"][np.ix_(rows, cols)])
     assert np.array_equal(acc, full["acc"][np.ix_(rows, cols)])
+
+
+# ----------------------------------------------------------------- GELU of the FFN up-projection
+def _bf16_all(lo, hi):
+    """Every finite bf16 value in [lo, hi] as (float32 array, uint16 bits)."""
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    keep = np.isfinite(vals) & (vals >= lo) & (vals <= hi)
+    return vals[keep], bits[keep]
+
+
+def test_gelu_within_erf_bound(oracle):
+    """Against x * (1 + erf(x / sqrt 2)) / 2 in fp64 (math.erf): Abramowitz &
+    Stegun 7.1.28 is within 3e-7 of erf, i.e. 1.5e-7 of Phi; the binary32
+    evaluation adds at most about 16 * 2^-24 relative in t^16, so
+    |g - gelu(x)| <= 1e-6 |x| + 2^-24 |g|.  A wrong coefficient, sign or
+    branch is off by far more."""
+    import math
+    rng = np.random.default_rng(5)
+    x = np.concatenate([np.linspace(-12, 12, 48001), rng.normal(0, 3, 20000),
+                        _bf16_all(-12, 12)[0]]).astype(np.float32)
+    g = oracle.gelu_f32(x).astype(np.float64)
+    xd = x.astype(np.float64)
+    exact = np.array([v * 0.5 * (1.0 + math.erf(v / math.sqrt(2.0))) for v in xd])
+    bound = 1e-6 * np.abs(xd) + 2.0 ** -24 * np.abs(exact)
+    assert np.all(np.abs(g - exact) <= bound)
+    # the error is not vacuous: it is the formula's, not zero
+    assert np.abs(g - exact).max() > 1e-9
+
+
+def test_gelu_matches_torch_bf16(oracle):
+    """bf16(gelu(x)) against torch.nn.functional.gelu (erf form) for every bf16
+    x with |x| <= 3: identical bits.  On 3 < |x| <= 4 at most 1 ulp apart.
+    (Below -5.5 torch's 1 + erf(x / sqrt 2) cancels to 0 while the formula
+    keeps the tail, so the two differ there by design.)"""
+    for lo, hi, max_ulp in ((-3.0, 3.0, 0), (-4.0, 4.0, 1)):
+        x, h = _bf16_all(lo, hi)
+        G = oracle.gelu_bf16(h)
+        T = torch.nn.functional.gelu(torch.from_numpy(x)).to(torch.bfloat16)
+        Tb = T.view(torch.int16).numpy().view(np.uint16)
+
+        def ordered(u):
+            u = u.astype(np.int64)
+            return np.where(u & 0x8000, 0x8000 - (u & 0x7FFF), u + 0x8000)
+        d = np.abs(ordered(G) - ordered(Tb))
+        assert d.max() <= max_ulp
+
+
+def test_gelu_special_values(oracle):
+    x = np.array([0.0, -0.0, 6.0, 7.5, 100.0, -100.0, -30.0], np.float32)
+    g = oracle.gelu_f32(x)
+    assert g[0] == 0 and not np.signbit(g[0])
+    assert g[1] == 0 and np.signbit(g[1])       # -0 * Phi keeps the sign
+    assert np.array_equal(g[2:5], x[2:5])       # Phi rounds to 1 in binary32
+    assert np.all(g[5:] <= 0) and np.all(g[5:] > -1e-30)
+    # Phi(x) + Phi(-x) = 1: g(x) - g(-x) = x up to the two roundings
+    rng = np.random.default_rng(6)
+    v = rng.normal(0, 2, 5000).astype(np.float32)
+    lhs = oracle.gelu_f32(v).astype(np.float64) - oracle.gelu_f32(-v).astype(np.float64)
+    assert np.all(np.abs(lhs - v) <= 2.0 ** -22 * np.abs(v))
+    # the minimum of gelu is about -0.17 near x = -0.75
+    xs = np.linspace(-3, 0, 30001).astype(np.float32)
+    gs = oracle.gelu_f32(xs)
+    assert abs(float(xs[np.argmin(gs)]) + 0.7518) < 2e-3 and abs(float(gs.min()) + 0.16997) < 1e-4
+
+
+def test_ffn_up_gelu_quant_composition(oracle):
+    """G is the GELU of the post-scale Linear's bf16 output, and (Gq, sg) its
+    1x128 quantization: sg = absmax(|G| of the block) / 127 exactly, and
+    Gq * sg reproduces G within half a step."""
+    rng = np.random.default_rng(7)
+    M, N, K = 5, 384, 256
+    X = oracle.bf16_from_f32(rng.normal(0, 1, (M, K)).astype(np.float32))
+    W = oracle.bf16_from_f32(rng.normal(0, 0.1, (N, K)).astype(np.float32))
+    b = oracle.bf16_from_f32(rng.normal(0, 0.5, N).astype(np.float32))
+    r = oracle.ffn_up_gelu_quant(X, W, b)
+    lin = oracle.linear_postscale(X, W, b)
+    assert np.array_equal(r["Y"], lin["Y"])
+    assert np.array_equal(r["G"], oracle.gelu_bf16(lin["Y"]))
+    G = oracle.f32_from_bf16(r["G"]).reshape(M, N // 128, 128)
+    amax = np.abs(G).max(axis=2)
+    assert np.array_equal(r["sg"], (amax / np.float32(127)).astype(np.float32))
+    deq = r["Gq"].reshape(M, N // 128, 128).astype(np.float64) * r["sg"][:, :, None].astype(np.float64)
+    assert np.all(np.abs(deq - G) <= 0.5 * r["sg"][:, :, None] * (1 + 1e-6))
+    assert np.abs(r["Gq"]).max() == 127
