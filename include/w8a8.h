@@ -188,6 +188,42 @@ W8A8_API w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, cons
                                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Fused FFN up-projection as the blockwise down-projection consumes it.  The
+ * pages tune the post-scale kernel for "LTX FFN shapes" ("Differences From
+ * TurboDiffusion") and name no activation; the FFN's activation is taken to
+ * be GELU in its erf form.  Computes, with the post-scale Linear of
+ * w8a8_linear_postscale:
+ *   y = bf16(((acc * sx) * sw) + bias),  g = bf16(gelu(y)),
+ *   sg[m][j] = absmax(|g[m, 128j .. 128j+127]|) / 127,
+ *   codes = clamp(rne(g / sg), -127, 127) per 1x128 block,
+ * and writes the exact bf16 image of the codes, which w8a8_gemm_blockwise_images
+ * takes as its activation operand (1x128 activation scales sg).  gelu(x) =
+ * x * Phi(x) with erf from Abramowitz & Stegun 7.1.28 (|error| <= 3e-7),
+ * evaluated in a fixed binary32 order; on every bf16 input with |x| <= 3 it
+ * equals torch's erf-form GELU rounded to bf16.
+ *   X [M,K] bf16, Wimg [N,K] bf16 image (w8a8_pack_weight), sw [N] fp32,
+ *   bias [N] bf16 or NULL, Gimg [M,N] bf16 out, sg [M][N/128] fp32 out,
+ *   sx [M] fp32 out, Xq [M,K] int8 out or NULL, workspace of
+ *   w8a8_linear_workspace_size(M,N,K) bytes, 256-byte aligned.
+ *   N % 128 == 0 (else W8A8_ERR_SHAPE).
+ */
+W8A8_API w8a8_status w8a8_linear_postscale_gelu_quant(const void* X, const void* Wimg, const float* sw,
+                                                      const void* bias, void* Gimg, float* sg, int64_t M, int64_t N,
+                                                      int64_t K, float* sx, int8_t* Xq, void* workspace,
+                                                      size_t workspace_bytes, void* stream);
+
+/*
+ * Blockwise GEMM on operand images: Ximg [M,K] and Wimg [N,K] are exact bf16
+ * images of int8 codes (from w8a8_linear_postscale_gelu_quant and
+ * w8a8_pack_weight), sx [M][K/128], sw [ceil(N/128)][K/128], bias [N] bf16 or
+ * NULL, Y [M,N] bf16 out.  Same arithmetic as w8a8_gemm_blockwise.  K % 128
+ * == 0.  Needs no workspace.
+ */
+W8A8_API w8a8_status w8a8_gemm_blockwise_images(const void* Ximg, const float* sx, const void* Wimg, const float* sw,
+                                                const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
+                                                void* stream);
+
+/*
  * Allocation-free variant of w8a8_gemm_postscale (the pages have no
  * counterpart: this is a library convenience).  Same arguments, results and
  * checks, minus the workspace: the scratch lives in a fixed 64 MiB device

@@ -333,3 +333,51 @@ def test_int8linear_module(w8a8, oracle, mode):
     ref = oracle.linear_postscale(X, W, b) if mode == "postscale" else oracle.linear_blockwise(X, W, b)
     d = assert_bf16_close(bits(y.reshape(15, 200)), ref["Y"], 1)
     assert d.max() == 0
+
+
+# ----------------------------------------------------------------- FFN up: GELU + 1x128 quantization epilogue
+@pytest.mark.parametrize("M,N,K,bias", [
+    (64, 256, 256, True),      # one tile
+    (5, 384, 512, True),       # few tokens (this epilogue never swaps operands)
+    (300, 640, 1040, True),    # ragged M, K not a multiple of 64
+    (1000, 1408, 2048, False),
+    (2100, 2560, 512, True),   # several tiles in both directions
+])
+def test_ffn_up_gelu_quant(w8a8, oracle, M, N, K, bias):
+    X = rand_bf16((M, K), seed=40 + M, outliers=0.01, oscale=20.0)
+    W = rand_bf16((N, K), seed=41 + N, scale=0.05)
+    b = rand_bf16((N,), seed=42, scale=0.5) if bias else None
+    tail_blocks = bias and N >= 384
+    if tail_blocks:
+        # blocks whose GELU output is tiny (y ~ -6) or exactly zero (y ~ -1000)
+        b[128:256] = -6.0
+        b[-128:] = -1000.0
+    ref = oracle.ffn_up_gelu_quant(bits(X), bits(W), None if b is None else bits(b))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV))
+    G, sg, sx, Xq = w8a8.linear_postscale_gelu_quant(X.to(DEV), w8a8.pack_weight(Wq), sw,
+                                                      None if b is None else b.to(DEV), codes=True)
+    assert np.array_equal(Xq.cpu().numpy(), ref["Xq"])
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), ref["sx"].view(np.uint32))
+    Gf = G.float().cpu()
+    assert torch.equal(Gf, Gf.round()) and Gf.abs().max() <= 127
+    assert np.array_equal(Gf.to(torch.int8).numpy(), ref["Gq"])
+    assert np.array_equal(sg.cpu().numpy().view(np.uint32), ref["sg"].view(np.uint32))
+    if tail_blocks:
+        assert np.all(ref["sg"][:, -1] == 0) and np.all(ref["sg"][:, 1] > 0)
+    assert w8a8.get_device_error() == (0, 0)
+    # the blockwise down-projection consumes the image and the 1x128 scales
+    N2 = 200
+    W2 = rand_bf16((N2, N), seed=43, scale=0.02)
+    Wq2, sw2 = w8a8.quantize_weight(W2.to(DEV), w8a8.BLOCK)
+    Y2 = w8a8.gemm_blockwise_images(G, sg, w8a8.pack_weight(Wq2), sw2)
+    oWq2, osw2 = oracle.quantize_weight(bits(W2), oracle.BLOCK)
+    acc2 = oracle.gemm_blockwise_f32(ref["Gq"], ref["sg"], oWq2, osw2)
+    d = assert_bf16_close(bits(Y2), oracle.epilogue_blockwise(acc2), 1)
+    assert d.max() == 0
+
+
+def test_ffn_up_gelu_quant_rejects_bad_arguments(w8a8):
+    X = torch.zeros((4, 64), dtype=torch.bfloat16, device=DEV)
+    Wimg = torch.zeros((200, 64), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):  # N not a multiple of 128
+        w8a8.linear_postscale_gelu_quant(X, Wimg, torch.ones(200, device=DEV))

@@ -45,6 +45,8 @@ SIGNATURES = [
     ("w8a8_linear_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w8a8_linear_postscale", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_linear_blockwise", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    ("w8a8_linear_postscale_gelu_quant", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    ("w8a8_gemm_blockwise_images", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_gemm_postscale_noalloc", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -296,6 +298,54 @@ def linear_postscale(X, Wimg, sw, bias=None, out=None, workspace=None, sx_out=No
 def linear_blockwise(X, Wimg, sw, bias=None, out=None, workspace=None, sx_out=None, codes=False):
     """Fused W8A8 Linear, blockwise (1x128 activation, 128x128 weight scales)."""
     return _linear("w8a8_linear_blockwise", BLOCK, X, Wimg, sw, bias, out, workspace, sx_out, codes)
+
+
+def linear_postscale_gelu_quant(X, Wimg, sw, bias=None, out=None, sg_out=None, workspace=None, sx_out=None,
+                                codes=False):
+    """Fused FFN up-projection: post-scale W8A8 Linear, GELU, then 1x128
+    quantization of the GELU output, which is returned as the exact bf16 image
+    of its codes.  N % 128 == 0.  Returns (Gimg [M,N] bf16, sg [M,N/128],
+    sx [M], Xq or None)."""
+    _need(X, torch.bfloat16, "X", 2)
+    _need(Wimg, torch.bfloat16, "Wimg", 2)
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = X.shape
+    N = Wimg.shape[0]
+    G = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    sg = sg_out if sg_out is not None else torch.empty((M, N // BLOCK_SIZE), dtype=torch.float32, device=X.device)
+    sx = sx_out if sx_out is not None else torch.empty((M,), dtype=torch.float32, device=X.device)
+    Xq = None
+    if codes is True:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    elif isinstance(codes, torch.Tensor):
+        Xq = codes
+    ws = workspace
+    if ws is None:
+        ws = torch.empty(max(linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=X.device)
+    _check("w8a8_linear_postscale_gelu_quant",
+           lib().w8a8_linear_postscale_gelu_quant(_ptr(X), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(G), _ptr(sg), M, N,
+                                                  K, _ptr(sx), _ptr(Xq), _ptr(ws), ws.numel(), _stream()))
+    return G, sg, sx, Xq
+
+
+def gemm_blockwise_images(Ximg, sx, Wimg, sw, bias=None, out=None):
+    """Blockwise GEMM on exact bf16 images of int8 codes (for example the
+    output of linear_postscale_gelu_quant and a packed weight)."""
+    _need(Ximg, torch.bfloat16, "Ximg", 2)
+    _need(Wimg, torch.bfloat16, "Wimg", 2)
+    _need(sx, torch.float32, "sx")
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = Ximg.shape
+    N = Wimg.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Ximg.device)
+    _check("w8a8_gemm_blockwise_images",
+           lib().w8a8_gemm_blockwise_images(_ptr(Ximg), _ptr(sx), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
+                                            _stream()))
+    return Y
 
 
 def get_device_error():

@@ -130,7 +130,7 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
 // GEMM on bf16 operand images, with the timing hook around the launch.
 w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float* sx, const float* sw,
                             const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* partial,
-                            const DeviceInfo& dev, cudaStream_t st) {
+                            const DeviceInfo& dev, cudaStream_t st, float* sg = nullptr) {
     void* enc = encode_fn();
     if (!enc) return W8A8_ERR_CUDA;
     w8a8::GemmArgs a;
@@ -142,6 +142,7 @@ w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float
     a.N = N;
     a.K = K;
     a.partial = static_cast<int32_t*>(partial);
+    a.sg = sg;
     cudaError_t e;
     if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
     e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
@@ -176,6 +177,29 @@ w8a8_status run_linear(bool block, const void* X, const void* Wimg, const float*
     void* partial = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K * 2);
     return run_gemm_images(block ? w8a8::kEpiBlockwiseBf16 : w8a8::kEpiPostscaleBf16, ws, Wimg, sx, sw, bias, Y, M,
                            N, K, partial, dev, st);
+}
+
+// Checks and launches of the fused FFN up-projection (quant, GEMM with the
+// GELU + 1x128 quantization epilogue).
+w8a8_status run_linear_gelu_quant(const void* X, const void* Wimg, const float* sw, const void* bias, void* Gimg,
+                                  float* sg, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq, void* ws,
+                                  size_t ws_bytes, cudaStream_t st) {
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, false);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX || N % 128 != 0) return W8A8_ERR_SHAPE;
+    if (M == 0 || N == 0) return W8A8_OK;
+    if (!X || !Wimg || !sw || !Gimg || !sg || !sx) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wimg) || !aligned16(sw) || !aligned16(Gimg) || !aligned16(sg) ||
+        !aligned16(sx) || (Xq && !aligned16(Xq)) || (bias && !aligned16(bias)))
+        return W8A8_ERR_ALIGNMENT;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w8a8_linear_workspace_size(M, N, K))
+        return W8A8_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    cudaError_t e = w8a8::launch_quant_rows(X, M, K, Xq, ws, sx, dev.num_sms, st);
+    if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
+    return run_gemm_images(w8a8::kEpiGeluQuant, ws, Wimg, sx, sw, bias, Gimg, M, N, K, nullptr, dev, st, sg);
 }
 
 w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
@@ -310,6 +334,30 @@ w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, const float* 
                                   size_t workspace_bytes, void* stream) {
     return run_linear(true, X, Wimg, sw, bias, Y, M, N, K, sx, Xq, workspace, workspace_bytes,
                       static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_linear_postscale_gelu_quant(const void* X, const void* Wimg, const float* sw, const void* bias,
+                                             void* Gimg, float* sg, int64_t M, int64_t N, int64_t K, float* sx,
+                                             int8_t* Xq, void* workspace, size_t workspace_bytes, void* stream) {
+    return run_linear_gelu_quant(X, Wimg, sw, bias, Gimg, sg, M, N, K, sx, Xq, workspace, workspace_bytes,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_gemm_blockwise_images(const void* Ximg, const float* sx, const void* Wimg, const float* sw,
+                                       const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream) {
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, true);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0 || N == 0) return W8A8_OK;
+    if (!Ximg || !sx || !Wimg || !sw || !Y) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(Ximg) || !aligned16(sx) || !aligned16(Wimg) || !aligned16(sw) || !aligned16(Y) ||
+        (bias && !aligned16(bias)))
+        return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    return run_gemm_images(w8a8::kEpiBlockwiseBf16, Ximg, Wimg, sx, sw, bias, Y, M, N, K, nullptr, dev,
+                           static_cast<cudaStream_t>(stream));
 }
 
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {

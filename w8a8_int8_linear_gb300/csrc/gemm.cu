@@ -48,6 +48,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "quant_core.cuh"
 
 namespace w8a8 {
 namespace {
@@ -116,6 +117,7 @@ struct KParams {
     int k_split;    // work units per tile, each over split_stages K stages (1: no split)
     int split_stages;
     int32_t* partial;  // k_split > 1: int32 partial sums [k_split][N][M] in kernel dims
+    float* sg;         // kEpiGeluQuant: block scales [M][N/128]
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
@@ -275,13 +277,31 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
     }
 }
 
+// Stage 16 bf16 columns (8 packed words) of each of the warp's 32 rows in a
+// 1 KB buffer with the 32-byte swizzle (16-byte chunk index XOR bit 2 of the
+// row, which spreads each quarter-warp over 8 bank groups) and store them as
+// one 16 x 32 box from one lane.  Two buffers per warp alternate; a buffer is
+// rewritten only after the store issued from it two groups ago has read it.
+// Out-of-range rows and columns are clipped by the TMA unit.
+__device__ __forceinline__ void stage_store16(const uint32_t (&o)[8], const CUtensorMap* tmY, int col, int row_base,
+                                              uint8_t* stg, int& sbuf, int lane) {
+    uint8_t* buf = stg + sbuf * STAGE_OUT_BYTES;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    const int sw = (lane >> 2) & 1;
+    *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (0 ^ sw)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (1 ^ sw)) = make_uint4(o[4], o[5], o[6], o[7]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmY, buf, col, row_base);
+        bulk_commit_group();
+    }
+    sbuf ^= 1;
+}
+
 // bf16 output of one warp's 32 rows x COLS columns through shared memory and
-// TMA stores: 16-column groups, each written by the 32 lanes (one row each)
-// into a 1 KB staging buffer with the 32-byte swizzle (16-byte chunk index
-// XOR bit 2 of the row, which spreads each quarter-warp over 8 bank groups),
-// then stored by one lane as a 16 x 32 box.  Two buffers per warp alternate;
-// a buffer is rewritten only after the store issued from it two groups ago
-// has read it.  Out-of-range rows and columns are clipped by the TMA unit.
+// TMA stores, 16 columns at a time (stage_store16).
 template <int EPI, int COLS>
 __device__ __forceinline__ void store_rows_tma(const typename AccType<EPI>::T (&acc)[COLS], const KParams& p,
                                                const CUtensorMap* tmY, int row, int row_base, int col0,
@@ -342,19 +362,92 @@ __device__ __forceinline__ void store_rows_tma(const typename AccType<EPI>::T (&
             }
             o[e >> 1] = pack_bf16x2(v0, v1);
         }
-        uint8_t* buf = stg + sbuf * STAGE_OUT_BYTES;
-        if (lane == 0) bulk_wait_group_read<1>();  // the store that last used `buf` has read it
-        __syncwarp();
-        const int sw = (lane >> 2) & 1;
-        *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (0 ^ sw)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (1 ^ sw)) = make_uint4(o[4], o[5], o[6], o[7]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tmY, buf, col, row_base);
-            bulk_commit_group();
+        stage_store16(o, tmY, col, row_base, stg, sbuf, lane);
+    }
+}
+
+// GELU in its erf form, x * Phi(x), with erf from Abramowitz & Stegun,
+// Handbook of Mathematical Functions, formula 7.1.28 (|error| <= 3e-7):
+// for z = |x| / sqrt 2 and p = 1 + a1 z + ... + a6 z^6, Phi(-|x|) = p^-16 / 2
+// and Phi(|x|) = 1 - p^-16 / 2.  Every binary32 operation is rounded on its
+// own, in a fixed order (Horner from a6 down, four squarings, one correctly
+// rounded reciprocal), so the bits are reproducible anywhere.
+__device__ __forceinline__ float gelu_erf(float x) {
+    const float z = __fmul_rn(fabsf(x), 0.70710678118654752f);
+    float t = 0.0000430638f;
+    t = __fadd_rn(__fmul_rn(t, z), 0.0002765672f);
+    t = __fadd_rn(__fmul_rn(t, z), 0.0001520143f);
+    t = __fadd_rn(__fmul_rn(t, z), 0.0092705272f);
+    t = __fadd_rn(__fmul_rn(t, z), 0.0422820123f);
+    t = __fadd_rn(__fmul_rn(t, z), 0.0705230784f);
+    t = __fadd_rn(__fmul_rn(t, z), 1.0f);
+    t = __fmul_rn(t, t);
+    t = __fmul_rn(t, t);
+    t = __fmul_rn(t, t);
+    t = __fmul_rn(t, t);
+    const float h = __fmul_rn(0.5f, __frcp_rn(t));
+    return __fmul_rn(x, x >= 0.0f ? __fsub_rn(1.0f, h) : h);
+}
+
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// FFN up-projection epilogue.  For this thread's row and its 128 columns --
+// exactly one 1x128 block of the down-projection's input --
+//   y = bf16(((acc * sx) * sw) + bias)   (the post-scale epilogue),
+//   g = bf16(gelu(y)),
+//   s = absmax(|g|) / 127, codes = clamp(rne(g / s), -127, 127),
+// with the scale written to sg[row][col0 / 128] and the exact bf16 image of
+// the codes (the down-projection GEMM's A operand) stored through TMA.
+template <int COLS>
+__device__ __forceinline__ void store_gelu_quant(const int32_t (&acc)[COLS], const KParams& p,
+                                                 const CUtensorMap* tmY, int row, int row_base, int col0,
+                                                 uint8_t* stg, int& sbuf, int lane) {
+    static_assert(COLS == 128, "one 1x128 block per thread");
+    if (col0 >= p.N) return;  // N % 128 == 0: a block is all in range or all out
+    const float sxr = (row < p.M) ? __ldg(p.sx + row) : 0.0f;
+    const uint16_t* bias16 = reinterpret_cast<const uint16_t*>(p.bias);
+    uint32_t gw[COLS / 2];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < COLS; j += 8) {
+        const int col = col0 + j;
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.sw + col));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.sw + col + 4));
+        const float swc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        float bc[8];
+        if (p.bias) {
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col));
+            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                bc[2 * f] = __uint_as_float(bw[f] << 16);
+                bc[2 * f + 1] = __uint_as_float(bw[f] & 0xFFFF0000u);
+            }
         }
-        sbuf ^= 1;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e]), sxr), swc[e]);
+            float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e + 1]), sxr), swc[e + 1]);
+            if (p.bias) {
+                v0 = __fadd_rn(v0, bc[e]);
+                v1 = __fadd_rn(v1, bc[e + 1]);
+            }
+            const uint32_t g2 = pack_bf16x2(gelu_erf(round_bf16(v0)), gelu_erf(round_bf16(v1)));
+            gw[(j + e) >> 1] = g2;
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(g2)), fabsf(bf16_hi(g2))));
+        }
+    }
+    const RowScale sc = make_scale_div(amax);
+    if (row < p.M) p.sg[static_cast<int64_t>(row) * (p.N >> 7) + (col0 >> 7)] = sc.s;
+#pragma unroll
+    for (int g = 0; g < COLS; g += 16) {
+        const int w0 = g >> 1;
+        const uint2 c0 = quant_chunk(make_uint4(gw[w0], gw[w0 + 1], gw[w0 + 2], gw[w0 + 3]), sc);
+        const uint2 c1 = quant_chunk(make_uint4(gw[w0 + 4], gw[w0 + 5], gw[w0 + 6], gw[w0 + 7]), sc);
+        const uint32_t o[8] = {s8x2_to_bf16x2(c0.x, 0), s8x2_to_bf16x2(c0.x, 2), s8x2_to_bf16x2(c0.y, 0),
+                               s8x2_to_bf16x2(c0.y, 2), s8x2_to_bf16x2(c1.x, 0), s8x2_to_bf16x2(c1.x, 2),
+                               s8x2_to_bf16x2(c1.y, 0), s8x2_to_bf16x2(c1.y, 2)};
+        stage_store16(o, tmY, col0 + g, row_base, stg, sbuf, lane);
     }
 }
 
@@ -667,6 +760,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     else
                         store_swapped<EPI, HALF>(acc, p, &tmY, row_base, col0, stg, sbuf, lane);
                 }
+            } else if constexpr (EPI == kEpiGeluQuant) {
+                store_gelu_quant<HALF>(acc, p, &tmY, row, row_base, col0, stg, sbuf, lane);
             } else if (kBf16Out && p.tma_store) {
                 store_rows_tma<EPI, HALF>(acc, p, &tmY, row, row_base, col0, stg, sbuf, lane);
             } else {
@@ -735,7 +830,8 @@ DeviceLaunchInfo g_launch_info[64];
 
 template <int EPI, int BN, bool SWAP>
 constexpr int instance_id() {
-    return (EPI == kEpiPostscaleBf16 ? 0 : EPI == kEpiPostscaleS32 ? 8 : EPI == kEpiBlockwiseBf16 ? 16 : 17) +
+    return (EPI == kEpiPostscaleBf16 ? 0 : EPI == kEpiPostscaleS32 ? 8 : EPI == kEpiBlockwiseBf16 ? 16
+            : EPI == kEpiBlockwiseF32 ? 17 : 18) +
            (SWAP ? 4 : 0) +
            (BN == 256 ? 0 : BN == 224 ? 1 : BN == 192 ? 2 : BN == 128 ? 1 : BN == 64 ? 2 : 3);
 }
@@ -759,7 +855,7 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
         return cudaErrorInvalidValue;
     }
     CUtensorMap tmY = tmB;  // placeholder when the output is not written through TMA
-    constexpr bool kBf16Out = (EPI == kEpiPostscaleBf16 || EPI == kEpiBlockwiseBf16);
+    constexpr bool kBf16Out = (EPI == kEpiPostscaleBf16 || EPI == kEpiBlockwiseBf16 || EPI == kEpiGeluQuant);
     const int y_cols = SWAP ? p.M : p.N;  // Y is [tokens, output columns]
     const int y_rows = SWAP ? p.N : p.M;
     p.tma_store = (kBf16Out && (y_cols % 8) == 0) ? 1 : 0;
@@ -915,6 +1011,7 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     p.sw = a.sw;
     p.bias = static_cast<const __nv_bfloat16*>(a.bias);
     p.out = a.out;
+    p.sg = a.sg;
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
@@ -922,7 +1019,7 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     const bool blockwise = epilogue == kEpiBlockwiseBf16 || epilogue == kEpiBlockwiseF32;
     p.chunk_stages = blockwise ? BLOCK_CHUNK_STAGES : POSTSCALE_CHUNK_STAGES;
     p.kb_count = static_cast<int>(a.K / 128);
-    const bool swap = !blockwise && a.M <= kSwapMaxTokens;
+    const bool swap = !blockwise && epilogue != kEpiGeluQuant && a.M <= kSwapMaxTokens;
     p.k_split = 1;
     p.split_stages = p.k_stages;
     p.partial = nullptr;
@@ -955,6 +1052,10 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
             break;
         case kEpiBlockwiseF32:
             e = launch_one<kEpiBlockwiseF32, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
+            break;
+        case kEpiGeluQuant:
+            // 256-wide tiles: each epilogue thread holds one whole 1x128 block
+            e = launch_one<kEpiGeluQuant, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
             break;
         default: e = cudaErrorInvalidValue;
     }

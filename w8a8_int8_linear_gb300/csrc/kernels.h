@@ -27,6 +27,7 @@ enum GemmEpilogue : int {
     kEpiPostscaleS32 = 1,   // acc int32
     kEpiBlockwiseBf16 = 2,  // Y = bf16(acc_f32 + bias)
     kEpiBlockwiseF32 = 3,   // acc fp32
+    kEpiGeluQuant = 4,      // FFN up: bf16 image of the 1x128 codes of bf16(gelu(post-scale Y)), scales to sg
 };
 
 struct GemmArgs {
@@ -36,6 +37,7 @@ struct GemmArgs {
     void* out;         // Y bf16 / acc int32 / acc fp32, [M,N]
     int64_t M, N, K;
     int32_t* partial;  // split-K partial sums, splitk_partial_bytes(M,N,K) bytes (unused when that is 0)
+    float* sg;         // kEpiGeluQuant: 1x128 block scales of the GELU output [M][N/128]
 };
 
 // Split K for few-token post-scale GEMMs: the number of K splits (1: none)
