@@ -261,10 +261,12 @@ void orc_epilogue_blockwise(const float* acc, const uint16_t* bias, int64_t M, i
  * formula 7.1.28: for z >= 0, erf(z) = 1 - p(z)^-16 with
  * p(z) = 1 + a1 z + a2 z^2 + ... + a6 z^6 and |error| <= 3e-7.  So for
  * z = |x| / sqrt 2, Phi(-|x|) = p(z)^-16 / 2 and Phi(|x|) = 1 - p(z)^-16 / 2.
- * Evaluated in binary32, each operation rounded on its own, in exactly this
- * order (so that any implementation following it gets the same bits):
- *   z = |x| * 0.70710677;  t = a6; then for a5, a4, a3, a2, a1: t = t * z + a_i;
- *   t = t * z + 1;  t2 = t*t; t4 = t2*t2; t8 = t4*t4; t16 = t8*t8;
+ * Evaluated in binary32 in exactly this order, so that any implementation
+ * following it gets the same bits; fma(a, b, c) is the IEEE fused
+ * multiply-add (a * b + c rounded once), every other operation is rounded on
+ * its own:
+ *   z = |x| * 0.70710677;  t = a6; then for a5, a4, a3, a2, a1: t = fma(t, z, a_i);
+ *   t = fma(t, z, 1);  t2 = t*t; t4 = t2*t2; t8 = t4*t4; t16 = t8*t8;
  *   e = 1 / t16;  h = 0.5 * e;  phi = (x >= 0) ? 1 - h : h;  g = x * phi.
  * ------------------------------------------------------------------------ */
 static float orc_gelu(float x) {
@@ -272,12 +274,12 @@ static float orc_gelu(float x) {
     const float a4 = 0.0001520143f, a5 = 0.0002765672f, a6 = 0.0000430638f;
     const float z = fabsf(x) * 0.70710678118654752f;
     float t = a6;
-    t = t * z; t = t + a5;
-    t = t * z; t = t + a4;
-    t = t * z; t = t + a3;
-    t = t * z; t = t + a2;
-    t = t * z; t = t + a1;
-    t = t * z; t = t + 1.0f;
+    t = fmaf(t, z, a5);
+    t = fmaf(t, z, a4);
+    t = fmaf(t, z, a3);
+    t = fmaf(t, z, a2);
+    t = fmaf(t, z, a1);
+    t = fmaf(t, z, 1.0f);
     float t2 = t * t;
     float t4 = t2 * t2;
     float t8 = t4 * t4;
