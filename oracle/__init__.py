@@ -55,6 +55,8 @@ def lib():
         L.orc_gelu_f32.restype = None
         L.orc_gelu_bf16.argtypes = [P, I64, P]
         L.orc_gelu_bf16.restype = None
+        L.orc_norm_quant.argtypes = [P, P, P, ctypes.c_float, ctypes.c_int, I64, I64, P, P, P]
+        L.orc_norm_quant.restype = ctypes.c_int
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         L.orc_set_num_threads.restype = None
@@ -213,6 +215,28 @@ def ffn_up_gelu_quant(X, W, bias=None):
     Gq, sg = quantize_act(G, BLOCK)
     r.update(G=G, Gq=Gq, sg=sg)
     return r
+
+
+RMS_NORM = 0
+LAYER_NORM = 1
+
+
+def norm_quant(X, gamma=None, beta=None, eps=1e-6, kind=RMS_NORM):
+    """RMSNorm (kind 0) or LayerNorm (kind 1) of bf16 X [M,K] (uint16 bits),
+    statistics summed in the fixed chunk-and-tree order stated in
+    w8a8_oracle.c, then per-token quantization of the bf16 result.
+
+    Returns (Y bf16 bits [M,K], Xq int8 [M,K], sx fp32 [M])."""
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    g = None if gamma is None else _c(gamma, np.uint16)
+    b = None if beta is None else _c(beta, np.uint16)
+    Y = np.empty((M, K), np.uint16)
+    Xq = np.empty((M, K), np.int8)
+    sx = np.empty(M, np.float32)
+    if lib().orc_norm_quant(_p(X), _p(g), _p(b), float(eps), int(kind), M, K, _p(Y), _p(Xq), _p(sx)) != 0:
+        raise ValueError("norm_quant: K must be a positive multiple of 8, at most 65536")
+    return Y, Xq, sx
 
 
 def linear_sampled(X, W, bias, rows, cols, mode=PER_ROW):

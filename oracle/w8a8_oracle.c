@@ -300,3 +300,93 @@ void orc_gelu_bf16(const uint16_t* y, int64_t n, uint16_t* g) {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) g[i] = orc_f32_to_bf16(orc_gelu(orc_bf16_to_f32(y[i])));
 }
+
+/* ------------------------------------------------------------------------
+ * Normalization fused with per-token activation quantization.
+ *
+ * "TurboDiffusion Integration Notes", section "Reused Components": FastNorm
+ * replaces RMSNorm/LayerNorm with fused implementations, and W8A8 + FastNorm
+ * is the one combined stage of the section "End-to-End Result".  The
+ * acceleration overview's LayerNorm sketch (section "Custom Kernel
+ * Optimizations") computes the statistics, normalizes, then applies the
+ * affine transform.  Readings taken (the pages give no formula):
+ *   RMSNorm:   r = 1 / sqrt(S(x*x) / K + eps),      y = bf16((x * r) * gamma)
+ *   LayerNorm: mu = S(x) / K, d = x - mu,
+ *              r = 1 / sqrt(S(d*d) / K + eps),      y = bf16(((d * r) * gamma) + beta)
+ * (gamma and beta optional: a missing one skips its operation), then y is
+ * quantized per token like any activation.  The statistics come from one read
+ * of the row; the variance is taken about the mean (not E[x^2] - mu^2).
+ * sqrt and the divisions are IEEE binary32 operations.
+ *
+ * S() is a sum with a fixed order, stated here so that it does not depend on
+ * how an implementation spreads a row over threads: the row is cut into
+ * chunks of 8 consecutive elements; each chunk's terms are added left to
+ * right (t0 + t1, then + t2, ...); the chunk sums, zero-padded to P = the
+ * next power of two of K/8 entries, are added pairwise level by level
+ * (entry i of the next level = entry 2i + entry 2i+1) down to one value.
+ * Every term (x*x, d = x - mu, d*d) is rounded to binary32 on its own.
+ * ------------------------------------------------------------------------ */
+static float orc_tree_sum(float* part, int64_t P) {
+    for (int64_t w = P; w > 1; w >>= 1)
+        for (int64_t i = 0; i < w / 2; ++i) part[i] = part[2 * i] + part[2 * i + 1];
+    return part[0];
+}
+
+static int64_t orc_pow2_at_least(int64_t n) {
+    int64_t p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+/* kind 0: RMSNorm, 1: LayerNorm.  X, gamma, beta, Y are bf16 bit patterns;
+ * gamma / beta may be NULL.  Writes Y[M,K] (the normalized bf16 output), then
+ * its per-token quantization Xq[M,K] and sx[M].  Returns 0, or -1 for a bad
+ * shape (K % 8 != 0 or K > 65536). */
+int orc_norm_quant(const uint16_t* X, const uint16_t* gamma, const uint16_t* beta, float eps, int kind,
+                   int64_t M, int64_t K, uint16_t* Y, int8_t* Xq, float* sx) {
+    if (K <= 0 || K % 8 != 0 || K > 65536) return -1;
+    const int64_t C = K / 8;
+    const int64_t P = orc_pow2_at_least(C);
+    const float Kf = (float)K;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        float part[65536 / 8];
+        const uint16_t* x = X + m * K;
+        uint16_t* y = Y + m * K;
+        float mu = 0.0f;
+        if (kind == 1) {
+            for (int64_t c = 0; c < P; ++c) {
+                float s = 0.0f;
+                if (c < C) {
+                    s = orc_bf16_to_f32(x[8 * c]);
+                    for (int j = 1; j < 8; ++j) s = s + orc_bf16_to_f32(x[8 * c + j]);
+                }
+                part[c] = s;
+            }
+            mu = orc_tree_sum(part, P) / Kf;
+        }
+        for (int64_t c = 0; c < P; ++c) {
+            float s = 0.0f;
+            if (c < C) {
+                for (int j = 0; j < 8; ++j) {
+                    float d = orc_bf16_to_f32(x[8 * c + j]);
+                    if (kind == 1) d = d - mu;
+                    float t = d * d;
+                    s = (j == 0) ? t : s + t;
+                }
+            }
+            part[c] = s;
+        }
+        const float var = orc_tree_sum(part, P) / Kf;
+        const float r = 1.0f / sqrtf(var + eps);
+        for (int64_t k = 0; k < K; ++k) {
+            float d = orc_bf16_to_f32(x[k]);
+            if (kind == 1) d = d - mu;
+            float v = d * r;
+            if (gamma) v = v * orc_bf16_to_f32(gamma[k]);
+            if (kind == 1 && beta) v = v + orc_bf16_to_f32(beta[k]);
+            y[k] = orc_f32_to_bf16(v);
+        }
+    }
+    return orc_quantize_act(Y, M, K, 0, Xq, sx);
+}

@@ -444,3 +444,91 @@ def test_ffn_up_gelu_quant_composition(oracle):
     deq = r["Gq"].reshape(M, N // 128, 128).astype(np.float64) * r["sg"][:, :, None].astype(np.float64)
     assert np.all(np.abs(deq - G) <= 0.5 * r["sg"][:, :, None] * (1 + 1e-6))
     assert np.abs(r["Gq"]).max() == 127
+
+
+# ----------------------------------------------------------------- normalization fused with quantization
+def _ordered(u):
+    u = np.asarray(u).astype(np.int64)
+    return np.where(u & 0x8000, 0x8000 - (u & 0x7FFF), u + 0x8000)
+
+
+@pytest.mark.parametrize("K", [128, 4096, 5120])
+def test_layer_norm_matches_torch(oracle, K):
+    """Against torch.nn.functional.layer_norm in fp32 (a different summation
+    order), rounded to bf16: within 1 ulp everywhere, identical almost
+    everywhere; a missing beta or gamma skips exactly that operation."""
+    rng = np.random.default_rng(K)
+    Xf = (rng.normal(0.5, 2.0, (16, K)) * rng.choice([1.0, 30.0], (16, K), p=[0.99, 0.01])).astype(np.float32)
+    X = oracle.bf16_from_f32(Xf)
+    g = oracle.bf16_from_f32(rng.normal(1.0, 0.2, K).astype(np.float32))
+    b = oracle.bf16_from_f32(rng.normal(0.0, 0.2, K).astype(np.float32))
+    xt = torch.from_numpy(oracle.f32_from_bf16(X))
+    for gg, bb in ((g, b), (g, None), (None, None)):
+        Y, _, _ = oracle.norm_quant(X, gg, bb, 1e-5, oracle.LAYER_NORM)
+        T = torch.nn.functional.layer_norm(
+            xt, (K,), None if gg is None else torch.from_numpy(oracle.f32_from_bf16(gg)),
+            None if bb is None else torch.from_numpy(oracle.f32_from_bf16(bb)), 1e-5)
+        Tb = T.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        d = np.abs(_ordered(Y) - _ordered(Tb))
+        assert d.max() <= 1 and (d > 0).mean() < 2e-3
+
+
+@pytest.mark.parametrize("K", [256, 5120])
+def test_rms_norm_vs_fp64(oracle, K):
+    """Against x / sqrt(mean(x^2) + eps) * gamma in fp64 rounded to bf16."""
+    rng = np.random.default_rng(K + 1)
+    X = oracle.bf16_from_f32(rng.normal(0.0, 3.0, (16, K)).astype(np.float32))
+    g = oracle.bf16_from_f32(rng.normal(1.0, 0.2, K).astype(np.float32))
+    Y, Xq, sx = oracle.norm_quant(X, g, None, 1e-6, oracle.RMS_NORM)
+    x = oracle.f32_from_bf16(X).astype(np.float64)
+    ref = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + np.float64(np.float32(1e-6)))
+    ref = ref * oracle.f32_from_bf16(g).astype(np.float64)
+    d = np.abs(_ordered(Y) - _ordered(oracle.bf16_from_f32(ref.astype(np.float32))))
+    assert d.max() <= 1 and (d > 0).mean() < 2e-3
+    # the codes are the per-token quantization of the bf16 output
+    q2, s2 = oracle.quantize_act(Y, oracle.PER_ROW)
+    assert np.array_equal(Xq, q2) and np.array_equal(sx, s2)
+
+
+def test_norm_closed_forms(oracle):
+    K = 1024
+    # constant row c: RMSNorm gives c / sqrt(c^2 + eps) exactly rounded twice
+    c = np.float32(1.5)
+    X = oracle.bf16_from_f32(np.full((1, K), c, np.float32))
+    Y, Xq, sx = oracle.norm_quant(X, None, None, 0.0, oracle.RMS_NORM)
+    assert np.all(oracle.f32_from_bf16(Y) == 1.0)  # 1.5 / sqrt(2.25) == 1 exactly
+    assert np.all(Xq == 127) and sx[0] == np.float32(1.0) / np.float32(127)
+    # LayerNorm of a constant row: d = 0, so y = beta exactly (and +-0 without beta)
+    b = oracle.bf16_from_f32(np.linspace(-1, 1, K).astype(np.float32))
+    Y, Xq, sx = oracle.norm_quant(X, None, b, 1e-5, oracle.LAYER_NORM)
+    assert np.array_equal(Y[0], b)
+    # +-a alternating: mean 0 exactly, variance a^2; with eps = 0 every |y| = 1
+    a = np.float32(0.375)
+    X = oracle.bf16_from_f32(np.tile(np.array([a, -a], np.float32), K // 2)[None, :])
+    Y, Xq, sx = oracle.norm_quant(X, None, None, 0.0, oracle.LAYER_NORM)
+    assert np.array_equal(np.abs(oracle.f32_from_bf16(Y)), np.ones((1, K), np.float32))
+    assert np.array_equal(Xq[0], np.tile(np.array([127, -127], np.int8), K // 2))
+
+
+def test_norm_sum_order(oracle):
+    """The statistics use chunk sums of 8 then a pairwise tree, not a left-to-
+    right scan: a row where the two orders give different binary32 sums takes
+    the tree's value (checked through the LayerNorm mean, which shifts every
+    output)."""
+    K = 32  # 4 chunks: tree ((s0 + s1) + (s2 + s3))
+    x = np.zeros(K, np.float32)
+    x[0] = 2.0 ** 24          # chunk 0
+    x[8] = 1.0                # chunk 1: 2^24 + 1 rounds to 2^24 in a left-to-right scan ...
+    x[16] = 1.0               # chunk 2: ... and again, while the tree adds 1 + 1 = 2 first
+    x[24] = -(2.0 ** 24)      # chunk 3
+    tree = ((np.float32(2.0 ** 24) + np.float32(1.0)) + (np.float32(1.0) + np.float32(-(2.0 ** 24))))
+    scan = np.float32(0)
+    for v in x:
+        scan = np.float32(scan + v)
+    assert tree != scan       # the two orders really differ here (0 vs -2^24... or 2 vs 0)
+    X = oracle.bf16_from_f32(x[None, :])
+    mu_tree = np.float32(tree) / np.float32(K)
+    # y for an element equal to 0: -mu * r; its sign and size follow the tree mean
+    Y, _, _ = oracle.norm_quant(X, None, None, 1.0, oracle.LAYER_NORM)
+    y1 = oracle.f32_from_bf16(Y)[0, 1]
+    assert np.sign(y1) == -np.sign(mu_tree) or mu_tree == 0
