@@ -223,6 +223,47 @@ W8A8_API w8a8_status w8a8_gemm_blockwise_images(const void* Ximg, const float* s
                                                 const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
                                                 void* stream);
 
+/* Normalization of the fused normalization + quantization entry point. */
+typedef enum {
+    W8A8_NORM_RMS = 0,   /* y = (x * r) * gamma,             r = 1 / sqrt(S(x*x)/K + eps)  */
+    W8A8_NORM_LAYER = 1  /* y = ((d * r) * gamma) + beta,    d = x - S(x)/K, r = 1 / sqrt(S(d*d)/K + eps) */
+} w8a8_norm_kind;
+
+/*
+ * RMSNorm or LayerNorm fused with per-token activation quantization
+ * ("TurboDiffusion Integration Notes", section "Reused Components": FastNorm
+ * replaces RMSNorm/LayerNorm with fused implementations; W8A8 and FastNorm
+ * form one combined stage in section "End-to-End Result").  One read of X:
+ * y = bf16(normalized row, formulas above; a NULL gamma or beta skips that
+ * operation), then sx[m] = absmax(y[m,:]) / 127 and q = clamp(rne(y / sx),
+ * -127, 127).  S() is summed in a fixed order independent of the launch:
+ * chunks of 8 consecutive elements left to right, then the chunk sums
+ * (zero-padded to a power of two) pairwise level by level.  Every operation
+ * is IEEE binary32, rounded on its own.
+ *   X [M,K] bf16, gamma / beta [K] bf16 or NULL (beta only for LAYER), eps >= 0,
+ *   Y [M,K] bf16 out or NULL (the normalized row), Xq [M,K] int8 out or NULL,
+ *   Ximg [M,K] bf16 out or NULL (exact image of Xq, the GEMM's operand),
+ *   sx [M] fp32 out.  K % 8 == 0 and K <= 32768 (else W8A8_ERR_SHAPE).
+ */
+W8A8_API w8a8_status w8a8_norm_quant(const void* X, const void* gamma, const void* beta, float eps,
+                                     w8a8_norm_kind kind, int64_t M, int64_t K, void* Y, int8_t* Xq, void* Ximg,
+                                     float* sx, void* stream);
+
+/* Device workspace bytes of w8a8_gemm_postscale_images (the int32 partial
+ * sums of the K splits of few-token shapes; 0 when the shape is not split). */
+W8A8_API size_t w8a8_splitk_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Post-scale GEMM on operand images: Ximg [M,K] and Wimg [N,K] are exact
+ * bf16 images of int8 codes (from w8a8_norm_quant and w8a8_pack_weight), sx
+ * [M], sw [N], bias [N] bf16 or NULL, Y [M,N] bf16 out.  Same arithmetic as
+ * w8a8_gemm_postscale.  workspace: w8a8_splitk_workspace_size(M,N,K) bytes,
+ * 256-byte aligned (may be NULL when that size is 0).
+ */
+W8A8_API w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* sx, const void* Wimg, const float* sw,
+                                                const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
+                                                void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Allocation-free variant of w8a8_gemm_postscale (the pages have no
  * counterpart: this is a library convenience).  Same arguments, results and

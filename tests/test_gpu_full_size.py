@@ -76,3 +76,31 @@ def test_ffn_down_blockwise_32768x5120x13824(w8a8, oracle):
 @pytest.mark.parametrize("N", wl.RAGGED_N)
 def test_ragged_sweep(w8a8, oracle, M, N):
     run_case(w8a8, oracle, wl.ragged(M, N), rows_max=24, cols_max=24)
+
+
+def test_ffn_up_gelu_quant_full_size(w8a8, oracle):
+    """The fused FFN up-projection (GELU + 1x128 quantization epilogue) at
+    32768 x 13824 x 5120: codes and block scales of sampled rows and sampled
+    128-column blocks (every edge block of the 256-wide tiles among them)
+    against the oracle."""
+    rng = np.random.default_rng(1)
+    work = wl.FFN_UP
+    X = wl.make_x(work, DEV)
+    W = wl.make_w(work, DEV)
+    b = wl.make_bias(work, DEV)
+    Wq, sw = w8a8.quantize_weight(W)
+    G, sg, sx, _ = w8a8.linear_postscale_gelu_quant(X, w8a8.pack_weight(Wq), sw, b)
+    torch.cuda.synchronize()
+    assert w8a8.get_device_error() == (0, 0)
+    rows = sample(work.M, 128, rng, 40)
+    blocks = sample(work.N // 128, 2, rng, 12)
+    cols = (blocks[:, None] * 128 + np.arange(128)[None, :]).reshape(-1)
+    Xs = bits(X[torch.from_numpy(rows).to(DEV)])
+    Yo, _ = oracle.linear_sampled(Xs, bits(W), bits(b), np.arange(len(rows)), cols, oracle.PER_ROW)
+    Gq_o, sg_o = oracle.quantize_act(oracle.gelu_bf16(Yo), oracle.BLOCK)
+    r = torch.from_numpy(rows).to(DEV)
+    Gg = G[r][:, torch.from_numpy(cols).to(DEV)].float().cpu()
+    assert np.array_equal(Gg.to(torch.int8).numpy(), Gq_o)
+    sgg = sg[r][:, torch.from_numpy(blocks).to(DEV)].cpu().numpy()
+    assert np.array_equal(sgg.view(np.uint32), sg_o.view(np.uint32))
+    assert torch.isfinite(sg).all() and (G.abs() <= 127).all()

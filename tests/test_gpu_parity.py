@@ -381,3 +381,59 @@ def test_ffn_up_gelu_quant_rejects_bad_arguments(w8a8):
     Wimg = torch.zeros((200, 64), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(w8a8.W8A8Error, match="SHAPE"):  # N not a multiple of 128
         w8a8.linear_postscale_gelu_quant(X, Wimg, torch.ones(200, device=DEV))
+
+
+# ----------------------------------------------------------------- normalization fused with quantization
+@pytest.mark.parametrize("layer", [False, True])
+@pytest.mark.parametrize("M,K", [(1, 8), (7, 128), (33, 264), (300, 4096), (64, 5120), (5, 13824), (3, 32768),
+                                 (1000, 1040)])
+def test_norm_quant(w8a8, oracle, layer, M, K):
+    X = rand_bf16((M, K), seed=60 + K, scale=2.0, outliers=0.01, oscale=30.0)
+    if layer:
+        X = (X.float() + 0.75).to(torch.bfloat16)  # a nonzero mean
+    if M >= 7:
+        X[3] = 0.0                                  # an all-zero row: y = beta (or 0), s = 0
+        X[5] = 1.25                                 # a constant row
+    g = rand_bf16((K,), seed=61, scale=0.2) + 1.0
+    g = g.to(torch.bfloat16)
+    b = rand_bf16((K,), seed=62, scale=0.2) if layer else None
+    kind = oracle.LAYER_NORM if layer else oracle.RMS_NORM
+    for gg, bb in ((g, b), (None, None)):
+        Yo, Xqo, sxo = oracle.norm_quant(bits(X), None if gg is None else bits(gg), None if bb is None else bits(bb),
+                                         1e-5, kind)
+        Ximg, sx, Xq, Y = w8a8.norm_quant(X.to(DEV), None if gg is None else gg.to(DEV),
+                                          None if bb is None else bb.to(DEV), 1e-5, kind, codes=True, y=True)
+        assert np.array_equal(bits(Y), Yo)
+        assert np.array_equal(Xq.cpu().numpy(), Xqo)
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), sxo.view(np.uint32))
+        assert torch.equal(Ximg.float().cpu(), Xq.float().cpu())
+    assert w8a8.get_device_error() == (0, 0)
+
+
+def test_norm_then_postscale_gemm(w8a8, oracle):
+    """RMSNorm -> codes image -> post-scale GEMM on images, against the oracle
+    (few tokens, so the swapped split-K path, and a regular shape)."""
+    for M, N, K in ((5, 1536, 2048), (520, 640, 1024)):
+        X = rand_bf16((M, K), seed=70 + M, scale=1.5)
+        g = (rand_bf16((K,), seed=71, scale=0.1) + 1.0).to(torch.bfloat16)
+        W = rand_bf16((N, K), seed=72, scale=0.02)
+        bias = rand_bf16((N,), seed=73, scale=0.1)
+        _, Xqo, sxo = oracle.norm_quant(bits(X), bits(g), None, 1e-6, oracle.RMS_NORM)
+        oWq, osw = oracle.quantize_weight(bits(W), oracle.PER_ROW)
+        Yo = oracle.epilogue_postscale(oracle.gemm_s32(Xqo, oWq), sxo, osw, bits(bias))
+        Ximg, sx, _, _ = w8a8.norm_quant(X.to(DEV), g.to(DEV), None, 1e-6, w8a8.RMS_NORM)
+        Wq, sw = w8a8.quantize_weight(W.to(DEV))
+        Y = w8a8.gemm_postscale_images(Ximg, sx, w8a8.pack_weight(Wq), sw, bias.to(DEV))
+        d = assert_bf16_close(bits(Y), Yo, 1)
+        assert d.max() == 0
+
+
+def test_norm_quant_rejects_bad_arguments(w8a8):
+    X = torch.zeros((4, 36), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):       # K % 8 != 0
+        w8a8.norm_quant(X)
+    X = torch.zeros((2, 65536), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):       # K > 32768
+        w8a8.norm_quant(X)
+    with pytest.raises(w8a8.W8A8Error, match="INVALID_ARG"):  # negative eps
+        w8a8.norm_quant(torch.zeros((2, 64), dtype=torch.bfloat16, device=DEV), eps=-1.0)

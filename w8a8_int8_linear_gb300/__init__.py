@@ -47,6 +47,9 @@ SIGNATURES = [
     ("w8a8_linear_blockwise", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_linear_postscale_gelu_quant", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_images", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    ("w8a8_norm_quant", _I32, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64, _P, _P, _P, _P, _P]),
+    ("w8a8_splitk_workspace_size", _SZ, [_I64, _I64, _I64]),
+    ("w8a8_gemm_postscale_images", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_postscale_noalloc", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -345,6 +348,52 @@ def gemm_blockwise_images(Ximg, sx, Wimg, sw, bias=None, out=None):
     _check("w8a8_gemm_blockwise_images",
            lib().w8a8_gemm_blockwise_images(_ptr(Ximg), _ptr(sx), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
                                             _stream()))
+    return Y
+
+
+RMS_NORM = 0
+LAYER_NORM = 1
+
+
+def norm_quant(X, gamma=None, beta=None, eps=1e-6, kind=RMS_NORM, image=True, codes=False, y=False):
+    """RMSNorm (kind RMS_NORM) or LayerNorm (LAYER_NORM) of bf16 X [M,K]
+    fused with per-token quantization.  Returns (Ximg or None, sx, Xq or None,
+    Y or None): the bf16 image of the codes (image=True), the per-token
+    scales, the int8 codes (codes=True) and the normalized bf16 rows (y=True)."""
+    _need(X, torch.bfloat16, "X", 2)
+    M, K = X.shape
+    for t, name in ((gamma, "gamma"), (beta, "beta")):
+        if t is not None:
+            _need(t, torch.bfloat16, name, 1)
+    dev = X.device
+    Ximg = torch.empty((M, K), dtype=torch.bfloat16, device=dev) if image else None
+    Xq = torch.empty((M, K), dtype=torch.int8, device=dev) if codes else None
+    Y = torch.empty((M, K), dtype=torch.bfloat16, device=dev) if y else None
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    _check("w8a8_norm_quant", lib().w8a8_norm_quant(_ptr(X), _ptr(gamma), _ptr(beta), float(eps), int(kind), M, K,
+                                                    _ptr(Y), _ptr(Xq), _ptr(Ximg), _ptr(sx), _stream()))
+    return Ximg, sx, Xq, Y
+
+
+def gemm_postscale_images(Ximg, sx, Wimg, sw, bias=None, out=None, workspace=None):
+    """Post-scale GEMM on exact bf16 images of int8 codes (for example the
+    output of norm_quant and a packed weight)."""
+    _need(Ximg, torch.bfloat16, "Ximg", 2)
+    _need(Wimg, torch.bfloat16, "Wimg", 2)
+    _need(sx, torch.float32, "sx")
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = Ximg.shape
+    N = Wimg.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Ximg.device)
+    need = int(lib().w8a8_splitk_workspace_size(M, N, K))
+    ws = workspace
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=Ximg.device)
+    _check("w8a8_gemm_postscale_images",
+           lib().w8a8_gemm_postscale_images(_ptr(Ximg), _ptr(sx), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
+                                            _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
     return Y
 
 

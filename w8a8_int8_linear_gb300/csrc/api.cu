@@ -360,6 +360,50 @@ w8a8_status w8a8_gemm_blockwise_images(const void* Ximg, const float* sx, const 
                            static_cast<cudaStream_t>(stream));
 }
 
+w8a8_status w8a8_norm_quant(const void* X, const void* gamma, const void* beta, float eps, w8a8_norm_kind kind,
+                            int64_t M, int64_t K, void* Y, int8_t* Xq, void* Ximg, float* sx, void* stream) {
+    if (M < 0 || K <= 0) return W8A8_ERR_INVALID_ARG;
+    if (kind != W8A8_NORM_RMS && kind != W8A8_NORM_LAYER) return W8A8_ERR_INVALID_ARG;
+    if (K % 8 != 0 || K > 32768 || M > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0) return W8A8_OK;
+    if (!X || !sx) return W8A8_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f)) return W8A8_ERR_INVALID_ARG;  // also rejects NaN
+    if (!aligned16(X) || !aligned16(sx) || (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)) ||
+        (Y && !aligned16(Y)) || (Xq && !aligned16(Xq)) || (Ximg && !aligned16(Ximg)))
+        return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    w8a8_status s = current_device(&dev);
+    if (s != W8A8_OK) return s;
+    return from_cuda(w8a8::launch_norm_quant(X, gamma, beta, eps, kind == W8A8_NORM_LAYER ? 1 : 0, M, K, Y, Xq, Ximg,
+                                             sx, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w8a8_splitk_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return align256(w8a8::splitk_partial_bytes(M, N, K));
+}
+
+w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* sx, const void* Wimg, const float* sw,
+                                       const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, false);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0 || N == 0) return W8A8_OK;
+    if (!Ximg || !sx || !Wimg || !sw || !Y) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(Ximg) || !aligned16(sx) || !aligned16(Wimg) || !aligned16(sw) || !aligned16(Y) ||
+        (bias && !aligned16(bias)))
+        return W8A8_ERR_ALIGNMENT;
+    const size_t need = w8a8_splitk_workspace_size(M, N, K);
+    if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need))
+        return W8A8_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    return run_gemm_images(w8a8::kEpiPostscaleBf16, Ximg, Wimg, sx, sw, bias, Y, M, N, K, workspace, dev,
+                           static_cast<cudaStream_t>(stream));
+}
+
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2) +

@@ -369,27 +369,31 @@ __device__ __forceinline__ void store_rows_tma(const typename AccType<EPI>::T (&
 // GELU in its erf form, x * Phi(x), with erf from Abramowitz & Stegun,
 // Handbook of Mathematical Functions, formula 7.1.28 (|error| <= 3e-7):
 // for z = |x| / sqrt 2 and p = 1 + a1 z + ... + a6 z^6, Phi(-|x|) = p^-16 / 2
-// and Phi(|x|) = 1 - p^-16 / 2.  Every binary32 operation is rounded on its
-// own, in a fixed order (Horner from a6 down, four squarings, one correctly
-// rounded reciprocal), so the bits are reproducible anywhere.
-__device__ __forceinline__ float gelu_erf(float x) {
-    const float z = __fmul_rn(fabsf(x), 0.70710678118654752f);
-    float t = 0.0000430638f;
-    t = __fadd_rn(__fmul_rn(t, z), 0.0002765672f);
-    t = __fadd_rn(__fmul_rn(t, z), 0.0001520143f);
-    t = __fadd_rn(__fmul_rn(t, z), 0.0092705272f);
-    t = __fadd_rn(__fmul_rn(t, z), 0.0422820123f);
-    t = __fadd_rn(__fmul_rn(t, z), 0.0705230784f);
-    t = __fadd_rn(__fmul_rn(t, z), 1.0f);
-    t = __fmul_rn(t, t);
-    t = __fmul_rn(t, t);
-    t = __fmul_rn(t, t);
-    t = __fmul_rn(t, t);
-    const float h = __fmul_rn(0.5f, __frcp_rn(t));
-    return __fmul_rn(x, x >= 0.0f ? __fsub_rn(1.0f, h) : h);
+// and Phi(|x|) = 1 - p^-16 / 2.  Binary32 in a fixed order: the Horner steps
+// from a6 down are fused multiply-adds, the four squarings, the correctly
+// rounded reciprocal and the rest are each rounded on their own.  Two values
+// at a time on the packed fp32 pipe; returns bf16(gelu(x0)), bf16(gelu(x1))
+// packed (x0 in the low half).
+__device__ __forceinline__ uint32_t gelu_erf_bf16x2(float x0, float x1) {
+    const uint64_t z = f2_mul(f2_pack(fabsf(x0), fabsf(x1)), f2_pack(0.70710678118654752f, 0.70710678118654752f));
+    uint64_t t = f2_fma(f2_pack(0.0000430638f, 0.0000430638f), z, f2_pack(0.0002765672f, 0.0002765672f));
+    t = f2_fma(t, z, f2_pack(0.0001520143f, 0.0001520143f));
+    t = f2_fma(t, z, f2_pack(0.0092705272f, 0.0092705272f));
+    t = f2_fma(t, z, f2_pack(0.0422820123f, 0.0422820123f));
+    t = f2_fma(t, z, f2_pack(0.0705230784f, 0.0705230784f));
+    t = f2_fma(t, z, f2_pack(1.0f, 1.0f));
+    t = f2_mul(t, t);
+    t = f2_mul(t, t);
+    t = f2_mul(t, t);
+    t = f2_mul(t, t);
+    float t0, t1;
+    f2_unpack(t, t0, t1);
+    const float h0 = __fmul_rn(0.5f, __frcp_rn(t0));
+    const float h1 = __fmul_rn(0.5f, __frcp_rn(t1));
+    const float g0 = __fmul_rn(x0, x0 >= 0.0f ? __fsub_rn(1.0f, h0) : h0);
+    const float g1 = __fmul_rn(x1, x1 >= 0.0f ? __fsub_rn(1.0f, h1) : h1);
+    return pack_bf16x2(g0, g1);
 }
-
-__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 // FFN up-projection epilogue.  For this thread's row and its 128 columns --
 // exactly one 1x128 block of the down-projection's input --
@@ -398,56 +402,71 @@ __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(_
 //   s = absmax(|g|) / 127, codes = clamp(rne(g / s), -127, 127),
 // with the scale written to sg[row][col0 / 128] and the exact bf16 image of
 // the codes (the down-projection GEMM's A operand) stored through TMA.
+// The GELU pass is a rolled loop over four 32-column groups: each iteration
+// works on acc[0..31], then shifts the array down by 32 and parks its 16
+// packed results in acc[96..111], so the loop body has fixed register names
+// and the code stays small; afterwards group q's results sit in acc[32q ..
+// 32q + 15].
 template <int COLS>
-__device__ __forceinline__ void store_gelu_quant(const int32_t (&acc)[COLS], const KParams& p,
-                                                 const CUtensorMap* tmY, int row, int row_base, int col0,
-                                                 uint8_t* stg, int& sbuf, int lane) {
+__device__ __forceinline__ void store_gelu_quant(int32_t (&acc)[COLS], const KParams& p, const CUtensorMap* tmY,
+                                                 int row, int row_base, int col0, uint8_t* stg, int& sbuf,
+                                                 int lane) {
     static_assert(COLS == 128, "one 1x128 block per thread");
     if (col0 >= p.N) return;  // N % 128 == 0: a block is all in range or all out
     const float sxr = (row < p.M) ? __ldg(p.sx + row) : 0.0f;
     const uint16_t* bias16 = reinterpret_cast<const uint16_t*>(p.bias);
-    uint32_t gw[COLS / 2];
     float amax = 0.0f;
+#pragma unroll 1
+    for (int it = 0; it < 4; ++it) {
+        const int col = col0 + it * 32;
+        uint32_t gnew[16];
 #pragma unroll
-    for (int j = 0; j < COLS; j += 8) {
-        const int col = col0 + j;
-        const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.sw + col));
-        const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.sw + col + 4));
-        const float swc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        float bc[8];
-        if (p.bias) {
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col));
-            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                bc[2 * f] = __uint_as_float(bw[f] << 16);
-                bc[2 * f + 1] = __uint_as_float(bw[f] & 0xFFFF0000u);
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e]), sxr), swc[e]);
-            float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e + 1]), sxr), swc[e + 1]);
+        for (int j = 0; j < 32; j += 8) {
+            const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.sw + col + j));
+            const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.sw + col + j + 4));
+            const float swc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float bc[8];
             if (p.bias) {
-                v0 = __fadd_rn(v0, bc[e]);
-                v1 = __fadd_rn(v1, bc[e + 1]);
+                const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col + j));
+                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    bc[2 * f] = __uint_as_float(bw[f] << 16);
+                    bc[2 * f + 1] = __uint_as_float(bw[f] & 0xFFFF0000u);
+                }
             }
-            const uint32_t g2 = pack_bf16x2(gelu_erf(round_bf16(v0)), gelu_erf(round_bf16(v1)));
-            gw[(j + e) >> 1] = g2;
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(g2)), fabsf(bf16_hi(g2))));
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e]), sxr), swc[e]);
+                float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e + 1]), sxr), swc[e + 1]);
+                if (p.bias) {
+                    v0 = __fadd_rn(v0, bc[e]);
+                    v1 = __fadd_rn(v1, bc[e + 1]);
+                }
+                const uint32_t y2 = pack_bf16x2(v0, v1);  // y = bf16(...)
+                const uint32_t g2 = gelu_erf_bf16x2(bf16_lo(y2), bf16_hi(y2));
+                gnew[(j + e) >> 1] = g2;
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(g2)), fabsf(bf16_hi(g2))));
+            }
         }
+#pragma unroll
+        for (int i = 0; i < 96; ++i) acc[i] = acc[i + 32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[96 + i] = static_cast<int32_t>(gnew[i]);
     }
     const RowScale sc = make_scale_div(amax);
     if (row < p.M) p.sg[static_cast<int64_t>(row) * (p.N >> 7) + (col0 >> 7)] = sc.s;
 #pragma unroll
-    for (int g = 0; g < COLS; g += 16) {
-        const int w0 = g >> 1;
-        const uint2 c0 = quant_chunk(make_uint4(gw[w0], gw[w0 + 1], gw[w0 + 2], gw[w0 + 3]), sc);
-        const uint2 c1 = quant_chunk(make_uint4(gw[w0 + 4], gw[w0 + 5], gw[w0 + 6], gw[w0 + 7]), sc);
-        const uint32_t o[8] = {s8x2_to_bf16x2(c0.x, 0), s8x2_to_bf16x2(c0.x, 2), s8x2_to_bf16x2(c0.y, 0),
-                               s8x2_to_bf16x2(c0.y, 2), s8x2_to_bf16x2(c1.x, 0), s8x2_to_bf16x2(c1.x, 2),
-                               s8x2_to_bf16x2(c1.y, 0), s8x2_to_bf16x2(c1.y, 2)};
-        stage_store16(o, tmY, col0 + g, row_base, stg, sbuf, lane);
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int w0 = 32 * q + 8 * h;
+            const uint32_t* gw = reinterpret_cast<const uint32_t*>(acc);
+            const uint4 c0 = quant_chunk_img(make_uint4(gw[w0], gw[w0 + 1], gw[w0 + 2], gw[w0 + 3]), sc);
+            const uint4 c1 = quant_chunk_img(make_uint4(gw[w0 + 4], gw[w0 + 5], gw[w0 + 6], gw[w0 + 7]), sc);
+            const uint32_t o[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            stage_store16(o, tmY, col0 + 32 * q + 16 * h, row_base, stg, sbuf, lane);
+        }
     }
 }
 

@@ -134,6 +134,59 @@ __device__ __forceinline__ uint32_t s8x2_to_bf16x2(uint32_t w, int first) {
 
 // Write one chunk of 8 codes: as int8 to q[i] (when q is given) and as the
 // exact bf16 image of the codes to img[i] (when img is given).
+// Like quant_chunk, but returns the codes as their exact bf16 values (the
+// image the tensor-core GEMM reads): the rounded quotient rne(P) =
+// big - 1.5*2^23 is an integer in [-127, 127] held exactly in fp32, so it is
+// packed to bf16 directly.  -0 from the exact path is turned into +0, the
+// bf16 image of the code 0.
+__device__ __forceinline__ uint4 quant_chunk_img(const uint4& v, const RowScale& sc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float q[8];
+    if (sc.exact) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[2 * i] = __fadd_rn(static_cast<float>(quant_exact(bf16_lo(w[i]), sc.s)), 0.0f);
+            q[2 * i + 1] = __fadd_rn(static_cast<float>(quant_exact(bf16_hi(w[i]), sc.s)), 0.0f);
+        }
+    } else {
+        const uint64_t inv2 = f2_pack(sc.inv, sc.inv);
+        const uint64_t magic2 = f2_pack(kRoundMagic, kRoundMagic);
+        float dist[8];
+        float dmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t x2 = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+            const uint64_t bg = f2_fma(x2, inv2, magic2);  // rne(P) + 1.5*2^23
+            const uint64_t nr = f2_sub(magic2, bg);        // -rne(P), exact
+            const uint64_t d = f2_fma(x2, inv2, nr);       // P - rne(P), rounded once
+            float n0, n1, d0, d1;
+            f2_unpack(nr, n0, n1);
+            f2_unpack(d, d0, d1);
+            q[2 * i] = __fsub_rn(0.0f, n0);
+            q[2 * i + 1] = __fsub_rn(0.0f, n1);
+            dist[2 * i] = d0;
+            dist[2 * i + 1] = d1;
+            dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
+        }
+        if (!(dmax <= 0.5f - kTieGuard)) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (!(fabsf(dist[2 * i]) <= 0.5f - kTieGuard))
+                    q[2 * i] = __fadd_rn(static_cast<float>(quant_exact(bf16_lo(w[i]), sc.s)), 0.0f);
+                if (!(fabsf(dist[2 * i + 1]) <= 0.5f - kTieGuard))
+                    q[2 * i + 1] = __fadd_rn(static_cast<float>(quant_exact(bf16_hi(w[i]), sc.s)), 0.0f);
+            }
+        }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(q[2 * i], q[2 * i + 1]);
+        o[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ void put_codes(uint2* __restrict__ q, uint4* __restrict__ img, int64_t i, uint2 c) {
     if (q) __stcs(q + i, c);
     if (img) {
