@@ -41,12 +41,16 @@ def parse():
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (rows of X)")
     ap.add_argument("--report-configs", action="store_true",
                     help="time every workload (tiny, square, FFN up, FFN down, ragged sweep) and print a table")
+    ap.add_argument("--report-ffn", action="store_true",
+                    help="time the FFN block fused (GELU + 1x128 quant in the up-projection epilogue) and unfused")
+    ap.add_argument("--report-norm", action="store_true",
+                    help="time the fused norm + quantization kernel against torch's norm + this library's quant")
     ap.add_argument("--profile-once", action="store_true",
                     help="only the W warm-up and K plain steps, no flush or side measurements (for ncu)")
     return ap.parse_args()
 
 
-GEMM_SOURCES = ["gemm.cu", "ptx.cuh", "kernels.h", "w8a8_device_error.cuh"]
+GEMM_SOURCES = ["gemm.cu", "ptx.cuh", "kernels.h", "quant_core.cuh", "w8a8_device_error.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic_square_postscale_4096.txt")
 
 
@@ -580,12 +584,147 @@ def report_configs(args):
               f"{r['x_int8_mma_peak']} | {r['quant_gbs']:.0f} | {r['torch_bf16_tflops']} | {r['oracle_tops']} |")
 
 
+def report_ffn(args):
+    """FFN block at the FFN shapes (X [32768, 5120] -> up 13824 -> GELU ->
+    down 5120): the fused path (up-projection with the GELU + 1x128
+    quantization epilogue, then the blockwise GEMM on its code image) against
+    the same W8A8 kernels unfused (post-scale Linear to bf16, GELU as a torch
+    op, then the blockwise Linear's own 1x128 quantization and GEMM)."""
+    import torch
+    import w8a8_int8_linear_gb300 as w
+    from w8a8_int8_linear_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    up, down = wl.FFN_UP, wl.FFN_DOWN
+    M, N1, K1, N2 = up.M, up.N, up.K, down.N
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    X = wl.make_x(up, dev)
+    W1 = wl.make_w(up, dev)
+    b1 = wl.make_bias(up, dev)
+    W2 = wl.make_w(down, dev)
+    Wq1, sw1 = w.quantize_weight(W1, w.PER_ROW)
+    W1img = w.pack_weight(Wq1)
+    Wq2, sw2 = w.quantize_weight(W2, w.BLOCK)
+    W2img = w.pack_weight(Wq2)
+    del W1, W2, Wq1, Wq2
+    G = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+    sg = torch.empty((M, N1 // 128), dtype=torch.float32, device=dev)
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    Y1 = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty((M, N2), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(w.linear_workspace_size(M, N1, K1), w.linear_workspace_size(M, N2, N1)),
+                     dtype=torch.uint8, device=dev)
+
+    def timed(fn, reps=8):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c))
+        return statistics.median(ts)
+
+    t = {}
+    t["up_fused"] = timed(lambda: w.linear_postscale_gelu_quant(X, W1img, sw1, b1, out=G, sg_out=sg, workspace=ws,
+                                                                sx_out=sx))
+    t["down_on_image"] = timed(lambda: w.gemm_blockwise_images(G, sg, W2img, sw2, out=Y2))
+    t["up_plain"] = timed(lambda: w.linear_postscale(X, W1img, sw1, b1, out=Y1, workspace=ws, sx_out=sx))
+    t["gelu_torch"] = timed(lambda: torch.nn.functional.gelu(Y1))
+    sx2 = torch.empty((M, N1 // 128), dtype=torch.float32, device=dev)
+    t["down_linear"] = timed(lambda: w.linear_blockwise(Y1, W2img, sw2, out=Y2, workspace=ws, sx_out=sx2))
+    assert w.get_device_error() == (0, 0)
+    ops = 2.0 * M * K1 * N1 + 2.0 * M * N1 * N2
+    fused = t["up_fused"] + t["down_on_image"]
+    unfused = t["up_plain"] + t["gelu_torch"] + t["down_linear"]
+    r = dict(workload=f"ffn_block_{M}x{K1}-{N1}-{N2}", ms={k: round(v, 4) for k, v in t.items()},
+             fused_ms=round(fused, 4), unfused_ms=round(unfused, 4), fused_tops=round(ops / fused / 1e9, 1),
+             unfused_tops=round(ops / unfused / 1e9, 1), saved_ms=round(unfused - fused, 4))
+    print(json.dumps(r), flush=True)
+    return r
+
+
+def report_norm(args):
+    """Fused normalization + per-token quantization (one read of X, codes
+    image and scales out) at the square and FFN-up activation shapes, against
+    the unfused pair (torch's norm to bf16, then this library's quantization).
+    Algorithmic bytes: read X (2 B/element) + gamma/beta once, write the image
+    (2 B/element) and the scales."""
+    import torch
+    import w8a8_int8_linear_gb300 as w
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c))
+        return statistics.median(ts)
+
+    out = []
+    for (M, K) in ((4096, 4096), (32768, 5120)):
+        g = torch.Generator(device=dev).manual_seed(0)
+        X = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        gamma = (1.0 + 0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
+        beta = (0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
+        img = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        sx = torch.empty((M,), dtype=torch.float32, device=dev)
+        for kind, name in ((w.RMS_NORM, "rms"), (w.LAYER_NORM, "layer")):
+            bb = beta if kind == w.LAYER_NORM else None
+            lib = w.lib()
+            stream = w._stream
+
+            def fused():
+                w._check("w8a8_norm_quant", lib.w8a8_norm_quant(
+                    w._ptr(X), w._ptr(gamma), w._ptr(bb), 1e-5, kind, M, K, None, None, w._ptr(img), w._ptr(sx),
+                    stream()))
+
+            if kind == w.RMS_NORM:
+                def torch_norm():
+                    return torch.nn.functional.rms_norm(X, (K,), gamma, 1e-5)
+            else:
+                def torch_norm():
+                    return torch.nn.functional.layer_norm(X, (K,), gamma, beta, 1e-5)
+            Yn = torch_norm()
+            Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+            t_f = timed(fused)
+            t_n = timed(torch_norm)
+            t_q = timed(lambda: w.quantize_act(Yn, w.PER_ROW, out=(Xq, sx)))
+            bytes_ = M * K * 4 + M * 4 + K * 4
+            r = dict(workload=f"norm_quant_{name}_{M}x{K}", fused_us=round(t_f * 1e3, 2),
+                     unfused_us=round((t_n + t_q) * 1e3, 2), torch_norm_us=round(t_n * 1e3, 2),
+                     quant_us=round(t_q * 1e3, 2), fused_gbs=round(bytes_ / t_f / 1e6, 0),
+                     frac_hbm=round(bytes_ / t_f / 1e6 / peaks["hbm_gbs"], 3))
+            out.append(r)
+            print(json.dumps(r), flush=True)
+    assert w.get_device_error() == (0, 0)
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.report_configs:
         report_configs(args)
+    elif args.report_ffn:
+        report_ffn(args)
+    elif args.report_norm:
+        report_norm(args)
     else:
         run_w8a8(args)
 

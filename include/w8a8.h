@@ -243,7 +243,7 @@ typedef enum {
  *   X [M,K] bf16, gamma / beta [K] bf16 or NULL (beta only for LAYER), eps >= 0,
  *   Y [M,K] bf16 out or NULL (the normalized row), Xq [M,K] int8 out or NULL,
  *   Ximg [M,K] bf16 out or NULL (exact image of Xq, the GEMM's operand),
- *   sx [M] fp32 out.  K % 8 == 0 and K <= 32768 (else W8A8_ERR_SHAPE).
+ *   sx [M] fp32 out.  K % 8 == 0 and K <= 16384 (else W8A8_ERR_SHAPE).
  */
 W8A8_API w8a8_status w8a8_norm_quant(const void* X, const void* gamma, const void* beta, float eps,
                                      w8a8_norm_kind kind, int64_t M, int64_t K, void* Y, int8_t* Xq, void* Ximg,

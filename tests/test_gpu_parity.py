@@ -385,7 +385,7 @@ def test_ffn_up_gelu_quant_rejects_bad_arguments(w8a8):
 
 # ----------------------------------------------------------------- normalization fused with quantization
 @pytest.mark.parametrize("layer", [False, True])
-@pytest.mark.parametrize("M,K", [(1, 8), (7, 128), (33, 264), (300, 4096), (64, 5120), (5, 13824), (3, 32768),
+@pytest.mark.parametrize("M,K", [(1, 8), (7, 128), (33, 264), (300, 4096), (64, 5120), (5, 13824), (3, 16384),
                                  (1000, 1040)])
 def test_norm_quant(w8a8, oracle, layer, M, K):
     X = rand_bf16((M, K), seed=60 + K, scale=2.0, outliers=0.01, oscale=30.0)
@@ -432,8 +432,8 @@ def test_norm_quant_rejects_bad_arguments(w8a8):
     X = torch.zeros((4, 36), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(w8a8.W8A8Error, match="SHAPE"):       # K % 8 != 0
         w8a8.norm_quant(X)
-    X = torch.zeros((2, 65536), dtype=torch.bfloat16, device=DEV)
-    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):       # K > 32768
+    X = torch.zeros((2, 16392), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):       # K > 16384
         w8a8.norm_quant(X)
     with pytest.raises(w8a8.W8A8Error, match="INVALID_ARG"):  # negative eps
         w8a8.norm_quant(torch.zeros((2, 64), dtype=torch.bfloat16, device=DEV), eps=-1.0)

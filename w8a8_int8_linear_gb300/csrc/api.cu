@@ -364,7 +364,7 @@ w8a8_status w8a8_norm_quant(const void* X, const void* gamma, const void* beta, 
                             int64_t M, int64_t K, void* Y, int8_t* Xq, void* Ximg, float* sx, void* stream) {
     if (M < 0 || K <= 0) return W8A8_ERR_INVALID_ARG;
     if (kind != W8A8_NORM_RMS && kind != W8A8_NORM_LAYER) return W8A8_ERR_INVALID_ARG;
-    if (K % 8 != 0 || K > 32768 || M > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (K % 8 != 0 || K > 16384 || M > INT32_MAX) return W8A8_ERR_SHAPE;
     if (M == 0) return W8A8_OK;
     if (!X || !sx) return W8A8_ERR_INVALID_ARG;
     if (!(eps >= 0.0f)) return W8A8_ERR_INVALID_ARG;  // also rejects NaN

@@ -23,7 +23,7 @@ cudaError_t launch_quant_weight_block(const void* W, int64_t N, int64_t K, int8_
 cudaError_t launch_expand_s8_bf16(const int8_t* src, int64_t n, void* dst, int num_sms, cudaStream_t st);
 
 // RMSNorm (layer = 0) or LayerNorm (layer = 1) of bf16 X[M,K] fused with
-// per-token quantization; K % 8 == 0, K <= 32768.  gamma / beta (bf16 [K]) and
+// per-token quantization; K % 8 == 0, K <= 16384.  gamma / beta (bf16 [K]) and
 // the outputs Y (normalized bf16), Xq (int8), img (bf16 image of Xq) may be null.
 cudaError_t launch_norm_quant(const void* X, const void* gamma, const void* beta, float eps, int layer, int64_t M,
                               int64_t K, void* Y, int8_t* Xq, void* img, float* sx, cudaStream_t st);

@@ -14,13 +14,14 @@
 //
 // S() has a fixed order that does not depend on the launch shape: chunks of 8
 // consecutive elements summed left to right, then the chunk sums, zero-padded
-// to P = the next power of two of K/8, added pairwise level by level.  A CTA
-// of T threads gives thread t the C consecutive chunks [tC, (t+1)C) with
-// T*C = P (or T = 32 and only the first P/C threads holding chunks when
-// P/C < 32); the first log2(C) levels of the tree are inside a thread, the
-// next ones XOR shuffles between lanes (lane t and t^o hold adjacent subtrees;
-// IEEE addition is commutative, so both get the same sum), the last ones the
-// same butterfly over the per-warp sums.
+// to P = the next power of two of K/8, added pairwise level by level.  Thread
+// t of a row's CTA owns the C consecutive chunks [tC, (t+1)C), so the tree
+// spans P/C threads; only the warps that hold real chunks are launched (the
+// others would hold padding, whose subtree sums are +0 and enter the tree as
+// such).  The first log2(C) levels of the tree are inside a thread, the next
+// ones XOR shuffles between lanes (lane t and t^o hold adjacent subtrees; IEEE
+// addition is commutative, so both get the same sum), the last ones the same
+// butterfly over the per-warp sums.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -34,34 +35,36 @@ namespace w8a8 {
 
 namespace {
 
-// Pairwise tree over the block's per-thread subtree sums (threads [0, tree)
-// hold subtrees in chunk order; tree is a power of two).  Every thread gets
-// the total.
+// Pairwise tree over the per-thread subtree sums of `tree` threads (a power
+// of two) in chunk order.  Threads the launch leaves out (the warps from
+// blockDim.x / 32 up to tree / 32) would hold only padding; their subtree
+// sums are +0, which is what enters the tree in their place.  Every thread
+// gets the total.  `red` is this reduction's own scratch, so one barrier
+// suffices.
 __device__ __forceinline__ float tree_sum_block(float v, int tree, float* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int lanes = tree < 32 ? tree : 32;
     for (int o = 1; o < lanes; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
     if (tree <= 32) return __shfl_sync(0xffffffffu, v, 0);
     const int W = tree >> 5;
+    const int launched = static_cast<int>(blockDim.x >> 5);
     if (lane == 0) red[warp] = v;
     __syncthreads();
-    float t = (lane < W) ? red[lane] : 0.0f;
+    float t = (lane < W && lane < launched) ? red[lane] : 0.0f;
     for (int o = 1; o < W; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
-    t = __shfl_sync(0xffffffffu, t, 0);
-    __syncthreads();  // red[] is reused by the next reduction
-    return t;
+    return __shfl_sync(0xffffffffu, t, 0);
 }
 
 __device__ __forceinline__ float block_absmax(float v, float* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (nw == 1) return v;
     if (lane == 0) red[warp] = v;
     __syncthreads();
     float t = (lane < nw) ? red[lane] : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-    __syncthreads();
     return t;
 }
 
@@ -85,92 +88,129 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     }
 }
 
-template <int C>
-__global__ void __launch_bounds__(512) norm_quant_kernel(const uint4* __restrict__ X, const uint4* __restrict__ gamma,
-                                                         const uint4* __restrict__ beta, float eps, int layer,
-                                                         int K, int tree, uint4* __restrict__ Y,
-                                                         uint2* __restrict__ Xq, uint4* __restrict__ img,
-                                                         float* __restrict__ sx) {
-    __shared__ float red[32];
+// The normalized bf16 values of one chunk, packed.  d = x - mu and d * r run
+// two values at a time on the packed fp32 pipe (a subtraction feeding a
+// multiplication, which is never contracted); a product that an addition
+// consumes (gamma before beta) stays scalar with explicit rounding.
+__device__ __forceinline__ uint4 normalize_chunk(const uint4& v, const uint4* __restrict__ gamma,
+                                                 const uint4* __restrict__ beta, int layer, int c, float mu,
+                                                 float r) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t gw[4] = {0, 0, 0, 0}, bw[4] = {0, 0, 0, 0};
+    if (gamma) {
+        const uint4 t = __ldg(gamma + c);
+        gw[0] = t.x; gw[1] = t.y; gw[2] = t.z; gw[3] = t.w;
+    }
+    const bool add_beta = layer && beta;
+    if (add_beta) {
+        const uint4 t = __ldg(beta + c);
+        bw[0] = t.x; bw[1] = t.y; bw[2] = t.z; bw[3] = t.w;
+    }
+    const uint64_t r2 = f2_pack(r, r);
+    const uint64_t mu2 = f2_pack(mu, mu);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint64_t d = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+        if (layer) d = f2_sub(d, mu2);
+        float y0, y1;
+        if (add_beta) {
+            f2_unpack(d, y0, y1);
+            y0 = __fmul_rn(y0, r);
+            y1 = __fmul_rn(y1, r);
+            if (gamma) {
+                y0 = __fmul_rn(y0, bf16_lo(gw[i]));
+                y1 = __fmul_rn(y1, bf16_hi(gw[i]));
+            }
+            y0 = __fadd_rn(y0, bf16_lo(bw[i]));
+            y1 = __fadd_rn(y1, bf16_hi(bw[i]));
+        } else {
+            uint64_t t = f2_mul(d, r2);
+            if (gamma) t = f2_mul(t, f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i])));
+            f2_unpack(t, y0, y1);
+        }
+        __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+        o[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One CTA per row; thread t owns chunks [tC, (t+1)C).  The row stays in
+// registers as bf16, and so do its normalized values between the absmax and
+// the quantization.
+template <int C, int TMAX, int MINB>
+__global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __restrict__ X,
+                                                                const uint4* __restrict__ gamma,
+                                                                const uint4* __restrict__ beta, float eps,
+                                                                int layer, int K, int tree, uint4* __restrict__ Y,
+                                                                uint2* __restrict__ Xq, uint4* __restrict__ img,
+                                                                float* __restrict__ sx) {
+    __shared__ float red[3][32];
     const int64_t row = blockIdx.x;
     const int chunks = K >> 3;
     const uint4* x = X + row * chunks;
     const int c0 = threadIdx.x * C;
     uint4 v[C];
 #pragma unroll
-    for (int i = 0; i < C; ++i) v[i] = (c0 + i < chunks) ? __ldcs(x + c0 + i) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < C; ++i) v[i] = (c0 + i < chunks) ? __ldg(x + c0 + i) : make_uint4(0, 0, 0, 0);
     const float Kf = static_cast<float>(K);
     float mu = 0.0f;
     if (layer) {
         float s[C];
 #pragma unroll
         for (int i = 0; i < C; ++i) {
-            float f[8];
-            unpack8(v[i], f);
-            float a = f[0];
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            float a = bf16_lo(w[0]);
+            a = __fadd_rn(a, bf16_hi(w[0]));
 #pragma unroll
-            for (int j = 1; j < 8; ++j) a = __fadd_rn(a, f[j]);
+            for (int j = 1; j < 4; ++j) {
+                a = __fadd_rn(a, bf16_lo(w[j]));
+                a = __fadd_rn(a, bf16_hi(w[j]));
+            }
             s[i] = (c0 + i < chunks) ? a : 0.0f;
         }
-        mu = __fdiv_rn(tree_sum_block(tree_sum_local(s), tree, red), Kf);
+        mu = __fdiv_rn(tree_sum_block(tree_sum_local(s), tree, red[0]), Kf);
     }
     float s[C];
 #pragma unroll
     for (int i = 0; i < C; ++i) {
-        float f[8];
-        unpack8(v[i], f);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
         float a = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float d = layer ? __fsub_rn(f[j], mu) : f[j];
-            const float t = __fmul_rn(d, d);
-            a = (j == 0) ? t : __fadd_rn(a, t);
+        for (int j = 0; j < 4; ++j) {
+            float d0 = bf16_lo(w[j]), d1 = bf16_hi(w[j]);
+            if (layer) {
+                d0 = __fsub_rn(d0, mu);
+                d1 = __fsub_rn(d1, mu);
+            }
+            const float t0 = __fmul_rn(d0, d0), t1 = __fmul_rn(d1, d1);
+            a = (j == 0) ? t0 : __fadd_rn(a, t0);
+            a = __fadd_rn(a, t1);
         }
         s[i] = (c0 + i < chunks) ? a : 0.0f;
     }
-    const float var = __fdiv_rn(tree_sum_block(tree_sum_local(s), tree, red), Kf);
+    const float var = __fdiv_rn(tree_sum_block(tree_sum_local(s), tree, red[1]), Kf);
     const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
-    uint4 yv[C];
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < C; ++i) {
         const int c = c0 + i;
-        if (c >= chunks) {
-            yv[i] = make_uint4(0, 0, 0, 0);
-            continue;
+        if (c < chunks) {
+            v[i] = normalize_chunk(v[i], gamma, beta, layer, c, mu, r);  // v now holds y
+            amax = fmaxf(amax, chunk_absmax(v[i]));
         }
-        float f[8], g[8], b[8];
-        unpack8(v[i], f);
-        if (gamma) unpack8(__ldg(gamma + c), g);
-        if (layer && beta) unpack8(__ldg(beta + c), b);
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-            float y0 = __fmul_rn(layer ? __fsub_rn(f[j], mu) : f[j], r);
-            float y1 = __fmul_rn(layer ? __fsub_rn(f[j + 1], mu) : f[j + 1], r);
-            if (gamma) {
-                y0 = __fmul_rn(y0, g[j]);
-                y1 = __fmul_rn(y1, g[j + 1]);
-            }
-            if (layer && beta) {
-                y0 = __fadd_rn(y0, b[j]);
-                y1 = __fadd_rn(y1, b[j + 1]);
-            }
-            __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
-            o[j >> 1] = *reinterpret_cast<uint32_t*>(&h);
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(o[j >> 1])), fabsf(bf16_hi(o[j >> 1]))));
-        }
-        yv[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    amax = block_absmax(amax, red);
+    amax = block_absmax(amax, red[2]);
     const RowScale sc = make_scale_div(amax);
     if (threadIdx.x == 0) sx[row] = sc.s;
 #pragma unroll
     for (int i = 0; i < C; ++i) {
         const int c = c0 + i;
         if (c >= chunks) continue;
-        if (Y) Y[row * chunks + c] = yv[i];
-        if (Xq || img) put_codes(Xq, img, row * chunks + c, quant_chunk(yv[i], sc));
+        const int64_t o = row * chunks + c;
+        if (Y) Y[o] = v[i];
+        if (img) img[o] = quant_chunk_img(v[i], sc);
+        if (Xq) __stcs(Xq + o, quant_chunk(v[i], sc));
     }
 }
 
@@ -188,13 +228,18 @@ cudaError_t launch_norm_quant(const void* X, const void* gamma, const void* beta
     uint4* y = static_cast<uint4*>(Y);
     uint2* q = reinterpret_cast<uint2*>(Xq);
     uint4* im = static_cast<uint4*>(img);
+    // C chunks per thread; only the warps that hold real chunks are
+    // launched, the tree still spans P / C threads.
+    const int k = static_cast<int>(K);
+    auto warps_for = [&](int C) { return ((chunks + C - 1) / C + 31) / 32; };
     if (P <= 32) {
-        norm_quant_kernel<1><<<grid, 32, 0, st>>>(x, g, b, eps, layer, static_cast<int>(K), P, y, q, im, sx);
-    } else if (P <= 512) {
-        const int T = P / 4 < 32 ? 32 : P / 4;
-        norm_quant_kernel<4><<<grid, T, 0, st>>>(x, g, b, eps, layer, static_cast<int>(K), P / 4, y, q, im, sx);
+        norm_quant_kernel<1, 32, 16><<<grid, 32, 0, st>>>(x, g, b, eps, layer, k, P, y, q, im, sx);
+    } else if (P <= 1024) {
+        norm_quant_kernel<4, 256, 3><<<grid, 32 * warps_for(4), 0, st>>>(x, g, b, eps, layer, k, P / 4, y, q, im,
+                                                                          sx);
     } else {
-        norm_quant_kernel<8><<<grid, P / 8, 0, st>>>(x, g, b, eps, layer, static_cast<int>(K), P / 8, y, q, im, sx);
+        norm_quant_kernel<8, 256, 1><<<grid, 32 * warps_for(8), 0, st>>>(x, g, b, eps, layer, k, P / 8, y, q, im,
+                                                                          sx);
     }
     return cudaGetLastError();
 }

@@ -159,11 +159,9 @@ __device__ __forceinline__ uint4 quant_chunk_img(const uint4& v, const RowScale&
             const uint64_t bg = f2_fma(x2, inv2, magic2);  // rne(P) + 1.5*2^23
             const uint64_t nr = f2_sub(magic2, bg);        // -rne(P), exact
             const uint64_t d = f2_fma(x2, inv2, nr);       // P - rne(P), rounded once
-            float n0, n1, d0, d1;
-            f2_unpack(nr, n0, n1);
+            float d0, d1;
+            f2_unpack(f2_sub(bg, magic2), q[2 * i], q[2 * i + 1]);  // rne(P), exact (+0 for 0)
             f2_unpack(d, d0, d1);
-            q[2 * i] = __fsub_rn(0.0f, n0);
-            q[2 * i + 1] = __fsub_rn(0.0f, n1);
             dist[2 * i] = d0;
             dist[2 * i + 1] = d1;
             dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
