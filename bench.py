@@ -45,6 +45,8 @@ def parse():
                     help="time the FFN block fused (GELU + 1x128 quant in the up-projection epilogue) and unfused")
     ap.add_argument("--report-norm", action="store_true",
                     help="time the fused norm + quantization kernel against torch's norm + this library's quant")
+    ap.add_argument("--report-decode", action="store_true",
+                    help="few-token Linears in steady state (CUDA graph over weight copies larger than L2)")
     ap.add_argument("--profile-once", action="store_true",
                     help="only the W warm-up and K plain steps, no flush or side measurements (for ncu)")
     return ap.parse_args()
@@ -715,6 +717,68 @@ def report_norm(args):
     return out
 
 
+def report_decode(args):
+    """Few-token Linears (M <= 256 takes the swapped split-K path) in steady
+    state: one CUDA graph of C calls, each on its own weight copy, with the C
+    copies together larger than L2, replayed back to back; per-call time is
+    the replay time / C.  The same for torch's bf16 matmul on C bf16 weights."""
+    import torch
+    import w8a8_int8_linear_gb300 as w
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    K = 5120
+
+    def graph_time(fns, reps=10):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for f in fns:
+                f()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for f in fns:
+                f()
+        for _ in range(3):
+            g.replay()
+        ts = []
+        for _ in range(reps):
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c) * 1e3 / len(fns))
+        return statistics.median(ts)
+
+    out = []
+    gen = torch.Generator(device=dev).manual_seed(0)
+    for N in (3072, 5120, 13824):
+        C = max(4, -(-400_000_000 // (N * K * 2)))
+        Ws = [(0.02 * torch.randn((N, K), generator=gen, device=dev)).to(torch.bfloat16) for _ in range(C)]
+        packs = []
+        for W in Ws:
+            Wq, sw = w.quantize_weight(W)
+            packs.append((w.pack_weight(Wq), sw))
+        b = (0.01 * torch.randn((N,), generator=gen, device=dev)).to(torch.bfloat16)
+        for M in (1, 16, 77, 128, 256):
+            X = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            sx = torch.empty((M,), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(w.linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
+            t_lin = graph_time([lambda P=P: w.linear_postscale(X, P[0], P[1], b, out=Y, workspace=ws, sx_out=sx)
+                                for P in packs])
+            t_mm = graph_time([lambda W=W: torch.matmul(X, W.t(), out=Y) for W in Ws])
+            r = dict(workload=f"decode_{M}x{N}x{K}", copies=C, linear_us=round(t_lin, 2),
+                     torch_bf16_us=round(t_mm, 2), image_gbs=round(N * K * 2 / t_lin / 1e3, 0))
+            out.append(r)
+            print(json.dumps(r), flush=True)
+        del Ws, packs
+        torch.cuda.empty_cache()
+    assert w.get_device_error() == (0, 0)
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -725,6 +789,8 @@ def main():
         report_ffn(args)
     elif args.report_norm:
         report_norm(args)
+    elif args.report_decode:
+        report_decode(args)
     else:
         run_w8a8(args)
 
