@@ -81,16 +81,21 @@ constexpr int kSplitTargetUnits = 72;       // split K until about this many CTA
 constexpr int kSplitMinStages = 4;          // at least 256 K per split
 constexpr int kSplitMax = 8;
 
-// Per-tile-width constants.
-template <int BN_>
+// Shared memory of the FFN up-projection's staged GELU input: one bf16 row
+// of 128 columns per epilogue thread (8 warps x 32 rows x 256 bytes).
+constexpr uint32_t YSTAGE_BYTES = EPI_WARPS * 32 * 256;
+
+// Per-tile-width constants; EXTRA bytes of shared memory are taken from the ring.
+template <int BN_, uint32_t EXTRA = 0>
 struct Cfg {
     static constexpr int BN = BN_;
     static constexpr int HALF = BN / 2;  // B rows per CTA = output columns per epilogue warp
     static_assert(HALF % 16 == 0 && BN <= 256, "tile width");
     static constexpr uint32_t B_BYTES = HALF * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : int(RING_BUDGET / STAGE_BYTES);
-    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + 256;
+    static constexpr uint32_t RING = RING_BUDGET - EXTRA;
+    static constexpr int STAGES = (RING / STAGE_BYTES) > 8 ? 8 : int(RING / STAGE_BYTES);
+    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + EXTRA + 256;
     static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
     static constexpr int LDW = (HALF % 32 == 0) ? 32 : 16;  // TMEM load width (columns)
     static constexpr int GROUPS = HALF / LDW;
@@ -395,77 +400,100 @@ __device__ __forceinline__ uint32_t gelu_erf_bf16x2(float x0, float x1) {
     return pack_bf16x2(g0, g1);
 }
 
-// FFN up-projection epilogue.  For this thread's row and its 128 columns --
-// exactly one 1x128 block of the down-projection's input --
+// FFN up-projection epilogue, staged.  For each thread's row and its 128
+// columns -- exactly one 1x128 block of the down-projection's input --
 //   y = bf16(((acc * sx) * sw) + bias)   (the post-scale epilogue),
 //   g = bf16(gelu(y)),
 //   s = absmax(|g|) / 127, codes = clamp(rne(g / s), -127, 127),
 // with the scale written to sg[row][col0 / 128] and the exact bf16 image of
 // the codes (the down-projection GEMM's A operand) stored through TMA.
-// The GELU pass is a rolled loop over four 32-column groups: each iteration
-// works on acc[0..31], then shifts the array down by 32 and parks its 16
-// packed results in acc[96..111], so the loop body has fixed register names
-// and the code stays small; afterwards group q's results sit in acc[32q ..
-// 32q + 15].
+// y leaves the registers at the end of its tile: each thread parks its 256
+// bytes in its own row of shared memory (16-byte chunk j at position
+// j ^ (lane & 7), which puts the 8 lanes of a quarter-warp on 8 different
+// bank groups), and the GELU and quantization then run in eight slices
+// spread over the chunk folds of the next tile.
+struct GeluStage {
+    int row, row_base, col0;  // this thread's staged block
+    int slice;                // next slice, 0..7; 8 = nothing pending
+    float amax;
+    RowScale sc;
+};
+
+__device__ __forceinline__ uint4* ychunk(uint8_t* yrow, int j, int lane) {
+    return reinterpret_cast<uint4*>(yrow + ((j ^ (lane & 7)) << 4));
+}
+
 template <int COLS>
-__device__ __forceinline__ void store_gelu_quant(int32_t (&acc)[COLS], const KParams& p, const CUtensorMap* tmY,
-                                                 int row, int row_base, int col0, uint8_t* stg, int& sbuf,
-                                                 int lane) {
+__device__ __forceinline__ void stage_y(const int32_t (&acc)[COLS], const KParams& p, int row, int col0,
+                                        uint8_t* yrow, int lane) {
     static_assert(COLS == 128, "one 1x128 block per thread");
-    if (col0 >= p.N) return;  // N % 128 == 0: a block is all in range or all out
     const float sxr = (row < p.M) ? __ldg(p.sx + row) : 0.0f;
     const uint16_t* bias16 = reinterpret_cast<const uint16_t*>(p.bias);
-    float amax = 0.0f;
-#pragma unroll 1
-    for (int it = 0; it < 4; ++it) {
-        const int col = col0 + it * 32;
-        uint32_t gnew[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-            const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.sw + col + j));
-            const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.sw + col + j + 4));
-            const float swc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-            float bc[8];
-            if (p.bias) {
-                const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col + j));
-                const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    for (int j = 0; j < COLS / 8; ++j) {
+        const int col = col0 + 8 * j;
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.sw + col));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.sw + col + 4));
+        const float swc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        float bc[8];
+        if (p.bias) {
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias16 + col));
+            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    bc[2 * f] = __uint_as_float(bw[f] << 16);
-                    bc[2 * f + 1] = __uint_as_float(bw[f] & 0xFFFF0000u);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e]), sxr), swc[e]);
-                float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[j + e + 1]), sxr), swc[e + 1]);
-                if (p.bias) {
-                    v0 = __fadd_rn(v0, bc[e]);
-                    v1 = __fadd_rn(v1, bc[e + 1]);
-                }
-                const uint32_t y2 = pack_bf16x2(v0, v1);  // y = bf16(...)
-                const uint32_t g2 = gelu_erf_bf16x2(bf16_lo(y2), bf16_hi(y2));
-                gnew[(j + e) >> 1] = g2;
-                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(g2)), fabsf(bf16_hi(g2))));
+            for (int f = 0; f < 4; ++f) {
+                bc[2 * f] = __uint_as_float(bw[f] << 16);
+                bc[2 * f + 1] = __uint_as_float(bw[f] & 0xFFFF0000u);
             }
         }
+        uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 96; ++i) acc[i] = acc[i + 32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[96 + i] = static_cast<int32_t>(gnew[i]);
+        for (int e = 0; e < 8; e += 2) {
+            float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * j + e]), sxr), swc[e]);
+            float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[8 * j + e + 1]), sxr), swc[e + 1]);
+            if (p.bias) {
+                v0 = __fadd_rn(v0, bc[e]);
+                v1 = __fadd_rn(v1, bc[e + 1]);
+            }
+            o[e >> 1] = pack_bf16x2(v0, v1);
+        }
+        *ychunk(yrow, j, lane) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    const RowScale sc = make_scale_div(amax);
-    if (row < p.M) p.sg[static_cast<int64_t>(row) * (p.N >> 7) + (col0 >> 7)] = sc.s;
+}
+
+// One slice of the staged block.  Slices 0-3: g = bf16(gelu(y)) for columns
+// 32s .. 32s+31, written back in place, and the running absmax (after slice 3
+// the block scale is known and stored).  Slices 4-7: the codes of columns
+// 32(s-4) .. +31 as their bf16 image, out through two 16 x 32 TMA boxes.
+__device__ __forceinline__ void gelu_slice(GeluStage& gs, const KParams& p, const CUtensorMap* tmY, uint8_t* yrow,
+                                           uint8_t* stg, int& sbuf, int lane) {
+    const int s = gs.slice++;
+    if (s < 4) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 4; ++q) {
+            uint4* ptr = ychunk(yrow, 4 * s + q, lane);
+            const uint4 v = *ptr;
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t g[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                g[i] = gelu_erf_bf16x2(bf16_lo(w[i]), bf16_hi(w[i]));
+                gs.amax = fmaxf(gs.amax, fmaxf(fabsf(bf16_lo(g[i])), fabsf(bf16_hi(g[i]))));
+            }
+            *ptr = make_uint4(g[0], g[1], g[2], g[3]);
+        }
+        if (s == 3) {
+            gs.sc = make_scale_div(gs.amax);
+            if (gs.row < p.M) p.sg[static_cast<int64_t>(gs.row) * (p.N >> 7) + (gs.col0 >> 7)] = gs.sc.s;
+        }
+    } else {
+        const int b = s - 4;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int w0 = 32 * q + 8 * h;
-            const uint32_t* gw = reinterpret_cast<const uint32_t*>(acc);
-            const uint4 c0 = quant_chunk_img(make_uint4(gw[w0], gw[w0 + 1], gw[w0 + 2], gw[w0 + 3]), sc);
-            const uint4 c1 = quant_chunk_img(make_uint4(gw[w0 + 4], gw[w0 + 5], gw[w0 + 6], gw[w0 + 7]), sc);
+            const int j0 = 4 * b + 2 * h;
+            const uint4 c0 = quant_chunk_img(*ychunk(yrow, j0, lane), gs.sc);
+            const uint4 c1 = quant_chunk_img(*ychunk(yrow, j0 + 1, lane), gs.sc);
             const uint32_t o[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            stage_store16(o, tmY, col0 + 32 * q + 16 * h, row_base, stg, sbuf, lane);
+            stage_store16(o, tmY, gs.col0 + 32 * b + 16 * h, gs.row_base, stg, sbuf, lane);
         }
     }
 }
@@ -550,7 +578,7 @@ template <int EPI, int BN, bool SWAP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const KParams p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, EPI == kEpiGeluQuant ? YSTAGE_BYTES : 0u>;
     constexpr int STAGES = C::STAGES;
     constexpr int HALF = C::HALF;
     extern __shared__ uint8_t smem_raw[];
@@ -558,7 +586,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_BYTES;
     uint8_t* staging = sB + STAGES * C::B_BYTES;  // 1 KB aligned
-    uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
+    uint8_t* ystage = staging + STAGING_BYTES;  // kEpiGeluQuant only (1 KB aligned)
+    uint64_t* full = reinterpret_cast<uint64_t*>(ystage + (EPI == kEpiGeluQuant ? YSTAGE_BYTES : 0u));
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -705,6 +734,75 @@ __global__ void __launch_bounds__(THREADS, 1)
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
+        if constexpr (EPI == kEpiGeluQuant) {
+            // Tile t's y is staged at the end of t; its eight GELU /
+            // quantization slices run ceil(8 / chunks) at a time after the
+            // chunk folds of tile t+1 (the rest at its last chunk, or after
+            // the last tile), so the MMA never waits behind a whole tile's
+            // GELU for a free accumulator buffer.
+            uint8_t* yrow = ystage + (warp - EPI_WARP0) * (32 * 256) + lane * 256;
+            GeluStage gs;
+            gs.row = gs.row_base = gs.col0 = 0;
+            gs.slice = 8;
+            gs.amax = 0.0f;
+            gs.sc = make_scale_div(0.0f);
+            for (int u = cluster; ok; u += nclusters) {
+                const bool real = u < p.num_tiles;
+                if (!real && gs.slice >= 8) break;
+                int nchunks = 0, row_base = 0, col0 = 0;
+                if (real) {
+                    const Unit w = unit_coords(u, p);
+                    nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
+                    row_base = w.mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
+                    col0 = w.nb * BN + half * HALF;
+                }
+                const int passes = nchunks > 0 ? nchunks : 1;
+                const int per = (8 + passes - 1) / passes;
+                int32_t acc[HALF];
+#pragma unroll
+                for (int e = 0; e < HALF; ++e) acc[e] = 0;
+                for (int c = 0; c < passes; ++c) {
+                    if (real) {
+                        if (!mbar_wait(&acc_full[buf], buf_phase, kSiteEpiAccFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                               static_cast<uint32_t>(buf * BN + half * HALF);
+                        uint32_t ra[LDW], rb[LDW];
+                        tmem_ld_cols<LDW>(taddr, ra);
+                        tmem_wait_cols(ra);
+#pragma unroll
+                        for (int j = 0; j < GROUPS; ++j) {
+                            uint32_t(&cur)[LDW] = (j & 1) ? rb : ra;
+                            uint32_t(&nxt)[LDW] = (j & 1) ? ra : rb;
+                            if (j + 1 < GROUPS) tmem_ld_cols<LDW>(taddr + (j + 1) * LDW, nxt);
+#pragma unroll
+                            for (int e = 0; e < LDW; ++e) acc[j * LDW + e] += __float2int_rz(__uint_as_float(cur[e]));
+                            if (j + 1 < GROUPS) tmem_wait_cols(nxt);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_cluster_relaxed(leader_acc_empty0 + static_cast<uint32_t>(buf) * 8u);
+                        buf ^= 1;
+                        if (buf == 0) buf_phase ^= 1u;
+                    }
+                    int todo = (c + 1 == passes) ? 8 : per;
+                    while (gs.slice < 8 && todo-- > 0) gelu_slice(gs, p, &tmY, yrow, stg, sbuf, lane);
+                }
+                if (!ok || !real) break;
+                if (col0 < p.N) {
+                    stage_y<HALF>(acc, p, row_base + lane, col0, yrow, lane);
+                    gs.row = row_base + lane;
+                    gs.row_base = row_base;
+                    gs.col0 = col0;
+                    gs.slice = 0;
+                    gs.amax = 0.0f;
+                }
+            }
+        } else {
         for (int u = cluster; ok && u < p.num_tiles; u += nclusters) {
             const Unit w = unit_coords(u, p);
             const int mb = w.mb, nb = w.nb;
@@ -779,14 +877,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     else
                         store_swapped<EPI, HALF>(acc, p, &tmY, row_base, col0, stg, sbuf, lane);
                 }
-            } else if constexpr (EPI == kEpiGeluQuant) {
-                store_gelu_quant<HALF>(acc, p, &tmY, row, row_base, col0, stg, sbuf, lane);
             } else if (kBf16Out && p.tma_store) {
                 store_rows_tma<EPI, HALF>(acc, p, &tmY, row, row_base, col0, stg, sbuf, lane);
             } else {
                 store_row<EPI, HALF>(acc, p, row, col0);
             }
         }
+        }  // EPI != kEpiGeluQuant
         if (lane == 0) bulk_wait_group_all();  // this warp's output stores have completed
         __syncwarp();
     }
@@ -861,7 +958,7 @@ constexpr int instance_id() {
 template <int EPI, int BN, bool SWAP>
 cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
                        int num_sms, cudaStream_t st, char* detail, size_t n) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, EPI == kEpiGeluQuant ? YSTAGE_BYTES : 0u>;
     CUtensorMap tmA, tmB;
     CUresult r = make_map(encode, &tmA, Ab, p.K, p.M, BK, BM);
     if (r != CUDA_SUCCESS) {
