@@ -759,7 +759,7 @@ def report_decode(args):
         packs = []
         for W in Ws:
             Wq, sw = w.quantize_weight(W)
-            packs.append((w.pack_weight(Wq), sw))
+            packs.append((w.pack_weight(Wq), sw, Wq))
         b = (0.01 * torch.randn((N,), generator=gen, device=dev)).to(torch.bfloat16)
         for M in (1, 16, 77, 128, 256):
             X = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
@@ -769,8 +769,14 @@ def report_decode(args):
             t_lin = graph_time([lambda P=P: w.linear_postscale(X, P[0], P[1], b, out=Y, workspace=ws, sx_out=sx)
                                 for P in packs])
             t_mm = graph_time([lambda W=W: torch.matmul(X, W.t(), out=Y) for W in Ws])
+            # the GEMM on int8 codes (X quantized beforehand): streams int8 weights
+            Xq, sxq = w.quantize_act(X)
+            wsg = torch.empty(max(w.workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
+            t_g8 = graph_time([lambda P=P: w.gemm_postscale(Xq, sxq, P[2], P[1], b, out=Y, workspace=wsg)
+                               for P in packs])
             r = dict(workload=f"decode_{M}x{N}x{K}", copies=C, linear_us=round(t_lin, 2),
-                     torch_bf16_us=round(t_mm, 2), image_gbs=round(N * K * 2 / t_lin / 1e3, 0))
+                     gemm_int8_us=round(t_g8, 2), torch_bf16_us=round(t_mm, 2),
+                     image_gbs=round(N * K * 2 / t_lin / 1e3, 0), int8_gbs=round(N * K / t_g8 / 1e3, 0))
             out.append(r)
             print(json.dumps(r), flush=True)
         del Ws, packs

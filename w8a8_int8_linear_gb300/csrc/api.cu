@@ -130,7 +130,8 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
 // GEMM on bf16 operand images, with the timing hook around the launch.
 w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float* sx, const float* sw,
                             const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* partial,
-                            const DeviceInfo& dev, cudaStream_t st, float* sg = nullptr) {
+                            const DeviceInfo& dev, cudaStream_t st, float* sg = nullptr,
+                            bool weights_settled = false, bool int8_operands = false) {
     void* enc = encode_fn();
     if (!enc) return W8A8_ERR_CUDA;
     w8a8::GemmArgs a;
@@ -143,6 +144,8 @@ w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float
     a.K = K;
     a.partial = static_cast<int32_t*>(partial);
     a.sg = sg;
+    a.weights_settled = weights_settled;
+    a.int8_operands = int8_operands;
     cudaError_t e;
     if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
     e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
@@ -175,8 +178,10 @@ w8a8_status run_linear(bool block, const void* X, const void* Wimg, const float*
                           : w8a8::launch_quant_rows(X, M, K, Xq, ws, sx, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
     void* partial = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K * 2);
+    // Wimg predates the quantization kernel just launched (which waited for
+    // all earlier work), so the GEMM may start reading it before that kernel ends.
     return run_gemm_images(block ? w8a8::kEpiBlockwiseBf16 : w8a8::kEpiPostscaleBf16, ws, Wimg, sx, sw, bias, Y, M,
-                           N, K, partial, dev, st);
+                           N, K, partial, dev, st, nullptr, true);
 }
 
 // Checks and launches of the fused FFN up-projection (quant, GEMM with the
@@ -199,7 +204,7 @@ w8a8_status run_linear_gelu_quant(const void* X, const void* Wimg, const float* 
     if ((s = current_device(&dev)) != W8A8_OK) return s;
     cudaError_t e = w8a8::launch_quant_rows(X, M, K, Xq, ws, sx, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
-    return run_gemm_images(w8a8::kEpiGeluQuant, ws, Wimg, sx, sw, bias, Gimg, M, N, K, nullptr, dev, st, sg);
+    return run_gemm_images(w8a8::kEpiGeluQuant, ws, Wimg, sx, sw, bias, Gimg, M, N, K, nullptr, dev, st, sg, true);
 }
 
 w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
@@ -208,6 +213,10 @@ w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* W
     void* enc = encode_fn();
     if (!enc) return W8A8_ERR_CUDA;
     uint8_t* w = static_cast<uint8_t*>(ws);
+    if (w8a8::gemm_takes_int8(epi, M)) {
+        // few tokens: the GEMM streams the int8 codes itself, no images
+        return run_gemm_images(epi, Xq, Wq, sx, sw, bias, out, M, N, K, w, dev, st, nullptr, false, true);
+    }
     void* Ab = w;
     void* Bb = w + align256(static_cast<size_t>(M) * K * 2);
     void* partial = static_cast<uint8_t*>(Bb) + align256(static_cast<size_t>(N) * K * 2);

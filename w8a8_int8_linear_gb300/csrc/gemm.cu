@@ -40,6 +40,7 @@
 // folded.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -77,6 +78,7 @@ constexpr int POSTSCALE_CHUNK_STAGES = 16;  // 1024 K: 127*127*1024 < 2^24
 constexpr int BLOCK_CHUNK_STAGES = 2;       // one 128-wide scale block
 constexpr int GROUP_M = 8;                  // tile raster: bands of 8 row tiles (2048 rows)
 constexpr int kSwapMaxTokens = 256;         // post-scale GEMMs with M <= this swap operands
+constexpr int kInt8MaxTokens = 128;         // ... and with M <= this can stream int8 operands
 constexpr int kSplitTargetUnits = 72;       // split K until about this many CTA-pair work units exist
 constexpr int kSplitMinStages = 4;          // at least 256 K per split
 constexpr int kSplitMax = 8;
@@ -123,6 +125,8 @@ struct KParams {
     int split_stages;
     int32_t* partial;  // k_split > 1: int32 partial sums [k_split][N][M] in kernel dims
     float* sg;         // kEpiGeluQuant: block scales [M][N/128]
+    int a_settled;     // operand A (resp. B) was complete before the previous kernel in the
+    int b_settled;     // stream started, so it may be read before the grid dependency wait
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
@@ -578,6 +582,7 @@ template <int EPI, int BN, bool SWAP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const KParams p) {
+    grid_launch_dependents();
     using C = Cfg<BN, EPI == kEpiGeluQuant ? YSTAGE_BYTES : 0u>;
     constexpr int STAGES = C::STAGES;
     constexpr int HALF = C::HALF;
@@ -627,14 +632,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     // Everything above overlaps the tail of the kernel that wrote the
     // operands and scales (programmatic dependent launch); nothing below
-    // reads global memory before that kernel has completed.
-    grid_dependency_wait();
+    // reads global memory before that kernel has completed -- except the
+    // producer's first fills of a settled operand (a weight image packed
+    // before the previous kernel started), which it issues before its own
+    // dependency wait.
+    if (warp != 0) grid_dependency_wait();
     const uint32_t tmem_base = *tmem_slot;
     if (warp < EPI_WARP0) {
       regs_dec<REGS_LOW>();
       if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
-        if (elect_one_sync()) {
+        const bool elected = elect_one_sync();
+        // Stages of the first unit whose settled operand went out before the
+        // dependency wait (the ring's first fills need no empty wait).
+        int pre = 0;
+        if (elected && (p.a_settled || p.b_settled) && cluster < p.num_tiles) {
+            const Unit w = unit_coords(cluster, p);
+            pre = min(STAGES, w.ks1 - w.ks0);
+            const int a_row = w.mb * TILE_M + static_cast<int>(rank) * BM;
+            const int b_row = w.nb * BN + static_cast<int>(rank) * HALF;
+            for (int i = 0; i < pre; ++i) {
+                if (leader) mbar_arrive_expect_tx(&full[i], 2 * C::STAGE_BYTES);
+                const uint32_t bar = map_to_rank(smem_u32(&full[i]), 0);
+                if (p.a_settled) tma_load_2d_pair(sA + i * A_BYTES, &tmA, bar, (w.ks0 + i) * BK, a_row);
+                else tma_load_2d_pair(sB + i * C::B_BYTES, &tmB, bar, (w.ks0 + i) * BK, b_row);
+            }
+        }
+        grid_dependency_wait();
+        if (elected) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_phase = 0;
@@ -644,14 +669,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int a_row = w.mb * TILE_M + static_cast<int>(rank) * BM;
                 const int b_row = w.nb * BN + static_cast<int>(rank) * HALF;
                 for (int ks = w.ks0; ks < w.ks1; ++ks) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
                     const uint32_t bar = map_to_rank(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, ks * BK, a_row);
-                    tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar, ks * BK, b_row);
+                    if (u == cluster && ks - w.ks0 < pre) {
+                        // first fill, settled half already in flight
+                        if (p.a_settled) tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar, ks * BK, b_row);
+                        else tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, ks * BK, a_row);
+                    } else {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                        tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, ks * BK, a_row);
+                        tma_load_2d_pair(sB + stage * C::B_BYTES, &tmB, bar, ks * BK, b_row);
+                    }
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -897,6 +928,356 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Few-token post-scale GEMM on int8 operands.  The weights are the large
+// operand of a few-token Linear and the whole cost at these sizes is their
+// read, so this variant streams them as int8 (half the bytes of the 16-bit
+// image) and widens them in shared memory.  Operands as in the swapped
+// launch: A = Wq [N,K] (kernel rows), B = Xq [M,K] (kernel columns, the
+// tokens).  One CTA per SM, no clusters: a CTA owns 128 weight rows (M = 128
+// MMAs), so a tile needs no other CTA and twice as many tiles feed the SMs.
+// Roles:
+//   warp 0      producer: TMA of the int8 tiles (128 rows x 64 K of A and
+//               BN rows x 64 K of B) into an int8 ring;
+//   warp 1      TMEM allocation and the MMAs (kind::f16 with fp16 operands;
+//               every int8 value is exact in fp16);
+//   warps 4-7   converters: int8 ring -> fp16 operand ring in the 128-byte
+//               swizzled K-major layout the MMA descriptors read.  A byte b
+//               (two's complement x) becomes fp16 bits 0x6400 | (b ^ 0x80),
+//               i.e. 1024 + x + 128, and subtracting 1152 leaves x exactly;
+//               one byte permute builds two such halves and one packed fp16
+//               subtraction finishes them;
+//   warps 8-11  epilogue, one per TMEM lane quarter, all BN columns each
+//               (chunk folds into int32, then the transposed store or the
+//               split-K partials).
+// Warps 2-3 are idle.  BN <= 128 (M <= 128 tokens).
+template <int BN_>
+struct CfgS8 {
+    static constexpr int BN = BN_;
+    static_assert(BN == 32 || BN == 64 || BN == 128, "token tile");
+    static constexpr int HALF = BN;                      // accumulator columns per epilogue warp (all of them)
+    static constexpr uint32_t A8_BYTES = BM * BK;        // 8 KB: 128 rows x 64 int8
+    static constexpr uint32_t B8_BYTES = BN * BK;
+    static constexpr uint32_t B16_BYTES = BN * BK * 2;
+    static constexpr int S16 = BN == 32 ? 8 : BN == 64 ? 6 : 4;  // deep: an MMA commit round trip gates each fp16 stage
+    static constexpr uint32_t RING16 = S16 * (A_BYTES + B16_BYTES);
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t RING8_BUDGET = MAX_DYN_SMEM - 1024 - BAR_BYTES - 512 - STAGING_BYTES - RING16;
+    static constexpr int S8 = (RING8_BUDGET / (A8_BYTES + B8_BYTES)) > 12 ? 12
+                                                                          : int(RING8_BUDGET / (A8_BYTES + B8_BYTES));
+    static_assert(S8 >= 2, "int8 ring");
+    static_assert(2 * (S8 + S16) + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
+    static constexpr size_t SMEM = 1024 + RING16 + size_t(S8) * (A8_BYTES + B8_BYTES) + STAGING_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+    static constexpr int LDW = (HALF % 32 == 0) ? 32 : 16;
+    static constexpr int GROUPS = HALF / LDW;
+};
+
+// 16 int8 -> 16 fp16 (exact), as two 16-byte groups.
+__device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t p0 = __byte_perm(w[i], 0x64646464u, 0x4140);  // halves 1024 + u0, 1024 + u1
+        const uint32_t p1 = __byte_perm(w[i], 0x64646464u, 0x4342);  // halves 1024 + u2, 1024 + u3
+        __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&p0), bias);
+        __half2 h1 = __hsub2(*reinterpret_cast<const __half2*>(&p1), bias);
+        o[2 * i] = *reinterpret_cast<uint32_t*>(&h0);
+        o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&h1);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Widen ROWS rows of an int8 tile (64-byte rows) into the fp16 tile (128-byte
+// rows, 16-byte chunk j at position j ^ (row & 7)).  Converter thread t (of
+// 128) owns source chunk c = t % 4 of rows t / 4 + 32 i: each warp's loads
+// cover 8 consecutive rows (512 contiguous bytes), the stores of a
+// quarter-warp land on 8 different bank groups, and every address is a
+// per-thread base plus a constant.
+template <int ROWS>
+__device__ __forceinline__ void widen_tile(const uint8_t* src, uint8_t* dst, int t) {
+    const int c = t & 3, r0 = t >> 2;
+    const uint8_t* s = src + r0 * 64 + c * 16;
+    uint8_t* d = dst + r0 * 128;
+    const int plo = ((2 * c) ^ (r0 & 7)) << 4, phi = ((2 * c + 1) ^ (r0 & 7)) << 4;  // r0 + 32i has the same row & 7
+#pragma unroll
+    for (int i = 0; i < ROWS / 32; ++i) {
+        uint4 lo, hi;
+        s8x16_to_f16(*reinterpret_cast<const uint4*>(s + i * 32 * 64), lo, hi);
+        *reinterpret_cast<uint4*>(d + i * 32 * 128 + plo) = lo;
+        *reinterpret_cast<uint4*>(d + i * 32 * 128 + phi) = hi;
+    }
+}
+
+enum WaitSiteS8 : int {
+    kSiteS8ProducerEmpty = 11,
+    kSiteS8ConvFull = 12,
+    kSiteS8ConvEmpty = 13,
+    kSiteS8MmaFull = 14,
+    kSiteS8ProducerDrain = 15,
+};
+
+constexpr int S8_TILE_M = BM;  // weight rows per CTA
+
+template <int EPI, int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_s8_swap_kernel(const __grid_constant__ CUtensorMap tmA8, const __grid_constant__ CUtensorMap tmB8,
+                        const __grid_constant__ CUtensorMap tmY, const KParams p) {
+    grid_launch_dependents();
+    using C = CfgS8<BN>;
+    constexpr int S8 = C::S8;
+    constexpr int S16 = C::S16;
+    constexpr int HALF = C::HALF;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA16 = smem;                          // S16 x 16 KB, 1 KB aligned
+    uint8_t* sB16 = sA16 + S16 * A_BYTES;          // S16 x B16_BYTES
+    uint8_t* sA8 = sB16 + S16 * C::B16_BYTES;      // S8 x 8 KB
+    uint8_t* sB8 = sA8 + S8 * C::A8_BYTES;         // S8 x B8_BYTES
+    uint8_t* staging = sB8 + S8 * C::B8_BYTES;     // 1 KB aligned: all sizes above are multiples of 1 KB
+    uint64_t* full8 = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
+    uint64_t* empty8 = full8 + S8;
+    uint64_t* full16 = empty8 + S8;
+    uint64_t* empty16 = full16 + S16;
+    uint64_t* acc_full = empty16 + S16;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* mma_drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = static_cast<int>(blockIdx.x);
+    const int nctas = static_cast<int>(gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S8; ++s) {
+            mbar_init(&full8[s], 1);   // the producer's arrive + the tile bytes
+            mbar_init(&empty8[s], 4);  // the four converter warps
+        }
+        for (int t = 0; t < S16; ++t) {
+            mbar_init(&full16[t], 4);   // the four converter warps
+            mbar_init(&empty16[t], 1);  // the MMA commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);  // the four epilogue warps
+        }
+        mbar_init(mma_drain, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA8);
+        tma_prefetch_desc(&tmB8);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // Weights settled before the previous kernel started may be read before
+    // the dependency wait (the producer's first fills); nothing else is.
+    if (warp != 0) grid_dependency_wait();
+    const uint32_t tmem_base = *tmem_slot;
+    if (warp < EPI_WARP0) {
+      regs_dec<REGS_LOW>();
+      if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const bool elected = elect_one_sync();
+        int pre = 0;
+        if (elected && p.a_settled && cta < p.num_tiles) {
+            const Unit w = unit_coords(cta, p);
+            pre = min(S8, w.ks1 - w.ks0);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full8[i], C::A8_BYTES + C::B8_BYTES);
+                tma_load_2d(sA8 + i * C::A8_BYTES, &tmA8, &full8[i], (w.ks0 + i) * BK, w.mb * S8_TILE_M);
+            }
+        }
+        grid_dependency_wait();
+        if (elected) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_phase = 0;
+            bool ok = true;
+            for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+                const Unit w = unit_coords(u, p);
+                const int a_row = w.mb * S8_TILE_M;
+                const int b_row = w.nb * BN;
+                for (int ks = w.ks0; ks < w.ks1; ++ks) {
+                    if (u == cta && ks - w.ks0 < pre) {
+                        tma_load_2d(sB8 + stage * C::B8_BYTES, &tmB8, &full8[stage], ks * BK, b_row);
+                    } else {
+                        if (!mbar_wait(&empty8[stage], phase ^ 1u, kSiteS8ProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full8[stage], C::A8_BYTES + C::B8_BYTES);
+                        tma_load_2d(sA8 + stage * C::A8_BYTES, &tmA8, &full8[stage], ks * BK, a_row);
+                        tma_load_2d(sB8 + stage * C::B8_BYTES, &tmB8, &full8[stage], ks * BK, b_row);
+                    }
+                    armed |= 1u << stage;
+                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S8) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy issued has landed before this CTA's shared memory is released.
+            for (int s = 0; s < S8; ++s)
+                if (armed & (1u << s)) mbar_wait(&full8[s], (armed_phase >> s) & 1u, kSiteS8ProducerDrain);
+        }
+      } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+                const Unit w = unit_coords(u, p);
+                const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
+                for (int c = 0; ok && c < nchunks; ++c) {
+                    if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                    const int s0 = w.ks0 + c * p.chunk_stages;
+                    const int s1 = min(w.ks1, s0 + p.chunk_stages);
+                    for (int ks = s0; ks < s1; ++ks) {
+                        if (!mbar_wait(&full16[stage], phase, kSiteS8MmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(sA16 + stage * A_BYTES);
+                        const uint32_t b_addr = smem_u32(sB16 + stage * C::B16_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t da = smem_desc_kmajor_sw128(a_addr + k * 32);
+                            const uint64_t db = smem_desc_kmajor_sw128(b_addr + k * 32);
+                            mma_bf16_ss(d_tmem, da, db, C::IDESC, (ks > s0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&empty16[stage]);
+                        if (++stage == S16) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&acc_full[buf]);
+                    buf ^= 1;
+                    if (buf == 0) buf_phase ^= 1u;
+                }
+            }
+            mma_commit(mma_drain);
+            mbar_wait(mma_drain, 0, kSiteMmaDrain);
+        }
+      }
+    } else if (warp < 8) {
+        regs_dec<80>();
+        // ------------------------------------------------------------ converters (warps 4-7)
+        const int ct = threadIdx.x - 128;  // 0..127
+        int s8 = 0, t16 = 0;
+        uint32_t ph8 = 0, ph16 = 0;
+        bool ok = true;
+        for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+            const Unit w = unit_coords(u, p);
+            for (int ks = w.ks0; ks < w.ks1; ++ks) {
+                if (!mbar_wait(&full8[s8], ph8, kSiteS8ConvFull) ||
+                    !mbar_wait(&empty16[t16], ph16 ^ 1u, kSiteS8ConvEmpty)) {
+                    ok = false;
+                    break;
+                }
+                widen_tile<BM>(sA8 + s8 * C::A8_BYTES, sA16 + t16 * A_BYTES, ct);
+                widen_tile<BN>(sB8 + s8 * C::B8_BYTES, sB16 + t16 * C::B16_BYTES, ct);
+                fence_proxy_async_smem();  // the MMA reads these through the async proxy
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&empty8[s8]);
+                    mbar_arrive(&full16[t16]);
+                }
+                if (++s8 == S8) {
+                    s8 = 0;
+                    ph8 ^= 1u;
+                }
+                if (++t16 == S16) {
+                    t16 = 0;
+                    ph16 ^= 1u;
+                }
+            }
+        }
+    } else {
+        regs_inc<232>();
+        // ------------------------------------------------------------ epilogue (warps 8-11)
+        constexpr int LDW = C::LDW;
+        constexpr int GROUPS = C::GROUPS;
+        const int quarter = warp & 3;
+        const int half = 0;
+        uint8_t* stg = staging + (warp - 8) * 2 * STAGE_OUT_BYTES;
+        int sbuf = 0;
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+            const Unit w = unit_coords(u, p);
+            const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
+            const int row_base = w.mb * S8_TILE_M + quarter * 32;
+            const int col0 = w.nb * BN + half * HALF;
+            int32_t acc[HALF];
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) acc[e] = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                if (!mbar_wait(&acc_full[buf], buf_phase, kSiteEpiAccFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(buf * BN + half * HALF);
+                uint32_t ra[LDW], rb[LDW];
+                tmem_ld_cols<LDW>(taddr, ra);
+                tmem_wait_cols(ra);
+#pragma unroll
+                for (int j = 0; j < GROUPS; ++j) {
+                    uint32_t(&cur)[LDW] = (j & 1) ? rb : ra;
+                    uint32_t(&nxt)[LDW] = (j & 1) ? ra : rb;
+                    if (j + 1 < GROUPS) tmem_ld_cols<LDW>(taddr + (j + 1) * LDW, nxt);
+#pragma unroll
+                    for (int e = 0; e < LDW; ++e) acc[j * LDW + e] += __float2int_rz(__uint_as_float(cur[e]));
+                    if (j + 1 < GROUPS) tmem_wait_cols(nxt);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                buf ^= 1;
+                if (buf == 0) buf_phase ^= 1u;
+            }
+            if (!ok) break;
+            if (p.k_split > 1)
+                store_partial<HALF>(acc, p, row_base, col0, w.split, lane);
+            else
+                store_swapped<EPI, HALF>(acc, p, &tmY, row_base, col0, stg, sbuf, lane);
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 // Split K, last step: Y[m][n] from the sum of the k_split int32 partials of
 // output (m, n) -- integer additions, exact in any order -- then the
 // post-scale epilogue in the unsplit kernel's operation order.  Launched as a
@@ -1072,10 +1453,100 @@ cudaError_t launch_swapped(const void* Ximg, const void* Wimg, PFN_cuTensorMapEn
     const int tokens = p.M;
     p.M = p.N;  // kernel rows: weight rows
     p.N = tokens;
+    const int settled = p.a_settled;
+    p.a_settled = p.b_settled;
+    p.b_settled = settled;
     if (tokens <= 32) return launch_one<EPI, 32, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
     if (tokens <= 64) return launch_one<EPI, 64, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
     if (tokens <= 128) return launch_one<EPI, 128, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
     return launch_one<EPI, 256, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
+}
+
+// The int8-operand swapped launch: Ab = Wq [N,K] int8 (kernel rows), Bb =
+// Xq [M,K] int8 (kernel columns); p in kernel dimensions.
+template <int EPI, int BN>
+cudaError_t launch_one_s8(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
+                          int num_sms, cudaStream_t st, char* detail, size_t n) {
+    using C = CfgS8<BN>;
+    auto map8 = [&](CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
+        cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+        cuuint32_t estr[2] = {1, 1};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    CUtensorMap tmA, tmB, tmY;
+    CUresult r = map8(&tmA, Ab, p.M, BM);
+    if (r != CUDA_SUCCESS) {
+        snprintf(detail, n, "cuTensorMapEncodeTiled(A int8: %d x %d) returned %d", p.M, p.K, (int)r);
+        return cudaErrorInvalidValue;
+    }
+    r = map8(&tmB, Bb, p.N, BN);
+    if (r != CUDA_SUCCESS) {
+        snprintf(detail, n, "cuTensorMapEncodeTiled(B int8: %d x %d) returned %d", p.N, p.K, (int)r);
+        return cudaErrorInvalidValue;
+    }
+    tmY = tmA;  // placeholder when the output is not written through TMA
+    p.tma_store = (EPI == kEpiPostscaleBf16 && (p.M % 8) == 0) ? 1 : 0;  // Y is [tokens, p.M]
+    if (p.tma_store) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.N)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.M) * 2};
+        cuuint32_t box[2] = {32u, 16u};
+        cuuint32_t estr[2] = {1, 1};
+        r = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            snprintf(detail, n, "cuTensorMapEncodeTiled(Y: %d x %d) returned %d", p.N, p.M, (int)r);
+            return cudaErrorInvalidValue;
+        }
+    }
+    p.num_m = (p.M + S8_TILE_M - 1) / S8_TILE_M;
+    p.num_n = (p.N + BN - 1) / BN;
+    p.num_tiles = p.num_m * p.num_n * p.k_split;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    DeviceLaunchInfo& info = g_launch_info[dev];
+    constexpr int id = 20 + (EPI == kEpiPostscaleS32 ? 4 : 0) + (BN == 32 ? 0 : BN == 64 ? 1 : BN == 128 ? 2 : 3);
+    static_assert(id < 32, "instance table");
+    if (!info.configured[id]) {
+        e = cudaFuncSetAttribute(gemm_s8_swap_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(C::SMEM));
+        if (e != cudaSuccess) return e;
+        info.configured[id] = true;
+    }
+    // persistent: one CTA per SM
+    const int ctas = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_s8_swap_kernel<EPI, BN>, tmA, tmB, tmY, p);
+}
+
+template <int EPI>
+cudaError_t launch_swapped_s8(const void* Xq, const void* Wq, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
+                              int num_sms, cudaStream_t st, char* detail, size_t n) {
+    const int tokens = p.M;
+    p.M = p.N;
+    p.N = tokens;
+    const int settled = p.a_settled;
+    p.a_settled = p.b_settled;
+    p.b_settled = settled;
+    if (tokens <= 32) return launch_one_s8<EPI, 32>(Wq, Xq, encode, p, num_sms, st, detail, n);
+    if (tokens <= 64) return launch_one_s8<EPI, 64>(Wq, Xq, encode, p, num_sms, st, detail, n);
+    return launch_one_s8<EPI, 128>(Wq, Xq, encode, p, num_sms, st, detail, n);
 }
 
 template <int EPI>
@@ -1099,6 +1570,10 @@ cudaError_t launch_finalize(const KParams& p, const GemmArgs& a, int num_sms, cu
 
 }  // namespace
 
+bool gemm_takes_int8(int epilogue, int64_t M) {
+    return (epilogue == kEpiPostscaleBf16 || epilogue == kEpiPostscaleS32) && M > 0 && M <= kInt8MaxTokens;
+}
+
 int splitk_plan(bool blockwise, int64_t M, int64_t N, int64_t K, int* split_stages) {
     const int64_t k_stages = (K + BK - 1) / BK;
     if (split_stages) *split_stages = static_cast<int>(k_stages);
@@ -1121,6 +1596,10 @@ size_t splitk_partial_bytes(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const GemmArgs& a, int num_sms,
                         void* encode_fn, cudaStream_t st, char* detail, size_t n) {
     if (n) detail[0] = 0;
+    if (a.int8_operands && !gemm_takes_int8(epilogue, a.M)) {
+        snprintf(detail, n, "int8 operands are taken only by the few-token post-scale GEMM");
+        return cudaErrorInvalidValue;
+    }
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encode_fn);
     KParams p;
     p.sx = a.sx;
@@ -1128,6 +1607,8 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     p.bias = static_cast<const __nv_bfloat16*>(a.bias);
     p.out = a.out;
     p.sg = a.sg;
+    p.a_settled = 0;
+    p.b_settled = a.weights_settled ? 1 : 0;  // B holds the weights (swapped launches exchange the flags)
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);
@@ -1156,12 +1637,16 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     cudaError_t e;
     switch (epilogue) {
         case kEpiPostscaleBf16:
-            e = swap ? launch_swapped<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
-                     : launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
+            e = (swap && a.int8_operands)
+                    ? launch_swapped_s8<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                : swap ? launch_swapped<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                       : launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
             break;
         case kEpiPostscaleS32:
-            e = swap ? launch_swapped<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
-                     : launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
+            e = (swap && a.int8_operands)
+                    ? launch_swapped_s8<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                : swap ? launch_swapped<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                       : launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
             break;
         case kEpiBlockwiseBf16:
             e = launch_one<kEpiBlockwiseBf16, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);

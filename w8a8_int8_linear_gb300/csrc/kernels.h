@@ -44,7 +44,13 @@ struct GemmArgs {
     int64_t M, N, K;
     int32_t* partial;  // split-K partial sums, splitk_partial_bytes(M,N,K) bytes (unused when that is 0)
     float* sg;         // kEpiGeluQuant: 1x128 block scales of the GELU output [M][N/128]
+    bool weights_settled;  // Bb was complete before the previous kernel in the stream started
+    bool int8_operands;    // Ab / Bb are the int8 codes themselves (gemm_takes_int8 shapes only)
 };
+
+// Whether launch_gemm takes int8 codes directly (instead of bf16 images) for
+// this epilogue and M: the few-token post-scale GEMM streams int8 operands.
+bool gemm_takes_int8(int epilogue, int64_t M);
 
 // Split K for few-token post-scale GEMMs: the number of K splits (1: none)
 // and, through split_stages, the 64-wide K stages each split covers.

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __r
                                                                 int layer, int K, int tree, uint4* __restrict__ Y,
                                                                 uint2* __restrict__ Xq, uint4* __restrict__ img,
                                                                 float* __restrict__ sx) {
+    grid_launch_dependents();
     __shared__ float red[3][32];
     const int64_t row = blockIdx.x;
     const int chunks = K >> 3;

@@ -39,6 +39,12 @@ __device__ __forceinline__ bool elect_one_sync() {
 // stream has completed and its memory is visible (a no-op when this kernel
 // was launched without the programmatic-serialization attribute).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream, when launched as a programmatic
+// dependent, be scheduled now; it still waits (grid_dependency_wait) for this
+// grid to complete before reading what this grid writes.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -79,6 +85,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // `kWaitLimitNs` of wall time, records `site` in the device error word and
 // returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a whole launch takes milliseconds
+
+// try_wait with cluster-scope acquire: pairs with release arrives issued by
+// threads of the other CTA of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (see mbar_wait).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_device_error(W8A8_DEVERR_TIMEOUT_BASE + site);
+            return false;
+        }
+    }
+}
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int site) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -131,6 +166,12 @@ __device__ __forceinline__ void cluster_sync() {
 // A release here would add a cluster-scope fence to every arrival.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrive on an mbarrier of either CTA of the cluster, releasing this thread's
+// prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -388,6 +429,11 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t smem_addr) {
 // M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// The same with fp16 A and B (both operands must share the type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n) {
+    return (1u << 4) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 }  // namespace w8a8

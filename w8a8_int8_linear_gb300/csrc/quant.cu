@@ -108,6 +108,7 @@ template <int CPT>
 __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
                                                              uint2* __restrict__ Aq, uint4* __restrict__ img,
                                                              float* __restrict__ s) {
+    grid_launch_dependents();
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
     if (row >= R) return;
@@ -141,6 +142,7 @@ template <int U>
 __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
                                                                   uint2* __restrict__ Aq, uint4* __restrict__ img,
                                                                   float* __restrict__ s) {
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= R) return;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(256, 4) quant_rows_warp2_kernel(const uint4* _
 __global__ void __launch_bounds__(256) quant_rows_2pass_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
                                                                uint2* __restrict__ Aq, uint4* __restrict__ img,
                                                                float* __restrict__ s) {
+    grid_launch_dependents();
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
     if (row >= R) return;
@@ -206,6 +209,7 @@ template <int UNROLL>
 __global__ void __launch_bounds__(256) quant_act_block_kernel(const uint4* __restrict__ X, int64_t n_blocks,
                                                               uint2* __restrict__ Xq, uint4* __restrict__ img,
                                                               float* __restrict__ sx) {
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int sub = lane & 3, bl = lane >> 2;
     const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(256) quant_weight_block_kernel(const uint4* __
 
 __global__ void __launch_bounds__(256) expand_s8_bf16_kernel(const uint4* __restrict__ src, int64_t n16,
                                                              uint4* __restrict__ dst) {
+    grid_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
         const uint4 v = __ldcs(src + i);
