@@ -47,6 +47,8 @@ def parse():
                     help="time the fused norm + quantization kernel against torch's norm + this library's quant")
     ap.add_argument("--report-decode", action="store_true",
                     help="few-token Linears in steady state (CUDA graph over weight copies larger than L2)")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="three launches of one kernel on a small case (for an ncu capture)")
     ap.add_argument("--profile-once", action="store_true",
                     help="only the W warm-up and K plain steps, no flush or side measurements (for ncu)")
     return ap.parse_args()
@@ -785,6 +787,46 @@ def report_decode(args):
     return out
 
 
+PROFILE_CASES = {
+    # name: (what, M, N, K)
+    "gelu_quant_4096x4096x2048": ("gelu_quant", 4096, 4096, 2048),
+    "norm_layer_8192x5120": ("norm_layer", 8192, 0, 5120),
+    "gemm_int8_decode_1x13824x5120": ("gemm_int8", 1, 13824, 5120),
+}
+
+
+def profile_case(name):
+    """A few launches of one kernel on a small case, for ncu (--set full):
+    three calls after the set-up, then a device-error check."""
+    import torch
+    import w8a8_int8_linear_gb300 as w
+    what, M, N, K = PROFILE_CASES[name]
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    X = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    if what == "norm_layer":
+        gamma = (1 + 0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
+        beta = (0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
+        fn = lambda: w.norm_quant(X, gamma, beta, 1e-5, w.LAYER_NORM)
+    else:
+        W = (0.05 * torch.randn((N, K), generator=g, device=dev)).to(torch.bfloat16)
+        Wq, sw = w.quantize_weight(W)
+        if what == "gelu_quant":
+            b = (0.5 * torch.randn((N,), generator=g, device=dev)).to(torch.bfloat16)
+            Wimg = w.pack_weight(Wq)
+            fn = lambda: w.linear_postscale_gelu_quant(X, Wimg, sw, b)
+        else:
+            Xq, sx = w.quantize_act(X)
+            fn = lambda: w.gemm_postscale(Xq, sx, Wq, sw)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    st, code = w.get_device_error()
+    assert st == 0 and code == 0, f"device error {code}"
+    print(json.dumps({"profile_case": name, "ok": True}))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -797,6 +839,8 @@ def main():
         report_norm(args)
     elif args.report_decode:
         report_decode(args)
+    elif args.profile_case:
+        profile_case(args.profile_case)
     else:
         run_w8a8(args)
 
