@@ -880,17 +880,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t(&cur)[LDW] = (j & 1) ? rb : ra;
                     uint32_t(&nxt)[LDW] = (j & 1) ? ra : rb;
                     if (j + 1 < GROUPS) tmem_ld_cols<LDW>(taddr + (j + 1) * LDW, nxt);
+                    if constexpr (kBlock) {
+                        // t = (P * sx) * sw; acc = acc + t, each rounded on its own.  The two
+                        // products of a column pair run on the packed fp32 pipe (a product
+                        // feeding a product, nothing to contract); the additions stay scalar
+                        // with explicit rounding (chained packed multiply-adds get contracted).
+                        const uint64_t sx2 = f2_pack(sxv, sxv), sw2 = f2_pack(swv, swv);
 #pragma unroll
-                    for (int e = 0; e < LDW; ++e) {
-                        const float v = __uint_as_float(cur[e]);
-                        if constexpr (kBlock) {
-                            // t = (P * sx) * sw; acc = acc + t, each rounded on its own.
-                            // Scalar operations: packed f32x2 forms measured slower here,
-                            // and chained packed multiply-adds get contracted.
-                            acc[j * LDW + e] = __fadd_rn(acc[j * LDW + e], __fmul_rn(__fmul_rn(v, sxv), swv));
-                        } else {
-                            acc[j * LDW + e] += __float2int_rz(v);
+                        for (int e = 0; e < LDW; e += 2) {
+                            float t0, t1;
+                            f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])),
+                                                    sx2),
+                                             sw2),
+                                      t0, t1);
+                            acc[j * LDW + e] = __fadd_rn(acc[j * LDW + e], t0);
+                            acc[j * LDW + e + 1] = __fadd_rn(acc[j * LDW + e + 1], t1);
                         }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < LDW; ++e) acc[j * LDW + e] += __float2int_rz(__uint_as_float(cur[e]));
                     }
                     if (j + 1 < GROUPS) tmem_wait_cols(nxt);
                 }
