@@ -84,12 +84,56 @@ def test_argument_checks_before_device(cdll):
     assert L.w8a8_gemm_blockwise_f32(fake, null, fake, fake, fake, 4, 4, 128, fake, 1 << 20, null) == 1
 
 
+def test_widened_entry_points_check_arguments_before_device(cdll):
+    """The fused FFN up-projection, the image GEMMs and the norm + quant
+    entry point validate shapes, pointers, alignment and workspace first."""
+    L, _ = cdll
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    odd = P(0x1001)
+    null = None
+    # norm + quant: kind, K % 8, K limit, eps, nothing to do, pointers, alignment
+    n = L.w8a8_norm_quant
+    assert n(fake, null, null, 1e-5, 5, 4, 64, null, null, fake, fake, null) == 1
+    assert n(fake, null, null, 1e-5, 0, 4, 12, null, null, fake, fake, null) == 3
+    assert n(fake, null, null, 1e-5, 0, 4, 16392, null, null, fake, fake, null) == 3
+    assert n(fake, null, null, -1.0, 1, 4, 64, null, null, fake, fake, null) == 1
+    assert n(fake, null, null, float("nan"), 1, 4, 64, null, null, fake, fake, null) == 1
+    assert n(null, null, null, 1e-5, 0, 0, 64, null, null, null, null, null) == 0
+    assert n(null, null, null, 1e-5, 0, 4, 64, null, null, fake, fake, null) == 1
+    assert n(fake, null, null, 1e-5, 0, 4, 64, null, null, fake, null, null) == 1
+    assert n(odd, null, null, 1e-5, 0, 4, 64, null, null, fake, fake, null) == 2
+    assert n(fake, odd, null, 1e-5, 0, 4, 64, null, null, fake, fake, null) == 2
+    # fused FFN up-projection: N % 128, pointers, workspace
+    f = L.w8a8_linear_postscale_gelu_quant
+    assert f(fake, fake, fake, null, fake, fake, 4, 200, 64, fake, null, fake, 1 << 20, null) == 3
+    assert f(fake, fake, fake, null, null, fake, 4, 256, 64, fake, null, fake, 1 << 20, null) == 1
+    assert f(fake, fake, fake, null, fake, fake, 4, 256, 64, fake, null, null, 1 << 20, null) == 7
+    assert f(null, null, null, null, null, null, 0, 256, 64, null, null, null, 0, null) == 0
+    # image GEMMs
+    assert L.w8a8_gemm_blockwise_images(fake, fake, fake, fake, null, fake, 4, 4, 100, null) == 3
+    assert L.w8a8_gemm_blockwise_images(fake, null, fake, fake, null, fake, 4, 4, 128, null) == 1
+    gi = L.w8a8_gemm_postscale_images
+    assert gi(fake, fake, fake, fake, null, fake, 4, 4, 20, null, 0, null) == 3
+    # a few-token shape that splits K needs the partial-sum workspace
+    assert L.w8a8_splitk_workspace_size(1, 4096, 4096) > 0
+    assert L.w8a8_splitk_workspace_size(4096, 4096, 4096) == 0
+    assert gi(fake, fake, fake, fake, null, fake, 1, 4096, 4096, null, 0, null) == 7
+    assert gi(fake, fake, fake, fake, odd, fake, 1, 4096, 4096, null, 0, null) == 2
+
+
 def test_workspace_size(cdll):
     L, _ = cdll
     assert L.w8a8_gemm_workspace_size(0, 5, 16) == 0
     # bf16 images of Xq [M,K] and Wq [N,K], each rounded up to 256 bytes
     assert L.w8a8_gemm_workspace_size(3, 5, 16) == 256 + 256
     assert L.w8a8_gemm_workspace_size(4096, 4096, 4096) == 2 * 4096 * 4096 * 2
+    # few tokens with split K: images plus int32 partial sums (S splits x M x N)
+    s = L.w8a8_splitk_workspace_size(1, 3072, 5120)
+    assert s >= 6 * 1 * 3072 * 4 and s % 256 == 0
+    assert L.w8a8_gemm_workspace_size(1, 3072, 5120) == 5120 * 2 + 3072 * 5120 * 2 + s
+    assert L.w8a8_linear_workspace_size(1, 3072, 5120) == 256 * ((5120 * 2 + 255) // 256) + s
+    assert L.w8a8_linear_workspace_size(4096, 4096, 4096) == 4096 * 4096 * 2
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
