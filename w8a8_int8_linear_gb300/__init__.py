@@ -421,3 +421,6 @@ def measure_imma_peak():
     v = ctypes.c_double(0.0)
     _check("w8a8_measure_imma_peak", lib().w8a8_measure_imma_peak(ctypes.byref(v), _stream()))
     return v.value
+
+
+from .module import Int8Linear  # noqa: E402  (the module uses the functions above)
