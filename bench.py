@@ -343,6 +343,18 @@ def run_w8a8(args):
     torch.cuda.synchronize()
     q_ms = statistics.median(a.elapsed_time(bb) for a, bb in qev)
     q_bytes = M * K * 2 + M * K + sx.numel() * 4
+    # the same bytes (read 2 B, write 1 B per element) moved by a plain
+    # streaming kernel under the same flush: the memory floor of the quant
+    scratch = torch.empty_like(Xq)
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+    for a, bb in cev:
+        flush.zero_()
+        a.record(stream)
+        w.stream_floor(X, scratch)
+        bb.record(stream)
+    torch.cuda.synchronize()
+    copy_ms = statistics.median(a.elapsed_time(bb) for a, bb in cev)
+    del scratch
 
     # comparison point: torch bf16 matmul at the same shape
     Xbf = X
@@ -428,7 +440,8 @@ def run_w8a8(args):
                               "exist on sm_103a"},
         "quant": {"kernel": "1x128 act quant" if blockwise else "per-token act quant", "ms": round(q_ms, 5), "gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
                   "frac_of_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                  "frac_of_8tbs": round(q_bytes / (q_ms * 1e-3) / 1e9 / 8000.0, 4)},
+                  "frac_of_8tbs": round(q_bytes / (q_ms * 1e-3) / 1e9 / 8000.0, 4),
+                  "stream_floor_ms": round(copy_ms, 5), "frac_of_stream_floor": round(copy_ms / q_ms, 4)},
         "comparison": {"torch_bf16_matmul_tflops": round(ops / (torch_ms * 1e-3) / 1e12, 1)},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

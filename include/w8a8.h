@@ -331,6 +331,16 @@ W8A8_API w8a8_status w8a8_set_gemm_timing_events(void* start, void* end);
  */
 W8A8_API w8a8_status w8a8_measure_imma_peak(double* tops, void* stream);
 
+/*
+ * Measurement helper (not part of the Linear): moves the bytes of an
+ * activation quantization -- reads n bf16 values from src, writes n bytes to
+ * dst (the high byte of each value) -- as a plain grid-stride stream.  Timed
+ * under the same conditions as w8a8_quantize_act on the same shape it gives
+ * the memory floor of that quantization.  n % 8 == 0; both pointers 16-byte
+ * aligned; asynchronous on `stream`.
+ */
+W8A8_API w8a8_status w8a8_stream_floor(const void* src, int64_t n, void* dst, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -56,6 +56,7 @@ SIGNATURES = [
     ("w8a8_get_device_error", _I32, [ctypes.POINTER(ctypes.c_int)]),
     ("w8a8_set_gemm_timing_events", _I32, [_P, _P]),
     ("w8a8_measure_imma_peak", _I32, [ctypes.POINTER(ctypes.c_double), _P]),
+    ("w8a8_stream_floor", _I32, [_P, _I64, _P, _P]),
 ]
 
 _lib = None
@@ -414,6 +415,17 @@ def set_gemm_timing_events(start=None, end=None):
             ev.record()  # materialize the underlying cudaEvent_t
         return ctypes.c_void_p(ev.cuda_event)
     _check("w8a8_set_gemm_timing_events", lib().w8a8_set_gemm_timing_events(handle(start), handle(end)))
+
+
+def stream_floor(src, dst):
+    """Move the bytes of an activation quantization of `src` (bf16) into
+    `dst` (int8, same element count) as a plain stream: the memory floor of
+    that quantization."""
+    _need(src, torch.bfloat16, "src")
+    _need(dst, torch.int8, "dst")
+    if dst.numel() != src.numel():
+        raise ValueError("dst must have as many elements as src")
+    _check("w8a8_stream_floor", lib().w8a8_stream_floor(_ptr(src), src.numel(), _ptr(dst), _stream()))
 
 
 def measure_imma_peak():

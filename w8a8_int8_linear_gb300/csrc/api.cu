@@ -521,4 +521,16 @@ w8a8_status w8a8_measure_imma_peak(double* tops, void* stream) {
     return from_cuda(w8a8::measure_imma_peak(tops, dev.num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+w8a8_status w8a8_stream_floor(const void* src, int64_t n, void* dst, void* stream) {
+    if (n < 0) return W8A8_ERR_INVALID_ARG;
+    if (n % 8 != 0) return W8A8_ERR_SHAPE;
+    if (n == 0) return W8A8_OK;
+    if (!src || !dst) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    w8a8_status s = current_device(&dev);
+    if (s != W8A8_OK) return s;
+    return from_cuda(w8a8::launch_stream_floor(src, n, dst, dev.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

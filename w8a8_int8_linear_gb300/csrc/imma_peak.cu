@@ -1,4 +1,4 @@
-// Measurement helper: sustained throughput of the warp-level INT8 tensor
+// Measurement helpers.  First: sustained throughput of the warp-level INT8 tensor
 // instruction (mma.sync m16n8k32, s8 x s8 -> s32) on this GPU.  It is the
 // measured denominator for "fraction of dense INT8 peak"; it is not part of
 // the Linear.  Each warp keeps 8 independent accumulators so the tensor pipe,
@@ -38,7 +38,32 @@ __global__ void __launch_bounds__(256) imma_peak_kernel(int iters) {
     if (s == 0x7FFFFFFF) g_sink = s;  // keeps the loop live; practically never taken
 }
 
+// Measurement helper: the memory traffic of an activation quantization --
+// read 2 bytes, write 1 byte per element -- as a plain grid-stride stream of
+// 16-byte loads and 8-byte stores with no arithmetic to speak of (each
+// output byte is the high byte of its input element).  Timed under the same
+// conditions as the quantization, it is the floor a streaming kernel of that
+// size reaches on this memory system.
+__global__ void __launch_bounds__(256) stream_floor_kernel(const uint4* __restrict__ src, int64_t n16,
+                                                           uint2* __restrict__ dst) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const uint4 v = __ldcs(src + i);
+        __stcs(dst + i, make_uint2(__byte_perm(v.x, v.y, 0x7531), __byte_perm(v.z, v.w, 0x7531)));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_stream_floor(const void* src, int64_t n, void* dst, int num_sms, cudaStream_t st) {
+    const int64_t n16 = n >> 3;  // 8 elements per 16-byte load
+    int64_t grid = (n16 + 255) / 256;
+    if (grid > static_cast<int64_t>(num_sms) * 8) grid = static_cast<int64_t>(num_sms) * 8;
+    if (grid < 1) grid = 1;
+    stream_floor_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint4*>(src), n16,
+                                                                     static_cast<uint2*>(dst));
+    return cudaGetLastError();
+}
 
 cudaError_t measure_imma_peak(double* tops, int num_sms, cudaStream_t st) {
     cudaError_t e = cudaSuccess;

@@ -75,4 +75,8 @@ cudaError_t quant_read_device_error(unsigned int* code);
 // Throughput kernel of warp-level INT8 MMAs; returns tera-ops per second.
 cudaError_t measure_imma_peak(double* tops, int num_sms, cudaStream_t st);
 
+// Streaming copy with the traffic of an activation quantization (n bf16 in,
+// n bytes out; n % 8 == 0), for the quantization's memory floor.
+cudaError_t launch_stream_floor(const void* src, int64_t n, void* dst, int num_sms, cudaStream_t st);
+
 }  // namespace w8a8
