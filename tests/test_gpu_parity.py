@@ -437,3 +437,43 @@ def test_norm_quant_rejects_bad_arguments(w8a8):
         w8a8.norm_quant(X)
     with pytest.raises(w8a8.W8A8Error, match="INVALID_ARG"):  # negative eps
         w8a8.norm_quant(torch.zeros((2, 64), dtype=torch.bfloat16, device=DEV), eps=-1.0)
+
+
+def test_int8linear_with_fused_norm(w8a8, oracle):
+    """Int8Linear(norm=...) = norm + per-token quant in one pass, then the
+    post-scale GEMM on the code image, against the oracle composition."""
+    torch.manual_seed(1)
+    for norm in ("rms", "layer"):
+        W = rand_bf16((300, 512), seed=80, scale=0.03)
+        b = rand_bf16((300,), seed=81, scale=0.1)
+        g = (rand_bf16((512,), seed=82, scale=0.1) + 1.0).to(torch.bfloat16)
+        be = rand_bf16((512,), seed=83, scale=0.1) if norm == "layer" else None
+        m = w8a8.Int8Linear(W.to(DEV), b.to(DEV), norm=norm, norm_weight=g.to(DEV),
+                            norm_bias=None if be is None else be.to(DEV), eps=1e-5)
+        x = rand_bf16((2, 7, 512), seed=84, scale=2.0)
+        y = m(x.to(DEV))
+        _, Xq, sx = oracle.norm_quant(bits(x.reshape(14, 512)), bits(g), None if be is None else bits(be), 1e-5,
+                                      oracle.RMS_NORM if norm == "rms" else oracle.LAYER_NORM)
+        Wq, sw = oracle.quantize_weight(bits(W), oracle.PER_ROW)
+        Yo = oracle.epilogue_postscale(oracle.gemm_s32(Xq, Wq), sx, sw, bits(b))
+        d = assert_bf16_close(bits(y.reshape(14, 300)), Yo, 1)
+        assert d.max() == 0
+
+
+def test_int8ffn_module(w8a8, oracle):
+    """Int8FFN: up-projection with the GELU + 1x128 quant epilogue, then the
+    blockwise down-projection on the code image, against the oracle."""
+    D, H, O = 256, 384, 200
+    Wu = rand_bf16((H, D), seed=90, scale=0.06)
+    bu = rand_bf16((H,), seed=91, scale=0.3)
+    Wd = rand_bf16((O, H), seed=92, scale=0.03)
+    bd = rand_bf16((O,), seed=93, scale=0.05)
+    m = w8a8.Int8FFN(Wu.to(DEV), Wd.to(DEV), bu.to(DEV), bd.to(DEV))
+    x = rand_bf16((3, 11, D), seed=94)
+    y = m(x.to(DEV))
+    assert y.shape == (3, 11, O)
+    r = oracle.ffn_up_gelu_quant(bits(x.reshape(33, D)), bits(Wu), bits(bu))
+    Wq2, sw2 = oracle.quantize_weight(bits(Wd), oracle.BLOCK)
+    Yo = oracle.epilogue_blockwise(oracle.gemm_blockwise_f32(r["Gq"], r["sg"], Wq2, sw2), bits(bd))
+    d = assert_bf16_close(bits(y.reshape(33, O)), Yo, 1)
+    assert d.max() == 0

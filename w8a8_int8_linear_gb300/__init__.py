@@ -435,4 +435,4 @@ def measure_imma_peak():
     return v.value
 
 
-from .module import Int8Linear  # noqa: E402  (the module uses the functions above)
+from .module import Int8FFN, Int8Linear  # noqa: E402  (the modules use the functions above)

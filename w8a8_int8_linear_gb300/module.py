@@ -12,17 +12,31 @@ shape runs the INT8 kernels.
 """
 import torch
 
-from . import BLOCK, PER_ROW, linear_blockwise, linear_postscale, linear_workspace_size, pack_weight, \
-    quantize_weight
+from . import BLOCK, LAYER_NORM, PER_ROW, RMS_NORM, gemm_blockwise_images, gemm_postscale_images, \
+    linear_blockwise, linear_postscale, linear_postscale_gelu_quant, linear_workspace_size, norm_quant, \
+    pack_weight, quantize_weight
 
 
 class Int8Linear(torch.nn.Module):
-    """y = W8A8(x) for x [..., in_features] bf16 on a sm_103 device."""
+    """y = W8A8(x) for x [..., in_features] bf16 on a sm_103 device.
 
-    def __init__(self, weight, bias=None, mode="postscale"):
+    With `norm` ("rms" or "layer", post-scale mode only) the module first
+    applies that normalization (optional `norm_weight` / `norm_bias`, `eps`)
+    and the normalized rows go straight to int8 codes in the same pass
+    ("Reused Components": FastNorm with W8A8)."""
+
+    def __init__(self, weight, bias=None, mode="postscale", norm=None, norm_weight=None, norm_bias=None, eps=1e-6):
         super().__init__()
         if mode not in ("postscale", "blockwise"):
             raise ValueError("mode must be 'postscale' or 'blockwise'")
+        if norm not in (None, "rms", "layer"):
+            raise ValueError("norm must be None, 'rms' or 'layer'")
+        if norm is not None and mode != "postscale":
+            raise ValueError("a fused norm needs per-token (post-scale) activation scales")
+        self.norm = norm
+        self.eps = float(eps)
+        for name, t in (("norm_weight", norm_weight), ("norm_bias", norm_bias)):
+            self.register_buffer(name, None if t is None else t.detach().to(torch.bfloat16).contiguous())
         if weight.dtype != torch.bfloat16 or not weight.is_cuda or weight.dim() != 2:
             raise ValueError("weight must be a 2-D bf16 CUDA tensor [out_features, in_features]")
         self.mode = mode
@@ -53,10 +67,61 @@ class Int8Linear(torch.nn.Module):
             raise TypeError("Int8Linear takes bf16 activations")
         lead = x.shape[:-1]
         x2 = x.reshape(-1, self.in_features).contiguous()
-        fn = linear_postscale if self.mode == "postscale" else linear_blockwise
-        y, _, _ = fn(x2, self.weight_image, self.weight_scale, self.bias,
-                     workspace=self._workspace(x2.shape[0], x2.device))
+        ws = self._workspace(x2.shape[0], x2.device)
+        if self.norm is not None:
+            kind = RMS_NORM if self.norm == "rms" else LAYER_NORM
+            ximg, sx, _, _ = norm_quant(x2, self.norm_weight, self.norm_bias, self.eps, kind)
+            y = gemm_postscale_images(ximg, sx, self.weight_image, self.weight_scale, self.bias, workspace=ws)
+        else:
+            fn = linear_postscale if self.mode == "postscale" else linear_blockwise
+            y, _, _ = fn(x2, self.weight_image, self.weight_scale, self.bias, workspace=ws)
         return y.reshape(*lead, self.out_features)
 
     def extra_repr(self):
-        return f"in_features={self.in_features}, out_features={self.out_features}, mode={self.mode}"
+        s = f"in_features={self.in_features}, out_features={self.out_features}, mode={self.mode}"
+        return s + (f", norm={self.norm}" if self.norm else "")
+
+
+class Int8FFN(torch.nn.Module):
+    """FFN y = down(GELU(up(x))) on the W8A8 path: the up-projection is a
+    post-scale Linear whose epilogue applies GELU and the 1x128 quantization
+    the blockwise down-projection consumes, so the hidden activation never
+    exists in bf16 ("Differences From TurboDiffusion": the post-scale kernel
+    for LTX FFN shapes; the original blockwise kernel).  up_weight [H, D],
+    down_weight [D_out, H], H % 128 == 0."""
+
+    def __init__(self, up_weight, down_weight, up_bias=None, down_bias=None):
+        super().__init__()
+        for name, t in (("up_weight", up_weight), ("down_weight", down_weight)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2:
+                raise ValueError(f"{name} must be a 2-D bf16 CUDA tensor")
+        self.hidden, self.in_features = up_weight.shape
+        self.out_features = down_weight.shape[0]
+        if down_weight.shape[1] != self.hidden or self.hidden % 128 != 0:
+            raise ValueError("down_weight must be [out, hidden] with hidden % 128 == 0")
+        wq, sw = quantize_weight(up_weight.contiguous(), PER_ROW)
+        self.register_buffer("up_image", pack_weight(wq))
+        self.register_buffer("up_scale", sw)
+        wq2, sw2 = quantize_weight(down_weight.contiguous(), BLOCK)
+        self.register_buffer("down_image", pack_weight(wq2))
+        self.register_buffer("down_scale", sw2)
+        self.register_buffer("up_bias", None if up_bias is None else up_bias.detach().to(torch.bfloat16).contiguous())
+        self.register_buffer("down_bias",
+                             None if down_bias is None else down_bias.detach().to(torch.bfloat16).contiguous())
+        self._ws = None
+
+    def forward(self, x):
+        if x.dtype != torch.bfloat16:
+            raise TypeError("Int8FFN takes bf16 activations")
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.in_features).contiguous()
+        M = x2.shape[0]
+        need = max(linear_workspace_size(M, self.hidden, self.in_features), 256)
+        if self._ws is None or self._ws.numel() < need or self._ws.device != x2.device:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=x2.device)
+        gimg, sg, _, _ = linear_postscale_gelu_quant(x2, self.up_image, self.up_scale, self.up_bias, workspace=self._ws)
+        y = gemm_blockwise_images(gimg, sg, self.down_image, self.down_scale, self.down_bias)
+        return y.reshape(*lead, self.out_features)
+
+    def extra_repr(self):
+        return f"in_features={self.in_features}, hidden={self.hidden}, out_features={self.out_features}"
