@@ -38,6 +38,23 @@
 //                with a remote arrive on the leader's barrier.
 // Two accumulator buffers let the MMA of chunk c+1 run while chunk c is
 // folded.
+//
+// Variants of the same kernel (each described where it is defined):
+//   - few tokens (M <= 256, post-scale): operands swapped so the weight rows
+//     take the 256-row side and the tokens the N side (32..256), Y written
+//     transposed; with few weight tiles, K split into units whose exact
+//     int32 partials a finalize kernel sums (store_swapped, store_partial,
+//     splitk_finalize_kernel);
+//   - FFN up-projection: the epilogue applies GELU and the 1x128
+//     quantization of the down-projection's input, staged through shared
+//     memory over the next tile's chunk folds (stage_y, gelu_slice);
+//   - few tokens on int8 operands (M <= 128): a single-CTA kernel that
+//     streams int8 weights and codes and widens them to fp16 in shared
+//     memory (gemm_s8_swap_kernel).
+// Every kernel triggers its dependents' launch at its start and waits on
+// its own prerequisite grid after its prologue (programmatic dependent
+// launch); weights packed before the previous kernel started may be read
+// before that wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
