@@ -313,6 +313,16 @@ W8A8_API w8a8_status w8a8_gemm_blockwise_f32(const int8_t* Xq, const float* sx, 
 W8A8_API w8a8_status w8a8_get_device_error(int* code);
 
 /*
+ * Failure-detection check (not part of the Linear): launches one CTA whose
+ * thread waits on an mbarrier that nothing arrives on.  The wait is bounded
+ * like every wait in the library's kernels (2 s of device time); when it
+ * runs out the kernel records a timeout in the device error word and returns
+ * normally, so the context stays usable.  A following w8a8_get_device_error
+ * reports W8A8_ERR_TIMEOUT with code 0x100 + 30.  Asynchronous on `stream`.
+ */
+W8A8_API w8a8_status w8a8_probe_wait_timeout(void* stream);
+
+/*
  * Measurement hook (not part of the Linear): while set, every GEMM entry
  * point called from this host thread records `start` immediately before and
  * `end` immediately after its tensor-core kernel launch, on the call's

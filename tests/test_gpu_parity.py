@@ -477,3 +477,23 @@ def test_int8ffn_module(w8a8, oracle):
     Yo = oracle.epilogue_blockwise(oracle.gemm_blockwise_f32(r["Gq"], r["sg"], Wq2, sw2), bits(bd))
     d = assert_bf16_close(bits(y.reshape(33, O)), Yo, 1)
     assert d.max() == 0
+
+
+# ----------------------------------------------------------------- failure detection
+def test_bounded_wait_timeout_is_reported_and_the_context_survives(w8a8, oracle):
+    """A kernel whose mbarrier wait nothing satisfies gives up after its
+    bound, records the timeout (code 0x100 + site) and returns; the host
+    reads W8A8_ERR_TIMEOUT, the word is cleared by the read, and the next
+    GEMM on the same context is exact."""
+    assert w8a8.get_device_error() == (0, 0)
+    w8a8.probe_wait_timeout()
+    st, code = w8a8.get_device_error()
+    assert st == 6 and code == 0x100 + 30  # W8A8_ERR_TIMEOUT, probe site
+    assert w8a8.get_device_error() == (0, 0)
+    X = rand_bf16((40, 256), seed=95)
+    W = rand_bf16((72, 256), seed=96, scale=0.03)
+    ref = oracle.linear_postscale(bits(X), bits(W), None)
+    Xq, sx = w8a8.quantize_act(X.to(DEV))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV))
+    assert np.array_equal(bits(w8a8.gemm_postscale(Xq, sx, Wq, sw)), ref["Y"])
+    assert w8a8.get_device_error() == (0, 0)

@@ -54,6 +54,7 @@ SIGNATURES = [
     ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_get_device_error", _I32, [ctypes.POINTER(ctypes.c_int)]),
+    ("w8a8_probe_wait_timeout", _I32, [_P]),
     ("w8a8_set_gemm_timing_events", _I32, [_P, _P]),
     ("w8a8_measure_imma_peak", _I32, [ctypes.POINTER(ctypes.c_double), _P]),
     ("w8a8_stream_floor", _I32, [_P, _I64, _P, _P]),
@@ -403,6 +404,12 @@ def get_device_error():
     code = ctypes.c_int(0)
     st = lib().w8a8_get_device_error(ctypes.byref(code))
     return st, code.value
+
+
+def probe_wait_timeout():
+    """Launch the failure-detection probe: a kernel whose bounded wait runs
+    out (nothing arrives) and records a timeout; read it with get_device_error."""
+    _check("w8a8_probe_wait_timeout", lib().w8a8_probe_wait_timeout(_stream()))
 
 
 def set_gemm_timing_events(start=None, end=None):

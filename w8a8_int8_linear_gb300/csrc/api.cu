@@ -504,6 +504,13 @@ w8a8_status w8a8_get_device_error(int* code) {
     return v ? W8A8_ERR_CUDA : W8A8_OK;
 }
 
+w8a8_status w8a8_probe_wait_timeout(void* stream) {
+    DeviceInfo dev;
+    w8a8_status s = current_device(&dev);
+    if (s != W8A8_OK) return s;
+    return from_cuda(w8a8::launch_wait_timeout_probe(static_cast<cudaStream_t>(stream)));
+}
+
 const char* w8a8_last_error_detail(void) { return t_detail; }
 
 w8a8_status w8a8_set_gemm_timing_events(void* start, void* end) {

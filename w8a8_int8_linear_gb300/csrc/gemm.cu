@@ -1694,6 +1694,30 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     return e;
 }
 
+namespace {
+
+constexpr int kSiteProbe = 30;
+
+// Failure-detection probe: one thread waits on an mbarrier that nothing
+// arrives on.  The bounded wait runs out, records the timeout in this
+// translation unit's device error word, and the kernel returns normally.
+__global__ void wait_timeout_probe_kernel() {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, kSiteProbe);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_probe(cudaStream_t st) {
+    wait_timeout_probe_kernel<<<1, 32, 0, st>>>();
+    return cudaGetLastError();
+}
+
 cudaError_t gemm_read_device_error(unsigned int* code) {
     unsigned int v = 0, z = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);

@@ -70,6 +70,9 @@ constexpr unsigned int kDeviceErrorTimeoutBase = 0x100;
 // Read and clear the device error words of the GEMM and quantization
 // translation units.
 cudaError_t gemm_read_device_error(unsigned int* code);
+// One CTA whose bounded mbarrier wait runs out (nothing arrives): records a
+// timeout in the GEMM translation unit's device error word and returns.
+cudaError_t launch_wait_timeout_probe(cudaStream_t st);
 cudaError_t quant_read_device_error(unsigned int* code);
 
 // Throughput kernel of warp-level INT8 MMAs; returns tera-ops per second.

@@ -86,6 +86,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a whole launch takes milliseconds
 
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_device_error(W8A8_DEVERR_TIMEOUT_BASE + site);
+            return false;
+        }
+    }
+}
+
 // try_wait with cluster-scope acquire: pairs with release arrives issued by
 // threads of the other CTA of the cluster.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -108,20 +122,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 #pragma unroll 1
         for (int i = 0; i < 256; ++i)
             if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_device_error(W8A8_DEVERR_TIMEOUT_BASE + site);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int site) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 256; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             record_device_error(W8A8_DEVERR_TIMEOUT_BASE + site);
             return false;
