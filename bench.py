@@ -567,6 +567,25 @@ def report_configs(args):
             c.record()
             torch.cuda.synchronize()
             tms.append(a.elapsed_time(c))
+        # torch's int8 GEMM (cuBLASLt, int32 out, no scales) where it runs
+        int_mm = None
+        if not blockwise:
+            try:
+                Xq8, _ = w.quantize_act(X, w.PER_ROW)
+                imms = []
+                for r in range(6):
+                    flush.zero_()
+                    a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    torch._int_mm(Xq8, Wq.t())
+                    c.record()
+                    torch.cuda.synchronize()
+                    if r:
+                        imms.append(a.elapsed_time(c))
+                int_mm = round(work.ops / statistics.median(imms) / 1e9, 1)
+                del Xq8
+            except (RuntimeError, AttributeError):
+                int_mm = None
         st, code = w.get_device_error()
         assert st == 0 and code == 0, f"device error {code}"
         # oracle on a bounded sample of rows (about a second of host time)
@@ -587,18 +606,20 @@ def report_configs(args):
                  tops=round(ops / step_ms / 1e9, 1), gemm_tflops=round(ops / gemm_ms / 1e9, 1),
                  gemm_frac_bf16_peak=round(ops / gemm_ms / 1e9 / peaks["bf16_tflops"], 3),
                  x_int8_mma_peak=round(ops / gemm_ms / 1e9 / imma, 2), quant_gbs=round(q_bytes / q_ms / 1e6, 0),
-                 torch_bf16_tflops=round(ops / statistics.median(tms) / 1e9, 1),
+                 torch_bf16_tflops=round(ops / statistics.median(tms) / 1e9, 1), torch_int_mm_tops=int_mm,
                  oracle_tops=round(2.0 * rows_s * N * K / odt / 1e12, 4), oracle_rows=rows_s)
         rows.append(r)
         print(json.dumps(r), flush=True)
         del X, W, Wq, Wimg, Y, Xq, ws
         torch.cuda.empty_cache()
     print(f"| workload | step ms | TOPS | GEMM TFLOP/s | of bf16 peak ({peaks['source']}) | x INT8 peak "
-          f"({imma:.0f} TOPS) | quant GB/s | torch bf16 TFLOP/s | oracle TOPS ({oracle.num_threads()} cores) |")
-    print("|---|---|---|---|---|---|---|---|---|")
+          f"({imma:.0f} TOPS) | quant GB/s | torch bf16 TFLOP/s | torch _int_mm TOPS | "
+          f"oracle TOPS ({oracle.num_threads()} cores) |")
+    print("|---|---|---|---|---|---|---|---|---|---|")
     for r in rows:
         print(f"| {r['workload']} | {r['step_ms']} | {r['tops']} | {r['gemm_tflops']} | {r['gemm_frac_bf16_peak']} | "
-              f"{r['x_int8_mma_peak']} | {r['quant_gbs']:.0f} | {r['torch_bf16_tflops']} | {r['oracle_tops']} |")
+              f"{r['x_int8_mma_peak']} | {r['quant_gbs']:.0f} | {r['torch_bf16_tflops']} | "
+              f"{'-' if r['torch_int_mm_tops'] is None else r['torch_int_mm_tops']} | {r['oracle_tops']} |")
 
 
 def report_ffn(args):
