@@ -119,6 +119,8 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * images of Xq and Wq (every int8 value is exact in bf16) and, for few-token
  * post-scale shapes (M <= 256 with few 256-row weight tiles), the int32
  * partial sums of the K splits.  The same size serves both scale modes.
+ * (With M <= 128 the post-scale GEMM streams the int8 codes directly and uses
+ * only the partial-sum part.)
  */
 W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
