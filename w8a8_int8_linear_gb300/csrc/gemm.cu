@@ -26,7 +26,7 @@
 // The pair shares each tile: CTA r loads rows [128r, 128r+128) of the A tile
 // and rows [r*BN/2, (r+1)*BN/2) of the B tile into its own shared memory.
 //   warp 0       TMA producer (both CTAs): bf16 A and B stages, 128-byte
-//                swizzle, 6-deep ring; completion is counted on the leader's
+//                swizzle, 6- or 7-deep ring; completion is counted on the leader's
 //                barrier;
 //   warp 1       TMEM allocator (both CTAs) and, in the leader only, the MMA
 //                issuer: tcgen05.mma.cta_group::2 (M = 256, N = BN) into one
@@ -79,7 +79,8 @@ constexpr uint32_t MAX_DYN_SMEM = 232448;  // 227 KB opt-in shared memory per bl
 // Output staging for the TMA-store epilogue: per epilogue warp, two 1 KB
 // buffers of 32 rows x 16 bf16 columns (32-byte swizzle).
 constexpr uint32_t STAGE_OUT_BYTES = 32 * 16 * 2;
-constexpr uint32_t STAGING_BYTES = 8 * 2 * STAGE_OUT_BYTES;
+constexpr int OUT_BUFS = 1;  // staging buffers per epilogue warp
+constexpr uint32_t STAGING_BYTES = 8 * OUT_BUFS * STAGE_OUT_BYTES;
 constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - 256 - 512 - STAGING_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 4;  // warps 0-3: producer, MMA issuer, two idle; warps 4-11: epilogue
@@ -306,13 +307,15 @@ __device__ __forceinline__ void store_row(const typename AccType<EPI>::T (&acc)[
 // Stage 16 bf16 columns (8 packed words) of each of the warp's 32 rows in a
 // 1 KB buffer with the 32-byte swizzle (16-byte chunk index XOR bit 2 of the
 // row, which spreads each quarter-warp over 8 bank groups) and store them as
-// one 16 x 32 box from one lane.  Two buffers per warp alternate; a buffer is
-// rewritten only after the store issued from it two groups ago has read it.
+// one 16 x 32 box from one lane.  OUT_BUFS buffers per warp rotate; a buffer
+// is rewritten only after the store issued from it has read it.  One buffer
+// per warp measured as fast as two and leaves room for a 7th ring stage at
+// BN = 224.
 // Out-of-range rows and columns are clipped by the TMA unit.
 __device__ __forceinline__ void stage_store16(const uint32_t (&o)[8], const CUtensorMap* tmY, int col, int row_base,
                                               uint8_t* stg, int& sbuf, int lane) {
     uint8_t* buf = stg + sbuf * STAGE_OUT_BYTES;
-    if (lane == 0) bulk_wait_group_read<1>();
+    if (lane == 0) bulk_wait_group_read<OUT_BUFS - 1>();
     __syncwarp();
     const int sw = (lane >> 2) & 1;
     *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (0 ^ sw)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -323,7 +326,7 @@ __device__ __forceinline__ void stage_store16(const uint32_t (&o)[8], const CUte
         tma_store_2d(tmY, buf, col, row_base);
         bulk_commit_group();
     }
-    sbuf ^= 1;
+    sbuf = (sbuf + 1) % OUT_BUFS;
 }
 
 // bf16 output of one warp's 32 rows x COLS columns through shared memory and
@@ -574,7 +577,7 @@ __device__ __forceinline__ void store_swapped(const int32_t (&acc)[COLS], const 
             }
             if (p.tma_store) {
                 uint8_t* buf = stg + sbuf * STAGE_OUT_BYTES;
-                if (lane == 0) bulk_wait_group_read<1>();
+                if (lane == 0) bulk_wait_group_read<OUT_BUFS - 1>();
                 __syncwarp();
 #pragma unroll
                 for (int e = 0; e < 16; ++e) *reinterpret_cast<uint16_t*>(buf + e * 64 + lane * 2) = y[e];
@@ -584,7 +587,7 @@ __device__ __forceinline__ void store_swapped(const int32_t (&acc)[COLS], const 
                     tma_store_2d(tmY, buf, n_base, t0);
                     bulk_commit_group();
                 }
-                sbuf ^= 1;
+                sbuf = (sbuf + 1) % OUT_BUFS;
             } else if (n < Nout) {
                 uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
@@ -777,7 +780,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = (warp - EPI_WARP0) >> 2;      // which column half of the tile
         const uint32_t leader_acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
         constexpr bool kBf16Out = (EPI == kEpiPostscaleBf16 || EPI == kEpiBlockwiseBf16);
-        uint8_t* stg = staging + (warp - EPI_WARP0) * 2 * STAGE_OUT_BYTES;
+        uint8_t* stg = staging + (warp - EPI_WARP0) * OUT_BUFS * STAGE_OUT_BYTES;
         int sbuf = 0;
         int buf = 0;
         uint32_t buf_phase = 0;
@@ -1246,7 +1249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         constexpr int GROUPS = C::GROUPS;
         const int quarter = warp & 3;
         const int half = 0;
-        uint8_t* stg = staging + (warp - 8) * 2 * STAGE_OUT_BYTES;
+        uint8_t* stg = staging + (warp - 8) * OUT_BUFS * STAGE_OUT_BYTES;
         int sbuf = 0;
         int buf = 0;
         uint32_t buf_phase = 0;
