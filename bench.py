@@ -754,10 +754,12 @@ def report_norm(args):
 
 
 def report_decode(args):
-    """Few-token Linears (M <= 256 takes the swapped split-K path) in steady
-    state: one CUDA graph of C calls, each on its own weight copy, with the C
-    copies together larger than L2, replayed back to back; per-call time is
-    the replay time / C.  The same for torch's bf16 matmul on C bf16 weights."""
+    """Few-token Linears in steady state: one CUDA graph of C calls, each on
+    its own weight copy, with the C copies together larger than L2, replayed
+    back to back; per-call time is the replay time / C.  Columns: the fused
+    Linear on the packed image (swapped split-K tensor-core path), the fused
+    Linear on the int8 codes (a GEMV up to 8 tokens), the GEMM on int8 codes
+    quantized beforehand, and torch's bf16 matmul on C bf16 weights."""
     import torch
     import w8a8_int8_linear_gb300 as w
     dev = torch.device("cuda", 0)
@@ -797,7 +799,7 @@ def report_decode(args):
             Wq, sw = w.quantize_weight(W)
             packs.append((w.pack_weight(Wq), sw, Wq))
         b = (0.01 * torch.randn((N,), generator=gen, device=dev)).to(torch.bfloat16)
-        for M in (1, 16, 77, 128, 256):
+        for M in (1, 2, 4, 8, 16, 77, 128, 256):
             X = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
             Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             sx = torch.empty((M,), dtype=torch.float32, device=dev)
@@ -810,9 +812,14 @@ def report_decode(args):
             wsg = torch.empty(max(w.workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
             t_g8 = graph_time([lambda P=P: w.gemm_postscale(Xq, sxq, P[2], P[1], b, out=Y, workspace=wsg)
                                for P in packs])
+            # the fused Linear on the int8 codes (quantization + GEMV up to 8 tokens)
+            wsc = torch.empty(max(w.linear_codes_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
+            t_codes = graph_time([lambda P=P: w.linear_postscale_codes(X, P[2], P[1], b, out=Y, workspace=wsc,
+                                                                       sx_out=sx) for P in packs])
             r = dict(workload=f"decode_{M}x{N}x{K}", copies=C, linear_us=round(t_lin, 2),
-                     gemm_int8_us=round(t_g8, 2), torch_bf16_us=round(t_mm, 2),
-                     image_gbs=round(N * K * 2 / t_lin / 1e3, 0), int8_gbs=round(N * K / t_g8 / 1e3, 0))
+                     linear_codes_us=round(t_codes, 2), gemm_int8_us=round(t_g8, 2), torch_bf16_us=round(t_mm, 2),
+                     image_gbs=round(N * K * 2 / t_lin / 1e3, 0), int8_gbs=round(N * K / t_g8 / 1e3, 0),
+                     codes_gbs=round(N * K / t_codes / 1e3, 0))
             out.append(r)
             print(json.dumps(r), flush=True)
         del Ws, packs
@@ -826,6 +833,7 @@ PROFILE_CASES = {
     "gelu_quant_4096x4096x2048": ("gelu_quant", 4096, 4096, 2048),
     "norm_layer_8192x5120": ("norm_layer", 8192, 0, 5120),
     "gemm_int8_decode_1x13824x5120": ("gemm_int8", 1, 13824, 5120),
+    "linear_codes_decode_1x13824x5120": ("linear_codes", 1, 13824, 5120),
 }
 
 
@@ -849,6 +857,9 @@ def profile_case(name):
             b = (0.5 * torch.randn((N,), generator=g, device=dev)).to(torch.bfloat16)
             Wimg = w.pack_weight(Wq)
             fn = lambda: w.linear_postscale_gelu_quant(X, Wimg, sw, b)
+        elif what == "linear_codes":
+            b = (0.5 * torch.randn((N,), generator=g, device=dev)).to(torch.bfloat16)
+            fn = lambda: w.linear_postscale_codes(X, Wq, sw, b)
         else:
             Xq, sx = w.quantize_act(X)
             fn = lambda: w.gemm_postscale(Xq, sx, Wq, sw)

@@ -120,7 +120,8 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * post-scale shapes (M <= 256 with few 256-row weight tiles), the int32
  * partial sums of the K splits.  The same size serves both scale modes.
  * (With M <= 128 the post-scale GEMM streams the int8 codes directly and uses
- * only the partial-sum part.)
+ * only the partial-sum part; with M <= 8 and M * K <= 131072 it is a GEMV on
+ * the CUDA cores that uses none of it.)
  */
 W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -132,7 +133,9 @@ W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   (per output channel), bias [N] bf16 or NULL, Y [M,N] bf16 out.
  *   workspace: device buffer of at least w8a8_gemm_workspace_size(M,N,K)
  *   bytes, 256-byte aligned, owned by the caller, not read after the call's
- *   work completes on `stream`.
+ *   work completes on `stream`.  With M <= 8 and M * K <= 131072 the GEMM is
+ *   a GEMV on the CUDA cores that needs no workspace (workspace may be NULL
+ *   and workspace_bytes 0); this also holds for w8a8_gemm_postscale_s32.
  */
 W8A8_API w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
                                 const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
@@ -179,6 +182,32 @@ W8A8_API size_t w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
 W8A8_API w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, const float* sw, const void* bias,
                                            void* Y, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq,
                                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes of w8a8_linear_postscale_codes: 0 when M <= 8 and
+ * M * K <= 131072 (one kernel, no workspace); otherwise room for the int8
+ * codes of X (M * K bytes, rounded up to 256; unused when the caller passes
+ * Xq) plus w8a8_gemm_workspace_size(M,N,K). */
+W8A8_API size_t w8a8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Fused W8A8 Linear, post-scale, against the int8 weight codes themselves
+ * (no bf16 image): per-token quantization of X, then the post-scale GEMM of
+ * w8a8_gemm_postscale.  Meant for a handful of tokens (decoding): with
+ * M <= 8 and M * K <= 131072 it is one kernel, a GEMV on the CUDA cores in
+ * which every CTA quantizes X into its shared memory while its first weight
+ * loads are in flight, and each weight code is read once.  Any M is
+ * accepted (larger shapes run the quantization kernel and then the GEMM);
+ * for many tokens w8a8_linear_postscale on a packed image is faster.
+ * Results are identical to w8a8_quantize_act (PER_ROW) + w8a8_gemm_postscale
+ * on the same inputs.
+ *   X [M,K] bf16, Wq [N,K] int8 (w8a8_quantize_weight, PER_ROW), sw [N] fp32,
+ *   bias [N] bf16 or NULL, Y [M,N] bf16 out, sx [M] fp32 out, Xq [M,K] int8
+ *   out or NULL, workspace of w8a8_linear_codes_workspace_size(M,N,K) bytes,
+ *   256-byte aligned (may be NULL when that size is 0).
+ */
+W8A8_API w8a8_status w8a8_linear_postscale_codes(const void* X, const int8_t* Wq, const float* sw, const void* bias,
+                                                 void* Y, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Fused W8A8 Linear, blockwise: 1x128 activation quantization followed by the
@@ -271,7 +300,8 @@ W8A8_API w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* s
  * counterpart: this is a library convenience).  Same arguments, results and
  * checks, minus the workspace: the scratch lives in a fixed 64 MiB device
  * array inside the library, so the shape must satisfy
- * w8a8_gemm_workspace_size(M,N,K) <= 64 MiB (for example M = N = K = 4096),
+ * w8a8_gemm_workspace_size(M,N,K) <= 64 MiB (for example M = N = K = 4096)
+ * or M <= 8 with M * K <= 131072 (the few-token GEMV needs no scratch),
  * else W8A8_ERR_WORKSPACE and nothing is launched.
  *
  * For callers that cannot allocate device memory at the call site, for

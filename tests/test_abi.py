@@ -76,9 +76,11 @@ def test_argument_checks_before_device(cdll):
     assert g(null, null, null, null, null, null, 4, 0, 16, null, 0, null) == 0
     assert g(fake, null, fake, fake, null, fake, 4, 4, 16, fake, 1 << 20, null) == 1
     assert g(fake, fake, fake, fake, odd, fake, 4, 4, 16, fake, 1 << 20, null) == 2
-    assert g(fake, fake, fake, fake, null, fake, 4, 4, 16, null, 1 << 20, null) == 7
-    assert g(fake, fake, fake, fake, null, fake, 4, 4, 16, fake, 10, null) == 7
-    assert g(fake, fake, fake, fake, null, fake, 4, 4, 16, P(0x1010), 1 << 20, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 16, 4, 16, null, 1 << 20, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 16, 4, 16, fake, 10, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 16, 4, 16, P(0x1010), 1 << 20, null) == 7
+    # blockwise needs its workspace even for one token
+    assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 1, 4, 128, null, 0, null) == 7
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 4, 4, 64, fake, 1 << 20, null) == 3
     assert L.w8a8_gemm_postscale_s32(fake, fake, null, 4, 4, 16, fake, 1 << 20, null) == 1
     assert L.w8a8_gemm_blockwise_f32(fake, null, fake, fake, fake, 4, 4, 128, fake, 1 << 20, null) == 1
@@ -110,6 +112,18 @@ def test_widened_entry_points_check_arguments_before_device(cdll):
     assert f(fake, fake, fake, null, null, fake, 4, 256, 64, fake, null, fake, 1 << 20, null) == 1
     assert f(fake, fake, fake, null, fake, fake, 4, 256, 64, fake, null, null, 1 << 20, null) == 7
     assert f(null, null, null, null, null, null, 0, 256, 64, null, null, null, 0, null) == 0
+    # fused Linear on int8 weight codes: K rule, nothing to do, pointers, alignment, workspace
+    c = L.w8a8_linear_postscale_codes
+    assert c(fake, fake, fake, null, fake, 4, 4, 20, fake, null, fake, 1 << 20, null) == 3
+    assert c(null, null, null, null, null, 0, 4, 16, null, null, null, 0, null) == 0
+    assert c(fake, null, fake, null, fake, 4, 4, 16, fake, null, fake, 1 << 20, null) == 1
+    assert c(fake, fake, fake, null, fake, 4, 4, 16, null, null, fake, 1 << 20, null) == 1
+    assert c(odd, fake, fake, null, fake, 4, 4, 16, fake, null, fake, 1 << 20, null) == 2
+    assert c(fake, fake, fake, null, fake, 4, 4, 16, fake, odd, fake, 1 << 20, null) == 2
+    # (one or two tokens with M * K <= 131072: the one-kernel path needs no workspace)
+    assert c(fake, fake, fake, null, fake, 16, 4, 16, fake, null, null, 1 << 20, null) == 7
+    assert c(fake, fake, fake, null, fake, 16, 4, 16, fake, null, fake, 10, null) == 7
+    assert c(fake, fake, fake, null, fake, 2, 4, 131072, fake, null, null, 1 << 20, null) == 7
     # image GEMMs
     assert L.w8a8_gemm_blockwise_images(fake, fake, fake, fake, null, fake, 4, 4, 100, null) == 3
     assert L.w8a8_gemm_blockwise_images(fake, null, fake, fake, null, fake, 4, 4, 128, null) == 1
@@ -134,6 +148,19 @@ def test_workspace_size(cdll):
     assert L.w8a8_gemm_workspace_size(1, 3072, 5120) == 5120 * 2 + 3072 * 5120 * 2 + s
     assert L.w8a8_linear_workspace_size(1, 3072, 5120) == 256 * ((5120 * 2 + 255) // 256) + s
     assert L.w8a8_linear_workspace_size(4096, 4096, 4096) == 4096 * 4096 * 2
+    # the fused Linear on codes: nothing for the one-kernel GEMV (M <= 2,
+    # M * K <= 131072), the codes of X before the GEMV (M <= 8), else the codes
+    # plus the GEMM's workspace
+    assert L.w8a8_linear_codes_workspace_size(0, 3072, 5120) == 0
+    assert L.w8a8_linear_codes_workspace_size(1, 3072, 5120) == 0
+    assert L.w8a8_linear_codes_workspace_size(2, 64, 65536) == 0
+    assert L.w8a8_linear_codes_workspace_size(1, 64, 131072) == 0
+    assert L.w8a8_linear_codes_workspace_size(3, 5, 16) == 256
+    assert L.w8a8_linear_codes_workspace_size(8, 13824, 16384) == 8 * 16384
+    assert (L.w8a8_linear_codes_workspace_size(8, 64, 16400) ==
+            256 * ((8 * 16400 + 255) // 256) + L.w8a8_gemm_workspace_size(8, 64, 16400))
+    assert (L.w8a8_linear_codes_workspace_size(16, 4096, 4096) ==
+            16 * 4096 + L.w8a8_gemm_workspace_size(16, 4096, 4096))
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -144,6 +144,50 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
+# At most 8 tokens (M * K <= 131072): a CUDA-core GEMV on the int8 codes
+# (dp4a), the activation codes staged in each CTA's shared memory.  Warps own
+# balanced ranges of weight-row groups (1 row for up to 2 tokens, 2 rows for
+# 3..8) and walk each row in steps of 4 x 512 bytes, prefetching the next
+# step.  The shapes cover every token count, K shorter than one slice, a
+# partial last step, many steps per row, N below one group per warp, odd,
+# and larger than the persistent grid's warp count, the shared-memory limit,
+# and one shape just past it (the int8-operand tensor-core kernel).
+@pytest.mark.parametrize("M,N,K,bias", [
+    (1, 1, 16, True),          # one output, one 16-byte slice
+    (2, 3, 48, False),
+    (3, 7, 528, True),         # odd N with 2-row groups, partial step
+    (4, 33, 2064, False),
+    (5, 300, 5120, True),
+    (6, 1031, 1040, False),
+    (7, 64, 16384, True),      # 16 steps per row
+    (8, 777, 4112, True),      # 8-token accumulators, odd N
+    (1, 3072, 5120, False),    # the decode shape
+    (8, 9999, 256, False),     # more row groups than the grid's warps
+    (8, 300, 16384, True),     # 128 KB of codes: the shared-memory limit
+    (8, 100, 16400, False),    # past it: the tensor-core kernel
+])
+def test_gemm_postscale_gemv(w8a8, oracle, M, N, K, bias):
+    check_postscale(w8a8, oracle, M, N, K, bias)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 24, 131072), (8, 40, 16384)])
+def test_gemv_exactness_at_max_k(w8a8, oracle, M, N, K):
+    """All-+-127 codes at the largest K the GEMV takes for this M: at one
+    token |acc| reaches 127*127*131072 = 2,114,060,288, just inside int32."""
+    g = torch.Generator().manual_seed(12)
+    Xq = ((torch.randint(0, 2, (M, K), generator=g) * 2 - 1) * 127).to(torch.int8)
+    Wq = ((torch.randint(0, 2, (N, K), generator=g) * 2 - 1) * 127).to(torch.int8)
+    Xq[0] = 127
+    Wq[0] = 127
+    Wq[1] = -127
+    assert w8a8.gemv_takes(M, K)
+    ref = oracle.gemm_s32(Xq.numpy(), Wq.numpy())
+    acc = w8a8.gemm_postscale_s32(Xq.to(DEV), Wq.to(DEV)).cpu().numpy()
+    assert acc[0, 0] == 16129 * K and acc[0, 1] == -16129 * K
+    assert np.array_equal(acc, ref)
+    assert w8a8.get_device_error() == (0, 0)
+
+
 def check_postscale(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=1 + M, outliers=0.01, oscale=20.0)
     W = rand_bf16((N, K), seed=2 + N, scale=0.02)
@@ -217,9 +261,14 @@ def test_gemm_rejects_bad_arguments(w8a8):
     with pytest.raises(ValueError):
         w8a8.gemm_postscale(Xq, torch.ones(4, device=DEV), Wq, torch.ones(4, device=DEV))
     with pytest.raises(w8a8.W8A8Error, match="WORKSPACE"):
-        w8a8.gemm_postscale(torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
+        w8a8.gemm_postscale(torch.zeros((16, 32), dtype=torch.int8, device=DEV), torch.ones(16, device=DEV),
                             torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
                             workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    # up to 8 tokens the GEMV needs no workspace: a short one is fine
+    Y = w8a8.gemm_postscale(torch.ones((8, 32), dtype=torch.int8, device=DEV), torch.ones(8, device=DEV),
+                            torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
+                            workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert torch.all(Y.float() == 32.0)
 
 
 # ----------------------------------------------------------------- blockwise GEMM
@@ -290,6 +339,52 @@ def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
     assert w8a8.get_device_error() == (0, 0)
 
 
+# The fused Linear on int8 weight codes: one GEMV kernel that quantizes X in
+# every CTA for one or two tokens (M * K <= 131072); the quantization kernel
+# and then the GEMV (weights read before its dependency wait) up to 8 tokens;
+# else the quantization kernel and the int8-operand tensor-core kernel (up to
+# 128 tokens) or operand images.
+@pytest.mark.parametrize("M,N,K,bias", [(1, 3072, 5120, True), (2, 1000, 4096, False), (2, 7, 16, True),
+                                        (3, 520, 1040, False), (8, 4096, 4096, True),
+                                        (5, 1000, 16, True), (8, 520, 16384, False), (1, 300, 131072, True),
+                                        (2, 300, 131072, False), (9, 600, 2048, True), (77, 3072, 5120, False),
+                                        (300, 520, 1040, True)])
+def test_linear_postscale_codes(w8a8, oracle, M, N, K, bias):
+    X = rand_bf16((M, K), seed=45 + M, outliers=0.01, oscale=20.0)
+    W = rand_bf16((N, K), seed=46 + N, scale=0.02)
+    b = rand_bf16((N,), seed=47, scale=0.01) if bias else None
+    ref = oracle.linear_postscale(bits(X), bits(W), None if b is None else bits(b))
+    Wq, sw = w8a8.quantize_weight(W.to(DEV))
+    bd = None if b is None else b.to(DEV)
+    Y, sx, Xq = w8a8.linear_postscale_codes(X.to(DEV), Wq, sw, bd, codes=True)
+    assert np.array_equal(Xq.cpu().numpy(), ref["Xq"])
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), ref["sx"].view(np.uint32))
+    d = assert_bf16_close(bits(Y), ref["Y"], 1)
+    assert d.max() == 0
+    # codes kept in the workspace instead: same output
+    Y2, _, none = w8a8.linear_postscale_codes(X.to(DEV), Wq, sw, bd)
+    assert none is None and torch.equal(Y2, Y)
+    assert w8a8.get_device_error() == (0, 0)
+
+
+def test_linear_postscale_codes_rejects_bad_arguments(w8a8):
+    X = torch.zeros((4, 64), dtype=torch.bfloat16, device=DEV)
+    Wq = torch.zeros((8, 64), dtype=torch.int8, device=DEV)
+    sw = torch.ones(8, device=DEV)
+    with pytest.raises(w8a8.W8A8Error, match="WORKSPACE"):
+        w8a8.linear_postscale_codes(torch.zeros((16, 64), dtype=torch.bfloat16, device=DEV), Wq, sw,
+                                    workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    with pytest.raises(w8a8.W8A8Error, match="SHAPE"):
+        w8a8.linear_postscale_codes(torch.zeros((4, 24), dtype=torch.bfloat16, device=DEV),
+                                    torch.zeros((8, 24), dtype=torch.int8, device=DEV), sw)
+    Y, sx, _ = w8a8.linear_postscale_codes(torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV), Wq, sw)
+    assert Y.shape == (0, 8)
+    # all-zero tokens: the output is the bias exactly
+    b = rand_bf16((8,), seed=48).to(DEV)
+    Y, sx, _ = w8a8.linear_postscale_codes(X, Wq, sw, b)
+    assert torch.equal(Y, b.expand(4, 8)) and torch.all(sx == 0)
+
+
 @pytest.mark.parametrize("M,N,K,bias", [(64, 256, 256, False), (300, 456, 1408, True), (1, 130, 13824, False)])
 def test_linear_blockwise_fused(w8a8, oracle, M, N, K, bias):
     X = torch.nn.functional.gelu(rand_bf16((M, K), seed=50 + M).float()).to(torch.bfloat16)
@@ -332,6 +427,21 @@ def test_int8linear_module(w8a8, oracle, mode):
     b = bits(lin.bias)
     ref = oracle.linear_postscale(X, W, b) if mode == "postscale" else oracle.linear_blockwise(X, W, b)
     d = assert_bf16_close(bits(y.reshape(15, 200)), ref["Y"], 1)
+    assert d.max() == 0
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_int8linear_module_decode(w8a8, oracle, M):
+    """Up to 8 tokens the post-scale module runs the GEMV on the int8 codes."""
+    from w8a8_int8_linear_gb300.module import Int8Linear
+    torch.manual_seed(2)
+    lin = torch.nn.Linear(1040, 300, bias=True).to(DEV).to(torch.bfloat16)
+    m = Int8Linear.from_linear(lin)
+    x = rand_bf16((M, 1, 1040), seed=62 + M, outliers=0.01, oscale=20.0).to(DEV)
+    y = m(x)
+    assert y.shape == (M, 1, 300)
+    ref = oracle.linear_postscale(bits(x.reshape(M, 1040)), bits(lin.weight), bits(lin.bias))
+    d = assert_bf16_close(bits(y.reshape(M, 300)), ref["Y"], 1)
     assert d.max() == 0
 
 
@@ -441,22 +551,25 @@ def test_norm_quant_rejects_bad_arguments(w8a8):
 
 def test_int8linear_with_fused_norm(w8a8, oracle):
     """Int8Linear(norm=...) = norm + per-token quant in one pass, then the
-    post-scale GEMM on the code image, against the oracle composition."""
+    post-scale GEMM on the code image (on the int8 codes, as a GEMV, for up
+    to 8 tokens), against the oracle composition."""
     torch.manual_seed(1)
-    for norm in ("rms", "layer"):
+    for norm, lead in (("rms", (2, 7)), ("layer", (2, 7)), ("rms", (1, 3)), ("layer", (8,))):  # 3, 8: the GEMV
+        T = int(np.prod(lead))
         W = rand_bf16((300, 512), seed=80, scale=0.03)
         b = rand_bf16((300,), seed=81, scale=0.1)
         g = (rand_bf16((512,), seed=82, scale=0.1) + 1.0).to(torch.bfloat16)
         be = rand_bf16((512,), seed=83, scale=0.1) if norm == "layer" else None
         m = w8a8.Int8Linear(W.to(DEV), b.to(DEV), norm=norm, norm_weight=g.to(DEV),
                             norm_bias=None if be is None else be.to(DEV), eps=1e-5)
-        x = rand_bf16((2, 7, 512), seed=84, scale=2.0)
+        x = rand_bf16((*lead, 512), seed=84 + T, scale=2.0)
         y = m(x.to(DEV))
-        _, Xq, sx = oracle.norm_quant(bits(x.reshape(14, 512)), bits(g), None if be is None else bits(be), 1e-5,
+        assert y.shape == (*lead, 300)
+        _, Xq, sx = oracle.norm_quant(bits(x.reshape(T, 512)), bits(g), None if be is None else bits(be), 1e-5,
                                       oracle.RMS_NORM if norm == "rms" else oracle.LAYER_NORM)
         Wq, sw = oracle.quantize_weight(bits(W), oracle.PER_ROW)
         Yo = oracle.epilogue_postscale(oracle.gemm_s32(Xq, Wq), sx, sw, bits(b))
-        d = assert_bf16_close(bits(y.reshape(14, 300)), Yo, 1)
+        d = assert_bf16_close(bits(y.reshape(T, 300)), Yo, 1)
         assert d.max() == 0
 
 

@@ -45,6 +45,8 @@ SIGNATURES = [
     ("w8a8_linear_workspace_size", _SZ, [_I64, _I64, _I64]),
     ("w8a8_linear_postscale", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_linear_blockwise", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    ("w8a8_linear_codes_workspace_size", _SZ, [_I64, _I64, _I64]),
+    ("w8a8_linear_postscale_codes", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_linear_postscale_gelu_quant", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_images", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_norm_quant", _I32, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -168,6 +170,22 @@ def _workspace(ws, M, N, K, device):
     return ws.get(M, N, K, device)
 
 
+# Up to this many tokens, with M * K up to GEMV_MAX_CODE_BYTES, the post-scale
+# GEMM is a CUDA-core GEMV on the int8 codes, which needs no workspace.
+GEMV_MAX_TOKENS = 8
+GEMV_MAX_CODE_BYTES = 131072
+
+
+def gemv_takes(M, K):
+    return 1 <= M <= GEMV_MAX_TOKENS and M * K <= GEMV_MAX_CODE_BYTES
+
+
+def _postscale_workspace(ws, M, N, K, device):
+    if ws is None and gemv_takes(M, K):
+        return None
+    return _workspace(ws, M, N, K, device)
+
+
 def gemm_postscale(Xq, sx, Wq, sw, bias=None, out=None, workspace=None):
     """Y bf16 [M,N] = bf16(((acc * sx[m]) * sw[n]) + bias[n]), acc = Xq . Wq^T exact in int32."""
     _need(Xq, torch.int8, "Xq", 2)
@@ -179,10 +197,10 @@ def gemm_postscale(Xq, sx, Wq, sw, bias=None, out=None, workspace=None):
     M, K = Xq.shape
     N = Wq.shape[0]
     Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
-    ws = _workspace(workspace, M, N, K, Xq.device)
+    ws = _postscale_workspace(workspace, M, N, K, Xq.device)
     _check("w8a8_gemm_postscale",
            lib().w8a8_gemm_postscale(_ptr(Xq), _ptr(sx), _ptr(Wq), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
-                                     _ptr(ws), ws.numel(), _stream()))
+                                     _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
     return Y
 
 
@@ -233,9 +251,10 @@ def gemm_postscale_s32(Xq, Wq, workspace=None):
     M, K = Xq.shape
     N = Wq.shape[0]
     acc = torch.empty((M, N), dtype=torch.int32, device=Xq.device)
-    ws = _workspace(workspace, M, N, K, Xq.device)
+    ws = _postscale_workspace(workspace, M, N, K, Xq.device)
     _check("w8a8_gemm_postscale_s32",
-           lib().w8a8_gemm_postscale_s32(_ptr(Xq), _ptr(Wq), _ptr(acc), M, N, K, _ptr(ws), ws.numel(), _stream()))
+           lib().w8a8_gemm_postscale_s32(_ptr(Xq), _ptr(Wq), _ptr(acc), M, N, K, _ptr(ws),
+                                         0 if ws is None else ws.numel(), _stream()))
     return acc
 
 
@@ -303,6 +322,40 @@ def linear_postscale(X, Wimg, sw, bias=None, out=None, workspace=None, sx_out=No
 def linear_blockwise(X, Wimg, sw, bias=None, out=None, workspace=None, sx_out=None, codes=False):
     """Fused W8A8 Linear, blockwise (1x128 activation, 128x128 weight scales)."""
     return _linear("w8a8_linear_blockwise", BLOCK, X, Wimg, sw, bias, out, workspace, sx_out, codes)
+
+
+def linear_codes_workspace_size(M, N, K):
+    return int(lib().w8a8_linear_codes_workspace_size(M, N, K))
+
+
+def linear_postscale_codes(X, Wq, sw, bias=None, out=None, workspace=None, sx_out=None, codes=False):
+    """Fused W8A8 Linear, post-scale, against the int8 weight codes (no
+    image): per-token quantization of X, then the post-scale GEMM; with at
+    most 8 tokens (M * K <= 131072) one GEMV kernel that quantizes X itself
+    and reads each weight code once.  Returns (Y, sx, Xq or None);
+    codes=True also returns Xq."""
+    _need(X, torch.bfloat16, "X", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(sw, torch.float32, "sw")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = X.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    sx = sx_out if sx_out is not None else torch.empty((M,), dtype=torch.float32, device=X.device)
+    Xq = None
+    if codes is True:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    elif isinstance(codes, torch.Tensor):
+        Xq = codes
+    ws = workspace
+    need = linear_codes_workspace_size(M, N, K)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=X.device)
+    _check("w8a8_linear_postscale_codes",
+           lib().w8a8_linear_postscale_codes(_ptr(X), _ptr(Wq), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K, _ptr(sx),
+                                             _ptr(Xq), _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
+    return Y, sx, Xq
 
 
 def linear_postscale_gelu_quant(X, Wimg, sw, bias=None, out=None, sg_out=None, workspace=None, sx_out=None,

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/w8a8.h"
+#include "gemv.h"
 #include "kernels.h"
 
 namespace {
@@ -122,8 +123,9 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
     if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(out) || (sx && !aligned16(sx)) ||
         (sw && !aligned16(sw)) || (bias && !aligned16(bias)))
         return W8A8_ERR_ALIGNMENT;
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < w8a8_gemm_workspace_size(M, N, K))
-        return W8A8_ERR_WORKSPACE;
+    // the few-token post-scale GEMV needs no workspace
+    const size_t need = (!block && w8a8::gemv_takes(M, K)) ? 0 : w8a8_gemm_workspace_size(M, N, K);
+    if (need && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need)) return W8A8_ERR_WORKSPACE;
     return current_device(dev);
 }
 
@@ -207,15 +209,41 @@ w8a8_status run_linear_gelu_quant(const void* X, const void* Wimg, const float* 
     return run_gemm_images(w8a8::kEpiGeluQuant, ws, Wimg, sx, sw, bias, Gimg, M, N, K, nullptr, dev, st, sg, true);
 }
 
+// Few-token post-scale GEMM on the CUDA cores (with the per-token
+// quantization folded in when X is given instead of Xq), with the timing hook
+// around the launch.
+w8a8_status run_gemv(int epi, const void* X, const int8_t* Xq, float* sx, int8_t* Xq_out, const int8_t* Wq,
+                     const float* sw, const void* bias, void* out, int64_t M, int64_t N, int64_t K,
+                     bool weights_settled, const DeviceInfo& dev, cudaStream_t st) {
+    cudaError_t e;
+    if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
+    e = X ? w8a8::launch_gemv_s8_quant(X, sx, Xq_out, Wq, sw, bias, out, M, N, K, dev.num_sms, st)
+          : w8a8::launch_gemv_s8(epi, Xq, sx, Wq, sw, bias, out, M, N, K, weights_settled, dev.num_sms, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail("few-token GEMV launch", e);
+    }
+    if (t_gemm_end && (e = cudaEventRecord(t_gemm_end, st)) != cudaSuccess) return cuda_fail("event", e);
+    return W8A8_OK;
+}
+
+bool takes_gemv(int epi, int64_t M, int64_t K) {
+    return (epi == w8a8::kEpiPostscaleBf16 || epi == w8a8::kEpiPostscaleS32) && w8a8::gemv_takes(M, K);
+}
+
 w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
                      const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* ws, const DeviceInfo& dev,
-                     cudaStream_t st) {
+                     cudaStream_t st, bool weights_settled = false) {
+    // a handful of tokens: a GEMV streaming the int8 weight codes
+    if (takes_gemv(epi, M, K))
+        return run_gemv(epi, nullptr, Xq, const_cast<float*>(sx), nullptr, Wq, sw, bias, out, M, N, K,
+                        weights_settled, dev, st);
     void* enc = encode_fn();
     if (!enc) return W8A8_ERR_CUDA;
     uint8_t* w = static_cast<uint8_t*>(ws);
     if (w8a8::gemm_takes_int8(epi, M)) {
         // few tokens: the GEMM streams the int8 codes itself, no images
-        return run_gemm_images(epi, Xq, Wq, sx, sw, bias, out, M, N, K, w, dev, st, nullptr, false, true);
+        return run_gemm_images(epi, Xq, Wq, sx, sw, bias, out, M, N, K, w, dev, st, nullptr, weights_settled, true);
     }
     void* Ab = w;
     void* Bb = w + align256(static_cast<size_t>(M) * K * 2);
@@ -225,6 +253,50 @@ w8a8_status run_gemm(int epi, const int8_t* Xq, const float* sx, const int8_t* W
     e = w8a8::launch_expand_s8_bf16(Wq, N * K, Bb, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("expand Wq launch", e);
     return run_gemm_images(epi, Ab, Bb, sx, sw, bias, out, M, N, K, partial, dev, st);
+}
+
+bool linear_codes_fused(int64_t M, int64_t K) { return w8a8::gemv_takes(M, K) && M <= w8a8::kGemvFusedMaxTokens; }
+
+// The one-kernel GEMV path needs no workspace; otherwise the codes of X, plus
+// the GEMM's workspace unless the GEMM is the GEMV.
+size_t linear_codes_workspace(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || linear_codes_fused(M, K)) return 0;
+    size_t b = align256(static_cast<size_t>(M) * K);
+    if (!w8a8::gemv_takes(M, K))
+        b += align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2) +
+             align256(w8a8::splitk_partial_bytes(M, N, K));
+    return b;
+}
+
+// Checks and launches of the fused Linear on int8 weight codes: per-token
+// quantization of X, then the post-scale GEMM on the codes.
+w8a8_status run_linear_codes(const void* X, const int8_t* Wq, const float* sw, const void* bias, void* Y, int64_t M,
+                             int64_t N, int64_t K, float* sx, int8_t* Xq, void* ws, size_t ws_bytes,
+                             cudaStream_t st) {
+    if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
+    w8a8_status s = check_k(K, false);
+    if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX) return W8A8_ERR_SHAPE;
+    if (M == 0 || N == 0) return W8A8_OK;
+    if (!X || !Wq || !sw || !Y || !sx) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(sw) || !aligned16(Y) || !aligned16(sx) ||
+        (Xq && !aligned16(Xq)) || (bias && !aligned16(bias)))
+        return W8A8_ERR_ALIGNMENT;
+    const size_t need = linear_codes_workspace(M, N, K);
+    if (need && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need))
+        return W8A8_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
+    // one or two tokens: one kernel quantizes X in every CTA and streams the weight codes
+    if (linear_codes_fused(M, K))
+        return run_gemv(w8a8::kEpiPostscaleBf16, X, nullptr, sx, Xq, Wq, sw, bias, Y, M, N, K, false, dev, st);
+    int8_t* q = Xq ? Xq : static_cast<int8_t*>(ws);
+    void* rest = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K);
+    cudaError_t e = w8a8::launch_quant_rows(X, M, K, q, nullptr, sx, dev.num_sms, st);
+    if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
+    // Wq predates the quantization kernel just launched (which waited for all
+    // earlier work), so the GEMM may start reading it before that kernel ends.
+    return run_gemm(w8a8::kEpiPostscaleBf16, q, sx, Wq, sw, bias, Y, M, N, K, rest, dev, st, true);
 }
 
 // Scratch of the allocation-free GEMM entry point: a fixed device array,
@@ -338,6 +410,15 @@ w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, const float* 
                       static_cast<cudaStream_t>(stream));
 }
 
+size_t w8a8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K) { return linear_codes_workspace(M, N, K); }
+
+w8a8_status w8a8_linear_postscale_codes(const void* X, const int8_t* Wq, const float* sw, const void* bias, void* Y,
+                                        int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    return run_linear_codes(X, Wq, sw, bias, Y, M, N, K, sx, Xq, workspace, workspace_bytes,
+                            static_cast<cudaStream_t>(stream));
+}
+
 w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, const float* sw, const void* bias, void* Y,
                                   int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq, void* workspace,
                                   size_t workspace_bytes, void* stream) {
@@ -449,10 +530,10 @@ w8a8_status w8a8_gemm_postscale_noalloc(const int8_t* Xq, const float* sx, const
     w8a8_status s = check_k(K, false);
     if (s != W8A8_OK) return s;
     if (M == 0 || N == 0) return W8A8_OK;
-    if (w8a8_gemm_workspace_size(M, N, K) > kNoAllocScratchBytes) {
+    const size_t need = w8a8::gemv_takes(M, K) ? 0 : w8a8_gemm_workspace_size(M, N, K);
+    if (need > kNoAllocScratchBytes) {
         set_detail("shape %lld x %lld x %lld needs %zu bytes of scratch; the fixed no-alloc scratch holds %zu",
-                   (long long)M, (long long)N, (long long)K, w8a8_gemm_workspace_size(M, N, K),
-                   kNoAllocScratchBytes);
+                   (long long)M, (long long)N, (long long)K, need, kNoAllocScratchBytes);
         return W8A8_ERR_WORKSPACE;
     }
     void* scratch = nullptr;

@@ -6,15 +6,18 @@ describes what it does: weights quantized to INT8 once at model
 initialization, activations quantized dynamically before every Linear.  This
 module does exactly that through the library: the weight is quantized and its
 exact bf16 image packed once (`from_linear` / `__init__`), and every forward
-is one fused call (per-token or 1x128 quantization plus the INT8 GEMM).  It
-keeps no bf16 copy of the original weight and has no fallback path: every
-shape runs the INT8 kernels.
+is one fused call (per-token or 1x128 quantization plus the INT8 GEMM).  With
+at most 8 tokens (decoding) a post-scale forward runs against the int8 codes
+instead of the image: a GEMV that reads each weight byte once.  It keeps no
+bf16 copy of the original weight and has no fallback path: every shape runs
+the INT8 kernels.
 """
 import torch
 
-from . import BLOCK, LAYER_NORM, PER_ROW, RMS_NORM, gemm_blockwise_images, gemm_postscale_images, \
-    linear_blockwise, linear_postscale, linear_postscale_gelu_quant, linear_workspace_size, norm_quant, \
-    pack_weight, quantize_weight
+from . import BLOCK, GEMV_MAX_TOKENS, LAYER_NORM, PER_ROW, RMS_NORM, gemm_blockwise_images, gemm_postscale, \
+    gemm_postscale_images, linear_blockwise, linear_codes_workspace_size, linear_postscale, \
+    linear_postscale_codes, linear_postscale_gelu_quant, linear_workspace_size, norm_quant, pack_weight, \
+    quantize_weight
 
 
 class Int8Linear(torch.nn.Module):
@@ -56,8 +59,9 @@ class Int8Linear(torch.nn.Module):
         b = None if linear.bias is None else linear.bias.detach()
         return cls(w, b, mode)
 
-    def _workspace(self, M, device):
-        need = max(linear_workspace_size(M, self.out_features, self.in_features), 256)
+    def _workspace(self, M, device, codes=False):
+        size = linear_codes_workspace_size if codes else linear_workspace_size
+        need = max(size(M, self.out_features, self.in_features), 256)
         if self._ws is None or self._ws.numel() < need or self._ws.device != device:
             self._ws = torch.empty(need, dtype=torch.uint8, device=device)
         return self._ws
@@ -67,12 +71,24 @@ class Int8Linear(torch.nn.Module):
             raise TypeError("Int8Linear takes bf16 activations")
         lead = x.shape[:-1]
         x2 = x.reshape(-1, self.in_features).contiguous()
-        ws = self._workspace(x2.shape[0], x2.device)
+        M = x2.shape[0]
+        decode = self.mode == "postscale" and 0 < M <= GEMV_MAX_TOKENS
         if self.norm is not None:
             kind = RMS_NORM if self.norm == "rms" else LAYER_NORM
-            ximg, sx, _, _ = norm_quant(x2, self.norm_weight, self.norm_bias, self.eps, kind)
-            y = gemm_postscale_images(ximg, sx, self.weight_image, self.weight_scale, self.bias, workspace=ws)
+            if decode:
+                _, sx, xq, _ = norm_quant(x2, self.norm_weight, self.norm_bias, self.eps, kind, image=False,
+                                          codes=True)
+                y = gemm_postscale(xq, sx, self.weight_q, self.weight_scale, self.bias)
+            else:
+                ximg, sx, _, _ = norm_quant(x2, self.norm_weight, self.norm_bias, self.eps, kind)
+                y = gemm_postscale_images(ximg, sx, self.weight_image, self.weight_scale, self.bias,
+                                          workspace=self._workspace(M, x2.device))
+        elif decode:
+            ws = self._workspace(M, x2.device, codes=True) if linear_codes_workspace_size(
+                M, self.out_features, self.in_features) else None
+            y, _, _ = linear_postscale_codes(x2, self.weight_q, self.weight_scale, self.bias, workspace=ws)
         else:
+            ws = self._workspace(M, x2.device)
             fn = linear_postscale if self.mode == "postscale" else linear_blockwise
             y, _, _ = fn(x2, self.weight_image, self.weight_scale, self.bias, workspace=ws)
         return y.reshape(*lead, self.out_features)
