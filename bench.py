@@ -259,10 +259,22 @@ def run_w8a8(args):
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(w.linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    linear = w.linear_blockwise if blockwise else w.linear_postscale
+    # a handful of tokens (what Int8Linear runs for decoding): the fused Linear
+    # on the int8 weight codes, a CUDA-core GEMV bound by the weight stream
+    decode = not blockwise and w.gemv_takes(M, K)
+    if decode:
+        wsc = torch.empty(max(w.linear_codes_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
+
+        def call(Xin):
+            w.linear_postscale_codes(Xin, Wq, sw, b, out=Y, workspace=wsc, sx_out=sx)
+    else:
+        linear = w.linear_blockwise if blockwise else w.linear_postscale
+
+        def call(Xin):
+            linear(Xin, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
 
     def step():
-        linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
+        call(X)
 
     if args.profile_once:
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -277,7 +289,9 @@ def run_w8a8(args):
         return
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
-    launches_per_step = 2  # activation quant (writes the bf16 image of the codes), tensor-core GEMM
+    # activation quant (writes the bf16 image of the codes), tensor-core GEMM;
+    # decoding: one kernel for one or two tokens, else quant + GEMV
+    launches_per_step = 1 if decode and M <= 2 else 2
 
     # clock sampler runs through warm-up and the timed region
     gpu_uuid = None
@@ -381,7 +395,7 @@ def run_w8a8(args):
 
         def e2e_step():
             Xd.copy_(Xh, non_blocking=True)
-            linear(Xd, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
+            call(Xd)
             Yh.copy_(Y, non_blocking=True)
 
         for _ in range(3):
@@ -405,6 +419,26 @@ def run_w8a8(args):
 
     gemm_tflops = ops / (ms_gemm * 1e-3) / 1e12
     peak_bf16 = peaks["bf16_tflops"]
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f16, exact int8 products)",
+                "achieved": round(gemm_tflops, 2), "peak": peak_bf16, "unit": "TFLOP/s",
+                "frac": round(gemm_tflops / peak_bf16, 4), "traffic": recorded_traffic(work.name),
+                "traffic_source": "profiles/gemm_traffic_square_postscale_4096.txt (ncu dram bytes per "
+                                  "launch; null if the GEMM sources changed since the capture)",
+                "peak_source": f"bf16 dense burst, {peaks['source']}",
+                "algorithmic": f"2*M*N*K = {ops:.4g} ops per launch; operand images + Y = "
+                               f"{(2 * M * K + 2 * N * K + 2 * M * N) / 1e6:.1f} MB",
+                "gemm_ms": round(ms_gemm, 5)}
+    if decode:
+        # weight codes + X + Y + scales and bias, each once
+        gbytes = N * K + 2 * M * K + 2 * M * N + 4 * N + 4 * M + (2 * N if b is not None else 0)
+        gbs = gbytes / (ms_gemm * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "gemv_s8_kernel (dp4a on the CUDA cores)"
+                    + (", per-token quant folded in" if M <= 2 else ""),
+                    "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                    "peak_source": f"HBM copy bandwidth, {peaks['source']}",
+                    "algorithmic": f"{gbytes / 1e6:.2f} MB per launch (int8 weight codes, X, Y, scales, bias)",
+                    "gemm_ms": round(ms_gemm, 5)}
     line = {
         "metric": "W8A8 Linear TOPS (quant+GEMM) and % of GB300 dense INT8 peak; quant GB/s",
         "value": round(value, 2),
@@ -422,18 +456,11 @@ def run_w8a8(args):
         "config": {"workload": work.name, "M": M, "N": N, "K": K, "bias": b is not None,
                    "step": ("1x128 act quant + blockwise INT8 GEMM (bf16 out)" if blockwise else
                             "per-token act quant + post-scale INT8 GEMM (bf16 out)"),
-                   "api": "w8a8_linear_blockwise" if blockwise else "w8a8_linear_postscale",
+                   "api": ("w8a8_linear_blockwise" if blockwise else
+                           "w8a8_linear_postscale_codes" if decode else "w8a8_linear_postscale"),
                    "l2": "flushed between timed steps (256 MB write outside the step events)"},
         "impl": "w8a8",
-        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f16, exact int8 products)",
-                     "achieved": round(gemm_tflops, 2), "peak": peak_bf16, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / peak_bf16, 4), "traffic": recorded_traffic(work.name),
-                     "traffic_source": "profiles/gemm_traffic_square_postscale_4096.txt (ncu dram bytes per "
-                                       "launch; null if the GEMM sources changed since the capture)",
-                     "peak_source": f"bf16 dense burst, {peaks['source']}",
-                     "algorithmic": f"2*M*N*K = {ops:.4g} ops per launch; operand images + Y = "
-                                    f"{(2 * M * K + 2 * N * K + 2 * M * N) / 1e6:.1f} MB",
-                     "gemm_ms": round(ms_gemm, 5)},
+        "roofline": roofline,
         "int8_peak": {"measured_imma_tops": round(imma_tops, 1),
                       "frac_of_imma_peak": round(gemm_tflops / imma_tops, 3) if imma_tops else None,
                       "note": "mma.sync m16n8k32 s8 throughput measured on this GPU; tcgen05 kind::i8 does not "
@@ -534,8 +561,14 @@ def report_configs(args):
         ws = torch.empty(max(w.linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
         Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
         linear = w.linear_blockwise if blockwise else w.linear_postscale
+        decode = not blockwise and w.gemv_takes(M, K)  # a handful of tokens: the GEMV on the weight codes
+        if decode:
+            wsc = torch.empty(max(w.linear_codes_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
+            run = lambda: w.linear_postscale_codes(X, Wq, sw, b, out=Y, workspace=wsc, sx_out=sx)
+        else:
+            run = lambda: linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
         for _ in range(3):
-            linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
+            run()
         ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ga.record(); gb.record()
         steps, gemms, quants = [], [], []
@@ -544,7 +577,7 @@ def report_configs(args):
             a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             w.set_gemm_timing_events(ga, gb)
             a.record()
-            linear(X, Wimg, sw, b, out=Y, workspace=ws, sx_out=sx)
+            run()
             c.record()
             w.set_gemm_timing_events(None, None)
             torch.cuda.synchronize()
@@ -602,7 +635,8 @@ def report_configs(args):
         gemm_ms = statistics.median(gemms)
         q_ms = statistics.median(quants)
         q_bytes = M * K * 3 + sx.numel() * 4
-        r = dict(workload=work.name, M=M, N=N, K=K, mode=work.mode, step_ms=round(step_ms, 4),
+        r = dict(workload=work.name, M=M, N=N, K=K, mode=work.mode, path="gemv" if decode else "tcgen05",
+                 step_ms=round(step_ms, 4),
                  tops=round(ops / step_ms / 1e9, 1), gemm_tflops=round(ops / gemm_ms / 1e9, 1),
                  gemm_frac_bf16_peak=round(ops / gemm_ms / 1e9 / peaks["bf16_tflops"], 3),
                  x_int8_mma_peak=round(ops / gemm_ms / 1e9 / imma, 2), quant_gbs=round(q_bytes / q_ms / 1e6, 0),
