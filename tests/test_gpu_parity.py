@@ -356,7 +356,9 @@ def test_linear_postscale_codes(w8a8, oracle, M, N, K, bias):
     ref = oracle.linear_postscale(bits(X), bits(W), None if b is None else bits(b))
     Wq, sw = w8a8.quantize_weight(W.to(DEV))
     bd = None if b is None else b.to(DEV)
-    Y, sx, Xq = w8a8.linear_postscale_codes(X.to(DEV), Wq, sw, bd, codes=True)
+    # scales buffer filled with NaN: no CTA may read a scale another CTA writes
+    sx0 = torch.full((M,), float("nan"), device=DEV)
+    Y, sx, Xq = w8a8.linear_postscale_codes(X.to(DEV), Wq, sw, bd, codes=True, sx_out=sx0)
     assert np.array_equal(Xq.cpu().numpy(), ref["Xq"])
     assert np.array_equal(sx.cpu().numpy().view(np.uint32), ref["sx"].view(np.uint32))
     d = assert_bf16_close(bits(Y), ref["Y"], 1)
@@ -443,6 +445,43 @@ def test_int8linear_module_decode(w8a8, oracle, M):
     ref = oracle.linear_postscale(bits(x.reshape(M, 1040)), bits(lin.weight), bits(lin.bias))
     d = assert_bf16_close(bits(y.reshape(M, 300)), ref["Y"], 1)
     assert d.max() == 0
+
+
+# ----------------------------------------------------------------- host-to-host pipeline
+def test_host_pipeline_matches_direct_calls(w8a8):
+    """HostPipeline overlaps each batch's copies with its neighbours' Linears;
+    every result equals a direct call on the same batch, at every depth."""
+    M, N, K = 300, 520, 1040
+    W = rand_bf16((N, K), seed=90, scale=0.02).to(DEV)
+    Wq, sw = w8a8.quantize_weight(W)
+    Wimg = w8a8.pack_weight(Wq)
+    b = rand_bf16((N,), seed=91, scale=0.01).to(DEV)
+    xs = [rand_bf16((M, K), seed=100 + i, outliers=0.01, oscale=20.0).pin_memory() for i in range(7)]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(7)]
+    ws = torch.empty(w8a8.linear_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    refs = [w8a8.linear_postscale(x.to(DEV), Wimg, sw, b)[0].cpu() for x in xs]
+    for depth in (1, 2, 3):
+        for y in ys:
+            y.fill_(float("nan"))
+        pipe = w8a8.HostPipeline(lambda X, Y: w8a8.linear_postscale(X, Wimg, sw, b, out=Y, workspace=ws),
+                                 (M, K), (M, N), DEV, depth=depth)
+        pipe.run(xs, ys)
+        torch.cuda.synchronize()
+        for y, r in zip(ys, refs):
+            assert torch.equal(y, r)
+    # one token per batch on the weight codes, the batch index picking a weight copy
+    Wq2 = [Wq, Wq.flip(0).contiguous()]
+    sw2 = [sw, sw.flip(0).contiguous()]
+    xs1 = [x[:1].contiguous().pin_memory() for x in xs]
+    ys1 = [torch.empty((1, N), dtype=torch.bfloat16).pin_memory() for _ in xs1]
+    pipe = w8a8.HostPipeline(lambda X, Y, i: w8a8.linear_postscale_codes(X, Wq2[i % 2], sw2[i % 2], None, out=Y),
+                             (1, K), (1, N), DEV, depth=2, pass_index=True)
+    pipe.run(xs1, ys1)
+    torch.cuda.synchronize()
+    for i, (x, y) in enumerate(zip(xs1, ys1)):
+        ref, _, _ = w8a8.linear_postscale_codes(x.to(DEV), Wq2[i % 2], sw2[i % 2], None)
+        assert torch.equal(y, ref.cpu())
+    assert w8a8.get_device_error() == (0, 0)
 
 
 # ----------------------------------------------------------------- FFN up: GELU + 1x128 quantization epilogue

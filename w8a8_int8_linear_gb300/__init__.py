@@ -495,4 +495,5 @@ def measure_imma_peak():
     return v.value
 
 
-from .module import Int8FFN, Int8Linear  # noqa: E402  (the modules use the functions above)
+from .module import Int8FFN, Int8Linear
+from .pipeline import HostPipeline  # noqa: E402  (the modules use the functions above)

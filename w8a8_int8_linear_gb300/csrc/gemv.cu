@@ -77,9 +77,11 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Per-token quantization of the M rows of X into the CTA's shared memory:
 // s = absmax / 127 and the codes of quant_chunk, as the activation quantizer
-// computes them.  CTA 0 also stores the scales and, if asked, the codes.
+// computes them.  Every CTA keeps its own scales in shared memory (sxs) for
+// its epilogue; CTA 0 also stores them and, if asked, the codes to global
+// memory, which no other CTA reads.
 template <int MT>
-__device__ __forceinline__ void stage_quantized(const GemvParams& p, int4* xs4, float (*red)[MT]) {
+__device__ __forceinline__ void stage_quantized(const GemvParams& p, int4* xs4, float (*red)[MT], float* sxs) {
     const uint4* X = static_cast<const uint4*>(p.x);  // 8 bf16 per 16-byte chunk
     const int k8 = p.K >> 3;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -106,7 +108,10 @@ __device__ __forceinline__ void stage_quantized(const GemvParams& p, int4* xs4, 
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) a = fmaxf(a, red[w][m]);
             const RowScale sc = make_scale_div(a);
-            if (first && threadIdx.x == 0) p.sx[m] = sc.s;
+            if (threadIdx.x == 0) {
+                sxs[m] = sc.s;
+                if (first) p.sx[m] = sc.s;
+            }
             for (int c = threadIdx.x; c < k8; c += kThreads) {
                 const int64_t i = static_cast<int64_t>(m) * k8 + c;
                 const uint2 q = quant_chunk(__ldg(X + i), sc);
@@ -124,6 +129,7 @@ template <int MT, int R, int U, int MINB, int EPI, bool QUANT>
 __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_constant__ GemvParams p) {
     extern __shared__ int4 xs4[];  // the M x K activation codes, row-major
     __shared__ float red[kWarps][MT];
+    __shared__ float sxs[MT];      // this CTA's activation scales (quantizing kernel)
     grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int M = p.M, N = p.N, K = p.K;
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_co
     grid_dependency_wait();
     if (!p.settled && busy) load(g, 0, cur);
     if constexpr (QUANT) {
-        stage_quantized<MT>(p, xs4, red);
+        stage_quantized<MT>(p, xs4, red, sxs);
     } else {
         const int4* src = static_cast<const int4*>(p.x);
         for (int i = threadIdx.x; i < M * kq; i += kThreads) xs4[i] = __ldg(src + i);
@@ -212,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_co
                         if constexpr (EPI == kEpiPostscaleS32) {
                             static_cast<int32_t*>(p.out)[o] = v;
                         } else {
-                            float y = __fmul_rn(__fmul_rn(__int2float_rn(v), p.sx[m]), __ldg(p.sw + row));
+                            const float sxm = QUANT ? sxs[m] : p.sx[m];
+                            float y = __fmul_rn(__fmul_rn(__int2float_rn(v), sxm), __ldg(p.sw + row));
                             if (p.bias) y = __fadd_rn(y, __bfloat162float(p.bias[row]));
                             static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(y);
                         }
