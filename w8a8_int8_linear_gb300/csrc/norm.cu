@@ -88,10 +88,10 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     }
 }
 
-// The normalized bf16 values of one chunk, packed.  d = x - mu and d * r run
-// two values at a time on the packed fp32 pipe (a subtraction feeding a
-// multiplication, which is never contracted); a product that an addition
-// consumes (gamma before beta) stays scalar with explicit rounding.
+// The normalized bf16 values of one chunk, packed.  d = x - mu, d * r and
+// (d * r) * gamma run two values at a time on the packed fp32 pipe (a
+// subtraction feeding a multiplication and products feeding products, which
+// are never contracted); the beta addition is scalar with explicit rounding.
 __device__ __forceinline__ uint4 normalize_chunk(const uint4& v, const uint4* __restrict__ gamma,
                                                  const uint4* __restrict__ beta, int layer, int c, float mu,
                                                  float r) {
@@ -114,20 +114,12 @@ __device__ __forceinline__ uint4 normalize_chunk(const uint4& v, const uint4* __
         uint64_t d = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
         if (layer) d = f2_sub(d, mu2);
         float y0, y1;
+        uint64_t t = f2_mul(d, r2);
+        if (gamma) t = f2_mul(t, f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i])));
+        f2_unpack(t, y0, y1);
         if (add_beta) {
-            f2_unpack(d, y0, y1);
-            y0 = __fmul_rn(y0, r);
-            y1 = __fmul_rn(y1, r);
-            if (gamma) {
-                y0 = __fmul_rn(y0, bf16_lo(gw[i]));
-                y1 = __fmul_rn(y1, bf16_hi(gw[i]));
-            }
             y0 = __fadd_rn(y0, bf16_lo(bw[i]));
             y1 = __fadd_rn(y1, bf16_hi(bw[i]));
-        } else {
-            uint64_t t = f2_mul(d, r2);
-            if (gamma) t = f2_mul(t, f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i])));
-            f2_unpack(t, y0, y1);
         }
         __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
         o[i] = *reinterpret_cast<uint32_t*>(&h);
@@ -172,6 +164,10 @@ __global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __r
         }
         mu = __fdiv_rn(tree_sum_block(tree_sum_local(s), tree, red[0]), Kf);
     }
+    // d = x - mu and d * d two values at a time on the packed fp32 pipe (a
+    // subtraction feeding a multiplication, a product feeding nothing packed);
+    // the sum stays a scalar chain with explicit rounding.
+    const uint64_t mu2 = f2_pack(mu, mu);
     float s[C];
 #pragma unroll
     for (int i = 0; i < C; ++i) {
@@ -179,12 +175,10 @@ __global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __r
         float a = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float d0 = bf16_lo(w[j]), d1 = bf16_hi(w[j]);
-            if (layer) {
-                d0 = __fsub_rn(d0, mu);
-                d1 = __fsub_rn(d1, mu);
-            }
-            const float t0 = __fmul_rn(d0, d0), t1 = __fmul_rn(d1, d1);
+            uint64_t d = f2_pack(bf16_lo(w[j]), bf16_hi(w[j]));
+            if (layer) d = f2_sub(d, mu2);
+            float t0, t1;
+            f2_unpack(f2_mul(d, d), t0, t1);
             a = (j == 0) ? t0 : __fadd_rn(a, t0);
             a = __fadd_rn(a, t1);
         }
