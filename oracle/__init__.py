@@ -51,12 +51,14 @@ def lib():
         L.orc_bf16_from_f32.restype = None
         L.orc_f32_from_bf16.argtypes = [P, I64, P]
         L.orc_f32_from_bf16.restype = None
-        L.orc_gelu_f32.argtypes = [P, I64, P]
-        L.orc_gelu_f32.restype = None
+        L.orc_gelu_f64.argtypes = [P, I64, P]
+        L.orc_gelu_f64.restype = None
         L.orc_gelu_bf16.argtypes = [P, I64, P]
         L.orc_gelu_bf16.restype = None
         L.orc_norm_quant.argtypes = [P, P, P, ctypes.c_float, ctypes.c_int, I64, I64, P, P, P]
         L.orc_norm_quant.restype = ctypes.c_int
+        L.orc_norm_quant_fixed_order.argtypes = [P, P, P, ctypes.c_float, ctypes.c_int, I64, I64, P, P, P]
+        L.orc_norm_quant_fixed_order.restype = ctypes.c_int
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_num_threads.argtypes = [ctypes.c_int]
         L.orc_set_num_threads.restype = None
@@ -186,17 +188,18 @@ def linear_blockwise(X, W, bias=None):
     return dict(Xq=Xq, sx=sx, Wq=Wq, sw=sw, acc=acc, Y=Y)
 
 
-def gelu_f32(x):
-    """GELU (erf form, erf by Abramowitz & Stegun 7.1.28) of fp32 values, in
-    the fixed binary32 operation order stated in w8a8_oracle.c."""
-    x = _c(x, np.float32)
+def gelu_f64(x):
+    """GELU in its erf form, x * Phi(x), of fp64 values, evaluated in fp64 with
+    the C library's erfc (Phi(x) = erfc(-x / sqrt 2) / 2)."""
+    x = _c(x, np.float64)
     g = np.empty_like(x)
-    lib().orc_gelu_f32(_p(x), x.size, _p(g))
+    lib().orc_gelu_f64(_p(x), x.size, _p(g))
     return g
 
 
 def gelu_bf16(Y):
-    """bf16(gelu(Y)) for bf16 Y given as uint16 bit patterns."""
+    """bf16(fp32(gelu(Y))) for bf16 Y given as uint16 bit patterns: the fp64
+    value of the plain definition rounded to fp32, then to bf16."""
     Y = _c(Y, np.uint16)
     G = np.empty_like(Y)
     lib().orc_gelu_bf16(_p(Y), Y.size, _p(G))
@@ -221,12 +224,7 @@ RMS_NORM = 0
 LAYER_NORM = 1
 
 
-def norm_quant(X, gamma=None, beta=None, eps=1e-6, kind=RMS_NORM):
-    """RMSNorm (kind 0) or LayerNorm (kind 1) of bf16 X [M,K] (uint16 bits),
-    statistics summed in the fixed chunk-and-tree order stated in
-    w8a8_oracle.c, then per-token quantization of the bf16 result.
-
-    Returns (Y bf16 bits [M,K], Xq int8 [M,K], sx fp32 [M])."""
+def _norm_quant(fn, X, gamma, beta, eps, kind):
     X = _c(X, np.uint16)
     M, K = X.shape
     g = None if gamma is None else _c(gamma, np.uint16)
@@ -234,9 +232,28 @@ def norm_quant(X, gamma=None, beta=None, eps=1e-6, kind=RMS_NORM):
     Y = np.empty((M, K), np.uint16)
     Xq = np.empty((M, K), np.int8)
     sx = np.empty(M, np.float32)
-    if lib().orc_norm_quant(_p(X), _p(g), _p(b), float(eps), int(kind), M, K, _p(Y), _p(Xq), _p(sx)) != 0:
-        raise ValueError("norm_quant: K must be a positive multiple of 8, at most 65536")
+    if fn(_p(X), _p(g), _p(b), float(eps), int(kind), M, K, _p(Y), _p(Xq), _p(sx)) != 0:
+        raise ValueError("norm_quant: bad shape")
     return Y, Xq, sx
+
+
+def norm_quant(X, gamma=None, beta=None, eps=1e-6, kind=RMS_NORM):
+    """RMSNorm (kind 0) or LayerNorm (kind 1) of bf16 X [M,K] (uint16 bits) by
+    the plain definition: fp64 statistics (left-to-right sums) and fp64
+    normalization, rounded to fp32 and then bf16; then per-token
+    quantization of the bf16 result.
+
+    Returns (Y bf16 bits [M,K], Xq int8 [M,K], sx fp32 [M])."""
+    return _norm_quant(lib().orc_norm_quant, X, gamma, beta, eps, kind)
+
+
+def norm_quant_fixed_order(X, gamma=None, beta=None, eps=1e-6, kind=RMS_NORM):
+    """The same normalization stated in binary32 with one fixed summation
+    order (chunks of 8, then a pairwise tree; see w8a8_oracle.c), then the
+    per-token quantization.  K % 8 == 0, K <= 65536.
+
+    Returns (Y bf16 bits [M,K], Xq int8 [M,K], sx fp32 [M])."""
+    return _norm_quant(lib().orc_norm_quant_fixed_order, X, gamma, beta, eps, kind)
 
 
 def linear_sampled(X, W, bias, rows, cols, mode=PER_ROW):

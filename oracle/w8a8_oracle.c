@@ -253,52 +253,29 @@ void orc_epilogue_blockwise(const float* acc, const uint16_t* bias, int64_t M, i
  * The pages tune the post-scale kernel for "LTX FFN shapes" ("TurboDiffusion
  * Integration Notes", section "Differences From TurboDiffusion") and name no
  * activation.  Reading taken: the FFN's activation is GELU in its erf form,
- * gelu(x) = x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2, applied to the
- * bf16 output of the up-projection, rounded back to bf16, and that tensor is
- * what the down-projection quantizes in 1x128 blocks.
+ *   gelu(x) = x * Phi(x),  Phi(x) = (1 + erf(x / sqrt 2)) / 2,
+ * applied to the bf16 output of the up-projection; the value is rounded to
+ * binary32 and then to bf16 (round to nearest even both times), and that
+ * tensor is what the down-projection quantizes in 1x128 blocks.
  *
- * erf comes from Abramowitz & Stegun, Handbook of Mathematical Functions,
- * formula 7.1.28: for z >= 0, erf(z) = 1 - p(z)^-16 with
- * p(z) = 1 + a1 z + a2 z^2 + ... + a6 z^6 and |error| <= 3e-7.  So for
- * z = |x| / sqrt 2, Phi(-|x|) = p(z)^-16 / 2 and Phi(|x|) = 1 - p(z)^-16 / 2.
- * Evaluated in binary32 in exactly this order, so that any implementation
- * following it gets the same bits; fma(a, b, c) is the IEEE fused
- * multiply-add (a * b + c rounded once), every other operation is rounded on
- * its own:
- *   z = |x| * 0.70710677;  t = a6; then for a5, a4, a3, a2, a1: t = fma(t, z, a_i);
- *   t = fma(t, z, 1);  t2 = t*t; t4 = t2*t2; t8 = t4*t4; t16 = t8*t8;
- *   e = 1 / t16;  h = 0.5 * e;  phi = (x >= 0) ? 1 - h : h;  g = x * phi.
+ * This is the plain definition, evaluated in binary64 with the C library:
+ * Phi(x) is written as erfc(-x / sqrt 2) / 2, the same function as
+ * (1 + erf(x / sqrt 2)) / 2 without the cancellation of 1 + erf for
+ * negative x (below x = -8 the erf form is 0 in binary64 while Phi is still
+ * above 1e-16).
  * ------------------------------------------------------------------------ */
-static float orc_gelu(float x) {
-    const float a1 = 0.0705230784f, a2 = 0.0422820123f, a3 = 0.0092705272f;
-    const float a4 = 0.0001520143f, a5 = 0.0002765672f, a6 = 0.0000430638f;
-    const float z = fabsf(x) * 0.70710678118654752f;
-    float t = a6;
-    t = fmaf(t, z, a5);
-    t = fmaf(t, z, a4);
-    t = fmaf(t, z, a3);
-    t = fmaf(t, z, a2);
-    t = fmaf(t, z, a1);
-    t = fmaf(t, z, 1.0f);
-    float t2 = t * t;
-    float t4 = t2 * t2;
-    float t8 = t4 * t4;
-    float t16 = t8 * t8;
-    float e = 1.0f / t16;
-    float h = 0.5f * e;
-    float phi = (x >= 0.0f) ? 1.0f - h : h;
-    return x * phi;
+static double orc_gelu_f64_one(double x) { return 0.5 * x * erfc(-x * 0.70710678118654752440); }
+
+/* g[i] = gelu(x[i]) in binary64 (for the pins of the definition). */
+void orc_gelu_f64(const double* x, int64_t n, double* g) {
+    for (int64_t i = 0; i < n; ++i) g[i] = orc_gelu_f64_one(x[i]);
 }
 
-/* g[i] = gelu(x[i]) in binary32 (for the accuracy checks of the formula). */
-void orc_gelu_f32(const float* x, int64_t n, float* g) {
-    for (int64_t i = 0; i < n; ++i) g[i] = orc_gelu(x[i]);
-}
-
-/* G = bf16(gelu(Y)) for bf16 Y (bit patterns in, bit patterns out). */
+/* G = bf16(fp32(gelu(Y))) for bf16 Y (bit patterns in, bit patterns out). */
 void orc_gelu_bf16(const uint16_t* y, int64_t n, uint16_t* g) {
 #pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < n; ++i) g[i] = orc_f32_to_bf16(orc_gelu(orc_bf16_to_f32(y[i])));
+    for (int64_t i = 0; i < n; ++i)
+        g[i] = orc_f32_to_bf16((float)orc_gelu_f64_one((double)orc_bf16_to_f32(y[i])));
 }
 
 /* ------------------------------------------------------------------------
@@ -310,22 +287,64 @@ void orc_gelu_bf16(const uint16_t* y, int64_t n, uint16_t* g) {
  * acceleration overview's LayerNorm sketch (section "Custom Kernel
  * Optimizations") computes the statistics, normalizes, then applies the
  * affine transform.  Readings taken (the pages give no formula):
+ *   RMSNorm:   y = (x / sqrt(mean(x^2) + eps)) * gamma
+ *   LayerNorm: y = ((x - mu) / sqrt(var + eps)) * gamma + beta,
+ *              mu = mean(x), var = mean((x - mu)^2)  (biased, about the mean)
+ * (gamma and beta optional: a missing one is 1, resp. 0), then y is quantized
+ * per token like any activation.
+ *
+ * orc_norm_quant is the plain definition: the statistics are sums over the
+ * row in binary64 taken left to right, and every operation up to y is a
+ * binary64 operation; y is then rounded to binary32 and to bf16.
+ *
+ * orc_norm_quant_fixed_order is a second, binary32 statement of the same
+ * formulas with one fixed summation order, kept as a bit-exact description
+ * of a particular evaluation (independent of any thread layout):
  *   RMSNorm:   r = 1 / sqrt(S(x*x) / K + eps),      y = bf16((x * r) * gamma)
  *   LayerNorm: mu = S(x) / K, d = x - mu,
  *              r = 1 / sqrt(S(d*d) / K + eps),      y = bf16(((d * r) * gamma) + beta)
- * (gamma and beta optional: a missing one skips its operation), then y is
- * quantized per token like any activation.  The statistics come from one read
- * of the row; the variance is taken about the mean (not E[x^2] - mu^2).
- * sqrt and the divisions are IEEE binary32 operations.
- *
- * S() is a sum with a fixed order, stated here so that it does not depend on
- * how an implementation spreads a row over threads: the row is cut into
- * chunks of 8 consecutive elements; each chunk's terms are added left to
- * right (t0 + t1, then + t2, ...); the chunk sums, zero-padded to P = the
- * next power of two of K/8 entries, are added pairwise level by level
- * (entry i of the next level = entry 2i + entry 2i+1) down to one value.
- * Every term (x*x, d = x - mu, d*d) is rounded to binary32 on its own.
+ * with every operation rounded to binary32 on its own, sqrt and the
+ * divisions IEEE, and S() the row cut into chunks of 8 consecutive elements,
+ * each chunk summed left to right, the chunk sums zero-padded to P = the next
+ * power of two of K/8 entries and added pairwise level by level (entry i of
+ * the next level = entry 2i + entry 2i+1) down to one value.
  * ------------------------------------------------------------------------ */
+
+/* kind 0: RMSNorm, 1: LayerNorm.  X, gamma, beta, Y are bf16 bit patterns;
+ * gamma / beta may be NULL.  Writes Y[M,K] (the normalized bf16 output), then
+ * its per-token quantization Xq[M,K] and sx[M].  Returns 0, or -1 for a bad
+ * shape (K <= 0). */
+int orc_norm_quant(const uint16_t* X, const uint16_t* gamma, const uint16_t* beta, float eps, int kind,
+                   int64_t M, int64_t K, uint16_t* Y, int8_t* Xq, float* sx) {
+    if (K <= 0) return -1;
+    const double Kd = (double)K;
+    const double epsd = (double)eps;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* x = X + m * K;
+        uint16_t* y = Y + m * K;
+        double mu = 0.0;
+        if (kind == 1) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += (double)orc_bf16_to_f32(x[k]);
+            mu = s / Kd;
+        }
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double d = (double)orc_bf16_to_f32(x[k]) - mu;
+            ss += d * d;
+        }
+        const double rs = sqrt(ss / Kd + epsd);
+        for (int64_t k = 0; k < K; ++k) {
+            double v = ((double)orc_bf16_to_f32(x[k]) - mu) / rs;
+            if (gamma) v = v * (double)orc_bf16_to_f32(gamma[k]);
+            if (kind == 1 && beta) v = v + (double)orc_bf16_to_f32(beta[k]);
+            y[k] = orc_f32_to_bf16((float)v);
+        }
+    }
+    return orc_quantize_act(Y, M, K, 0, Xq, sx);
+}
+
 static float orc_tree_sum(float* part, int64_t P) {
     for (int64_t w = P; w > 1; w >>= 1)
         for (int64_t i = 0; i < w / 2; ++i) part[i] = part[2 * i] + part[2 * i + 1];
@@ -338,12 +357,10 @@ static int64_t orc_pow2_at_least(int64_t n) {
     return p;
 }
 
-/* kind 0: RMSNorm, 1: LayerNorm.  X, gamma, beta, Y are bf16 bit patterns;
- * gamma / beta may be NULL.  Writes Y[M,K] (the normalized bf16 output), then
- * its per-token quantization Xq[M,K] and sx[M].  Returns 0, or -1 for a bad
- * shape (K % 8 != 0 or K > 65536). */
-int orc_norm_quant(const uint16_t* X, const uint16_t* gamma, const uint16_t* beta, float eps, int kind,
-                   int64_t M, int64_t K, uint16_t* Y, int8_t* Xq, float* sx) {
+/* The fixed-order binary32 statement above.  Same arguments; returns -1 for
+ * a bad shape (K % 8 != 0 or K > 65536). */
+int orc_norm_quant_fixed_order(const uint16_t* X, const uint16_t* gamma, const uint16_t* beta, float eps, int kind,
+                               int64_t M, int64_t K, uint16_t* Y, int8_t* Xq, float* sx) {
     if (K <= 0 || K % 8 != 0 || K > 65536) return -1;
     const int64_t C = K / 8;
     const int64_t P = orc_pow2_at_least(C);

@@ -370,59 +370,100 @@ def _bf16_all(lo, hi):
     return vals[keep], bits[keep]
 
 
-def test_gelu_within_erf_bound(oracle):
-    """Against x * (1 + erf(x / sqrt 2)) / 2 in fp64 (math.erf): Abramowitz &
-    Stegun 7.1.28 is within 3e-7 of erf, i.e. 1.5e-7 of Phi; the binary32
-    evaluation adds at most about 16 * 2^-24 relative in t^16, so
-    |g - gelu(x)| <= 1e-6 |x| + 2^-24 |g|.  A wrong coefficient, sign or
-    branch is off by far more."""
-    import math
-    rng = np.random.default_rng(5)
-    x = np.concatenate([np.linspace(-12, 12, 48001), rng.normal(0, 3, 20000),
-                        _bf16_all(-12, 12)[0]]).astype(np.float32)
-    g = oracle.gelu_f32(x).astype(np.float64)
+def _bf16_of_f64(v):
+    """fp64 -> fp32 -> bf16 bits (round to nearest even both times), by torch."""
+    t = torch.from_numpy(np.asarray(v, np.float64).astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_gelu_matches_scipy_ndtr_on_every_bf16(oracle):
+    """Against x * ndtr(x), ndtr being scipy's standard normal CDF (the Cephes
+    routine, another implementation of Phi), rounded the same way: identical
+    bits on every finite bf16 input."""
+    sp = pytest.importorskip("scipy.special")
+    x, h = _bf16_all(-np.inf, np.inf)
+    G = oracle.gelu_bf16(h)
     xd = x.astype(np.float64)
-    exact = np.array([v * 0.5 * (1.0 + math.erf(v / math.sqrt(2.0))) for v in xd])
-    bound = 1e-6 * np.abs(xd) + 2.0 ** -24 * np.abs(exact)
-    assert np.all(np.abs(g - exact) <= bound)
-    # the error is not vacuous: it is the formula's, not zero
-    assert np.abs(g - exact).max() > 1e-9
+    want = _bf16_of_f64(xd * sp.ndtr(xd))
+    assert np.array_equal(G, want)
+
+
+def test_gelu_correctly_rounded_against_mpmath(oracle):
+    """Against x * Phi(x) in 40-digit arithmetic (mpmath.ncdf): the binary64
+    evaluation rounds to the same bf16 on a sample of 4000 bf16 inputs
+    spanning [-14, 14], where the result is neither x nor 0."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    x, h = _bf16_all(-14.0, 14.0)
+    sel = np.linspace(0, x.size - 1, 4000).astype(np.int64)
+    x, h = x[sel], h[sel]
+    exact = np.array([float(mpmath.mpf(float(v)) * mpmath.ncdf(mpmath.mpf(float(v)))) for v in x])
+    assert np.array_equal(oracle.gelu_bf16(h), _bf16_of_f64(exact))
+
+
+def test_gelu_normal_table_values(oracle):
+    """Phi from a printed table of the standard normal distribution
+    (Phi(0.5) = 0.6914624613, Phi(1) = 0.8413447461, Phi(2) = 0.9772498681,
+    Phi(3) = 0.9986501020) and Phi(-x) = 1 - Phi(x)."""
+    table = {0.5: 0.6914624613, 1.0: 0.8413447461, 2.0: 0.9772498681, 3.0: 0.9986501020}
+    x = np.array(list(table) + [-v for v in table], np.float64)
+    phi = np.array(list(table.values()) + [1.0 - v for v in table.values()])
+    g = oracle.gelu_f64(x)
+    assert np.all(np.abs(g - x * phi) <= 1e-10 * np.abs(x))
+
+
+def test_gelu_tail_asymptotic_series(oracle):
+    """For x <= -8, Phi(x) = phi(x) / |x| * (1 - 1/x^2 + 3/x^4 - 15/x^6 +
+    105/x^8 - ...), phi the normal density; the truncated series is within
+    its next term (945/x^10 < 1e-6).  This catches a 1 + erf(x / sqrt 2)
+    evaluation, which loses all accuracy there."""
+    x = -np.linspace(8.0, 37.0, 2901)
+    x2 = x * x
+    series = 1 - 1 / x2 + 3 / x2 ** 2 - 15 / x2 ** 3 + 105 / x2 ** 4
+    phi = np.exp(-x2 / 2) / np.sqrt(2 * np.pi)
+    want = x * phi / np.abs(x) * series
+    g = oracle.gelu_f64(x)
+    assert np.all(np.abs(g - want) <= 2e-6 * np.abs(want))
+
+
+def test_gelu_special_values(oracle):
+    g = oracle.gelu_f64(np.array([0.0, -0.0]))
+    assert g[0] == 0 and not np.signbit(g[0])
+    assert g[1] == 0 and np.signbit(g[1])       # -0 * Phi keeps the sign
+    # Phi(x) + Phi(-x) = 1, so g(x) - g(-x) = x
+    rng = np.random.default_rng(6)
+    v = rng.normal(0, 3, 5000)
+    assert np.all(np.abs(oracle.gelu_f64(v) - oracle.gelu_f64(-v) - v) <= 1e-15 * (1 + np.abs(v)))
+    # the minimum of gelu sits where g'(x) = Phi(x) + x phi(x) = 0, found here
+    # with scipy's ndtr and a bracketing root finder
+    sp = pytest.importorskip("scipy.special")
+    from scipy.optimize import brentq
+    xm = brentq(lambda t: sp.ndtr(t) + t * np.exp(-t * t / 2) / np.sqrt(2 * np.pi), -1.0, -0.5, xtol=1e-14)
+    xs = np.linspace(xm - 1e-3, xm + 1e-3, 20001)
+    gs = oracle.gelu_f64(xs)
+    assert abs(xs[np.argmin(gs)] - xm) <= 2e-7 and abs(gs.min() - xm * sp.ndtr(xm)) <= 1e-15
+    # bf16: g = x from x = 4 up (Phi rounds away), -0 far below zero, x / 2 for tiny x
+    x, h = _bf16_all(4.0, np.inf)
+    assert np.array_equal(oracle.gelu_bf16(h), h)
+    x, h = _bf16_all(-np.inf, -14.0)
+    assert np.all(oracle.gelu_bf16(h) == 0x8000)
+    x, h = _bf16_all(2.0 ** -120, 2.0 ** -12)
+    assert np.array_equal(oracle.gelu_bf16(h), _bf16_of_f64(x.astype(np.float64) / 2))
 
 
 def test_gelu_matches_torch_bf16(oracle):
-    """bf16(gelu(x)) against torch.nn.functional.gelu (erf form) for every bf16
-    x with |x| <= 3: identical bits.  On 3 < |x| <= 4 at most 1 ulp apart.
-    (Below -5.5 torch's 1 + erf(x / sqrt 2) cancels to 0 while the formula
-    keeps the tail, so the two differ there by design.)"""
-    for lo, hi, max_ulp in ((-3.0, 3.0, 0), (-4.0, 4.0, 1)):
+    """torch.nn.functional.gelu (erf form, evaluated in fp32) rounded to bf16:
+    identical on every bf16 |x| <= 3, never more than 1 ulp apart on
+    -4 <= x <= 5.  (Further down torch's fp32 1 + erf(x / sqrt 2) has lost
+    most of its relative accuracy: Phi(-4.4) is 5e-6, 85 units of fp32
+    rounding near 1.)"""
+    for lo, hi, max_ulp in ((-3.0, 3.0, 0), (-4.0, 5.0, 1)):
         x, h = _bf16_all(lo, hi)
         G = oracle.gelu_bf16(h)
         T = torch.nn.functional.gelu(torch.from_numpy(x)).to(torch.bfloat16)
         Tb = T.view(torch.int16).numpy().view(np.uint16)
-
-        def ordered(u):
-            u = u.astype(np.int64)
-            return np.where(u & 0x8000, 0x8000 - (u & 0x7FFF), u + 0x8000)
-        d = np.abs(ordered(G) - ordered(Tb))
+        d = np.abs(_ordered(G) - _ordered(Tb))
         assert d.max() <= max_ulp
-
-
-def test_gelu_special_values(oracle):
-    x = np.array([0.0, -0.0, 6.0, 7.5, 100.0, -100.0, -30.0], np.float32)
-    g = oracle.gelu_f32(x)
-    assert g[0] == 0 and not np.signbit(g[0])
-    assert g[1] == 0 and np.signbit(g[1])       # -0 * Phi keeps the sign
-    assert np.array_equal(g[2:5], x[2:5])       # Phi rounds to 1 in binary32
-    assert np.all(g[5:] <= 0) and np.all(g[5:] > -1e-30)
-    # Phi(x) + Phi(-x) = 1: g(x) - g(-x) = x up to the two roundings
-    rng = np.random.default_rng(6)
-    v = rng.normal(0, 2, 5000).astype(np.float32)
-    lhs = oracle.gelu_f32(v).astype(np.float64) - oracle.gelu_f32(-v).astype(np.float64)
-    assert np.all(np.abs(lhs - v) <= 2.0 ** -22 * np.abs(v))
-    # the minimum of gelu is about -0.17 near x = -0.75
-    xs = np.linspace(-3, 0, 30001).astype(np.float32)
-    gs = oracle.gelu_f32(xs)
-    assert abs(float(xs[np.argmin(gs)]) + 0.7518) < 2e-3 and abs(float(gs.min()) + 0.16997) < 1e-4
 
 
 def test_ffn_up_gelu_quant_composition(oracle):
@@ -452,9 +493,13 @@ def _ordered(u):
     return np.where(u & 0x8000, 0x8000 - (u & 0x7FFF), u + 0x8000)
 
 
+NORMS = ("norm_quant", "norm_quant_fixed_order")
+
+
+@pytest.mark.parametrize("fn", NORMS)
 @pytest.mark.parametrize("K", [128, 4096, 5120])
-def test_layer_norm_matches_torch(oracle, K):
-    """Against torch.nn.functional.layer_norm in fp32 (a different summation
+def test_layer_norm_matches_torch(oracle, fn, K):
+    """Against torch.nn.functional.layer_norm in fp32 (another summation
     order), rounded to bf16: within 1 ulp everywhere, identical almost
     everywhere; a missing beta or gamma skips exactly that operation."""
     rng = np.random.default_rng(K)
@@ -464,7 +509,7 @@ def test_layer_norm_matches_torch(oracle, K):
     b = oracle.bf16_from_f32(rng.normal(0.0, 0.2, K).astype(np.float32))
     xt = torch.from_numpy(oracle.f32_from_bf16(X))
     for gg, bb in ((g, b), (g, None), (None, None)):
-        Y, _, _ = oracle.norm_quant(X, gg, bb, 1e-5, oracle.LAYER_NORM)
+        Y, _, _ = getattr(oracle, fn)(X, gg, bb, 1e-5, oracle.LAYER_NORM)
         T = torch.nn.functional.layer_norm(
             xt, (K,), None if gg is None else torch.from_numpy(oracle.f32_from_bf16(gg)),
             None if bb is None else torch.from_numpy(oracle.f32_from_bf16(bb)), 1e-5)
@@ -473,48 +518,96 @@ def test_layer_norm_matches_torch(oracle, K):
         assert d.max() <= 1 and (d > 0).mean() < 2e-3
 
 
+@pytest.mark.parametrize("fn", NORMS)
 @pytest.mark.parametrize("K", [256, 5120])
-def test_rms_norm_vs_fp64(oracle, K):
-    """Against x / sqrt(mean(x^2) + eps) * gamma in fp64 rounded to bf16."""
+def test_rms_norm_matches_torch(oracle, fn, K):
+    """Against torch.nn.functional.rms_norm in fp32, rounded to bf16; the
+    codes are the per-token quantization of the bf16 output."""
     rng = np.random.default_rng(K + 1)
     X = oracle.bf16_from_f32(rng.normal(0.0, 3.0, (16, K)).astype(np.float32))
     g = oracle.bf16_from_f32(rng.normal(1.0, 0.2, K).astype(np.float32))
-    Y, Xq, sx = oracle.norm_quant(X, g, None, 1e-6, oracle.RMS_NORM)
-    x = oracle.f32_from_bf16(X).astype(np.float64)
-    ref = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + np.float64(np.float32(1e-6)))
-    ref = ref * oracle.f32_from_bf16(g).astype(np.float64)
-    d = np.abs(_ordered(Y) - _ordered(oracle.bf16_from_f32(ref.astype(np.float32))))
+    Y, Xq, sx = getattr(oracle, fn)(X, g, None, 1e-6, oracle.RMS_NORM)
+    T = torch.nn.functional.rms_norm(torch.from_numpy(oracle.f32_from_bf16(X)), (K,),
+                                     torch.from_numpy(oracle.f32_from_bf16(g)), 1e-6)
+    Tb = T.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    d = np.abs(_ordered(Y) - _ordered(Tb))
     assert d.max() <= 1 and (d > 0).mean() < 2e-3
-    # the codes are the per-token quantization of the bf16 output
     q2, s2 = oracle.quantize_act(Y, oracle.PER_ROW)
     assert np.array_equal(Xq, q2) and np.array_equal(sx, s2)
 
 
+def _norm_exact(x, g, b, eps, layer, mpmath):
+    """One row by exact rational statistics and a 50-digit square root."""
+    xs = [Fraction(float(v)) for v in x]
+    K = len(xs)
+    mu = sum(xs, Fraction(0)) / K if layer else Fraction(0)
+    var = sum(((v - mu) ** 2 for v in xs), Fraction(0)) / K
+    den = mpmath.sqrt(mpmath.mpf(var.numerator) / var.denominator + mpmath.mpf(float(np.float32(eps))))
+    out = []
+    for i, v in enumerate(xs):
+        y = (mpmath.mpf((v - mu).numerator) / (v - mu).denominator) / den
+        if g is not None:
+            y = y * float(g[i])
+        if layer and b is not None:
+            y = y + float(b[i])
+        out.append(float(y))
+    return np.array(out)
+
+
+def test_norm_plain_against_exact_arithmetic(oracle):
+    """The plain definition against exact rational mean and variance and a
+    50-digit square root, rounded to fp32 and bf16: identical bits, for
+    LayerNorm and RMSNorm, with and without gamma/beta, on random rows and on
+    rows whose fp32 sums would cancel (2^24 + 1 + 1 - 2^24)."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(11)
+    rows = [rng.normal(0.3, 2.0, 24) for _ in range(12)]
+    c = np.zeros(32)
+    c[0], c[8], c[16], c[24] = 2.0 ** 24, 1.0, 1.0, -(2.0 ** 24)
+    rows.append(c)
+    rows.append(np.full(16, 1000.0) + rng.integers(-3, 4, 16) * 8.0)  # large mean, small spread
+    for row in rows:
+        K = len(row)
+        X = oracle.bf16_from_f32(row.astype(np.float32)[None, :])
+        x = oracle.f32_from_bf16(X)[0]
+        g = oracle.bf16_from_f32(rng.normal(1.0, 0.3, K).astype(np.float32))
+        b = oracle.bf16_from_f32(rng.normal(0.0, 0.3, K).astype(np.float32))
+        for layer in (False, True):
+            for gg, bb in ((None, None), (g, b)):
+                Y, _, _ = oracle.norm_quant(X, gg, bb, 1e-5, oracle.LAYER_NORM if layer else oracle.RMS_NORM)
+                want = _norm_exact(x, None if gg is None else oracle.f32_from_bf16(gg),
+                                   None if bb is None else oracle.f32_from_bf16(bb), 1e-5, layer, mpmath)
+                assert np.array_equal(Y[0], _bf16_of_f64(want))
+
+
 def test_norm_closed_forms(oracle):
     K = 1024
-    # constant row c: RMSNorm gives c / sqrt(c^2 + eps) exactly rounded twice
-    c = np.float32(1.5)
-    X = oracle.bf16_from_f32(np.full((1, K), c, np.float32))
-    Y, Xq, sx = oracle.norm_quant(X, None, None, 0.0, oracle.RMS_NORM)
-    assert np.all(oracle.f32_from_bf16(Y) == 1.0)  # 1.5 / sqrt(2.25) == 1 exactly
-    assert np.all(Xq == 127) and sx[0] == np.float32(1.0) / np.float32(127)
-    # LayerNorm of a constant row: d = 0, so y = beta exactly (and +-0 without beta)
-    b = oracle.bf16_from_f32(np.linspace(-1, 1, K).astype(np.float32))
-    Y, Xq, sx = oracle.norm_quant(X, None, b, 1e-5, oracle.LAYER_NORM)
-    assert np.array_equal(Y[0], b)
-    # +-a alternating: mean 0 exactly, variance a^2; with eps = 0 every |y| = 1
-    a = np.float32(0.375)
-    X = oracle.bf16_from_f32(np.tile(np.array([a, -a], np.float32), K // 2)[None, :])
-    Y, Xq, sx = oracle.norm_quant(X, None, None, 0.0, oracle.LAYER_NORM)
-    assert np.array_equal(np.abs(oracle.f32_from_bf16(Y)), np.ones((1, K), np.float32))
-    assert np.array_equal(Xq[0], np.tile(np.array([127, -127], np.int8), K // 2))
+    for fn in NORMS:
+        f = getattr(oracle, fn)
+        # constant row c, eps = 0: RMSNorm gives c / |c| = 1 exactly
+        c = np.float32(1.5)
+        X = oracle.bf16_from_f32(np.full((1, K), c, np.float32))
+        Y, Xq, sx = f(X, None, None, 0.0, oracle.RMS_NORM)
+        assert np.all(oracle.f32_from_bf16(Y) == 1.0)
+        assert np.all(Xq == 127) and sx[0] == np.float32(1.0) / np.float32(127)
+        # LayerNorm of a constant row: x - mu = 0, so y = beta exactly
+        b = oracle.bf16_from_f32(np.linspace(-1, 1, K).astype(np.float32))
+        Y, Xq, sx = f(X, None, b, 1e-5, oracle.LAYER_NORM)
+        assert np.array_equal(Y[0], b)
+        # +-a alternating: mean 0, variance a^2; with eps = 0 every |y| = 1
+        a = np.float32(0.375)
+        X2 = oracle.bf16_from_f32(np.tile(np.array([a, -a], np.float32), K // 2)[None, :])
+        Y, Xq, sx = f(X2, None, None, 0.0, oracle.LAYER_NORM)
+        assert np.array_equal(np.abs(oracle.f32_from_bf16(Y)), np.ones((1, K), np.float32))
+        assert np.array_equal(Xq[0], np.tile(np.array([127, -127], np.int8), K // 2))
 
 
-def test_norm_sum_order(oracle):
-    """The statistics use chunk sums of 8 then a pairwise tree, not a left-to-
-    right scan: a row where the two orders give different binary32 sums takes
-    the tree's value (checked through the LayerNorm mean, which shifts every
-    output)."""
+def test_norm_fixed_order_sum(oracle):
+    """The fixed-order statement sums chunks of 8 and then a pairwise tree,
+    not a left-to-right scan: on a row where the two orders give different
+    binary32 sums it takes the tree's value, while the plain definition takes
+    the exact one."""
     K = 32  # 4 chunks: tree ((s0 + s1) + (s2 + s3))
     x = np.zeros(K, np.float32)
     x[0] = 2.0 ** 24          # chunk 0
@@ -525,10 +618,26 @@ def test_norm_sum_order(oracle):
     scan = np.float32(0)
     for v in x:
         scan = np.float32(scan + v)
-    assert tree != scan       # the two orders really differ here (0 vs -2^24... or 2 vs 0)
+    assert tree != scan
     X = oracle.bf16_from_f32(x[None, :])
     mu_tree = np.float32(tree) / np.float32(K)
-    # y for an element equal to 0: -mu * r; its sign and size follow the tree mean
-    Y, _, _ = oracle.norm_quant(X, None, None, 1.0, oracle.LAYER_NORM)
-    y1 = oracle.f32_from_bf16(Y)[0, 1]
+    Y, _, _ = oracle.norm_quant_fixed_order(X, None, None, 1.0, oracle.LAYER_NORM)
+    y1 = oracle.f32_from_bf16(Y)[0, 1]     # an element equal to 0: -mu * r
     assert np.sign(y1) == -np.sign(mu_tree) or mu_tree == 0
+    # exact mean 2 / 32 > 0: the plain definition gives y < 0 there
+    Yp, _, _ = oracle.norm_quant(X, None, None, 1.0, oracle.LAYER_NORM)
+    assert oracle.f32_from_bf16(Yp)[0, 1] < 0
+
+
+def test_norm_fixed_order_within_one_ulp_of_plain(oracle):
+    rng = np.random.default_rng(13)
+    for K in (264, 5120):
+        X = oracle.bf16_from_f32((rng.normal(0.75, 2.0, (32, K)) *
+                                  rng.choice([1.0, 30.0], (32, K), p=[0.99, 0.01])).astype(np.float32))
+        g = oracle.bf16_from_f32(rng.normal(1.0, 0.2, K).astype(np.float32))
+        b = oracle.bf16_from_f32(rng.normal(0.0, 0.2, K).astype(np.float32))
+        for kind, bb in ((oracle.RMS_NORM, None), (oracle.LAYER_NORM, b)):
+            Yp, _, _ = oracle.norm_quant(X, g, bb, 1e-5, kind)
+            Yf, _, _ = oracle.norm_quant_fixed_order(X, g, bb, 1e-5, kind)
+            d = np.abs(_ordered(Yp) - _ordered(Yf))
+            assert d.max() <= 1 and (d > 0).mean() < 2e-3
