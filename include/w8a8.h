@@ -119,9 +119,11 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * images of Xq and Wq (every int8 value is exact in bf16) and, for few-token
  * post-scale shapes (M <= 256 with few 256-row weight tiles), the int32
  * partial sums of the K splits.  The same size serves both scale modes.
- * (With M <= 128 the post-scale GEMM streams the int8 codes directly and uses
- * only the partial-sum part; with M <= 8 and M * K <= 131072 it is a GEMV on
- * the CUDA cores that uses none of it.)
+ * The post-scale entry points (w8a8_gemm_postscale, _s32, _noalloc) need less
+ * for few tokens and accept it: with M <= 8 and M * K <= 131072 the GEMM is a
+ * GEMV on the CUDA cores that needs no workspace; otherwise, with M <= 128,
+ * it streams the int8 codes itself and needs only the partial sums
+ * (w8a8_splitk_workspace_size(M,N,K) bytes, possibly 0).
  */
 W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -133,9 +135,10 @@ W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   (per output channel), bias [N] bf16 or NULL, Y [M,N] bf16 out.
  *   workspace: device buffer of at least w8a8_gemm_workspace_size(M,N,K)
  *   bytes, 256-byte aligned, owned by the caller, not read after the call's
- *   work completes on `stream`.  With M <= 8 and M * K <= 131072 the GEMM is
- *   a GEMV on the CUDA cores that needs no workspace (workspace may be NULL
- *   and workspace_bytes 0); this also holds for w8a8_gemm_postscale_s32.
+ *   work completes on `stream`.  Few tokens need less (see
+ *   w8a8_gemm_workspace_size): nothing with M <= 8 and M * K <= 131072
+ *   (workspace may be NULL and workspace_bytes 0), the K-split partial sums
+ *   only with M <= 128; this also holds for w8a8_gemm_postscale_s32.
  */
 W8A8_API w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
                                 const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
@@ -229,9 +232,11 @@ W8A8_API w8a8_status w8a8_linear_blockwise(const void* X, const void* Wimg, cons
  *   codes = clamp(rne(g / sg), -127, 127) per 1x128 block,
  * and writes the exact bf16 image of the codes, which w8a8_gemm_blockwise_images
  * takes as its activation operand (1x128 activation scales sg).  gelu(x) =
- * x * Phi(x) with erf from Abramowitz & Stegun 7.1.28 (|error| <= 3e-7),
- * evaluated in a fixed binary32 order; on every bf16 input with |x| <= 3 it
- * equals torch's erf-form GELU rounded to bf16.
+ * x * Phi(x), Phi(x) = erfc(-x / sqrt 2) / 2 = (1 + erf(x / sqrt 2)) / 2, with
+ * erfc from the Chebyshev-fitted formula of Numerical Recipes in C (2nd ed.,
+ * section 6.2, fractional error < 1.2e-7) evaluated in binary32; g is within
+ * 1 bf16 ulp of the bf16 of the exact GELU for every bf16 input
+ * (w8a8_gelu_bf16 exports the same function for testing).
  *   X [M,K] bf16, Wimg [N,K] bf16 image (w8a8_pack_weight), sw [N] fp32,
  *   bias [N] bf16 or NULL, Gimg [M,N] bf16 out, sg [M][N/128] fp32 out,
  *   sx [M] fp32 out, Xq [M,K] int8 out or NULL, workspace of
@@ -299,10 +304,13 @@ W8A8_API w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* s
  * Allocation-free variant of w8a8_gemm_postscale (the pages have no
  * counterpart: this is a library convenience).  Same arguments, results and
  * checks, minus the workspace: the scratch lives in a fixed 64 MiB device
- * array inside the library, so the shape must satisfy
- * w8a8_gemm_workspace_size(M,N,K) <= 64 MiB (for example M = N = K = 4096)
- * or M <= 8 with M * K <= 131072 (the few-token GEMV needs no scratch),
- * else W8A8_ERR_WORKSPACE and nothing is launched.
+ * array inside the library, so the shape's scratch need must fit in it, else
+ * W8A8_ERR_WORKSPACE and nothing is launched.  The need is that of
+ * w8a8_gemm_postscale: nothing with M <= 8 and M * K <= 131072 (the
+ * few-token GEMV), the K-split partial sums with M <= 128
+ * (w8a8_splitk_workspace_size, a few MB at most: for example M = 77,
+ * N = 13824, K = 5120 fits), else w8a8_gemm_workspace_size(M,N,K) (for example
+ * M = N = K = 4096 fits exactly).
  *
  * For callers that cannot allocate device memory at the call site, for
  * example code running inside a host callback or a real-time loop where
@@ -334,6 +342,16 @@ W8A8_API w8a8_status w8a8_gemm_postscale_s32(const int8_t* Xq, const int8_t* Wq,
 W8A8_API w8a8_status w8a8_gemm_blockwise_f32(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
                                     float* acc, int64_t M, int64_t N, int64_t K, void* workspace,
                                     size_t workspace_bytes, void* stream);
+
+/*
+ * Test export of the FFN up-projection's activation (not part of the
+ * Linear): G[i] = bf16(gelu(Y[i])) for n bf16 values, computed by the same
+ * device function as the epilogue of w8a8_linear_postscale_gelu_quant, so
+ * that its values can be checked on every bf16 input.  Y and G are device
+ * pointers, 16-byte aligned; n % 8 == 0 (else W8A8_ERR_SHAPE).  Asynchronous
+ * on `stream`.
+ */
+W8A8_API w8a8_status w8a8_gelu_bf16(const void* Y, int64_t n, void* G, void* stream);
 
 /*
  * Reads and clears the device-side error word of the current device.

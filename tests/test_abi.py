@@ -76,9 +76,16 @@ def test_argument_checks_before_device(cdll):
     assert g(null, null, null, null, null, null, 4, 0, 16, null, 0, null) == 0
     assert g(fake, null, fake, fake, null, fake, 4, 4, 16, fake, 1 << 20, null) == 1
     assert g(fake, fake, fake, fake, odd, fake, 4, 4, 16, fake, 1 << 20, null) == 2
-    assert g(fake, fake, fake, fake, null, fake, 16, 4, 16, null, 1 << 20, null) == 7
-    assert g(fake, fake, fake, fake, null, fake, 16, 4, 16, fake, 10, null) == 7
-    assert g(fake, fake, fake, fake, null, fake, 16, 4, 16, P(0x1010), 1 << 20, null) == 7
+    # (more than 128 tokens: the bf16-image path, which needs the workspace)
+    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, null, 1 << 20, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, fake, 10, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, P(0x1010), 1 << 20, null) == 7
+    # 9..128 tokens stream the int8 codes: only the split-K partial sums
+    # (77 x 3072 splits K; 77 x 13824 has enough tiles not to)
+    s = L.w8a8_splitk_workspace_size(77, 3072, 5120)
+    assert s > 0 and L.w8a8_splitk_workspace_size(77, 13824, 5120) == 0
+    assert g(fake, fake, fake, fake, null, fake, 77, 3072, 5120, null, 0, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 77, 3072, 5120, fake, s - 256, null) == 7
     # blockwise needs its workspace even for one token
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 1, 4, 128, null, 0, null) == 7
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 4, 4, 64, fake, 1 << 20, null) == 3
@@ -134,6 +141,26 @@ def test_widened_entry_points_check_arguments_before_device(cdll):
     assert L.w8a8_splitk_workspace_size(4096, 4096, 4096) == 0
     assert gi(fake, fake, fake, fake, null, fake, 1, 4096, 4096, null, 0, null) == 7
     assert gi(fake, fake, fake, fake, odd, fake, 1, 4096, 4096, null, 0, null) == 2
+
+
+def test_noalloc_and_gelu_export_check_arguments_before_device(cdll):
+    L, _ = cdll
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    odd = P(0x1001)
+    null = None
+    na = L.w8a8_gemm_postscale_noalloc
+    assert na(fake, fake, fake, fake, null, fake, -1, 4, 16, null) == 1
+    assert na(fake, fake, fake, fake, null, fake, 4, 4, 20, null) == 3
+    assert na(fake, fake, fake, fake, null, fake, 1 << 31, 4, 16, null) == 3      # M > INT32_MAX: SHAPE
+    assert na(null, null, null, null, null, null, 0, 4, 16, null) == 0
+    assert na(fake, fake, fake, fake, null, fake, 4097, 4096, 4096, null) == 7   # beyond the 64 MiB scratch
+    g = L.w8a8_gelu_bf16
+    assert g(fake, -8, fake, null) == 1
+    assert g(fake, 12, fake, null) == 3
+    assert g(null, 0, null, null) == 0
+    assert g(null, 8, fake, null) == 1
+    assert g(odd, 8, fake, null) == 2
 
 
 def test_workspace_size(cdll):

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_bf16_close, bits, edge_indices
+from gpu_helpers import assert_bf16_close, assert_quant_follows_plain, bits, edge_indices
 from w8a8_int8_linear_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -82,7 +82,8 @@ def test_ffn_up_gelu_quant_full_size(w8a8, oracle):
     """The fused FFN up-projection (GELU + 1x128 quantization epilogue) at
     32768 x 13824 x 5120: codes and block scales of sampled rows and sampled
     128-column blocks (every edge block of the 256-wide tiles among them)
-    against the oracle."""
+    against the plain oracle (erf GELU in fp64), with the tolerance rule of
+    the small-size test (assert_quant_follows_plain)."""
     rng = np.random.default_rng(1)
     work = wl.FFN_UP
     X = wl.make_x(work, DEV)
@@ -97,10 +98,13 @@ def test_ffn_up_gelu_quant_full_size(w8a8, oracle):
     cols = (blocks[:, None] * 128 + np.arange(128)[None, :]).reshape(-1)
     Xs = bits(X[torch.from_numpy(rows).to(DEV)])
     Yo, _ = oracle.linear_sampled(Xs, bits(W), bits(b), np.arange(len(rows)), cols, oracle.PER_ROW)
-    Gq_o, sg_o = oracle.quantize_act(oracle.gelu_bf16(Yo), oracle.BLOCK)
+    Gp = oracle.gelu_bf16(Yo)
+    Gq_p, sg_p = oracle.quantize_act(Gp, oracle.BLOCK)
+    Yd = torch.from_numpy(np.ascontiguousarray(Yo).view(np.int16)).view(torch.bfloat16).to(DEV)
+    Gk = bits(w8a8.gelu_bf16(Yd))
     r = torch.from_numpy(rows).to(DEV)
     Gg = G[r][:, torch.from_numpy(cols).to(DEV)].float().cpu()
-    assert np.array_equal(Gg.to(torch.int8).numpy(), Gq_o)
     sgg = sg[r][:, torch.from_numpy(blocks).to(DEV)].cpu().numpy()
-    assert np.array_equal(sgg.view(np.uint32), sg_o.view(np.uint32))
+    differing = assert_quant_follows_plain(oracle, Gk, Gp, Gg.to(torch.int8).numpy(), sgg, Gq_p, sg_p, 128)
+    assert differing <= max(1, sg_p.size // 100)
     assert torch.isfinite(sg).all() and (G.abs() <= 127).all()

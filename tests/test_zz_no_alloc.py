@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_bf16_close, bits
+from gpu_helpers import assert_bf16_close, bits, edge_indices
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -71,3 +71,50 @@ def test_noalloc_repeat_same_shape_and_limit(w8a8):
     assert st == 7
     assert "no-alloc scratch holds" in L.w8a8_last_error_detail().decode()
     assert torch.all(Y == 0)
+
+
+def test_noalloc_few_token_paths(w8a8):
+    """The two few-token routes use the scratch differently: the GEMV (M <= 8)
+    needs none, the int8-operand GEMM (9..128 tokens) only its split-K
+    partial sums at the start of the array.  77 x 13824 x 5120 would need
+    ~142 MB as bf16 images but fits through the int8 route; two calls in a
+    row each, against the workspace entry point."""
+    L = w8a8.lib()
+    for (M, N, K, seed) in [(4, 3072, 5120, 4), (77, 13824, 5120, 5), (77, 13824, 5120, 6)]:
+        X, W, b = _inputs(M, N, K, seed, True)
+        Xq, sx = w8a8.quantize_act(X)
+        Wq, sw = w8a8.quantize_weight(W)
+        Y_ref = w8a8.gemm_postscale(Xq, sx, Wq, sw, b)
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+        assert _call_noalloc(L, Xq, sx, Wq, sw, b, Y) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(Y, Y_ref)
+    assert w8a8.get_device_error() == (0, 0)
+
+
+def test_noalloc_against_oracle_and_allocates_nothing(w8a8, oracle):
+    """At the 64 MiB limit (4096 x 4096 x 4096): sampled outputs (every tile
+    edge and random points) against the CPU oracle, and a second call that
+    changes neither the device's free memory nor torch's allocation count."""
+    L = w8a8.lib()
+    M = N = K = 4096
+    X, W, b = _inputs(M, N, K, 7, True)
+    Xq, sx = w8a8.quantize_act(X)
+    Wq, sw = w8a8.quantize_weight(W)
+    Y = torch.zeros((M, N), dtype=torch.bfloat16, device=DEV)
+    assert _call_noalloc(L, Xq, sx, Wq, sw, b, Y) == 0  # warm-up: kernels loaded
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    Y.zero_()
+    assert _call_noalloc(L, Xq, sx, Wq, sw, b, Y) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0 and torch.cuda.memory_allocated() == alloc0
+    rng = np.random.default_rng(0)
+    rows = edge_indices(M, 128, 16, rng)
+    cols = edge_indices(N, 224, 16, rng)
+    Xs = bits(X[torch.from_numpy(rows).to(DEV)])
+    Yo, _ = oracle.linear_sampled(Xs, bits(W), bits(b), np.arange(len(rows)), cols, oracle.PER_ROW)
+    Yg = bits(Y[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)])
+    d = assert_bf16_close(Yg, Yo, 1)
+    assert d.max() == 0
+    assert w8a8.get_device_error() == (0, 0)

@@ -55,6 +55,7 @@ SIGNATURES = [
     ("w8a8_gemm_postscale_noalloc", _I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     ("w8a8_gemm_postscale_s32", _I32, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     ("w8a8_gemm_blockwise_f32", _I32, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    ("w8a8_gelu_bf16", _I32, [_P, _I64, _P, _P]),
     ("w8a8_get_device_error", _I32, [ctypes.POINTER(ctypes.c_int)]),
     ("w8a8_probe_wait_timeout", _I32, [_P]),
     ("w8a8_set_gemm_timing_events", _I32, [_P, _P]),
@@ -450,6 +451,16 @@ def gemm_postscale_images(Ximg, sx, Wimg, sw, bias=None, out=None, workspace=Non
            lib().w8a8_gemm_postscale_images(_ptr(Ximg), _ptr(sx), _ptr(Wimg), _ptr(sw), _ptr(bias), _ptr(Y), M, N, K,
                                             _ptr(ws), 0 if ws is None else ws.numel(), _stream()))
     return Y
+
+
+def gelu_bf16(Y, out=None):
+    """Test export: bf16(gelu(Y)) elementwise with the FFN up-projection
+    epilogue's device function (Y bf16 on the device, numel % 8 == 0)."""
+    _need(Y, torch.bfloat16, "Y")
+    G = torch.empty_like(Y) if out is None else out
+    _need(G, torch.bfloat16, "out")
+    _check("w8a8_gelu_bf16", lib().w8a8_gelu_bf16(_ptr(Y), Y.numel(), _ptr(G), _stream()))
+    return G
 
 
 def get_device_error():

@@ -105,6 +105,16 @@ w8a8_status check_k(int64_t K, bool block) {
     return W8A8_OK;
 }
 
+// Workspace bytes the post-scale GEMM (int8 codes in) uses for this shape:
+// none for the few-token GEMV, the int32 partial sums of the K splits when the
+// GEMM streams the int8 codes itself (M <= 128), else the bf16 images of Xq and
+// Wq plus those partial sums (w8a8_gemm_workspace_size).  M, N, K > 0.
+size_t postscale_gemm_need(int64_t M, int64_t N, int64_t K) {
+    if (w8a8::gemv_takes(M, K)) return 0;
+    if (w8a8::gemm_takes_int8(w8a8::kEpiPostscaleBf16, M)) return align256(w8a8::splitk_partial_bytes(M, N, K));
+    return w8a8_gemm_workspace_size(M, N, K);
+}
+
 // Shared checks of the GEMM entry points.  need_sx/need_sw: scale pointers
 // used by this variant.
 w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw, const void* bias,
@@ -123,8 +133,7 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
     if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(out) || (sx && !aligned16(sx)) ||
         (sw && !aligned16(sw)) || (bias && !aligned16(bias)))
         return W8A8_ERR_ALIGNMENT;
-    // the few-token post-scale GEMV needs no workspace
-    const size_t need = (!block && w8a8::gemv_takes(M, K)) ? 0 : w8a8_gemm_workspace_size(M, N, K);
+    const size_t need = block ? w8a8_gemm_workspace_size(M, N, K) : postscale_gemm_need(M, N, K);
     if (need && (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need)) return W8A8_ERR_WORKSPACE;
     return current_device(dev);
 }
@@ -529,16 +538,18 @@ w8a8_status w8a8_gemm_postscale_noalloc(const int8_t* Xq, const float* sx, const
     if (M < 0 || N < 0) return W8A8_ERR_INVALID_ARG;
     w8a8_status s = check_k(K, false);
     if (s != W8A8_OK) return s;
+    if (M > INT32_MAX || N > INT32_MAX) return W8A8_ERR_SHAPE;
     if (M == 0 || N == 0) return W8A8_OK;
-    const size_t need = w8a8::gemv_takes(M, K) ? 0 : w8a8_gemm_workspace_size(M, N, K);
+    const size_t need = postscale_gemm_need(M, N, K);
     if (need > kNoAllocScratchBytes) {
         set_detail("shape %lld x %lld x %lld needs %zu bytes of scratch; the fixed no-alloc scratch holds %zu",
                    (long long)M, (long long)N, (long long)K, need, kNoAllocScratchBytes);
         return W8A8_ERR_WORKSPACE;
     }
+    DeviceInfo dev;
+    if ((s = current_device(&dev)) != W8A8_OK) return s;
     void* scratch = nullptr;
     if ((s = noalloc_scratch(&scratch)) != W8A8_OK) return s;
-    DeviceInfo dev;
     bool none;
     s = check_gemm(Xq, sx, Wq, sw, bias, Y, M, N, K, false, true, scratch, kNoAllocScratchBytes, &dev, &none);
     if (s != W8A8_OK || none) return s;
@@ -567,6 +578,18 @@ w8a8_status w8a8_gemm_blockwise_f32(const int8_t* Xq, const float* sx, const int
     if (s != W8A8_OK || none) return s;
     return run_gemm(w8a8::kEpiBlockwiseF32, Xq, sx, Wq, sw, nullptr, acc, M, N, K, workspace, dev,
                     static_cast<cudaStream_t>(stream));
+}
+
+w8a8_status w8a8_gelu_bf16(const void* Y, int64_t n, void* G, void* stream) {
+    if (n < 0) return W8A8_ERR_INVALID_ARG;
+    if (n % 8 != 0) return W8A8_ERR_SHAPE;
+    if (n == 0) return W8A8_OK;
+    if (!Y || !G) return W8A8_ERR_INVALID_ARG;
+    if (!aligned16(Y) || !aligned16(G)) return W8A8_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    w8a8_status s = current_device(&dev);
+    if (s != W8A8_OK) return s;
+    return from_cuda(w8a8::launch_gelu_bf16(Y, n, G, dev.num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 w8a8_status w8a8_get_device_error(int* code) {

@@ -64,6 +64,7 @@
 #include <cstdint>
 #include <cstdio>
 
+#include "gelu.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "quant_core.cuh"
@@ -395,39 +396,10 @@ __device__ __forceinline__ void store_rows_tma(const typename AccType<EPI>::T (&
     }
 }
 
-// GELU in its erf form, x * Phi(x), with erf from Abramowitz & Stegun,
-// Handbook of Mathematical Functions, formula 7.1.28 (|error| <= 3e-7):
-// for z = |x| / sqrt 2 and p = 1 + a1 z + ... + a6 z^6, Phi(-|x|) = p^-16 / 2
-// and Phi(|x|) = 1 - p^-16 / 2.  Binary32 in a fixed order: the Horner steps
-// from a6 down are fused multiply-adds, the four squarings, the correctly
-// rounded reciprocal and the rest are each rounded on their own.  Two values
-// at a time on the packed fp32 pipe; returns bf16(gelu(x0)), bf16(gelu(x1))
-// packed (x0 in the low half).
-__device__ __forceinline__ uint32_t gelu_erf_bf16x2(float x0, float x1) {
-    const uint64_t z = f2_mul(f2_pack(fabsf(x0), fabsf(x1)), f2_pack(0.70710678118654752f, 0.70710678118654752f));
-    uint64_t t = f2_fma(f2_pack(0.0000430638f, 0.0000430638f), z, f2_pack(0.0002765672f, 0.0002765672f));
-    t = f2_fma(t, z, f2_pack(0.0001520143f, 0.0001520143f));
-    t = f2_fma(t, z, f2_pack(0.0092705272f, 0.0092705272f));
-    t = f2_fma(t, z, f2_pack(0.0422820123f, 0.0422820123f));
-    t = f2_fma(t, z, f2_pack(0.0705230784f, 0.0705230784f));
-    t = f2_fma(t, z, f2_pack(1.0f, 1.0f));
-    t = f2_mul(t, t);
-    t = f2_mul(t, t);
-    t = f2_mul(t, t);
-    t = f2_mul(t, t);
-    float t0, t1;
-    f2_unpack(t, t0, t1);
-    const float h0 = __fmul_rn(0.5f, __frcp_rn(t0));
-    const float h1 = __fmul_rn(0.5f, __frcp_rn(t1));
-    const float g0 = __fmul_rn(x0, x0 >= 0.0f ? __fsub_rn(1.0f, h0) : h0);
-    const float g1 = __fmul_rn(x1, x1 >= 0.0f ? __fsub_rn(1.0f, h1) : h1);
-    return pack_bf16x2(g0, g1);
-}
-
 // FFN up-projection epilogue, staged.  For each thread's row and its 128
 // columns -- exactly one 1x128 block of the down-projection's input --
 //   y = bf16(((acc * sx) * sw) + bias)   (the post-scale epilogue),
-//   g = bf16(gelu(y)),
+//   g = bf16(gelu(y))  (gelu.cuh),
 //   s = absmax(|g|) / 127, codes = clamp(rne(g / s), -127, 127),
 // with the scale written to sg[row][col0 / 128] and the exact bf16 image of
 // the codes (the down-projection GEMM's A operand) stored through TMA.
@@ -500,7 +472,7 @@ __device__ __forceinline__ void gelu_slice(GeluStage& gs, const KParams& p, cons
             uint32_t g[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                g[i] = gelu_erf_bf16x2(bf16_lo(w[i]), bf16_hi(w[i]));
+                g[i] = gelu_bf16x2(bf16_lo(w[i]), bf16_hi(w[i]));
                 gs.amax = fmaxf(gs.amax, fmaxf(fabsf(bf16_lo(g[i])), fabsf(bf16_hi(g[i]))));
             }
             *ptr = make_uint4(g[0], g[1], g[2], g[3]);

@@ -22,6 +22,10 @@ cudaError_t launch_quant_weight_block(const void* W, int64_t N, int64_t K, int8_
 // Exact int8 -> bf16 image of n values (n % 16 == 0).
 cudaError_t launch_expand_s8_bf16(const int8_t* src, int64_t n, void* dst, int num_sms, cudaStream_t st);
 
+// Test export of the FFN up-projection's activation: G[i] = bf16(gelu(Y[i]))
+// for n bf16 values (n % 8 == 0), with the GEMM epilogue's device function.
+cudaError_t launch_gelu_bf16(const void* Y, int64_t n, void* G, int num_sms, cudaStream_t st);
+
 // RMSNorm (layer = 0) or LayerNorm (layer = 1) of bf16 X[M,K] fused with
 // per-token quantization; K % 8 == 0, K <= 16384.  gamma / beta (bf16 [K]) and
 // the outputs Y (normalized bf16), Xq (int8), img (bf16 image of Xq) may be null.

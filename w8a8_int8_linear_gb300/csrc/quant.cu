@@ -38,6 +38,7 @@
 
 #include <cstdint>
 
+#include "gelu.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "quant_core.cuh"
@@ -102,12 +103,16 @@ __device__ __forceinline__ float block_max(float v, float* red) {
     return r;
 }
 
-// One CTA per row of A[R,K]; the row stays in registers (CPT 16-byte chunks
-// per thread) between the absmax pass and the quantize pass.
-template <int CPT>
-__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
-                                                             uint2* __restrict__ Aq, uint4* __restrict__ img,
-                                                             float* __restrict__ s) {
+// One CTA of T threads per row of A[R,K]; the row stays in registers (CPT
+// 16-byte chunks per thread) between the absmax pass and the quantize pass,
+// so it is read from memory once.  MINB CTAs per SM bound the registers
+// (65536 / (T * MINB) per thread); with many rows, small CTAs and many of them
+// per SM keep the most bytes in flight (one 64-thread CTA per 5120-wide row,
+// 16 per SM: 160 KB of loads in flight per SM).
+template <int CPT, int T, int MINB, int OUT>
+__global__ void __launch_bounds__(T, MINB) quant_rows_reg_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
+                                                                 uint2* __restrict__ Aq, uint4* __restrict__ img,
+                                                                 float* __restrict__ s) {
     grid_launch_dependents();
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
@@ -118,19 +123,21 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const uint4* __rest
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
-        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * blockDim.x;
-        if (c < chunks) {
-            v[i] = __ldcs(a + c);
-            amax = fmaxf(amax, chunk_absmax(v[i]));
-        }
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
+        if (c < chunks) v[i] = __ldcs(a + c);
     }
-    amax = block_max(amax, red);
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
+        if (c < chunks) amax = fmaxf(amax, chunk_absmax(v[i]));
+    }
+    amax = T > 32 ? block_max(amax, red) : warp_max(amax);
     const RowScale sc = make_scale_div(amax);
     if (threadIdx.x == 0) s[row] = sc.s;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
-        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * blockDim.x;
-        if (c < chunks) put_codes(Aq, img, row * chunks + c, quant_chunk(v[i], sc));
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
+        if (c < chunks) emit_chunk<OUT>(Aq, img, row * chunks + c, v[i], sc);
     }
 }
 
@@ -294,6 +301,22 @@ __global__ void __launch_bounds__(256) expand_s8_bf16_kernel(const uint4* __rest
     }
 }
 
+// Test export of the FFN up-projection's activation: G[i] = bf16(gelu(Y[i]))
+// with the epilogue's own device function (gelu.cuh), 8 values per thread.
+__global__ void __launch_bounds__(256) gelu_bf16_kernel(const uint4* __restrict__ y, int64_t n8,
+                                                        uint4* __restrict__ g) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const uint4 v = y[i];
+        uint4 o;
+        o.x = gelu_bf16x2(bf16_lo(v.x), bf16_hi(v.x));
+        o.y = gelu_bf16x2(bf16_lo(v.y), bf16_hi(v.y));
+        o.z = gelu_bf16x2(bf16_lo(v.z), bf16_hi(v.z));
+        o.w = gelu_bf16x2(bf16_lo(v.w), bf16_hi(v.w));
+        g[i] = o;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, void* img, float* s, int num_sms,
@@ -303,21 +326,31 @@ cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, v
     uint2* q = reinterpret_cast<uint2*>(Aq);
     uint4* im = static_cast<uint4*>(img);
     const dim3 grid(static_cast<unsigned>(R));
-    // One 128-thread CTA per row for rows of up to 512 chunks (K <= 4096).
-    // Longer rows: few of them (about one wave) still get a CTA each, 256
-    // threads with the row in registers, so the row is read once with every
-    // load in flight; many long rows go two-pass warp-per-row.
-    const bool few = R <= static_cast<int64_t>(num_sms) * 8;
+    // Many rows (at least 16 per SM): CTAs sized for bytes in flight.  Fewer
+    // rows: 128- or 256-thread CTAs, so that each row's loads spread over
+    // more threads and the few rows finish sooner.
+    const bool many = R >= static_cast<int64_t>(num_sms) * 16;
+    const int out = (q ? kOutCodes : 0) | (im ? kOutImage : 0);
+    auto reg = [&](auto kern, int threads) { kern<<<grid, threads, 0, st>>>(a, R, K, q, im, s); };
+#define W8A8_ROWS(CPT, T, MINB)                                                       \
+    (out == kOutCodes   ? reg(quant_rows_reg_kernel<CPT, T, MINB, kOutCodes>, T)      \
+     : out == kOutImage ? reg(quant_rows_reg_kernel<CPT, T, MINB, kOutImage>, T)      \
+                        : reg(quant_rows_reg_kernel<CPT, T, MINB, kOutBoth>, T))
     if (chunks <= 128)
-        quant_rows_reg_kernel<1><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
+        W8A8_ROWS(1, 128, 8);
     else if (chunks <= 256)
-        quant_rows_reg_kernel<2><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
+        W8A8_ROWS(2, 128, 8);
     else if (chunks <= 512)
-        quant_rows_reg_kernel<4><<<grid, 128, 0, st>>>(a, R, K, q, im, s);
-    else if (few && chunks <= 1024)
-        quant_rows_reg_kernel<4><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
-    else if (few && chunks <= 2048)
-        quant_rows_reg_kernel<8><<<grid, 256, 0, st>>>(a, R, K, q, im, s);
+        W8A8_ROWS(4, 128, 8);
+    else if (many && chunks <= 640)
+        W8A8_ROWS(10, 64, 16);
+    else if (many && chunks <= 1024)
+        W8A8_ROWS(8, 128, 8);
+    else if (chunks <= 1024)
+        W8A8_ROWS(4, 256, 1);
+    else if (chunks <= 2048)
+        W8A8_ROWS(8, 256, 4);
+#undef W8A8_ROWS
     else if (chunks <= 16384)
         quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, im, s);
     else
@@ -331,7 +364,7 @@ cudaError_t launch_quant_act_block(const void* X, int64_t M, int64_t K, int8_t* 
     constexpr int kUnroll = 2;
     const int64_t warps_needed = (n_blocks + 8 * kUnroll - 1) / (8 * kUnroll);
     int64_t grid = (warps_needed + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     quant_act_block_kernel<kUnroll><<<static_cast<unsigned>(grid), 256, 0, st>>>(
@@ -355,6 +388,17 @@ cudaError_t launch_expand_s8_bf16(const int8_t* src, int64_t n, void* dst, int n
     if (grid < 1) grid = 1;
     expand_s8_bf16_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(reinterpret_cast<const uint4*>(src), n16,
                                                                        static_cast<uint4*>(dst));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gelu_bf16(const void* Y, int64_t n, void* G, int num_sms, cudaStream_t st) {
+    const int64_t n8 = n >> 3;
+    int64_t grid = (n8 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    gelu_bf16_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint4*>(Y), n8,
+                                                                  static_cast<uint4*>(G));
     return cudaGetLastError();
 }
 

@@ -42,7 +42,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Exact path: IEEE quotient, round half to even, clamp.
-__device__ __noinline__ int quant_exact(float x, float s) {
+__device__ __forceinline__ int quant_exact(float x, float s) {
     if (s == 0.0f) return 0;
     float r = rintf(__fdiv_rn(x, s));
     r = fminf(fmaxf(r, -kQMax), kQMax);
@@ -88,7 +88,6 @@ __device__ __forceinline__ uint2 quant_chunk(const uint4& v, const RowScale& sc)
     const uint64_t magic2 = f2_pack(kRoundMagic, kRoundMagic);
     uint32_t big[8];
     float dmax = 0.0f;
-    float dist[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint64_t x2 = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
@@ -100,16 +99,19 @@ __device__ __forceinline__ uint2 quant_chunk(const uint4& v, const RowScale& sc)
         f2_unpack(d, d0, d1);
         big[2 * i] = __float_as_uint(b0);
         big[2 * i + 1] = __float_as_uint(b1);
-        dist[2 * i] = d0;
-        dist[2 * i + 1] = d1;
         dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
     }
     if (!(dmax <= 0.5f - kTieGuard)) {
+        // rare: recompute each remainder (the same operations give the same
+        // values) rather than keep all eight live on the common path
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            if (!(fabsf(dist[2 * i]) <= 0.5f - kTieGuard)) big[2 * i] = quant_byte_exact(bf16_lo(w[i]), sc.s);
-            if (!(fabsf(dist[2 * i + 1]) <= 0.5f - kTieGuard))
-                big[2 * i + 1] = quant_byte_exact(bf16_hi(w[i]), sc.s);
+            const uint64_t x2 = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+            const uint64_t bg = f2_fma(x2, inv2, magic2);
+            float d0, d1;
+            f2_unpack(f2_fma(x2, inv2, f2_sub(magic2, bg)), d0, d1);
+            if (!(fabsf(d0) <= 0.5f - kTieGuard)) big[2 * i] = quant_byte_exact(bf16_lo(w[i]), sc.s);
+            if (!(fabsf(d1) <= 0.5f - kTieGuard)) big[2 * i + 1] = quant_byte_exact(bf16_hi(w[i]), sc.s);
         }
     }
     // low byte of each value, four to a word
@@ -151,7 +153,6 @@ __device__ __forceinline__ uint4 quant_chunk_img(const uint4& v, const RowScale&
     } else {
         const uint64_t inv2 = f2_pack(sc.inv, sc.inv);
         const uint64_t magic2 = f2_pack(kRoundMagic, kRoundMagic);
-        float dist[8];
         float dmax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -162,16 +163,19 @@ __device__ __forceinline__ uint4 quant_chunk_img(const uint4& v, const RowScale&
             float d0, d1;
             f2_unpack(f2_sub(bg, magic2), q[2 * i], q[2 * i + 1]);  // rne(P), exact (+0 for 0)
             f2_unpack(d, d0, d1);
-            dist[2 * i] = d0;
-            dist[2 * i + 1] = d1;
             dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
         }
         if (!(dmax <= 0.5f - kTieGuard)) {
+            // rare: recompute each remainder instead of keeping all eight live
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (!(fabsf(dist[2 * i]) <= 0.5f - kTieGuard))
+                const uint64_t x2 = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+                const uint64_t bg = f2_fma(x2, inv2, magic2);
+                float d0, d1;
+                f2_unpack(f2_fma(x2, inv2, f2_sub(magic2, bg)), d0, d1);
+                if (!(fabsf(d0) <= 0.5f - kTieGuard))
                     q[2 * i] = __fadd_rn(static_cast<float>(quant_exact(bf16_lo(w[i]), sc.s)), 0.0f);
-                if (!(fabsf(dist[2 * i + 1]) <= 0.5f - kTieGuard))
+                if (!(fabsf(d1) <= 0.5f - kTieGuard))
                     q[2 * i + 1] = __fadd_rn(static_cast<float>(quant_exact(bf16_hi(w[i]), sc.s)), 0.0f);
             }
         }
@@ -183,6 +187,30 @@ __device__ __forceinline__ uint4 quant_chunk_img(const uint4& v, const RowScale&
         o[i] = *reinterpret_cast<uint32_t*>(&h);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Outputs of a quantization kernel, fixed at compile time.
+enum QuantOut : int { kOutCodes = 1, kOutImage = 2, kOutBoth = 3 };
+
+// Quantize chunk i of 8 values and write the int8 codes to q[i] and/or their
+// exact bf16 image to img[i], as OUT says.
+template <int OUT>
+__device__ __forceinline__ void emit_chunk(uint2* __restrict__ q, uint4* __restrict__ img, int64_t i, const uint4& v,
+                                           const RowScale& sc) {
+    if constexpr (OUT == kOutImage) {
+        img[i] = quant_chunk_img(v, sc);
+    } else {
+        const uint2 c = quant_chunk(v, sc);
+        __stcs(q + i, c);
+        if constexpr (OUT == kOutBoth) {
+            uint4 o;
+            o.x = s8x2_to_bf16x2(c.x, 0);
+            o.y = s8x2_to_bf16x2(c.x, 2);
+            o.z = s8x2_to_bf16x2(c.y, 0);
+            o.w = s8x2_to_bf16x2(c.y, 2);
+            img[i] = o;
+        }
+    }
 }
 
 __device__ __forceinline__ void put_codes(uint2* __restrict__ q, uint4* __restrict__ img, int64_t i, uint2 c) {
