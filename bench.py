@@ -3,10 +3,12 @@
 A step is one pass of the hot path over one batch: dynamic per-token
 activation quantization of X followed by the post-scale INT8 GEMM, through the
 fused Linear entry point (two kernels: quantize-to-image, tensor-core GEMM).
-Weights are quantized and packed once, before timing.  The default workload is the square
-post-scale case (X [4096,4096] with 1% outlier channels x20, W [4096,4096]
-~N(0,0.02), no bias).  Inputs are resident in HBM; L2 (129 MB) is flushed
-between timed steps by writing a 256 MB buffer outside the per-step events.
+Weights are quantized and packed once, before timing.  The default workload is
+the DiT FFN up-projection (X [32768, 5120] with 0.5% outlier channels x30,
+W [13824, 5120] ~N(0, 0.015), bias ~N(0, 0.01)): quant + GEMM timed end to
+end.  Inputs are resident in HBM; between timed steps L2 holds none of a
+step's inputs (the steps rotate over copies of X and the weights, together
+larger than L2; tiny shapes flush L2 with a 256 MB write instead).
 
 Prints ONE JSON line on rank 0.  `--impl reference` times the CPU oracle on
 the host cores instead (bounded samples of the same workload).
@@ -35,7 +37,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="w8a8", choices=["w8a8", "reference"])
-    ap.add_argument("--workload", default="square_postscale_4096")
+    ap.add_argument("--workload", default="ffn_up_postscale_32768x13824x5120")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (rows of X)")
@@ -54,8 +56,11 @@ def parse():
     return ap.parse_args()
 
 
-GEMM_SOURCES = ["gemm.cu", "ptx.cuh", "kernels.h", "quant_core.cuh", "w8a8_device_error.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic_square_postscale_4096.txt")
+GEMM_SOURCES = ["gemm.cu", "ptx.cuh", "kernels.h", "quant_core.cuh", "gelu.cuh", "w8a8_device_error.cuh"]
+
+
+def traffic_file(workload):
+    return os.path.join(ROOT, "profiles", f"gemm_traffic_{workload}.txt")
 
 
 def gemm_source_hash():
@@ -69,21 +74,33 @@ def gemm_source_hash():
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per GEMM launch from the committed ncu capture, or None when
-    the capture is for another workload or the kernel changed since."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
+    """DRAM bytes per GEMM launch of this workload from its committed ncu
+    record (profiles/gemm_traffic_<workload>.txt), scaled to the full launch
+    when the record was captured on a cut-down M (traffic grows with the
+    row bands processed); None when there is no record or the GEMM sources
+    changed since it was taken.  Returns (bytes, source description)."""
+    path = traffic_file(workload)
+    if not os.path.exists(path):
+        return None, f"no record {os.path.relpath(path, ROOT)}"
     kv = {}
-    for line in open(TRAFFIC_FILE):
+    for line in open(path):
         if "=" in line and not line.lstrip().startswith("#"):
             k, v = line.split("=", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("workload") != workload or kv.get("gemm_source_sha256_16") != gemm_source_hash():
-        return None
+    rel = os.path.relpath(path, ROOT)
+    if kv.get("workload") != workload:
+        return None, f"{rel}: other workload"
+    if kv.get("gemm_source_sha256_16") != gemm_source_hash():
+        return None, f"{rel}: GEMM sources changed since the capture"
     try:
-        return float(kv["dram_bytes_read"]) + float(kv["dram_bytes_write"])
+        t = float(kv["dram_bytes_read"]) + float(kv["dram_bytes_write"])
+        scale = float(kv.get("scale_to_full", "1"))
     except (KeyError, ValueError):
-        return None
+        return None, f"{rel}: unreadable"
+    how = f"{rel} (ncu dram bytes per launch"
+    if scale != 1.0:
+        how += f", captured at M = {kv.get('captured_M')} and scaled by {scale:g} to the full M"
+    return t * scale, how + ")"
 
 
 def load_peaks():
@@ -189,29 +206,48 @@ def max_over_ranks(v, world):
 
 
 # ----------------------------------------------------------------- CPU oracle timing
-def oracle_sample_run(work, rows, X_bits, W_bits, b_bits):
-    """One bounded sample of the step on the host: quantize `rows` rows of X,
-    then the post-scale GEMM of those rows against all N outputs (weights
-    pre-quantized, as in the timed GPU step).  Returns (seconds, ops)."""
-    import numpy as np
+def oracle_weights(work, W):
+    """The oracle's quantized weights for the step (done once, outside the
+    timed samples, as the GPU step's weights are)."""
     import oracle
+    from w8a8_int8_linear_gb300.workloads import bf16_bits
+    mode = oracle.BLOCK if work.mode == "blockwise" else oracle.PER_ROW
+    return oracle.quantize_weight(bf16_bits(W), mode)
+
+
+def oracle_sample_run(work, rows, X_bits, Wq_sw, b_bits):
+    """One bounded sample of the step on the host: quantize `rows` rows of X
+    (per token, or in 1x128 blocks for the blockwise workload), then the GEMM
+    of those rows against all N outputs with its epilogue (weights quantized
+    beforehand, as in the timed GPU step).  Returns (seconds, ops)."""
+    import oracle
+    Wq, sw = Wq_sw
     t0 = time.perf_counter()
-    Xq, sx = oracle.quantize_act(X_bits[:rows], oracle.PER_ROW)
-    Wq, sw = W_bits
-    acc = oracle.gemm_s32(Xq, Wq)
-    oracle.epilogue_postscale(acc, sx, sw, b_bits)
+    if work.mode == "blockwise":
+        Xq, sx = oracle.quantize_act(X_bits[:rows], oracle.BLOCK)
+        acc = oracle.gemm_blockwise_f32(Xq, sx, Wq, sw)
+        oracle.epilogue_blockwise(acc, b_bits)
+    else:
+        Xq, sx = oracle.quantize_act(X_bits[:rows], oracle.PER_ROW)
+        acc = oracle.gemm_s32(Xq, Wq)
+        oracle.epilogue_postscale(acc, sx, sw, b_bits)
     dt = time.perf_counter() - t0
     return dt, 2.0 * rows * work.N * work.K
 
 
+def _step_words(work):
+    return ("1x128 act quant + blockwise GEMM with the per-128-K fold + epilogue" if work.mode == "blockwise"
+            else "per-token quant + int32 GEMM + epilogue")
+
+
 def cpu_baseline(work, X, W, b, target_s=10.0):
-    """The oracle, as it stands, on blocks of 256 rows of the same X until
-    about `target_s` seconds of host time have been spent."""
+    """The oracle, as it stands, on blocks of rows of the same X until about
+    `target_s` seconds of host time have been spent."""
     import oracle
     from w8a8_int8_linear_gb300.workloads import bf16_bits
     rows_max = min(work.M, 4096)
     Xb = bf16_bits(X[:rows_max])
-    Wq_o = oracle.quantize_weight(bf16_bits(W), oracle.PER_ROW)
+    Wq_o = oracle_weights(work, W)
     bb = None if b is None else bf16_bits(b)
     blk = min(256, rows_max)
     total_t, total_ops, rows_done, r0 = 0.0, 0.0, 0, 0
@@ -224,8 +260,8 @@ def cpu_baseline(work, X, W, b, target_s=10.0):
         rows_done += blk
         r0 += blk
     return dict(value=total_ops / total_t / 1e12, unit="TOPS", cores=oracle.num_threads(), kind="oracle",
-                sample=f"{rows_done} rows of X in blocks of {blk} (per-token quant + int32 GEMM + epilogue vs all "
-                       f"{work.N} outputs, weights pre-quantized), {total_t:.1f} s of host time")
+                sample=f"{rows_done} rows of X in blocks of {blk} ({_step_words(work)} vs all {work.N} outputs, "
+                       f"weights quantized beforehand), {total_t:.1f} s of host time")
 
 
 # ----------------------------------------------------------------- main arm
@@ -406,28 +442,22 @@ def run_w8a8(args):
     ops = work.ops
     value = world * ops / (ms_step * 1e-3) / 1e12
 
-    # quant kernel alone (HBM bound): bytes = read X bf16 + write Xq int8 + sx
-    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-    for a, bb in qev:
-        flush.zero_()
+    # the quantization kernel alone (HBM bound), on the step's X copies in the
+    # same rotation (a copy's bytes were last read more than an L2 earlier):
+    # algorithmic bytes = read X bf16 + write Xq int8 + the scales
+    q_in = Xs if rotate else [X]
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for i in range(3):
+        w.quantize_act(q_in[i % len(q_in)], mode, out=(Xq, sx))
+    for i, (a, bb) in enumerate(qev):
+        if not rotate:
+            flush.zero_()
         a.record(stream)
-        w.quantize_act(X, mode, out=(Xq, sx))
+        w.quantize_act(q_in[i % len(q_in)], mode, out=(Xq, sx))
         bb.record(stream)
     torch.cuda.synchronize()
     q_ms = statistics.median(a.elapsed_time(bb) for a, bb in qev)
     q_bytes = M * K * 2 + M * K + sx.numel() * 4
-    # the same bytes (read 2 B, write 1 B per element) moved by a plain
-    # streaming kernel under the same flush: the memory floor of the quant
-    scratch = torch.empty_like(Xq)
-    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-    for a, bb in cev:
-        flush.zero_()
-        a.record(stream)
-        w.stream_floor(X, scratch)
-        bb.record(stream)
-    torch.cuda.synchronize()
-    copy_ms = statistics.median(a.elapsed_time(bb) for a, bb in cev)
-    del scratch
 
     # comparison point: torch bf16 matmul at the same shape
     Xbf = X
@@ -508,7 +538,7 @@ def run_w8a8(args):
         del w_copies, pipe
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not blockwise:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(work, X, W, b)
 
     gemm_tflops = ops / (ms_gemm * 1e-3) / 1e12
@@ -516,14 +546,17 @@ def run_w8a8(args):
     # bf16 figure; shorter launches: the burst figure
     long_kernel = ms_gemm >= 1.0
     peak_bf16 = peaks["bf16_tflops_sustained"] if long_kernel else peaks["bf16_tflops"]
+    traffic, traffic_source = recorded_traffic(work.name)
+    alg_bytes = 2 * M * K + 2 * N * K + 2 * M * N  # operand images + Y
     roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05 kind::f16, exact int8 products)",
                 "achieved": round(gemm_tflops, 2), "peak": peak_bf16, "unit": "TFLOP/s",
-                "frac": round(gemm_tflops / peak_bf16, 4), "traffic": recorded_traffic(work.name),
-                "traffic_source": "profiles/gemm_traffic_square_postscale_4096.txt (ncu dram bytes per "
-                                  "launch; null if the GEMM sources changed since the capture)",
+                "frac": round(gemm_tflops / peak_bf16, 4), "traffic": traffic,
+                "traffic_source": traffic_source,
+                "algorithmic_bytes": alg_bytes,
+                "traffic_over_algorithmic": None if traffic is None else round(traffic / alg_bytes, 3),
                 "peak_source": f"bf16 dense {'sustained' if long_kernel else 'burst'}, {peaks['source']}",
                 "algorithmic": f"2*M*N*K = {ops:.4g} ops per launch; operand images + Y = "
-                               f"{(2 * M * K + 2 * N * K + 2 * M * N) / 1e6:.1f} MB",
+                               f"{alg_bytes / 1e6:.1f} MB",
                 "gemm_ms": round(ms_gemm, 5)}
     kernel_events = {"how": "the kernel's launch bracketed by CUDA events on its stream in a second pass of the "
                             "same steps; ms_per_step comes from the first pass, without those events, which "
@@ -572,10 +605,14 @@ def run_w8a8(args):
                       "frac_of_imma_peak": round(gemm_tflops / imma_tops, 3) if imma_tops else None,
                       "note": "mma.sync m16n8k32 s8 throughput measured on this GPU; tcgen05 kind::i8 does not "
                               "exist on sm_103a"},
-        "quant": {"kernel": "1x128 act quant" if blockwise else "per-token act quant", "ms": round(q_ms, 5), "gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+        "quant": {"kernel": ("1x128 act quant" if blockwise else "per-token act quant") + " (w8a8_quantize_act, "
+                            "int8 codes + fp32 scales)",
+                  "ms": round(q_ms, 5), "gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+                  "bytes": q_bytes,
                   "frac_of_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                  "peak_gbs": peaks["hbm_gbs"], "peak_source": f"HBM copy bandwidth, {peaks['source']}",
                   "frac_of_8tbs": round(q_bytes / (q_ms * 1e-3) / 1e9 / 8000.0, 4),
-                  "stream_floor_ms": round(copy_ms, 5), "frac_of_stream_floor": round(copy_ms / q_ms, 4)},
+                  "l2": "same input rotation as the step" if rotate else "256 MB write flush before each launch"},
         "comparison": {"torch_bf16_matmul_tflops": round(ops / (torch_ms * 1e-3) / 1e12, 1)},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -597,7 +634,6 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    import torch
     import oracle
     from w8a8_int8_linear_gb300 import workloads as wl
     from w8a8_int8_linear_gb300.workloads import bf16_bits
@@ -607,7 +643,7 @@ def run_reference(args):
     W = wl.make_w(work, "cpu")
     b = wl.make_bias(work, "cpu")
     Xb = bf16_bits(X)
-    Wq_o = oracle.quantize_weight(bf16_bits(W), oracle.PER_ROW)
+    Wq_o = oracle_weights(work, W)
     bb = None if b is None else bf16_bits(b)
     for _ in range(args.warmup):
         oracle_sample_run(work, rows, Xb, Wq_o, bb)
@@ -617,7 +653,7 @@ def run_reference(args):
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = ops / (ms * 1e-3) / 1e12
-    sample = f"{rows} of {work.M} rows per step (quant + int32 GEMM + epilogue vs all {work.N} outputs)"
+    sample = f"{rows} of {work.M} rows per step ({_step_words(work)} vs all {work.N} outputs)"
     print(json.dumps({
         "metric": "W8A8 Linear TOPS (quant+GEMM) and % of GB300 dense INT8 peak; quant GB/s",
         "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
