@@ -95,7 +95,14 @@ static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= THREADS * 168, "register split
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int POSTSCALE_CHUNK_STAGES = 16;  // 1024 K: 127*127*1024 < 2^24
 constexpr int BLOCK_CHUNK_STAGES = 2;       // one 128-wide scale block
-constexpr int GROUP_M = 8;                  // tile raster: bands of 8 row tiles (2048 rows)
+// Tile raster: consecutive tiles walk the row tiles of a band of group_m row
+// tiles (a KParams value) before moving to the next column tile, so a band's
+// A rows stay in L2 while the B columns stream past.  The post-scale GEMM
+// takes bands of 16 row tiles (4096 rows: the weight image is read once per
+// band, and a band of A is 42 MB at K = 5120); the blockwise GEMM keeps 8.
+constexpr int GROUP_M_POSTSCALE = 16;
+constexpr int GROUP_M_BLOCKWISE = 8;
+constexpr int SCALE_PREFETCH = 4;           // blockwise: per-block scales loaded this many chunks ahead
 constexpr int kSwapMaxTokens = 256;         // post-scale GEMMs with M <= this swap operands
 constexpr int kInt8MaxTokens = 128;         // ... and with M <= this can stream int8 operands
 constexpr int kSplitTargetUnits = 72;       // split K until about this many CTA-pair work units exist
@@ -146,13 +153,14 @@ struct KParams {
     float* sg;         // kEpiGeluQuant: block scales [M][N/128]
     int a_settled;     // operand A (resp. B) was complete before the previous kernel in the
     int b_settled;     // stream started, so it may be read before the grid dependency wait
+    int group_m;       // row tiles per raster band
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-    const int per_group = GROUP_M * num_n;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group_m, int& mb, int& nb) {
+    const int per_group = group_m * num_n;
     const int group = tile / per_group;
-    const int first_m = group * GROUP_M;
-    const int gm = min(num_m - first_m, GROUP_M);
+    const int first_m = group * group_m;
+    const int gm = min(num_m - first_m, group_m);
     const int local = tile - group * per_group;
     mb = first_m + local % gm;
     nb = local / gm;
@@ -167,7 +175,7 @@ __device__ __forceinline__ Unit unit_coords(int u, const KParams& p) {
     Unit w;
     const int tile = u / p.k_split;
     w.split = u - tile * p.k_split;
-    tile_coords(tile, p.num_m, p.num_n, w.mb, w.nb);
+    tile_coords(tile, p.num_m, p.num_n, p.group_m, w.mb, w.nb);
     w.ks0 = w.split * p.split_stages;
     w.ks1 = min(p.k_stages, w.ks0 + p.split_stages);
     return w;
@@ -837,23 +845,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             T acc[HALF];
 #pragma unroll
             for (int e = 0; e < HALF; ++e) acc[e] = T(0);
-            // blockwise: the scales of chunk c are loaded during chunk c-1
+            // blockwise: the per-block scales of chunk c are loaded SCALE_PREFETCH
+            // chunks ahead (a row's scales are 4-byte loads scattered over 32
+            // rows per warp; one chunk ahead left their latency exposed)
             const float* sx_row = p.sx + static_cast<int64_t>(row < p.M ? row : 0) * p.kb_count;
             const float* sw_row = p.sw + static_cast<int64_t>(col0 < p.N ? (col0 >> 7) : 0) * p.kb_count;
-            float sx_next = 0.0f, sw_next = 0.0f;
+            float sxq[SCALE_PREFETCH], swq[SCALE_PREFETCH];
             if constexpr (kBlock) {
-                if (row < p.M) sx_next = __ldg(sx_row);
-                if (col0 < p.N) sw_next = __ldg(sw_row);
+#pragma unroll
+                for (int i = 0; i < SCALE_PREFETCH; ++i) {
+                    sxq[i] = (row < p.M && i < nchunks) ? __ldg(sx_row + i) : 0.0f;
+                    swq[i] = (col0 < p.N && i < nchunks) ? __ldg(sw_row + i) : 0.0f;
+                }
             }
             for (int c = 0; c < nchunks; ++c) {
                 float sxv = 0.0f, swv = 0.0f;
                 if constexpr (kBlock) {
-                    sxv = sx_next;
-                    swv = sw_next;
-                    if (c + 1 < nchunks) {
-                        if (row < p.M) sx_next = __ldg(sx_row + c + 1);
-                        if (col0 < p.N) sw_next = __ldg(sw_row + c + 1);
+                    sxv = sxq[0];
+                    swv = swq[0];
+#pragma unroll
+                    for (int i = 0; i + 1 < SCALE_PREFETCH; ++i) {
+                        sxq[i] = sxq[i + 1];
+                        swq[i] = swq[i + 1];
                     }
+                    const int cn = c + SCALE_PREFETCH;
+                    sxq[SCALE_PREFETCH - 1] = (row < p.M && cn < nchunks) ? __ldg(sx_row + cn) : 0.0f;
+                    swq[SCALE_PREFETCH - 1] = (col0 < p.N && cn < nchunks) ? __ldg(sw_row + cn) : 0.0f;
                 }
                 if (!mbar_wait(&acc_full[buf], buf_phase, kSiteEpiAccFull)) {
                     ok = false;
@@ -1609,6 +1626,8 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     p.sg = a.sg;
     p.a_settled = 0;
     p.b_settled = a.weights_settled ? 1 : 0;  // B holds the weights (swapped launches exchange the flags)
+    p.group_m = (epilogue == kEpiBlockwiseBf16 || epilogue == kEpiBlockwiseF32) ? GROUP_M_BLOCKWISE
+                                                                                : GROUP_M_POSTSCALE;
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.K = static_cast<int>(a.K);

@@ -42,7 +42,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Exact path: IEEE quotient, round half to even, clamp.
-__device__ __forceinline__ int quant_exact(float x, float s) {
+__device__ __noinline__ int quant_exact(float x, float s) {
     if (s == 0.0f) return 0;
     float r = rintf(__fdiv_rn(x, s));
     r = fminf(fmaxf(r, -kQMax), kQMax);
