@@ -1011,6 +1011,8 @@ def report_decode(args):
 
 PROFILE_CASES = {
     # name: (what, M, N, K)
+    "quant_rows_32768x5120": ("quant_rows", 32768, 0, 5120),
+    "quant_block_32768x13824": ("quant_block", 32768, 0, 13824),
     "gelu_quant_4096x4096x2048": ("gelu_quant", 4096, 4096, 2048),
     "norm_layer_8192x5120": ("norm_layer", 8192, 0, 5120),
     "gemm_int8_decode_1x13824x5120": ("gemm_int8", 1, 13824, 5120),
@@ -1027,7 +1029,12 @@ def profile_case(name):
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(0)
     X = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
-    if what == "norm_layer":
+    if what in ("quant_rows", "quant_block"):
+        mode = w.PER_ROW if what == "quant_rows" else w.BLOCK
+        Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        sx = torch.empty((M,) if mode == w.PER_ROW else (M, K // 128), dtype=torch.float32, device=dev)
+        fn = lambda: w.quantize_act(X, mode, out=(Xq, sx))
+    elif what == "norm_layer":
         gamma = (1 + 0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
         beta = (0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
         fn = lambda: w.norm_quant(X, gamma, beta, 1e-5, w.LAYER_NORM)
