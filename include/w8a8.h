@@ -122,8 +122,10 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * The post-scale entry points (w8a8_gemm_postscale, _s32, _noalloc) need less
  * for few tokens and accept it: with M <= 8 and M * K <= 131072 the GEMM is a
  * GEMV on the CUDA cores that needs no workspace; otherwise, with M <= 128,
- * it streams the int8 codes itself and needs only the partial sums
- * (w8a8_splitk_workspace_size(M,N,K) bytes, possibly 0).
+ * it streams the int8 weight codes itself and needs the fp16 image of Xq
+ * (M * K * 2 bytes, rounded up to 256) and, when N <= 76 * 128 and K > 384
+ * (shapes whose K it may split), int32 sums (M * N * 4 bytes) and counters
+ * (16 bytes per 128 rows of N), each rounded up to 256.
  */
 W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -137,8 +139,9 @@ W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   bytes, 256-byte aligned, owned by the caller, not read after the call's
  *   work completes on `stream`.  Few tokens need less (see
  *   w8a8_gemm_workspace_size): nothing with M <= 8 and M * K <= 131072
- *   (workspace may be NULL and workspace_bytes 0), the K-split partial sums
- *   only with M <= 128; this also holds for w8a8_gemm_postscale_s32.
+ *   (workspace may be NULL and workspace_bytes 0), the fp16 image of Xq plus,
+ *   for shapes whose K may be split, int32 sums and counters with M <= 128;
+ *   this also holds for w8a8_gemm_postscale_s32.
  */
 W8A8_API w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
                                 const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* workspace,
@@ -189,7 +192,9 @@ W8A8_API w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, cons
 /* Device workspace bytes of w8a8_linear_postscale_codes: 0 when M <= 8 and
  * M * K <= 131072 (one kernel, no workspace); otherwise room for the int8
  * codes of X (M * K bytes, rounded up to 256; unused when the caller passes
- * Xq) plus w8a8_gemm_workspace_size(M,N,K). */
+ * Xq) plus what w8a8_gemm_postscale needs for the shape (nothing for the
+ * GEMV, the int8 path's scratch with M <= 128, else
+ * w8a8_gemm_workspace_size(M,N,K)). */
 W8A8_API size_t w8a8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -307,10 +312,10 @@ W8A8_API w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* s
  * array inside the library, so the shape's scratch need must fit in it, else
  * W8A8_ERR_WORKSPACE and nothing is launched.  The need is that of
  * w8a8_gemm_postscale: nothing with M <= 8 and M * K <= 131072 (the
- * few-token GEMV), the K-split partial sums with M <= 128
- * (w8a8_splitk_workspace_size, a few MB at most: for example M = 77,
- * N = 13824, K = 5120 fits), else w8a8_gemm_workspace_size(M,N,K) (for example
- * M = N = K = 4096 fits exactly).
+ * few-token GEMV), the fp16 image of Xq plus any K-split sums with M <= 128
+ * (a few MB: for example M = 77, N = 13824, K = 5120 needs 788 KB), else
+ * w8a8_gemm_workspace_size(M,N,K) (for example M = N = K = 4096 fits
+ * exactly).
  *
  * For callers that cannot allocate device memory at the call site, for
  * example code running inside a host callback or a real-time loop where

@@ -80,12 +80,14 @@ def test_argument_checks_before_device(cdll):
     assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, null, 1 << 20, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, fake, 10, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, P(0x1010), 1 << 20, null) == 7
-    # 9..128 tokens stream the int8 codes: only the split-K partial sums
-    # (77 x 3072 splits K; 77 x 13824 has enough tiles not to)
-    s = L.w8a8_splitk_workspace_size(77, 3072, 5120)
-    assert s > 0 and L.w8a8_splitk_workspace_size(77, 13824, 5120) == 0
+    # 9..128 tokens stream the int8 codes: the fp16 image of Xq, plus int32
+    # sums [M][N] and one counter per 32 weight rows where K may be split
+    # (77 x 3072: 24 weight tiles; 77 x 13824 has 108, too many to split)
+    s = s8_need(77, 3072, 5120)
     assert g(fake, fake, fake, fake, null, fake, 77, 3072, 5120, null, 0, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 77, 3072, 5120, fake, s - 256, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 77, 13824, 5120, fake, s8_need(77, 13824, 5120) - 256, null) == 7
+    assert s8_need(77, 13824, 5120) == _a256(77 * 5120 * 2)
     # blockwise needs its workspace even for one token
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 1, 4, 128, null, 0, null) == 7
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 4, 4, 64, fake, 1 << 20, null) == 3
@@ -163,6 +165,21 @@ def test_noalloc_and_gelu_export_check_arguments_before_device(cdll):
     assert g(odd, 8, fake, null) == 2
 
 
+def _a256(v):
+    return (v + 255) // 256 * 256
+
+
+def s8_need(M, N, K):
+    """Workspace of the GEMM on int8 operands (9..128 tokens): the fp16 image
+    of Xq, and where K may be split (at most 76 tiles of 128 weight rows, at
+    least 4 stages of 128 K) int32 sums [M][N] and 4 counters per tile."""
+    tiles = -(-N // 128)
+    b = _a256(M * K * 2)
+    if tiles <= 76 and -(-K // 128) >= 4:
+        b += _a256(M * N * 4) + _a256(tiles * 16)
+    return b
+
+
 def test_workspace_size(cdll):
     L, _ = cdll
     assert L.w8a8_gemm_workspace_size(0, 5, 16) == 0
@@ -184,10 +201,13 @@ def test_workspace_size(cdll):
     assert L.w8a8_linear_codes_workspace_size(1, 64, 131072) == 0
     assert L.w8a8_linear_codes_workspace_size(3, 5, 16) == 256
     assert L.w8a8_linear_codes_workspace_size(8, 13824, 16384) == 8 * 16384
-    assert (L.w8a8_linear_codes_workspace_size(8, 64, 16400) ==
-            256 * ((8 * 16400 + 255) // 256) + L.w8a8_gemm_workspace_size(8, 64, 16400))
-    assert (L.w8a8_linear_codes_workspace_size(16, 4096, 4096) ==
-            16 * 4096 + L.w8a8_gemm_workspace_size(16, 4096, 4096))
+    assert L.w8a8_linear_codes_workspace_size(8, 64, 16400) == _a256(8 * 16400) + s8_need(8, 64, 16400)
+    assert L.w8a8_linear_codes_workspace_size(16, 4096, 4096) == 16 * 4096 + s8_need(16, 4096, 4096)
+    assert L.w8a8_linear_codes_workspace_size(77, 13824, 5120) == _a256(77 * 5120) + s8_need(77, 13824, 5120)
+    assert L.w8a8_linear_codes_workspace_size(200, 64, 256) == 200 * 256 + L.w8a8_gemm_workspace_size(200, 64, 256)
+    # the public size covers every path, the int8 path's need included
+    for M, N, K in [(128, 4096, 16), (128, 4096, 512), (9, 9728, 512), (128, 128, 131072)]:
+        assert L.w8a8_gemm_workspace_size(M, N, K) >= s8_need(M, N, K)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -267,11 +267,13 @@ def test_gemm_rejects_bad_arguments(w8a8):
         w8a8.gemm_postscale(torch.zeros((200, 32), dtype=torch.int8, device=DEV), torch.ones(200, device=DEV),
                             torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
                             workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
-    # 9..128 tokens stream the int8 codes and need only the K-split partial
-    # sums (none for this shape): a short workspace is fine
-    Y = w8a8.gemm_postscale(torch.ones((16, 32), dtype=torch.int8, device=DEV), torch.ones(16, device=DEV),
-                            torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
-                            workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    # 9..128 tokens stream the int8 codes and need only the fp16 image of Xq
+    # (K too short to split): 16 x 32 x 2 bytes, rounded up to 256
+    args = (torch.ones((16, 32), dtype=torch.int8, device=DEV), torch.ones(16, device=DEV),
+            torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV))
+    with pytest.raises(w8a8.W8A8Error, match="WORKSPACE"):
+        w8a8.gemm_postscale(*args, workspace=torch.empty(768, dtype=torch.uint8, device=DEV))
+    Y = w8a8.gemm_postscale(*args, workspace=torch.empty(1024, dtype=torch.uint8, device=DEV))
     assert torch.all(Y.float() == 32.0)
     # up to 8 tokens the GEMV needs no workspace: a short one is fine
     Y = w8a8.gemm_postscale(torch.ones((8, 32), dtype=torch.int8, device=DEV), torch.ones(8, device=DEV),

@@ -48,6 +48,13 @@ w8a8_status cuda_fail(const char* what, cudaError_t e) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Workspace of the GEMM on bf16 operand images: the images of Xq and Wq and
+// the int32 partial sums of the K splits.
+size_t image_gemm_need(int64_t M, int64_t N, int64_t K) {
+    return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2) +
+           align256(w8a8::splitk_partial_bytes(M, N, K));
+}
+
 // Current device must be compute capability 10.3.
 w8a8_status current_device(DeviceInfo* out) {
     int dev = 0;
@@ -106,13 +113,14 @@ w8a8_status check_k(int64_t K, bool block) {
 }
 
 // Workspace bytes the post-scale GEMM (int8 codes in) uses for this shape:
-// none for the few-token GEMV, the int32 partial sums of the K splits when the
-// GEMM streams the int8 codes itself (M <= 128), else the bf16 images of Xq and
-// Wq plus those partial sums (w8a8_gemm_workspace_size).  M, N, K > 0.
+// none for the few-token GEMV; when the GEMM streams the int8 codes itself
+// (M <= 128), the fp16 image of Xq and, where K may be split, int32 sums and
+// counters; else the bf16 images of Xq and Wq plus the partial sums of the
+// K splits.  M, N, K > 0.
 size_t postscale_gemm_need(int64_t M, int64_t N, int64_t K) {
     if (w8a8::gemv_takes(M, K)) return 0;
-    if (w8a8::gemm_takes_int8(w8a8::kEpiPostscaleBf16, M)) return align256(w8a8::splitk_partial_bytes(M, N, K));
-    return w8a8_gemm_workspace_size(M, N, K);
+    if (w8a8::gemm_takes_int8(w8a8::kEpiPostscaleBf16, M)) return w8a8::s8_workspace_bytes(M, N, K);
+    return image_gemm_need(M, N, K);
 }
 
 // Shared checks of the GEMM entry points.  need_sx/need_sw: scale pointers
@@ -270,11 +278,7 @@ bool linear_codes_fused(int64_t M, int64_t K) { return w8a8::gemv_takes(M, K) &&
 // the GEMM's workspace unless the GEMM is the GEMV.
 size_t linear_codes_workspace(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || linear_codes_fused(M, K)) return 0;
-    size_t b = align256(static_cast<size_t>(M) * K);
-    if (!w8a8::gemv_takes(M, K))
-        b += align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2) +
-             align256(w8a8::splitk_partial_bytes(M, N, K));
-    return b;
+    return align256(static_cast<size_t>(M) * K) + postscale_gemm_need(M, N, K);
 }
 
 // Checks and launches of the fused Linear on int8 weight codes: per-token
@@ -505,8 +509,9 @@ w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* sx, const 
 
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(N) * K * 2) +
-           align256(w8a8::splitk_partial_bytes(M, N, K));
+    const size_t img = image_gemm_need(M, N, K);
+    const size_t s8 = w8a8::gemm_takes_int8(w8a8::kEpiPostscaleBf16, M) ? w8a8::s8_workspace_bytes(M, N, K) : 0;
+    return img > s8 ? img : s8;
 }
 
 w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,

@@ -49,8 +49,9 @@
 //     quantization of the down-projection's input, staged through shared
 //     memory over the next tile's chunk folds (stage_y, gelu_slice);
 //   - few tokens on int8 operands (M <= 128): a single-CTA kernel that
-//     streams int8 weights and codes and widens them to fp16 in shared
-//     memory (gemm_s8_swap_kernel).
+//     streams the int8 weight codes, widens them into tensor memory and
+//     multiplies them with an fp16 image of the tokens (gemm_s8_kernel,
+//     after s8_prep_kernel).
 // Every kernel triggers its dependents' launch at its start and waits on
 // its own prerequisite grid after its prologue (programmatic dependent
 // launch); weights packed before the previous kernel started may be read
@@ -150,6 +151,8 @@ struct KParams {
     int k_split;    // work units per tile, each over split_stages K stages (1: no split)
     int split_stages;
     int32_t* partial;  // k_split > 1: int32 partial sums [k_split][N][M] in kernel dims
+                       // (the int8-operand kernel: one zeroed sum buffer [N][M])
+    int32_t* counters; // the int8-operand kernel with k_split > 1: zeroed arrivals per 32-row group
     float* sg;         // kEpiGeluQuant: block scales [M][N/128]
     int a_settled;     // operand A (resp. B) was complete before the previous kernel in the
     int b_settled;     // stream started, so it may be read before the grid dependency wait
@@ -958,39 +961,69 @@ __global__ void __launch_bounds__(THREADS, 1)
 //               BN rows x 64 K of B) into an int8 ring;
 //   warp 1      TMEM allocation and the MMAs (kind::f16 with fp16 operands;
 //               every int8 value is exact in fp16);
-//   warps 4-7   converters: int8 ring -> fp16 operand ring in the 128-byte
-//               swizzled K-major layout the MMA descriptors read.  A byte b
-//               (two's complement x) becomes fp16 bits 0x6400 | (b ^ 0x80),
-//               i.e. 1024 + x + 128, and subtracting 1152 leaves x exactly;
-//               one byte permute builds two such halves and one packed fp16
-//               subtraction finishes them;
-//   warps 8-11  epilogue, one per TMEM lane quarter, all BN columns each
+//   warps 4-11  converters, two warpgroups taking alternate stages (each
+//               stage is widened by the four warps of one group, so two
+//               stages widen at once): int8 ring -> fp16 operand ring in the
+//               128-byte swizzled K-major layout the MMA descriptors read.  A
+//               byte b (two's complement x) becomes fp16 bits
+//               0x6400 | (b ^ 0x80), i.e. 1024 + x + 128, and subtracting 1152
+//               leaves x exactly; one byte permute builds two such halves and
+//               one packed fp16 subtraction finishes them;
+//   warps 12-15 epilogue, one per TMEM lane quarter, all BN columns each
 //               (chunk folds into int32, then the transposed store or the
 //               split-K partials).
-// Warps 2-3 are idle.  BN <= 128 (M <= 128 tokens).
+// Warps 2-3 are idle.  BN <= 128 (M <= 128 tokens).  One converter group
+// widening every stage was the limit (a stage's 8-32 KB took 490-770
+// clocks with one warp per scheduler); two groups halve that.
+// ---------------------------------------------------------------- few tokens on int8 weight codes
+//
+// gemm_s8_kernel: Y[t][n] for at most 128 tokens, reading each int8 weight
+// code once.  The kernel's rows are weight rows n (128 per tile, one CTA per
+// tile and K split), its columns the tokens (BN >= tokens: one column tile).
+// Each 128-K stage:
+//   - TMA brings the int8 weight tile [128 rows x 128 bytes] and the fp16
+//     image of the tokens [BN rows x 128 K] (two 64-element boxes), both with
+//     the 128-byte swizzle, into one shared-memory slot;
+//   - a converter warpgroup widens the weight tile into tensor memory, one
+//     weight row per thread (64 columns of fp16 pairs, tcgen05.st);
+//   - one thread issues eight tcgen05.mma with A in tensor memory and B in
+//     shared memory; their commit frees the slot and the tensor-memory stage.
+// fp16 holds every int8 value exactly, and within a chunk of eight stages
+// (1024 K, |sum| <= 127 * 127 * 1024 < 2^24) the fp32 accumulation is exact;
+// the epilogue folds each chunk into int32.  With K split, each unit adds its
+// int32 sums into a zeroed buffer with integer atomics (exact in any order)
+// and the warp whose arrival completes a 32-row group writes that group's Y.
+// Two converter warpgroups take alternate stages.
+constexpr int S8_BK = 128;                   // K per stage (bytes of an int8 weight row)
+constexpr int S8_CHUNK_STAGES = 8;           // 1024 K per exact fp32 chunk
+constexpr uint32_t S8_A_BYTES = BM * S8_BK;  // 16 KB
+constexpr int S8_SPLIT_MAX_TILES = 76;       // K splits only when the weight rows make at most this many tiles
+constexpr int S8_SPLIT_MAX = 8;
+
 template <int BN_>
 struct CfgS8 {
     static constexpr int BN = BN_;
-    static_assert(BN == 32 || BN == 64 || BN == 128, "token tile");
-    static constexpr int HALF = BN;                      // accumulator columns per epilogue warp (all of them)
-    static constexpr uint32_t A8_BYTES = BM * BK;        // 8 KB: 128 rows x 64 int8
-    static constexpr uint32_t B8_BYTES = BN * BK;
-    static constexpr uint32_t B16_BYTES = BN * BK * 2;
-    static constexpr int S16 = BN == 32 ? 8 : BN == 64 ? 6 : 4;  // deep: an MMA commit round trip gates each fp16 stage
-    static constexpr uint32_t RING16 = S16 * (A_BYTES + B16_BYTES);
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "token tile");
+    static constexpr uint32_t B_BOX_BYTES = BN * 128;    // BN rows x 64 fp16
+    static constexpr uint32_t B_BYTES = 2 * B_BOX_BYTES;
+    static constexpr uint32_t SLOT = S8_A_BYTES + B_BYTES;
+    static constexpr uint32_t A_TMEM0 = 2 * BN;          // after the two accumulator buffers
+    static constexpr int S16 = int((TMEM_COLS - A_TMEM0) / 64) > 7 ? 7 : int((TMEM_COLS - A_TMEM0) / 64);
+    static_assert(S16 >= 3 && A_TMEM0 + 64 * S16 <= TMEM_COLS, "tensor memory");
+    static constexpr uint32_t SX_BYTES = 512;            // the tile's token scales
     static constexpr uint32_t BAR_BYTES = 512;
-    static constexpr uint32_t RING8_BUDGET = MAX_DYN_SMEM - 1024 - BAR_BYTES - 512 - STAGING_BYTES - RING16;
-    static constexpr int S8 = (RING8_BUDGET / (A8_BYTES + B8_BYTES)) > 12 ? 12
-                                                                          : int(RING8_BUDGET / (A8_BYTES + B8_BYTES));
-    static_assert(S8 >= 2, "int8 ring");
+    static constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - SX_BYTES - BAR_BYTES;
+    static constexpr int S8 = int(RING_BUDGET / SLOT) > 12 ? 12 : int(RING_BUDGET / SLOT);
+    static_assert(S8 >= 3, "ring");
     static_assert(2 * (S8 + S16) + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
-    static constexpr size_t SMEM = 1024 + RING16 + size_t(S8) * (A8_BYTES + B8_BYTES) + STAGING_BYTES + BAR_BYTES;
+    static constexpr size_t SMEM = 1024 + size_t(S8) * SLOT + SX_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
-    static constexpr int LDW = (HALF % 32 == 0) ? 32 : 16;
-    static constexpr int GROUPS = HALF / LDW;
+    static constexpr int LDW = 16;  // tensor-memory loads of 16 columns: the 128 int32 sums stay in registers
+    static constexpr int GROUPS = BN / LDW;
 };
 
-// 16 int8 -> 16 fp16 (exact), as two 16-byte groups.
+// 16 int8 -> 16 fp16 (exact), as two 16-byte groups: the byte b ^ 0x80 goes
+// under the exponent of 1024 (0x64xx is 1024 + (b ^ 0x80)) and 1152 comes off.
 __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& lo, uint4& hi) {
     const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
@@ -1008,24 +1041,65 @@ __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& lo, uint4& h
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// Widen ROWS rows of an int8 tile (64-byte rows) into the fp16 tile (128-byte
-// rows, 16-byte chunk j at position j ^ (row & 7)).  Converter thread t (of
-// 128) owns source chunk c = t % 4 of rows t / 4 + 32 i: each warp's loads
-// cover 8 consecutive rows (512 contiguous bytes), the stores of a
-// quarter-warp land on 8 different bank groups, and every address is a
-// per-thread base plus a constant.
-template <int ROWS>
-__device__ __forceinline__ void widen_tile(const uint8_t* src, uint8_t* dst, int t) {
-    const int c = t & 3, r0 = t >> 2;
-    const uint8_t* s = src + r0 * 64 + c * 16;
-    uint8_t* d = dst + r0 * 128;
-    const int plo = ((2 * c) ^ (r0 & 7)) << 4, phi = ((2 * c + 1) ^ (r0 & 7)) << 4;  // r0 + 32i has the same row & 7
+// Widen weight row r of an int8 stage (128 rows x 128 bytes, as TMA wrote it
+// with the 128-byte swizzle: 16-byte unit c of row r sits at unit c ^ (r & 7))
+// into tensor memory at taddr (this warp's lane quarter, the stage's first
+// column): 64 columns of fp16 pairs, element 2j in the low half of column j,
+// the layout tcgen05.mma reads an A operand from tensor memory in.  The eight
+// threads of a quarter-warp read eight different bank groups.
+__device__ __forceinline__ void widen_row_to_tmem(const uint8_t* stage, int r, uint32_t taddr) {
+    const uint8_t* row = stage + r * S8_BK;
+    const int sw = r & 7;
+    uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < ROWS / 32; ++i) {
-        uint4 lo, hi;
-        s8x16_to_f16(*reinterpret_cast<const uint4*>(s + i * 32 * 64), lo, hi);
-        *reinterpret_cast<uint4*>(d + i * 32 * 128 + plo) = lo;
-        *reinterpret_cast<uint4*>(d + i * 32 * 128 + phi) = hi;
+    for (int c = 0; c < 8; ++c) v[c] = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t o[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint4 lo, hi;
+            s8x16_to_f16(v[4 * h + c], lo, hi);
+            o[8 * c + 0] = lo.x;
+            o[8 * c + 1] = lo.y;
+            o[8 * c + 2] = lo.z;
+            o[8 * c + 3] = lo.w;
+            o[8 * c + 4] = hi.x;
+            o[8 * c + 5] = hi.y;
+            o[8 * c + 6] = hi.z;
+            o[8 * c + 7] = hi.w;
+        }
+        tmem_st_32x32b_x32(taddr + 32 * h, o);
+    }
+}
+
+// Output column n (a weight row) for the BN tokens of the tile:
+// y = ((float(acc) * sx[t]) * sw[n]) + bias[n], the operation order of every
+// other post-scale epilogue, or the int32 sums themselves.  Lanes hold
+// consecutive n, so each token's stores are contiguous.
+template <int EPI, int BN>
+__device__ __forceinline__ void s8_store(const int32_t (&acc)[BN], const KParams& p, int n, const float* sxs,
+                                         float swn, float bn) {
+    if (n >= p.M) return;
+    if constexpr (EPI == kEpiPostscaleS32) {
+        int32_t* out = static_cast<int32_t*>(p.out) + n;
+#pragma unroll
+        for (int t = 0; t < BN; ++t) {
+            if (t < p.N) *out = acc[t];
+            out += p.M;
+        }
+    } else {
+        uint16_t* out = static_cast<uint16_t*>(p.out) + n;
+#pragma unroll
+        for (int t = 0; t < BN; ++t) {
+            if (t < p.N) {
+                float v = __fmul_rn(__fmul_rn(__int2float_rn(acc[t]), sxs[t]), swn);
+                if (p.bias) v = __fadd_rn(v, bn);
+                __nv_bfloat16 h = __float2bfloat16_rn(v);
+                *out = *reinterpret_cast<uint16_t*>(&h);
+            }
+            out += p.M;
+        }
     }
 }
 
@@ -1035,27 +1109,36 @@ enum WaitSiteS8 : int {
     kSiteS8ConvEmpty = 13,
     kSiteS8MmaFull = 14,
     kSiteS8ProducerDrain = 15,
+    kSiteS8MmaSlot = 16,
 };
 
-constexpr int S8_TILE_M = BM;  // weight rows per CTA
+constexpr int S8_CONV_GROUPS = 2;                        // converter warpgroups
+constexpr int S8_EPI_WARP0 = 4 + 4 * S8_CONV_GROUPS;     // first epilogue warp
+constexpr int S8_THREADS = 32 * (S8_EPI_WARP0 + 4);
+// Register split: warpgroup 0 (producer, MMA) 56, converters 80, epilogue 232,
+// within the launch budget of S8_THREADS x 128 (512 threads at 128).
+static_assert(128 * 56 + 128 * S8_CONV_GROUPS * 80 + 128 * 232 <= S8_THREADS * (65536 / S8_THREADS),
+              "int8 kernel register split exceeds the launch budget");
+
+// Work unit u of the int8 kernel: weight tile mb, K stages [ks0, ks1).
+__device__ __forceinline__ void s8_unit(int u, const KParams& p, int& mb, int& ks0, int& ks1) {
+    mb = u / p.k_split;
+    ks0 = (u - mb * p.k_split) * p.split_stages;
+    ks1 = min(p.k_stages, ks0 + p.split_stages);
+}
 
 template <int EPI, int BN>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_s8_swap_kernel(const __grid_constant__ CUtensorMap tmA8, const __grid_constant__ CUtensorMap tmB8,
-                        const __grid_constant__ CUtensorMap tmY, const KParams p) {
+__global__ void __launch_bounds__(S8_THREADS, 1)
+    gemm_s8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const KParams p) {
     grid_launch_dependents();
     using C = CfgS8<BN>;
     constexpr int S8 = C::S8;
     constexpr int S16 = C::S16;
-    constexpr int HALF = C::HALF;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA16 = smem;                          // S16 x 16 KB, 1 KB aligned
-    uint8_t* sB16 = sA16 + S16 * A_BYTES;          // S16 x B16_BYTES
-    uint8_t* sA8 = sB16 + S16 * C::B16_BYTES;      // S8 x 8 KB
-    uint8_t* sB8 = sA8 + S8 * C::A8_BYTES;         // S8 x B8_BYTES
-    uint8_t* staging = sB8 + S8 * C::B8_BYTES;     // 1 KB aligned: all sizes above are multiples of 1 KB
-    uint64_t* full8 = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sxs = reinterpret_cast<float*>(ring + S8 * C::SLOT);
+    uint64_t* full8 = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sxs) + C::SX_BYTES);
     uint64_t* empty8 = full8 + S8;
     uint64_t* full16 = empty8 + S8;
     uint64_t* empty16 = full16 + S16;
@@ -1071,8 +1154,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S8; ++s) {
-            mbar_init(&full8[s], 1);   // the producer's arrive + the tile bytes
-            mbar_init(&empty8[s], 4);  // the four converter warps
+            mbar_init(&full8[s], 1);   // the producer's arrive + the slot's bytes
+            mbar_init(&empty8[s], 1);  // the MMA commit
         }
         for (int t = 0; t < S16; ++t) {
             mbar_init(&full16[t], 4);   // the four converter warps
@@ -1086,8 +1169,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA8);
-        tma_prefetch_desc(&tmB8);
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -1107,11 +1190,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool elected = elect_one_sync();
         int pre = 0;
         if (elected && p.a_settled && cta < p.num_tiles) {
-            const Unit w = unit_coords(cta, p);
-            pre = min(S8, w.ks1 - w.ks0);
+            int mb, ks0, ks1;
+            s8_unit(cta, p, mb, ks0, ks1);
+            pre = min(S8, ks1 - ks0);
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full8[i], C::A8_BYTES + C::B8_BYTES);
-                tma_load_2d(sA8 + i * C::A8_BYTES, &tmA8, &full8[i], (w.ks0 + i) * BK, w.mb * S8_TILE_M);
+                mbar_arrive_expect_tx(&full8[i], C::SLOT);
+                tma_load_2d(ring + i * C::SLOT, &tmA, &full8[i], (ks0 + i) * S8_BK, mb * BM);
             }
         }
         grid_dependency_wait();
@@ -1121,21 +1205,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t armed = 0, armed_phase = 0;
             bool ok = true;
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
-                const Unit w = unit_coords(u, p);
-                const int a_row = w.mb * S8_TILE_M;
-                const int b_row = w.nb * BN;
-                for (int ks = w.ks0; ks < w.ks1; ++ks) {
-                    if (u == cta && ks - w.ks0 < pre) {
-                        tma_load_2d(sB8 + stage * C::B8_BYTES, &tmB8, &full8[stage], ks * BK, b_row);
-                    } else {
+                int mb, ks0, ks1;
+                s8_unit(u, p, mb, ks0, ks1);
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    uint8_t* slot = ring + stage * C::SLOT;
+                    if (!(u == cta && ks - ks0 < pre)) {
                         if (!mbar_wait(&empty8[stage], phase ^ 1u, kSiteS8ProducerEmpty)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full8[stage], C::A8_BYTES + C::B8_BYTES);
-                        tma_load_2d(sA8 + stage * C::A8_BYTES, &tmA8, &full8[stage], ks * BK, a_row);
-                        tma_load_2d(sB8 + stage * C::B8_BYTES, &tmB8, &full8[stage], ks * BK, b_row);
+                        mbar_arrive_expect_tx(&full8[stage], C::SLOT);
+                        tma_load_2d(slot, &tmA, &full8[stage], ks * S8_BK, mb * BM);
                     }
+                    tma_load_2d(slot + S8_A_BYTES, &tmB, &full8[stage], ks * S8_BK, 0);
+                    tma_load_2d(slot + S8_A_BYTES + C::B_BOX_BYTES, &tmB, &full8[stage], ks * S8_BK + 64, 0);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S8) {
@@ -1151,14 +1234,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (elect_one_sync()) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int s8 = 0, t16 = 0;
+            uint32_t ph8 = 0, ph16 = 0;
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
-                const Unit w = unit_coords(u, p);
-                const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
+                int mb, ks0, ks1;
+                s8_unit(u, p, mb, ks0, ks1);
+                const int nchunks = (ks1 - ks0 + S8_CHUNK_STAGES - 1) / S8_CHUNK_STAGES;
                 for (int c = 0; ok && c < nchunks; ++c) {
                     if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteMmaAccEmpty)) {
                         ok = false;
@@ -1166,26 +1250,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                    const int s0 = w.ks0 + c * p.chunk_stages;
-                    const int s1 = min(w.ks1, s0 + p.chunk_stages);
+                    const int s0 = ks0 + c * S8_CHUNK_STAGES;
+                    const int s1 = min(ks1, s0 + S8_CHUNK_STAGES);
                     for (int ks = s0; ks < s1; ++ks) {
-                        if (!mbar_wait(&full16[stage], phase, kSiteS8MmaFull)) {
+                        // the slot's copies (the token image is read from it) and the widened weights
+                        if (!mbar_wait(&full8[s8], ph8, kSiteS8MmaSlot) ||
+                            !mbar_wait(&full16[t16], ph16, kSiteS8MmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(sA16 + stage * A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB16 + stage * C::B16_BYTES);
+                        const uint32_t a_tmem = tmem_base + C::A_TMEM0 + static_cast<uint32_t>(t16 * 64);
+                        const uint32_t b_addr = smem_u32(ring + s8 * C::SLOT + S8_A_BYTES);
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t da = smem_desc_kmajor_sw128(a_addr + k * 32);
-                            const uint64_t db = smem_desc_kmajor_sw128(b_addr + k * 32);
-                            mma_bf16_ss(d_tmem, da, db, C::IDESC, (ks > s0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < S8_BK / 16; ++k) {
+                            const uint64_t db = smem_desc_kmajor_sw128(b_addr + (k >> 2) * C::B_BOX_BYTES + (k & 3) * 32);
+                            mma_f16_ts(d_tmem, a_tmem + k * 8, db, C::IDESC, (ks > s0 || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(&empty16[stage]);
-                        if (++stage == S16) {
-                            stage = 0;
-                            phase ^= 1u;
+                        mma_commit(&empty16[t16]);
+                        mma_commit(&empty8[s8]);
+                        if (++s8 == S8) {
+                            s8 = 0;
+                            ph8 ^= 1u;
+                        }
+                        if (++t16 == S16) {
+                            t16 = 0;
+                            ph16 ^= 1u;
                         }
                     }
                     if (!ok) break;
@@ -1198,28 +1288,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(mma_drain, 0, kSiteMmaDrain);
         }
       }
-    } else if (warp < 8) {
+    } else if (warp < S8_EPI_WARP0) {
         regs_dec<80>();
-        // ------------------------------------------------------------ converters (warps 4-7)
-        const int ct = threadIdx.x - 128;  // 0..127
+        // ------------------------------------------------------------ converters (warps 4..S8_EPI_WARP0-1)
+        const int group = (warp - 4) >> 2;     // converter warpgroup
+        const int r = ((warp & 3) << 5) | lane;  // weight row of the tile = tensor-memory lane
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::A_TMEM0;
         int s8 = 0, t16 = 0;
         uint32_t ph8 = 0, ph16 = 0;
+        int g_stage = 0;                       // stage count of this CTA (all its units)
         bool ok = true;
         for (int u = cta; ok && u < p.num_tiles; u += nctas) {
-            const Unit w = unit_coords(u, p);
-            for (int ks = w.ks0; ks < w.ks1; ++ks) {
-                if (!mbar_wait(&full8[s8], ph8, kSiteS8ConvFull) ||
-                    !mbar_wait(&empty16[t16], ph16 ^ 1u, kSiteS8ConvEmpty)) {
-                    ok = false;
-                    break;
-                }
-                widen_tile<BM>(sA8 + s8 * C::A8_BYTES, sA16 + t16 * A_BYTES, ct);
-                widen_tile<BN>(sB8 + s8 * C::B8_BYTES, sB16 + t16 * C::B16_BYTES, ct);
-                fence_proxy_async_smem();  // the MMA reads these through the async proxy
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&empty8[s8]);
-                    mbar_arrive(&full16[t16]);
+            int mb, ks0, ks1;
+            s8_unit(u, p, mb, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks, ++g_stage) {
+                if (g_stage % S8_CONV_GROUPS == group) {
+                    if (!mbar_wait(&full8[s8], ph8, kSiteS8ConvFull) ||
+                        !mbar_wait(&empty16[t16], ph16 ^ 1u, kSiteS8ConvEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    widen_row_to_tmem(ring + s8 * C::SLOT, r, lane_base + static_cast<uint32_t>(t16 * 64));
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full16[t16]);
                 }
                 if (++s8 == S8) {
                     s8 = 0;
@@ -1233,32 +1327,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         regs_inc<232>();
-        // ------------------------------------------------------------ epilogue (warps 8-11)
+        // ------------------------------------------------------------ epilogue (the last four warps)
         constexpr int LDW = C::LDW;
         constexpr int GROUPS = C::GROUPS;
         const int quarter = warp & 3;
-        const int half = 0;
-        uint8_t* stg = staging + (warp - 8) * OUT_BUFS * STAGE_OUT_BYTES;
-        int sbuf = 0;
+        const int et = static_cast<int>(threadIdx.x) - 32 * S8_EPI_WARP0;  // 0..127
+        if (et < BN) sxs[et] = (EPI == kEpiPostscaleBf16 && et < p.N) ? __ldg(p.sx + et) : 0.0f;
+        named_bar_sync(1, 128);  // the four epilogue warps
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
         for (int u = cta; ok && u < p.num_tiles; u += nctas) {
-            const Unit w = unit_coords(u, p);
-            const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
-            const int row_base = w.mb * S8_TILE_M + quarter * 32;
-            const int col0 = w.nb * BN + half * HALF;
-            int32_t acc[HALF];
+            int mb, ks0, ks1;
+            s8_unit(u, p, mb, ks0, ks1);
+            const int nchunks = (ks1 - ks0 + S8_CHUNK_STAGES - 1) / S8_CHUNK_STAGES;
+            const int n = mb * BM + quarter * 32 + lane;  // output column (weight row)
+            float swn = 0.0f, bn = 0.0f;
+            if (EPI == kEpiPostscaleBf16 && n < p.M) {
+                swn = __ldg(p.sw + n);
+                if (p.bias) bn = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(p.bias) + n));
+            }
+            int32_t acc[BN];
 #pragma unroll
-            for (int e = 0; e < HALF; ++e) acc[e] = 0;
+            for (int e = 0; e < BN; ++e) acc[e] = 0;
             for (int c = 0; c < nchunks; ++c) {
                 if (!mbar_wait(&acc_full[buf], buf_phase, kSiteEpiAccFull)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(buf * BN + half * HALF);
+                const uint32_t taddr =
+                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
                 uint32_t ra[LDW], rb[LDW];
                 tmem_ld_cols<LDW>(taddr, ra);
                 tmem_wait_cols(ra);
@@ -1278,13 +1377,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (buf == 0) buf_phase ^= 1u;
             }
             if (!ok) break;
-            if (p.k_split > 1)
-                store_partial<HALF>(acc, p, row_base, col0, w.split, lane);
-            else
-                store_swapped<EPI, HALF>(acc, p, &tmY, row_base, col0, stg, sbuf, lane);
+            if (p.k_split == 1) {
+                s8_store<EPI, BN>(acc, p, n, sxs, swn, bn);
+            } else {
+                // add this unit's sums; the warp completing the row group writes it
+                if (n < p.M) {
+                    int32_t* dst = p.partial + n;  // [token][weight row]: stepped by one row of sums
+#pragma unroll
+                    for (int t = 0; t < BN; ++t) {
+                        if (t < p.N) atomicAdd(dst, acc[t]);
+                        dst += p.M;
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                int arrived = 0;
+                if (lane == 0) arrived = atomicAdd(p.counters + mb * 4 + quarter, 1);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == p.k_split - 1) {
+                    __threadfence();
+                    if (n < p.M) {
+                        const int32_t* src = p.partial + n;
+#pragma unroll
+                        for (int t = 0; t < BN; ++t) {
+                            if (t < p.N) acc[t] = __ldcg(src);
+                            src += p.M;
+                        }
+                    }
+                    s8_store<EPI, BN>(acc, p, n, sxs, swn, bn);
+                }
+            }
         }
-        if (lane == 0) bulk_wait_group_all();
-        __syncwarp();
     }
 
     tc_fence_before();
@@ -1293,6 +1416,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+}
+
+// First step of the int8-operand GEMM: the fp16 image of the tokens' codes
+// (the MMA's B operand) and, when K is split, zeroed int32 sums and arrival
+// counters.  It lets the GEMM launch at once (the GEMM's prologue and its
+// first weight loads overlap this kernel) and waits for its own predecessor,
+// which may be writing Xq.
+__global__ void __launch_bounds__(256) s8_prep_kernel(const uint4* __restrict__ xq, int64_t n16,
+                                                      uint4* __restrict__ img, uint4* __restrict__ zero,
+                                                      int64_t nz16) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i = i0; i < n16; i += stride) {
+        uint4 lo, hi;
+        s8x16_to_f16(__ldg(xq + i), lo, hi);
+        img[2 * i] = lo;
+        img[2 * i + 1] = hi;
+    }
+    for (int64_t i = i0; i < nz16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Split K, last step: Y[m][n] from the sum of the k_split int32 partials of
@@ -1479,91 +1623,161 @@ cudaError_t launch_swapped(const void* Ximg, const void* Wimg, PFN_cuTensorMapEn
     return launch_one<EPI, 256, true>(Wimg, Ximg, encode, p, num_sms, st, detail, n);
 }
 
-// The int8-operand swapped launch: Ab = Wq [N,K] int8 (kernel rows), Bb =
-// Xq [M,K] int8 (kernel columns); p in kernel dimensions.
-template <int EPI, int BN>
-cudaError_t launch_one_s8(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
-                          int num_sms, cudaStream_t st, char* detail, size_t n) {
-    using C = CfgS8<BN>;
-    auto map8 = [&](CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(rows)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-        cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-        cuuint32_t estr[2] = {1, 1};
-        return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    };
-    CUtensorMap tmA, tmB, tmY;
-    CUresult r = map8(&tmA, Ab, p.M, BM);
-    if (r != CUDA_SUCCESS) {
-        snprintf(detail, n, "cuTensorMapEncodeTiled(A int8: %d x %d) returned %d", p.M, p.K, (int)r);
-        return cudaErrorInvalidValue;
-    }
-    r = map8(&tmB, Bb, p.N, BN);
-    if (r != CUDA_SUCCESS) {
-        snprintf(detail, n, "cuTensorMapEncodeTiled(B int8: %d x %d) returned %d", p.N, p.K, (int)r);
-        return cudaErrorInvalidValue;
-    }
-    tmY = tmA;  // placeholder when the output is not written through TMA
-    p.tma_store = (EPI == kEpiPostscaleBf16 && (p.M % 8) == 0) ? 1 : 0;  // Y is [tokens, p.M]
-    if (p.tma_store) {
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.N)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.M) * 2};
-        cuuint32_t box[2] = {32u, 16u};
-        cuuint32_t estr[2] = {1, 1};
-        r = encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) {
-            snprintf(detail, n, "cuTensorMapEncodeTiled(Y: %d x %d) returned %d", p.N, p.M, (int)r);
-            return cudaErrorInvalidValue;
-        }
-    }
-    p.num_m = (p.M + S8_TILE_M - 1) / S8_TILE_M;
-    p.num_n = (p.N + BN - 1) / BN;
-    p.num_tiles = p.num_m * p.num_n * p.k_split;
+// Int8-operand GEMM plan for a weight matrix of N rows and K columns:
+// weight tiles, 128-K stages, and the K split (1: none).  K is split only
+// when the weight tiles alone leave most SMs idle; the split count comes from
+// the SM count, the need for the split buffers only from the shape.
+struct S8Plan {
+    int num_m, k_stages, k_split, split_stages;
+};
 
+bool s8_split_possible(int64_t N, int64_t K) {
+    return (N + BM - 1) / BM <= S8_SPLIT_MAX_TILES && (K + S8_BK - 1) / S8_BK >= 4;
+}
+
+S8Plan s8_plan(int64_t N, int64_t K, int num_sms) {
+    S8Plan pl;
+    pl.num_m = static_cast<int>((N + BM - 1) / BM);
+    pl.k_stages = static_cast<int>((K + S8_BK - 1) / S8_BK);
+    int s = 1;
+    if (s8_split_possible(N, K)) {
+        s = num_sms / pl.num_m;
+        if (s > S8_SPLIT_MAX) s = S8_SPLIT_MAX;
+        if (s > pl.k_stages / 2) s = pl.k_stages / 2;
+        if (s < 2) s = 1;
+    }
+    pl.split_stages = (pl.k_stages + s - 1) / s;  // no split is left empty
+    pl.k_split = (pl.k_stages + pl.split_stages - 1) / pl.split_stages;
+    return pl;
+}
+
+size_t s8_align(size_t v) { return (v + 255) & ~size_t(255); }
+
+template <int EPI, int BN>
+cudaError_t launch_s8_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const KParams& p, int ctas,
+                         cudaStream_t st) {
+    using C = CfgS8<BN>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     DeviceLaunchInfo& info = g_launch_info[dev];
-    constexpr int id = 20 + (EPI == kEpiPostscaleS32 ? 4 : 0) + (BN == 32 ? 0 : BN == 64 ? 1 : BN == 128 ? 2 : 3);
+    constexpr int id = 20 + (EPI == kEpiPostscaleS32 ? 5 : 0) +
+                       (BN == 16 ? 0 : BN == 32 ? 1 : BN == 64 ? 2 : BN == 96 ? 3 : 4);
     static_assert(id < 32, "instance table");
     if (!info.configured[id]) {
-        e = cudaFuncSetAttribute(gemm_s8_swap_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemm_s8_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::SMEM));
         if (e != cudaSuccess) return e;
         info.configured[id] = true;
     }
-    // persistent: one CTA per SM
-    const int ctas = p.num_tiles < num_sms ? p.num_tiles : num_sms;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(S8_THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_s8_swap_kernel<EPI, BN>, tmA, tmB, tmY, p);
+    return cudaLaunchKernelEx(&cfg, gemm_s8_kernel<EPI, BN>, tmA, tmB, p);
 }
 
+// The GEMM on int8 operands (M <= 128 tokens): s8_prep_kernel, then
+// gemm_s8_kernel with one CTA per work unit (at most one per SM).  a.partial
+// is the scratch of s8_workspace_bytes(M, N, K): the tokens' fp16 image, then
+// (when K may be split) the int32 sums [M][N] and the arrival counters.
 template <int EPI>
-cudaError_t launch_swapped_s8(const void* Xq, const void* Wq, PFN_cuTensorMapEncodeTiled_v12000 encode, KParams p,
-                              int num_sms, cudaStream_t st, char* detail, size_t n) {
-    const int tokens = p.M;
-    p.M = p.N;
-    p.N = tokens;
-    const int settled = p.a_settled;
-    p.a_settled = p.b_settled;
-    p.b_settled = settled;
-    if (tokens <= 32) return launch_one_s8<EPI, 32>(Wq, Xq, encode, p, num_sms, st, detail, n);
-    if (tokens <= 64) return launch_one_s8<EPI, 64>(Wq, Xq, encode, p, num_sms, st, detail, n);
-    return launch_one_s8<EPI, 128>(Wq, Xq, encode, p, num_sms, st, detail, n);
+cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num_sms,
+                      PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t st, char* detail, size_t n) {
+    const int64_t T = a.M, N = a.N, K = a.K;
+    const S8Plan pl = s8_plan(N, K, num_sms);
+    uint8_t* ws = reinterpret_cast<uint8_t*>(a.partial);
+    const size_t img_bytes = s8_align(static_cast<size_t>(T) * K * 2);
+    const size_t sum_bytes = s8_align(static_cast<size_t>(T) * N * 4);
+    const size_t cnt_bytes = s8_align(static_cast<size_t>(pl.num_m) * 16);
+
+    CUtensorMap tmA, tmB;
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+        cuuint32_t box[2] = {static_cast<cuuint32_t>(S8_BK), static_cast<cuuint32_t>(BM)};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            snprintf(detail, n, "cuTensorMapEncodeTiled(weight codes: %lld x %lld) returned %d", (long long)N,
+                     (long long)K, (int)r);
+            return cudaErrorInvalidValue;
+        }
+    }
+    const int bn = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 96 ? 96 : 128;
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(bn)};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            snprintf(detail, n, "cuTensorMapEncodeTiled(token image: %lld x %lld) returned %d", (long long)T,
+                     (long long)K, (int)r);
+            return cudaErrorInvalidValue;
+        }
+    }
+
+    // the token image, and zeroed sums and counters for a split K
+    const int64_t n16 = T * K / 16;
+    const int64_t nz16 = pl.k_split > 1 ? static_cast<int64_t>((sum_bytes + cnt_bytes) / 16) : 0;
+    int64_t grid = ((n16 > nz16 ? n16 : nz16) + 255) / 256;
+    if (grid > static_cast<int64_t>(num_sms) * 4) grid = static_cast<int64_t>(num_sms) * 4;
+    if (grid < 1) grid = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, s8_prep_kernel, static_cast<const uint4*>(Xq), n16,
+                                           reinterpret_cast<uint4*>(ws), reinterpret_cast<uint4*>(ws + img_bytes),
+                                           nz16);
+        if (e != cudaSuccess) return e;
+    }
+
+    KParams p{};
+    p.sx = a.sx;
+    p.sw = a.sw;
+    p.bias = static_cast<const __nv_bfloat16*>(a.bias);
+    p.out = a.out;
+    p.M = static_cast<int>(N);  // kernel rows: weight rows
+    p.N = static_cast<int>(T);  // kernel columns: tokens
+    p.K = static_cast<int>(K);
+    p.num_m = pl.num_m;
+    p.num_n = 1;
+    p.k_stages = pl.k_stages;
+    p.chunk_stages = S8_CHUNK_STAGES;
+    p.k_split = pl.k_split;
+    p.split_stages = pl.split_stages;
+    p.num_tiles = pl.num_m * pl.k_split;
+    p.partial = pl.k_split > 1 ? reinterpret_cast<int32_t*>(ws + img_bytes) : nullptr;
+    p.counters = pl.k_split > 1 ? reinterpret_cast<int32_t*>(ws + img_bytes + sum_bytes) : nullptr;
+    p.a_settled = a.weights_settled ? 1 : 0;
+    p.b_settled = 0;
+    const int ctas = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+    switch (bn) {
+        case 16: return launch_s8_bn<EPI, 16>(tmA, tmB, p, ctas, st);
+        case 32: return launch_s8_bn<EPI, 32>(tmA, tmB, p, ctas, st);
+        case 64: return launch_s8_bn<EPI, 64>(tmA, tmB, p, ctas, st);
+        case 96: return launch_s8_bn<EPI, 96>(tmA, tmB, p, ctas, st);
+        default: return launch_s8_bn<EPI, 128>(tmA, tmB, p, ctas, st);
+    }
 }
 
 template <int EPI>
@@ -1605,6 +1819,13 @@ int splitk_plan(bool blockwise, int64_t M, int64_t N, int64_t K, int* split_stag
     return static_cast<int>((k_stages + per - 1) / per);
 }
 
+size_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    size_t b = s8_align(static_cast<size_t>(M) * K * 2);
+    if (s8_split_possible(N, K))
+        b += s8_align(static_cast<size_t>(M) * N * 4) + s8_align(static_cast<size_t>((N + BM - 1) / BM) * 16);
+    return b;
+}
+
 size_t splitk_partial_bytes(int64_t M, int64_t N, int64_t K) {
     const int s = splitk_plan(false, M, N, K, nullptr);
     return s > 1 ? static_cast<size_t>(s) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4 : 0;
@@ -1618,6 +1839,18 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
         return cudaErrorInvalidValue;
     }
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encode_fn);
+    if (a.int8_operands) {
+        if (!a.partial) {
+            snprintf(detail, n, "int8-operand GEMM without its scratch");
+            return cudaErrorInvalidValue;
+        }
+        const cudaError_t e = epilogue == kEpiPostscaleS32
+                                  ? launch_s8<kEpiPostscaleS32>(Ab, Bb, a, num_sms, encode, st, detail, n)
+                                  : launch_s8<kEpiPostscaleBf16>(Ab, Bb, a, num_sms, encode, st, detail, n);
+        if (e != cudaSuccess && n && detail[0] == 0)
+            snprintf(detail, n, "int8-operand GEMM launch: %s", cudaGetErrorString(e));
+        return e;
+    }
     KParams p;
     p.sx = a.sx;
     p.sw = a.sw;
@@ -1656,16 +1889,12 @@ cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const Gemm
     cudaError_t e;
     switch (epilogue) {
         case kEpiPostscaleBf16:
-            e = (swap && a.int8_operands)
-                    ? launch_swapped_s8<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
-                : swap ? launch_swapped<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
-                       : launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
+            e = swap ? launch_swapped<kEpiPostscaleBf16>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                     : launch_bn<kEpiPostscaleBf16>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
             break;
         case kEpiPostscaleS32:
-            e = (swap && a.int8_operands)
-                    ? launch_swapped_s8<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
-                : swap ? launch_swapped<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
-                       : launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
+            e = swap ? launch_swapped<kEpiPostscaleS32>(Ab, Bb, encode, p, num_sms, st, detail, n)
+                     : launch_bn<kEpiPostscaleS32>(bn, Ab, Bb, encode, p, num_sms, st, detail, n);
             break;
         case kEpiBlockwiseBf16:
             e = launch_one<kEpiBlockwiseBf16, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);

@@ -46,7 +46,8 @@ struct GemmArgs {
     const void* bias;  // bf16 [N] or nullptr
     void* out;         // Y bf16 / acc int32 / acc fp32, [M,N]
     int64_t M, N, K;
-    int32_t* partial;  // split-K partial sums, splitk_partial_bytes(M,N,K) bytes (unused when that is 0)
+    int32_t* partial;  // split-K partial sums, splitk_partial_bytes(M,N,K) bytes (unused when that is 0);
+                       // with int8_operands, the scratch of s8_workspace_bytes(M,N,K) bytes (256-byte aligned)
     float* sg;         // kEpiGeluQuant: 1x128 block scales of the GELU output [M][N/128]
     bool weights_settled;  // Bb was complete before the previous kernel in the stream started
     bool int8_operands;    // Ab / Bb are the int8 codes themselves (gemm_takes_int8 shapes only)
@@ -61,6 +62,10 @@ bool gemm_takes_int8(int epilogue, int64_t M);
 int splitk_plan(bool blockwise, int64_t M, int64_t N, int64_t K, int* split_stages);
 // Bytes of int32 partial sums a post-scale GEMM of this shape needs (0 without split).
 size_t splitk_partial_bytes(int64_t M, int64_t N, int64_t K);
+// Scratch bytes of the GEMM on int8 operands (gemm_takes_int8 shapes): the
+// fp16 image of the tokens' codes and, when the shape may split K, int32 sums
+// [M][N] and arrival counters.
+size_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 // Tensor-core GEMM on the bf16 images (Ab [M,K], Bb [N,K]) of the int8
 // operands.  `encode` is the driver's cuTensorMapEncodeTiled.
