@@ -987,7 +987,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 //   - a converter warpgroup widens the weight tile into tensor memory, one
 //     weight row per thread (64 columns of fp16 pairs, tcgen05.st);
 //   - one thread issues eight tcgen05.mma with A in tensor memory and B in
-//     shared memory; their commit frees the slot and the tensor-memory stage.
+//     shared memory; their commit frees the slot and the tensor-memory stage
+//     of the same index (one ring: the producer's wait for a free slot also
+//     orders the converters' next writes of that tensor-memory stage after
+//     the MMAs that read it).
 // fp16 holds every int8 value exactly, and within a chunk of eight stages
 // (1024 K, |sum| <= 127 * 127 * 1024 < 2^24) the fp32 accumulation is exact;
 // the epilogue folds each chunk into int32.  With K split, each unit adds its
@@ -1008,15 +1011,16 @@ struct CfgS8 {
     static constexpr uint32_t B_BYTES = 2 * B_BOX_BYTES;
     static constexpr uint32_t SLOT = S8_A_BYTES + B_BYTES;
     static constexpr uint32_t A_TMEM0 = 2 * BN;          // after the two accumulator buffers
-    static constexpr int S16 = int((TMEM_COLS - A_TMEM0) / 64) > 7 ? 7 : int((TMEM_COLS - A_TMEM0) / 64);
-    static_assert(S16 >= 3 && A_TMEM0 + 64 * S16 <= TMEM_COLS, "tensor memory");
     static constexpr uint32_t SX_BYTES = 512;            // the tile's token scales
     static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - SX_BYTES - BAR_BYTES;
-    static constexpr int S8 = int(RING_BUDGET / SLOT) > 12 ? 12 : int(RING_BUDGET / SLOT);
-    static_assert(S8 >= 3, "ring");
-    static_assert(2 * (S8 + S16) + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
-    static constexpr size_t SMEM = 1024 + size_t(S8) * SLOT + SX_BYTES + BAR_BYTES;
+    // stages: shared-memory slots and 64-column tensor-memory stages alike
+    static constexpr int S_SMEM = int(RING_BUDGET / SLOT);
+    static constexpr int S_TMEM = int((TMEM_COLS - A_TMEM0) / 64);
+    static constexpr int S = S_SMEM < S_TMEM ? S_SMEM : S_TMEM;
+    static_assert(S >= 3 && A_TMEM0 + 64 * S <= TMEM_COLS, "ring");
+    static_assert(3 * S + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
+    static constexpr size_t SMEM = 1024 + size_t(S) * SLOT + SX_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
     static constexpr int LDW = 16;  // tensor-memory loads of 16 columns: the 128 int32 sums stay in registers
     static constexpr int GROUPS = BN / LDW;
@@ -1089,16 +1093,28 @@ __device__ __forceinline__ void s8_store(const int32_t (&acc)[BN], const KParams
             out += p.M;
         }
     } else {
+        // 16 tokens at a time: the scales are read before any of the group's
+        // stores (the compiler cannot tell shared and global memory apart here)
         uint16_t* out = static_cast<uint16_t*>(p.out) + n;
 #pragma unroll
-        for (int t = 0; t < BN; ++t) {
-            if (t < p.N) {
-                float v = __fmul_rn(__fmul_rn(__int2float_rn(acc[t]), sxs[t]), swn);
+        for (int g = 0; g < BN; g += 16) {
+            if (g >= p.N) break;
+            float sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = sxs[g + e];
+            uint16_t y[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float v = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sv[e]), swn);
                 if (p.bias) v = __fadd_rn(v, bn);
                 __nv_bfloat16 h = __float2bfloat16_rn(v);
-                *out = *reinterpret_cast<uint16_t*>(&h);
+                y[e] = *reinterpret_cast<uint16_t*>(&h);
             }
-            out += p.M;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (g + e < p.N) *out = y[e];
+                out += p.M;
+            }
         }
     }
 }
@@ -1106,10 +1122,8 @@ __device__ __forceinline__ void s8_store(const int32_t (&acc)[BN], const KParams
 enum WaitSiteS8 : int {
     kSiteS8ProducerEmpty = 11,
     kSiteS8ConvFull = 12,
-    kSiteS8ConvEmpty = 13,
     kSiteS8MmaFull = 14,
     kSiteS8ProducerDrain = 15,
-    kSiteS8MmaSlot = 16,
 };
 
 constexpr int S8_CONV_GROUPS = 2;                        // converter warpgroups
@@ -1133,16 +1147,14 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                    const KParams p) {
     grid_launch_dependents();
     using C = CfgS8<BN>;
-    constexpr int S8 = C::S8;
-    constexpr int S16 = C::S16;
+    constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* sxs = reinterpret_cast<float*>(ring + S8 * C::SLOT);
+    float* sxs = reinterpret_cast<float*>(ring + S * C::SLOT);
     uint64_t* full8 = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sxs) + C::SX_BYTES);
-    uint64_t* empty8 = full8 + S8;
-    uint64_t* full16 = empty8 + S8;
-    uint64_t* empty16 = full16 + S16;
-    uint64_t* acc_full = empty16 + S16;
+    uint64_t* full16 = full8 + S;
+    uint64_t* empty = full16 + S;
+    uint64_t* acc_full = empty + S;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* mma_drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
@@ -1153,13 +1165,10 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
     const int nctas = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S8; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full8[s], 1);   // the producer's arrive + the slot's bytes
-            mbar_init(&empty8[s], 1);  // the MMA commit
-        }
-        for (int t = 0; t < S16; ++t) {
-            mbar_init(&full16[t], 4);   // the four converter warps
-            mbar_init(&empty16[t], 1);  // the MMA commit
+            mbar_init(&full16[s], 4);  // the four converter warps of the stage's group
+            mbar_init(&empty[s], 1);   // the MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -1192,7 +1201,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
         if (elected && p.a_settled && cta < p.num_tiles) {
             int mb, ks0, ks1;
             s8_unit(cta, p, mb, ks0, ks1);
-            pre = min(S8, ks1 - ks0);
+            pre = min(S, ks1 - ks0);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full8[i], C::SLOT);
                 tma_load_2d(ring + i * C::SLOT, &tmA, &full8[i], (ks0 + i) * S8_BK, mb * BM);
@@ -1210,7 +1219,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                 for (int ks = ks0; ks < ks1; ++ks) {
                     uint8_t* slot = ring + stage * C::SLOT;
                     if (!(u == cta && ks - ks0 < pre)) {
-                        if (!mbar_wait(&empty8[stage], phase ^ 1u, kSiteS8ProducerEmpty)) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteS8ProducerEmpty)) {
                             ok = false;
                             break;
                         }
@@ -1221,24 +1230,26 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                     tma_load_2d(slot + S8_A_BYTES + C::B_BOX_BYTES, &tmB, &full8[stage], ks * S8_BK + 64, 0);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == S8) {
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             // Every copy issued has landed before this CTA's shared memory is released.
-            for (int s = 0; s < S8; ++s)
+            for (int s = 0; s < S; ++s)
                 if (armed & (1u << s)) mbar_wait(&full8[s], (armed_phase >> s) & 1u, kSiteS8ProducerDrain);
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (elect_one_sync()) {
-            int s8 = 0, t16 = 0;
-            uint32_t ph8 = 0, ph16 = 0;
+            int stage = 0;
+            uint32_t phase = 0;
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
+            // B descriptor of slot 0 (start address in bits 0-13, in 16-byte units)
+            const uint64_t desc0 = smem_desc_kmajor_sw128(smem_u32(ring + S8_A_BYTES));
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
                 int mb, ks0, ks1;
                 s8_unit(u, p, mb, ks0, ks1);
@@ -1253,29 +1264,25 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                     const int s0 = ks0 + c * S8_CHUNK_STAGES;
                     const int s1 = min(ks1, s0 + S8_CHUNK_STAGES);
                     for (int ks = s0; ks < s1; ++ks) {
-                        // the slot's copies (the token image is read from it) and the widened weights
-                        if (!mbar_wait(&full8[s8], ph8, kSiteS8MmaSlot) ||
-                            !mbar_wait(&full16[t16], ph16, kSiteS8MmaFull)) {
+                        // the widened weights; the converters waited for the slot's copies
+                        // (the token image the MMA reads from it) before arriving
+                        if (!mbar_wait(&full16[stage], phase, kSiteS8MmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_tmem = tmem_base + C::A_TMEM0 + static_cast<uint32_t>(t16 * 64);
-                        const uint32_t b_addr = smem_u32(ring + s8 * C::SLOT + S8_A_BYTES);
+                        const uint32_t a_tmem = tmem_base + C::A_TMEM0 + static_cast<uint32_t>(stage * 64);
+                        const uint64_t db = desc0 + static_cast<uint64_t>((stage * C::SLOT) >> 4);
+                        mma_f16_ts(d_tmem, a_tmem, db, C::IDESC, ks > s0 ? 1u : 0u);
 #pragma unroll
-                        for (int k = 0; k < S8_BK / 16; ++k) {
-                            const uint64_t db = smem_desc_kmajor_sw128(b_addr + (k >> 2) * C::B_BOX_BYTES + (k & 3) * 32);
-                            mma_f16_ts(d_tmem, a_tmem + k * 8, db, C::IDESC, (ks > s0 || k > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&empty16[t16]);
-                        mma_commit(&empty8[s8]);
-                        if (++s8 == S8) {
-                            s8 = 0;
-                            ph8 ^= 1u;
-                        }
-                        if (++t16 == S16) {
-                            t16 = 0;
-                            ph16 ^= 1u;
+                        for (int k = 1; k < S8_BK / 16; ++k)
+                            mma_f16_ts(d_tmem, a_tmem + k * 8,
+                                       db + static_cast<uint64_t>(((k >> 2) * C::B_BOX_BYTES + (k & 3) * 32) >> 4),
+                                       C::IDESC, 1u);
+                        mma_commit(&empty[stage]);
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
                     }
                     if (!ok) break;
@@ -1294,8 +1301,8 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
         const int group = (warp - 4) >> 2;     // converter warpgroup
         const int r = ((warp & 3) << 5) | lane;  // weight row of the tile = tensor-memory lane
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::A_TMEM0;
-        int s8 = 0, t16 = 0;
-        uint32_t ph8 = 0, ph16 = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         int g_stage = 0;                       // stage count of this CTA (all its units)
         bool ok = true;
         for (int u = cta; ok && u < p.num_tiles; u += nctas) {
@@ -1303,25 +1310,22 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             s8_unit(u, p, mb, ks0, ks1);
             for (int ks = ks0; ks < ks1; ++ks, ++g_stage) {
                 if (g_stage % S8_CONV_GROUPS == group) {
-                    if (!mbar_wait(&full8[s8], ph8, kSiteS8ConvFull) ||
-                        !mbar_wait(&empty16[t16], ph16 ^ 1u, kSiteS8ConvEmpty)) {
+                    // the slot's copies landed, so the MMAs that last read this
+                    // tensor-memory stage have completed (their commit freed the slot)
+                    if (!mbar_wait(&full8[stage], phase, kSiteS8ConvFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    widen_row_to_tmem(ring + s8 * C::SLOT, r, lane_base + static_cast<uint32_t>(t16 * 64));
+                    widen_row_to_tmem(ring + stage * C::SLOT, r, lane_base + static_cast<uint32_t>(stage * 64));
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full16[t16]);
+                    if (lane == 0) mbar_arrive(&full16[stage]);
                 }
-                if (++s8 == S8) {
-                    s8 = 0;
-                    ph8 ^= 1u;
-                }
-                if (++t16 == S16) {
-                    t16 = 0;
-                    ph16 ^= 1u;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
         }
