@@ -295,9 +295,9 @@ def run_w8a8(args):
     Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(w.linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    # a handful of tokens (what Int8Linear runs for decoding): the fused Linear
-    # on the int8 weight codes, a CUDA-core GEMV bound by the weight stream
-    decode = not blockwise and w.gemv_takes(M, K)
+    # few tokens (what Int8Linear runs for them): the fused Linear on the int8
+    # weight codes, which reads each weight byte once
+    decode = not blockwise and w.codes_preferred(M, N, K)
     w_dev = Wq if decode else Wimg  # the weight operand the step reads
     if decode:
         wsc = torch.empty(max(w.linear_codes_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
@@ -567,8 +567,10 @@ def run_w8a8(args):
         # weight codes + X + Y + scales and bias, each once
         gbytes = N * K + 2 * M * K + 2 * M * N + 4 * N + 4 * M + (2 * N if b is not None else 0)
         gbs = gbytes / (ms_gemm * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "gemv_s8_kernel (dp4a on the CUDA cores)"
-                    + (", per-token quant folded in" if M <= 2 else ""),
+        kern = ("gemv_s8_kernel (dp4a on the CUDA cores)" + (", per-token quant folded in" if M <= 2 else "")
+                if w.gemv_takes(M, K) else
+                "s8_prep_kernel + gemm_s8_kernel (int8 weight codes widened into tensor memory, tcgen05)")
+        roofline = {"bound": "hbm", "kernel": kern,
                     "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
                     "peak_source": f"HBM copy bandwidth, {peaks['source']}",
@@ -704,7 +706,7 @@ def report_configs(args):
         ws = torch.empty(max(w.linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
         Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
         linear = w.linear_blockwise if blockwise else w.linear_postscale
-        decode = not blockwise and w.gemv_takes(M, K)  # a handful of tokens: the GEMV on the weight codes
+        decode = not blockwise and w.codes_preferred(M, N, K)  # few tokens: the Linear on the weight codes
         if decode:
             wsc = torch.empty(max(w.linear_codes_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
             run = lambda: w.linear_postscale_codes(X, Wq, sw, b, out=Y, workspace=wsc, sx_out=sx)
@@ -782,7 +784,8 @@ def report_configs(args):
         gemm_ms = statistics.median(gemms)
         q_ms = statistics.median(quants)
         q_bytes = M * K * 3 + sx.numel() * 4
-        r = dict(workload=work.name, M=M, N=N, K=K, mode=work.mode, path="gemv" if decode else "tcgen05",
+        path = ("gemv on int8 codes" if w.gemv_takes(M, K) else "tcgen05 on int8 codes") if decode else "tcgen05"
+        r = dict(workload=work.name, M=M, N=N, K=K, mode=work.mode, path=path,
                  step_ms=round(step_ms, 4),
                  tops=round(ops / step_ms / 1e9, 1), gemm_tflops=round(ops / gemm_ms / 1e9, 1),
                  gemm_frac_bf16_peak=round(ops / gemm_ms / 1e9 / peaks["bf16_tflops"], 3),

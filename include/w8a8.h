@@ -120,7 +120,7 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * post-scale shapes (M <= 256 with few 256-row weight tiles), the int32
  * partial sums of the K splits.  The same size serves both scale modes.
  * The post-scale entry points (w8a8_gemm_postscale, _s32, _noalloc) need less
- * for few tokens and accept it: with M <= 8 and M * K <= 131072 the GEMM is a
+ * for few tokens and accept it: with M <= 4 and M * K <= 131072 the GEMM is a
  * GEMV on the CUDA cores that needs no workspace; otherwise, with M <= 128,
  * it streams the int8 weight codes itself and needs the fp16 image of Xq
  * (M * K * 2 bytes, rounded up to 256) and, when N <= 76 * 128 and K > 384
@@ -138,7 +138,7 @@ W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   workspace: device buffer of at least w8a8_gemm_workspace_size(M,N,K)
  *   bytes, 256-byte aligned, owned by the caller, not read after the call's
  *   work completes on `stream`.  Few tokens need less (see
- *   w8a8_gemm_workspace_size): nothing with M <= 8 and M * K <= 131072
+ *   w8a8_gemm_workspace_size): nothing with M <= 4 and M * K <= 131072
  *   (workspace may be NULL and workspace_bytes 0), the fp16 image of Xq plus,
  *   for shapes whose K may be split, int32 sums and counters with M <= 128;
  *   this also holds for w8a8_gemm_postscale_s32.
@@ -189,23 +189,24 @@ W8A8_API w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, cons
                                            void* Y, int64_t M, int64_t N, int64_t K, float* sx, int8_t* Xq,
                                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* Device workspace bytes of w8a8_linear_postscale_codes: 0 when M <= 8 and
+/* Device workspace bytes of w8a8_linear_postscale_codes: 0 when M <= 2 and
  * M * K <= 131072 (one kernel, no workspace); otherwise room for the int8
  * codes of X (M * K bytes, rounded up to 256; unused when the caller passes
  * Xq) plus what w8a8_gemm_postscale needs for the shape (nothing for the
- * GEMV, the int8 path's scratch with M <= 128, else
+ * GEMV, M <= 4; the int8 path's scratch with M <= 128; else
  * w8a8_gemm_workspace_size(M,N,K)). */
 W8A8_API size_t w8a8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
  * Fused W8A8 Linear, post-scale, against the int8 weight codes themselves
  * (no bf16 image): per-token quantization of X, then the post-scale GEMM of
- * w8a8_gemm_postscale.  Meant for a handful of tokens (decoding): with
- * M <= 8 and M * K <= 131072 it is one kernel, a GEMV on the CUDA cores in
- * which every CTA quantizes X into its shared memory while its first weight
- * loads are in flight, and each weight code is read once.  Any M is
- * accepted (larger shapes run the quantization kernel and then the GEMM);
- * for many tokens w8a8_linear_postscale on a packed image is faster.
+ * w8a8_gemm_postscale, which reads each weight code once.  Meant for few
+ * tokens (decoding): with M <= 2 and M * K <= 131072 it is one kernel, a
+ * GEMV on the CUDA cores in which every CTA quantizes X into its shared
+ * memory while its first weight loads are in flight; up to 4 tokens the
+ * quantization kernel and the GEMV; up to 128 tokens the quantization kernel
+ * and the int8-operand tensor-core GEMM.  Any M is accepted; for many
+ * tokens w8a8_linear_postscale on a packed image is faster.
  * Results are identical to w8a8_quantize_act (PER_ROW) + w8a8_gemm_postscale
  * on the same inputs.
  *   X [M,K] bf16, Wq [N,K] int8 (w8a8_quantize_weight, PER_ROW), sw [N] fp32,
@@ -311,7 +312,7 @@ W8A8_API w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* s
  * checks, minus the workspace: the scratch lives in a fixed 64 MiB device
  * array inside the library, so the shape's scratch need must fit in it, else
  * W8A8_ERR_WORKSPACE and nothing is launched.  The need is that of
- * w8a8_gemm_postscale: nothing with M <= 8 and M * K <= 131072 (the
+ * w8a8_gemm_postscale: nothing with M <= 4 and M * K <= 131072 (the
  * few-token GEMV), the fp16 image of Xq plus any K-split sums with M <= 128
  * (a few MB: for example M = 77, N = 13824, K = 5120 needs 788 KB), else
  * w8a8_gemm_workspace_size(M,N,K) (for example M = N = K = 4096 fits

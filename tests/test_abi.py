@@ -193,14 +193,15 @@ def test_workspace_size(cdll):
     assert L.w8a8_linear_workspace_size(1, 3072, 5120) == 256 * ((5120 * 2 + 255) // 256) + s
     assert L.w8a8_linear_workspace_size(4096, 4096, 4096) == 4096 * 4096 * 2
     # the fused Linear on codes: nothing for the one-kernel GEMV (M <= 2,
-    # M * K <= 131072), the codes of X before the GEMV (M <= 8), else the codes
+    # M * K <= 131072), the codes of X before the GEMV (M <= 4), else the codes
     # plus the GEMM's workspace
     assert L.w8a8_linear_codes_workspace_size(0, 3072, 5120) == 0
     assert L.w8a8_linear_codes_workspace_size(1, 3072, 5120) == 0
     assert L.w8a8_linear_codes_workspace_size(2, 64, 65536) == 0
     assert L.w8a8_linear_codes_workspace_size(1, 64, 131072) == 0
     assert L.w8a8_linear_codes_workspace_size(3, 5, 16) == 256
-    assert L.w8a8_linear_codes_workspace_size(8, 13824, 16384) == 8 * 16384
+    assert L.w8a8_linear_codes_workspace_size(4, 13824, 32768) == 4 * 32768
+    assert L.w8a8_linear_codes_workspace_size(8, 13824, 16384) == 8 * 16384 + s8_need(8, 13824, 16384)
     assert L.w8a8_linear_codes_workspace_size(8, 64, 16400) == _a256(8 * 16400) + s8_need(8, 64, 16400)
     assert L.w8a8_linear_codes_workspace_size(16, 4096, 4096) == 16 * 4096 + s8_need(16, 4096, 4096)
     assert L.w8a8_linear_codes_workspace_size(77, 13824, 5120) == _a256(77 * 5120) + s8_need(77, 13824, 5120)
@@ -208,6 +209,20 @@ def test_workspace_size(cdll):
     # the public size covers every path, the int8 path's need included
     for M, N, K in [(128, 4096, 16), (128, 4096, 512), (9, 9728, 512), (128, 128, 131072)]:
         assert L.w8a8_gemm_workspace_size(M, N, K) >= s8_need(M, N, K)
+
+
+def test_few_token_routing():
+    """The GEMV takes up to 4 tokens (their codes within 128 KB); the Linear
+    on int8 codes is preferred up to 32 tokens, up to 96 with at least 2^24
+    weights and up to 128 with at least 2^25."""
+    import w8a8_int8_linear_gb300 as w
+    assert w.gemv_takes(4, 5120) and not w.gemv_takes(5, 5120) and not w.gemv_takes(4, 32784)
+    assert w.gemv_takes(1, 131072) and not w.gemv_takes(0, 16)
+    assert w.codes_preferred(1, 3072, 5120) and w.codes_preferred(32, 3072, 5120)
+    assert not w.codes_preferred(33, 3072, 5120) and not w.codes_preferred(77, 3072, 5120)
+    assert w.codes_preferred(77, 5120, 5120) and not w.codes_preferred(97, 5120, 5120)
+    assert not w.codes_preferred(128, 5120, 5120) and w.codes_preferred(128, 13824, 5120)
+    assert not w.codes_preferred(129, 13824, 5120) and not w.codes_preferred(0, 13824, 5120)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -68,6 +68,27 @@ def test_ffn_up_32768x13824x5120(w8a8, oracle):
     run_case(w8a8, oracle, wl.FFN_UP, rows_max=64, cols_max=64)
 
 
+def test_ffn_up_full_row_bands(w8a8, oracle):
+    """Every output of two 128-row bands of the FFN up-projection (an
+    interior band and the last one, each 128 x 13824) from the fused Linear
+    the benchmark times, element by element against the oracle."""
+    work = wl.FFN_UP
+    X = wl.make_x(work, DEV)
+    W = wl.make_w(work, DEV)
+    b = wl.make_bias(work, DEV)
+    Wq, sw = w8a8.quantize_weight(W)
+    Y, sx, _ = w8a8.linear_postscale(X, w8a8.pack_weight(Wq), sw, b)
+    torch.cuda.synchronize()
+    assert w8a8.get_device_error() == (0, 0)
+    Wh, bh = bits(W), bits(b)
+    cols = np.arange(work.N)
+    for r0 in (12800, work.M - 128):
+        Xs = bits(X[r0:r0 + 128])
+        Yo, _ = oracle.linear_sampled(Xs, Wh, bh, np.arange(128), cols, oracle.PER_ROW)
+        d = assert_bf16_close(bits(Y[r0:r0 + 128]), Yo, 1)
+        assert d.max() == 0
+
+
 def test_ffn_down_blockwise_32768x5120x13824(w8a8, oracle):
     run_case(w8a8, oracle, wl.FFN_DOWN, rows_max=48, cols_max=48)
 

@@ -146,14 +146,15 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
-# At most 8 tokens (M * K <= 131072): a CUDA-core GEMV on the int8 codes
+# At most 4 tokens (M * K <= 131072): a CUDA-core GEMV on the int8 codes
 # (dp4a), the activation codes staged in each CTA's shared memory.  Warps own
 # balanced ranges of weight-row groups (1 row for up to 2 tokens, 2 rows for
-# 3..8) and walk each row in steps of 4 x 512 bytes, prefetching the next
+# 3..4) and walk each row in steps of 4 x 512 bytes, prefetching the next
 # step.  The shapes cover every token count, K shorter than one slice, a
 # partial last step, many steps per row, N below one group per warp, odd,
 # and larger than the persistent grid's warp count, the shared-memory limit,
-# and one shape just past it (the int8-operand tensor-core kernel).
+# and shapes past it; 5..8 tokens take the int8-operand tensor-core kernel
+# (its 16-token tile).
 @pytest.mark.parametrize("M,N,K,bias", [
     (1, 1, 16, True),          # one output, one 16-byte slice
     (2, 3, 48, False),
@@ -162,17 +163,18 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     (5, 300, 5120, True),
     (6, 1031, 1040, False),
     (7, 64, 16384, True),      # 16 steps per row
-    (8, 777, 4112, True),      # 8-token accumulators, odd N
+    (8, 777, 4112, True),      # the tensor-core kernel's 16-token tile, odd N
     (1, 3072, 5120, False),    # the decode shape
-    (8, 9999, 256, False),     # more row groups than the grid's warps
-    (8, 300, 16384, True),     # 128 KB of codes: the shared-memory limit
-    (8, 100, 16400, False),    # past it: the tensor-core kernel
+    (4, 9999, 256, False),     # more row groups than the grid's warps
+    (4, 300, 32768, True),     # 128 KB of codes: the shared-memory limit
+    (4, 100, 32784, False),    # past it: the tensor-core kernel
+    (8, 300, 16384, True),
 ])
 def test_gemm_postscale_gemv(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 24, 131072), (8, 40, 16384)])
+@pytest.mark.parametrize("M,N,K", [(1, 24, 131072), (4, 40, 32768)])
 def test_gemv_exactness_at_max_k(w8a8, oracle, M, N, K):
     """All-+-127 codes at the largest K the GEMV takes for this M: at one
     token |acc| reaches 127*127*131072 = 2,114,060,288, just inside int32."""
@@ -275,8 +277,8 @@ def test_gemm_rejects_bad_arguments(w8a8):
         w8a8.gemm_postscale(*args, workspace=torch.empty(768, dtype=torch.uint8, device=DEV))
     Y = w8a8.gemm_postscale(*args, workspace=torch.empty(1024, dtype=torch.uint8, device=DEV))
     assert torch.all(Y.float() == 32.0)
-    # up to 8 tokens the GEMV needs no workspace: a short one is fine
-    Y = w8a8.gemm_postscale(torch.ones((8, 32), dtype=torch.int8, device=DEV), torch.ones(8, device=DEV),
+    # up to 4 tokens the GEMV needs no workspace: a short one is fine
+    Y = w8a8.gemm_postscale(torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
                             torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
                             workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
     assert torch.all(Y.float() == 32.0)
@@ -353,7 +355,7 @@ def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
 
 # The fused Linear on int8 weight codes: one GEMV kernel that quantizes X in
 # every CTA for one or two tokens (M * K <= 131072); the quantization kernel
-# and then the GEMV (weights read before its dependency wait) up to 8 tokens;
+# and then the GEMV (weights read before its dependency wait) up to 4 tokens;
 # else the quantization kernel and the int8-operand tensor-core kernel (up to
 # 128 tokens) or operand images.
 @pytest.mark.parametrize("M,N,K,bias", [(1, 3072, 5120, True), (2, 1000, 4096, False), (2, 7, 16, True),
@@ -446,7 +448,8 @@ def test_int8linear_module(w8a8, oracle, mode):
 
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_int8linear_module_decode(w8a8, oracle, M):
-    """Up to 8 tokens the post-scale module runs the GEMV on the int8 codes."""
+    """With few tokens the post-scale module runs on the int8 codes (the GEMV
+    up to 4 tokens, the int8-operand tensor-core kernel beyond)."""
     from w8a8_int8_linear_gb300.module import Int8Linear
     torch.manual_seed(2)
     lin = torch.nn.Linear(1040, 300, bias=True).to(DEV).to(torch.bfloat16)
@@ -651,12 +654,12 @@ def test_norm_quant_rejects_bad_arguments(w8a8):
 
 def test_int8linear_with_fused_norm(w8a8, oracle):
     """Int8Linear(norm=...) = norm + per-token quant in one pass, then the
-    post-scale GEMM on the code image (on the int8 codes, as a GEMV, for up
-    to 8 tokens), against the oracle composition (with the fixed-order norm
+    post-scale GEMM on the code image (on the int8 codes where that is
+    faster: every shape here), against the oracle composition (with the fixed-order norm
     statement that the kernel matches bit for bit; test_norm_quant checks it
     against the plain definition)."""
     torch.manual_seed(1)
-    for norm, lead in (("rms", (2, 7)), ("layer", (2, 7)), ("rms", (1, 3)), ("layer", (8,))):  # 3, 8: the GEMV
+    for norm, lead in (("rms", (2, 7)), ("layer", (2, 7)), ("rms", (1, 3)), ("layer", (8,))):  # 3: the GEMV; 8, 14: the int8-operand kernel
         T = int(np.prod(lead))
         W = rand_bf16((300, 512), seed=80, scale=0.03)
         b = rand_bf16((300,), seed=81, scale=0.1)

@@ -173,12 +173,29 @@ def _workspace(ws, M, N, K, device):
 
 # Up to this many tokens, with M * K up to GEMV_MAX_CODE_BYTES, the post-scale
 # GEMM is a CUDA-core GEMV on the int8 codes, which needs no workspace.
-GEMV_MAX_TOKENS = 8
+GEMV_MAX_TOKENS = 4
 GEMV_MAX_CODE_BYTES = 131072
+# Up to this many tokens the post-scale GEMM on int8 codes streams the codes
+# itself (the int8-operand tensor-core kernel) instead of bf16 images.
+INT8_OPERAND_MAX_TOKENS = 128
 
 
 def gemv_takes(M, K):
     return 1 <= M <= GEMV_MAX_TOKENS and M * K <= GEMV_MAX_CODE_BYTES
+
+
+def codes_preferred(M, N, K):
+    """Whether a post-scale Linear of M tokens is faster on the int8 weight
+    codes (linear_postscale_codes: the GEMV, or the int8-operand kernel that
+    reads each weight byte once) than on the packed bf16 image.  Measured in
+    steady state on GB300 (K = 5120): the codes win up to 32 tokens at any N,
+    up to 96 tokens once the weights hold 2^24 values, and up to 128 tokens
+    once they hold 2^25; the image wins beyond, where its tensor-core tiles
+    have enough tokens to amortize the 2-byte weight read."""
+    if M < 1 or M > INT8_OPERAND_MAX_TOKENS:
+        return False
+    weights = N * K
+    return gemv_takes(M, K) or M <= 32 or (M <= 96 and weights >= 1 << 24) or weights >= 1 << 25
 
 
 def _postscale_workspace(ws, M, N, K, device):
@@ -331,9 +348,10 @@ def linear_codes_workspace_size(M, N, K):
 
 def linear_postscale_codes(X, Wq, sw, bias=None, out=None, workspace=None, sx_out=None, codes=False):
     """Fused W8A8 Linear, post-scale, against the int8 weight codes (no
-    image): per-token quantization of X, then the post-scale GEMM; with at
-    most 8 tokens (M * K <= 131072) one GEMV kernel that quantizes X itself
-    and reads each weight code once.  Returns (Y, sx, Xq or None);
+    image): per-token quantization of X, then the post-scale GEMM on the
+    codes, which reads each weight code once (one or two tokens: one GEMV
+    kernel that quantizes X itself; up to 4: the GEMV; up to 128: the
+    int8-operand tensor-core kernel).  Returns (Y, sx, Xq or None);
     codes=True also returns Xq."""
     _need(X, torch.bfloat16, "X", 2)
     _need(Wq, torch.int8, "Wq", 2)

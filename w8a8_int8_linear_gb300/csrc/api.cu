@@ -150,7 +150,8 @@ w8a8_status check_gemm(const int8_t* Xq, const float* sx, const int8_t* Wq, cons
 w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float* sx, const float* sw,
                             const void* bias, void* out, int64_t M, int64_t N, int64_t K, void* partial,
                             const DeviceInfo& dev, cudaStream_t st, float* sg = nullptr,
-                            bool weights_settled = false, bool int8_operands = false) {
+                            bool weights_settled = false, bool int8_operands = false,
+                            bool tokens_widened = false) {
     void* enc = encode_fn();
     if (!enc) return W8A8_ERR_CUDA;
     w8a8::GemmArgs a;
@@ -165,6 +166,7 @@ w8a8_status run_gemm_images(int epi, const void* Ab, const void* Bb, const float
     a.sg = sg;
     a.weights_settled = weights_settled;
     a.int8_operands = int8_operands;
+    a.tokens_widened = tokens_widened;
     cudaError_t e;
     if (t_gemm_start && (e = cudaEventRecord(t_gemm_start, st)) != cudaSuccess) return cuda_fail("event", e);
     e = w8a8::launch_gemm(epi, Ab, Bb, a, dev.num_sms, enc, st, t_detail, sizeof t_detail);
@@ -304,7 +306,18 @@ w8a8_status run_linear_codes(const void* X, const int8_t* Wq, const float* sw, c
     if (linear_codes_fused(M, K))
         return run_gemv(w8a8::kEpiPostscaleBf16, X, nullptr, sx, Xq, Wq, sw, bias, Y, M, N, K, false, dev, st);
     int8_t* q = Xq ? Xq : static_cast<int8_t*>(ws);
-    void* rest = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K);
+    uint8_t* rest = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K);
+    if (!w8a8::gemv_takes(M, K) && w8a8::gemm_takes_int8(w8a8::kEpiPostscaleBf16, M) &&
+        w8a8::quant_tokens_f16_takes(K)) {
+        // few tokens on the int8-operand GEMM: the quantization kernel also
+        // writes the GEMM's fp16 token image and zeroes its split-K sums
+        size_t zoff = 0, zbytes = 0;
+        w8a8::s8_scratch_zero(M, N, K, dev.num_sms, &zoff, &zbytes);
+        cudaError_t e = w8a8::launch_quant_tokens_f16(X, M, K, Xq, rest, sx, rest + zoff, zbytes, st);
+        if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
+        return run_gemm_images(w8a8::kEpiPostscaleBf16, Xq, Wq, sx, sw, bias, Y, M, N, K, rest, dev, st, nullptr,
+                               true, true, true);
+    }
     cudaError_t e = w8a8::launch_quant_rows(X, M, K, q, nullptr, sx, dev.num_sms, st);
     if (e != cudaSuccess) return cuda_fail("activation quant launch", e);
     // Wq predates the quantization kernel just launched (which waited for all

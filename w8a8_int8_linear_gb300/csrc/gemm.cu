@@ -952,29 +952,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Few-token post-scale GEMM on int8 operands.  The weights are the large
 // operand of a few-token Linear and the whole cost at these sizes is their
 // read, so this variant streams them as int8 (half the bytes of the 16-bit
-// image) and widens them in shared memory.  Operands as in the swapped
-// launch: A = Wq [N,K] (kernel rows), B = Xq [M,K] (kernel columns, the
-// tokens).  One CTA per SM, no clusters: a CTA owns 128 weight rows (M = 128
-// MMAs), so a tile needs no other CTA and twice as many tiles feed the SMs.
-// Roles:
-//   warp 0      producer: TMA of the int8 tiles (128 rows x 64 K of A and
-//               BN rows x 64 K of B) into an int8 ring;
-//   warp 1      TMEM allocation and the MMAs (kind::f16 with fp16 operands;
-//               every int8 value is exact in fp16);
-//   warps 4-11  converters, two warpgroups taking alternate stages (each
-//               stage is widened by the four warps of one group, so two
-//               stages widen at once): int8 ring -> fp16 operand ring in the
-//               128-byte swizzled K-major layout the MMA descriptors read.  A
-//               byte b (two's complement x) becomes fp16 bits
-//               0x6400 | (b ^ 0x80), i.e. 1024 + x + 128, and subtracting 1152
-//               leaves x exactly; one byte permute builds two such halves and
-//               one packed fp16 subtraction finishes them;
+// image).  One CTA per SM, no clusters: a CTA owns 128 weight rows (M = 128
+// MMAs, cta_group::1), so a tile needs no other CTA and twice as many tiles
+// feed the SMs.
+// Roles (512 threads):
+//   warp 0      producer: TMA of the slot's int8 weight tile and token image;
+//   warp 1      TMEM allocation and the MMAs (kind::f16, fp16 operands);
+//   warps 2-3   idle;
+//   warps 4-11  converters, two warpgroups taking alternate stages.  A byte b
+//               (two's complement x) becomes fp16 bits 0x6400 | (b ^ 0x80),
+//               i.e. 1024 + x + 128, and subtracting 1152 leaves x exactly;
+//               one byte permute builds two such halves and one packed fp16
+//               subtraction finishes them;
 //   warps 12-15 epilogue, one per TMEM lane quarter, all BN columns each
-//               (chunk folds into int32, then the transposed store or the
-//               split-K partials).
-// Warps 2-3 are idle.  BN <= 128 (M <= 128 tokens).  One converter group
-// widening every stage was the limit (a stage's 8-32 KB took 490-770
-// clocks with one warp per scheduler); two groups halve that.
+//               (chunk folds into int32, then Y or the split-K sums).
+// A weight stage widened in shared memory for the MMA to read costs three
+// shared-memory passes of its 16-bit form; written to tensor memory it costs
+// none, and the tokens, widened once by s8_prep_kernel, arrive by TMA.
 // ---------------------------------------------------------------- few tokens on int8 weight codes
 //
 // gemm_s8_kernel: Y[t][n] for at most 128 tokens, reading each int8 weight
@@ -1102,17 +1096,21 @@ __device__ __forceinline__ void s8_store(const int32_t (&acc)[BN], const KParams
             float sv[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) sv[e] = sxs[g + e];
-            uint16_t y[16];
+            uint32_t y[8];  // two tokens' bf16 per register: one paired conversion
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                float v = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sv[e]), swn);
-                if (p.bias) v = __fadd_rn(v, bn);
-                __nv_bfloat16 h = __float2bfloat16_rn(v);
-                y[e] = *reinterpret_cast<uint16_t*>(&h);
+            for (int e = 0; e < 16; e += 2) {
+                float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sv[e]), swn);
+                float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e + 1]), sv[e + 1]), swn);
+                if (p.bias) {
+                    v0 = __fadd_rn(v0, bn);
+                    v1 = __fadd_rn(v1, bn);
+                }
+                __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+                y[e / 2] = *reinterpret_cast<uint32_t*>(&h);
             }
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                if (g + e < p.N) *out = y[e];
+                if (g + e < p.N) *out = static_cast<uint16_t>(y[e / 2] >> (16 * (e & 1)));
                 out += p.M;
             }
         }
@@ -1733,13 +1731,14 @@ cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num
         }
     }
 
-    // the token image, and zeroed sums and counters for a split K
-    const int64_t n16 = T * K / 16;
+    // the token image, and zeroed sums and counters for a split K (unless the
+    // kernel before this one wrote them)
+    const int64_t n16 = a.tokens_widened ? 0 : T * K / 16;
     const int64_t nz16 = pl.k_split > 1 ? static_cast<int64_t>((sum_bytes + cnt_bytes) / 16) : 0;
     int64_t grid = ((n16 > nz16 ? n16 : nz16) + 255) / 256;
     if (grid > static_cast<int64_t>(num_sms) * 4) grid = static_cast<int64_t>(num_sms) * 4;
     if (grid < 1) grid = 1;
-    {
+    if (!a.tokens_widened) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1821,6 +1820,13 @@ int splitk_plan(bool blockwise, int64_t M, int64_t N, int64_t K, int* split_stag
     const int64_t per = (k_stages + s - 1) / s;  // stages per split; no split is left empty
     if (split_stages) *split_stages = static_cast<int>(per);
     return static_cast<int>((k_stages + per - 1) / per);
+}
+
+void s8_scratch_zero(int64_t M, int64_t N, int64_t K, int num_sms, size_t* offset, size_t* bytes) {
+    const S8Plan pl = s8_plan(N, K, num_sms);
+    *offset = s8_align(static_cast<size_t>(M) * K * 2);
+    *bytes = pl.k_split > 1 ? s8_align(static_cast<size_t>(M) * N * 4) + s8_align(static_cast<size_t>(pl.num_m) * 16)
+                            : 0;
 }
 
 size_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K) {

@@ -3,7 +3,7 @@
 // With a handful of tokens the post-scale Linear ("Differences From
 // TurboDiffusion": INT8 accumulation continuous over K, activation and weight
 // scales applied in the epilogue) is a stream of the weight codes, each byte
-// used M <= 8 times: no contraction dense enough for a tensor-core tile.  This
+// used M <= 4 times: no contraction dense enough for a tensor-core tile.  This
 // kernel streams the int8 codes once and forms the dot products with dp4a
 // (four int8 products summed into an int32).  The int32 sums are exact in any
 // order: |acc| <= 127 * 127 * K < 2^31 for K <= 131072.
@@ -241,9 +241,9 @@ template <int MT, int EPI, bool QUANT>
 cudaError_t launch_mt(const GemvParams& p, int num_sms, cudaStream_t st) {
     constexpr int R = MT <= 2 ? 1 : 2;  // rows sharing each activation read
     constexpr int U = 4 / R;            // 4 x 16 bytes of weights per lane and step
-    // CTAs per SM: 4 (64 registers) unless the accumulators, or the staging's
-    // scales next to the first weight loads, need more
-    constexpr int MINB = (MT >= 8 || (QUANT && MT >= 2)) ? 3 : 4;
+    // CTAs per SM: 4 (64 registers) unless the staging's scales next to the
+    // first weight loads need more
+    constexpr int MINB = (QUANT && MT >= 2) ? 3 : 4;
     static_assert(!QUANT || MT <= kGemvFusedMaxTokens, "the fused quantization is built for few tokens");
     static_assert(R * MT <= 32, "one writing lane per output of a group");
     auto kern = gemv_s8_kernel<MT, R, U, MINB, EPI, QUANT>;
@@ -279,8 +279,7 @@ cudaError_t launch_tokens(const GemvParams& p, int num_sms, cudaStream_t st) {
         return launch_mt<2, EPI, QUANT>(p, num_sms, st);
     } else {
         if (p.M <= 2) return launch_mt<2, EPI, QUANT>(p, num_sms, st);
-        if (p.M <= 4) return launch_mt<4, EPI, QUANT>(p, num_sms, st);
-        return launch_mt<8, EPI, QUANT>(p, num_sms, st);
+        return launch_mt<4, EPI, QUANT>(p, num_sms, st);
     }
 }
 

@@ -7,8 +7,9 @@
 
 namespace w8a8 {
 
-// Token counts up to this take the CUDA-core GEMV instead of the tensor cores,
-constexpr int64_t kGemvMaxTokens = 8;
+// Token counts up to this take the CUDA-core GEMV instead of the tensor cores
+// (from 5 tokens on, the int8-operand tensor-core kernel is faster),
+constexpr int64_t kGemvMaxTokens = 4;
 // ... when the M x K activation codes fit in one CTA's shared memory.
 constexpr int64_t kGemvMaxCodeBytes = 131072;
 

@@ -22,6 +22,15 @@ cudaError_t launch_quant_weight_block(const void* W, int64_t N, int64_t K, int8_
 // Exact int8 -> bf16 image of n values (n % 16 == 0).
 cudaError_t launch_expand_s8_bf16(const int8_t* src, int64_t n, void* dst, int num_sms, cudaStream_t st);
 
+// Per-token quantization of X [M,K] bf16 for the few-token GEMM on int8
+// weight codes: scales sx [M], codes Xq [M,K] (may be null), the fp16 image
+// of the codes img16 [M,K] (the GEMM's token operand, in the GEMM's scratch),
+// and zero_bytes (a multiple of 16) of zeros at zero (the GEMM's split-K sums
+// and counters).  For K <= 16384 (quant_tokens_f16_takes).
+bool quant_tokens_f16_takes(int64_t K);
+cudaError_t launch_quant_tokens_f16(const void* X, int64_t M, int64_t K, int8_t* Xq, void* img16, float* sx,
+                                    void* zero, size_t zero_bytes, cudaStream_t st);
+
 // Test export of the FFN up-projection's activation: G[i] = bf16(gelu(Y[i]))
 // for n bf16 values (n % 8 == 0), with the GEMM epilogue's device function.
 cudaError_t launch_gelu_bf16(const void* Y, int64_t n, void* G, int num_sms, cudaStream_t st);
@@ -51,6 +60,9 @@ struct GemmArgs {
     float* sg;         // kEpiGeluQuant: 1x128 block scales of the GELU output [M][N/128]
     bool weights_settled;  // Bb was complete before the previous kernel in the stream started
     bool int8_operands;    // Ab / Bb are the int8 codes themselves (gemm_takes_int8 shapes only)
+    bool tokens_widened;   // int8_operands: the scratch already holds the tokens' fp16 image and
+                           // zeroed split-K sums and counters (s8_scratch_zero), written by the
+                           // kernel just before this one
 };
 
 // Whether launch_gemm takes int8 codes directly (instead of bf16 images) for
@@ -66,6 +78,9 @@ size_t splitk_partial_bytes(int64_t M, int64_t N, int64_t K);
 // fp16 image of the tokens' codes and, when the shape may split K, int32 sums
 // [M][N] and arrival counters.
 size_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// The part of that scratch a launch on num_sms SMs needs zeroed (its split-K
+// sums and counters): bytes from offset, 0 bytes when K is not split.
+void s8_scratch_zero(int64_t M, int64_t N, int64_t K, int num_sms, size_t* offset, size_t* bytes);
 
 // Tensor-core GEMM on the bf16 images (Ab [M,K], Bb [N,K]) of the int8
 // operands.  `encode` is the driver's cuTensorMapEncodeTiled.

@@ -34,6 +34,7 @@
 // bound needs a normal s; a group whose scale is subnormal takes the exact
 // path for every element, which clamps.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -138,6 +139,69 @@ __global__ void __launch_bounds__(T, MINB) quant_rows_reg_kernel(const uint4* __
     for (int i = 0; i < CPT; ++i) {
         const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
         if (c < chunks) emit_chunk<OUT>(Aq, img, row * chunks + c, v[i], sc);
+    }
+}
+
+// 8 int8 codes -> their 8 exact fp16 values: the byte b ^ 0x80 under the
+// exponent of 1024 (0x64xx is 1024 + (b ^ 0x80)), less 1152.
+__device__ __forceinline__ uint4 s8x8_to_f16x8(uint2 c) {
+    const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const uint32_t w0 = c.x ^ 0x80808080u, w1 = c.y ^ 0x80808080u;
+    uint32_t p[4] = {__byte_perm(w0, 0x64646464u, 0x4140), __byte_perm(w0, 0x64646464u, 0x4342),
+                     __byte_perm(w1, 0x64646464u, 0x4140), __byte_perm(w1, 0x64646464u, 0x4342)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&p[i]), k1152);
+        p[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+// Per-token quantization feeding the few-token GEMM on int8 weight codes: one
+// CTA per row (kept in registers, as quant_rows_reg_kernel) writes the row's
+// scale, its codes when Aq is given, and the fp16 image of its codes (the
+// GEMM's token operand), and zeroes its share of the GEMM's split-K sums and
+// counters (nz16 16-byte words at zero).
+template <int CPT, int T>
+__global__ void __launch_bounds__(T) quant_tokens_f16_kernel(const uint4* __restrict__ A, int64_t R, int64_t K,
+                                                             uint2* __restrict__ Aq, uint4* __restrict__ img16,
+                                                             float* __restrict__ s, uint4* __restrict__ zero,
+                                                             int64_t nz16) {
+    grid_launch_dependents();
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    if (row >= R) return;
+    {
+        const int64_t per = (nz16 + R - 1) / R;
+        const int64_t z0 = row * per;
+        const int64_t z1 = z0 + per < nz16 ? z0 + per : nz16;
+        for (int64_t i = z0 + threadIdx.x; i < z1; i += T) zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int64_t chunks = K >> 3;
+    const uint4* a = A + row * chunks;
+    uint4 v[CPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
+        if (c < chunks) v[i] = __ldcs(a + c);
+    }
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
+        if (c < chunks) amax = fmaxf(amax, chunk_absmax(v[i]));
+    }
+    amax = block_max(amax, red);
+    const RowScale sc = make_scale_div(amax);
+    if (threadIdx.x == 0) s[row] = sc.s;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * T;
+        if (c < chunks) {
+            const uint2 code = quant_chunk(v[i], sc);
+            if (Aq) __stcs(Aq + row * chunks + c, code);
+            img16[row * chunks + c] = s8x8_to_f16x8(code);
+        }
     }
 }
 
@@ -355,6 +419,31 @@ cudaError_t launch_quant_rows(const void* A, int64_t R, int64_t K, int8_t* Aq, v
         quant_rows_warp2_kernel<8><<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(a, R, K, q, im, s);
     else
         quant_rows_2pass_kernel<<<grid, 256, 0, st>>>(a, R, K, q, im, s);
+    return cudaGetLastError();
+}
+
+bool quant_tokens_f16_takes(int64_t K) { return (K >> 3) <= 2048; }
+
+cudaError_t launch_quant_tokens_f16(const void* X, int64_t M, int64_t K, int8_t* Xq, void* img16, float* sx,
+                                    void* zero, size_t zero_bytes, cudaStream_t st) {
+    const int64_t chunks = K >> 3;
+    if (chunks > 2048) return cudaErrorInvalidValue;
+    const uint4* a = static_cast<const uint4*>(X);
+    uint2* q = reinterpret_cast<uint2*>(Xq);
+    uint4* im = static_cast<uint4*>(img16);
+    uint4* z = static_cast<uint4*>(zero);
+    const int64_t nz16 = static_cast<int64_t>(zero_bytes / 16);
+    const dim3 grid(static_cast<unsigned>(M));
+    if (chunks <= 128)
+        quant_tokens_f16_kernel<1, 128><<<grid, 128, 0, st>>>(a, M, K, q, im, sx, z, nz16);
+    else if (chunks <= 256)
+        quant_tokens_f16_kernel<2, 128><<<grid, 128, 0, st>>>(a, M, K, q, im, sx, z, nz16);
+    else if (chunks <= 512)
+        quant_tokens_f16_kernel<4, 128><<<grid, 128, 0, st>>>(a, M, K, q, im, sx, z, nz16);
+    else if (chunks <= 1024)
+        quant_tokens_f16_kernel<4, 256><<<grid, 256, 0, st>>>(a, M, K, q, im, sx, z, nz16);
+    else
+        quant_tokens_f16_kernel<8, 256><<<grid, 256, 0, st>>>(a, M, K, q, im, sx, z, nz16);
     return cudaGetLastError();
 }
 

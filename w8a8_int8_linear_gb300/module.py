@@ -7,14 +7,15 @@ initialization, activations quantized dynamically before every Linear.  This
 module does exactly that through the library: the weight is quantized and its
 exact bf16 image packed once (`from_linear` / `__init__`), and every forward
 is one fused call (per-token or 1x128 quantization plus the INT8 GEMM).  With
-at most 8 tokens (decoding) a post-scale forward runs against the int8 codes
-instead of the image: a GEMV that reads each weight byte once.  It keeps no
+few tokens (decoding, and up to 128 tokens where that is faster:
+`codes_preferred`) a post-scale forward runs against the int8 codes instead of
+the image, reading each weight byte once.  It keeps no
 bf16 copy of the original weight and has no fallback path: every shape runs
 the INT8 kernels.
 """
 import torch
 
-from . import BLOCK, GEMV_MAX_TOKENS, LAYER_NORM, PER_ROW, RMS_NORM, gemm_blockwise_images, gemm_postscale, \
+from . import BLOCK, LAYER_NORM, PER_ROW, RMS_NORM, codes_preferred, gemm_blockwise_images, gemm_postscale, \
     gemm_postscale_images, linear_blockwise, linear_codes_workspace_size, linear_postscale, \
     linear_postscale_codes, linear_postscale_gelu_quant, linear_workspace_size, norm_quant, pack_weight, \
     quantize_weight
@@ -72,7 +73,7 @@ class Int8Linear(torch.nn.Module):
         lead = x.shape[:-1]
         x2 = x.reshape(-1, self.in_features).contiguous()
         M = x2.shape[0]
-        decode = self.mode == "postscale" and 0 < M <= GEMV_MAX_TOKENS
+        decode = self.mode == "postscale" and codes_preferred(M, self.out_features, self.in_features)
         if self.norm is not None:
             kind = RMS_NORM if self.norm == "rms" else LAYER_NORM
             if decode:
