@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libw8a8_gb300.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemv.cu", "norm.cu", "imma_peak.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_s8.cu", "gemv.cu", "norm.cu", "imma_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-fmad=false", "-prec-div=true", "-prec-sqrt=true", "-ftz=false", "--expt-relaxed-constexpr"]

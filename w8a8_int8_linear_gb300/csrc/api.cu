@@ -617,9 +617,11 @@ w8a8_status w8a8_get_device_error(int* code) {
         cudaGetLastError();
         return W8A8_ERR_CUDA;
     }
-    unsigned int v = 0, vq = 0;
+    unsigned int v = 0, vs = 0, vq = 0;
     if (w8a8::gemm_read_device_error(&v) != cudaSuccess) return W8A8_ERR_CUDA;
+    if (w8a8::gemm_s8_read_device_error(&vs) != cudaSuccess) return W8A8_ERR_CUDA;
     if (w8a8::quant_read_device_error(&vq) != cudaSuccess) return W8A8_ERR_CUDA;
+    if (v == 0) v = vs;
     if (v == 0) v = vq;
     *code = static_cast<int>(v);
     if (v >= w8a8::kDeviceErrorTimeoutBase) return W8A8_ERR_TIMEOUT;

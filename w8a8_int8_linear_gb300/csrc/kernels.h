@@ -88,12 +88,19 @@ void s8_scratch_zero(int64_t M, int64_t N, int64_t K, int num_sms, size_t* offse
 cudaError_t launch_gemm(int epilogue, const void* Ab, const void* Bb, const GemmArgs& args, int num_sms,
                         void* encode_fn, cudaStream_t st, char* detail, size_t n);
 
+// The int8-operand GEMM (gemm_s8.cu) that launch_gemm routes
+// args.int8_operands calls to: Xq [M,K] and Wq [N,K] int8 codes, post-scale
+// epilogues only, args.partial its scratch of s8_workspace_bytes(M,N,K).
+cudaError_t launch_gemm_s8(int epilogue, const void* Xq, const void* Wq, const GemmArgs& args, int num_sms,
+                           void* encode_fn, cudaStream_t st, char* detail, size_t n);
+
 // Device error codes at or above this value mean a bounded wait ran out.
 constexpr unsigned int kDeviceErrorTimeoutBase = 0x100;
 
 // Read and clear the device error words of the GEMM and quantization
 // translation units.
 cudaError_t gemm_read_device_error(unsigned int* code);
+cudaError_t gemm_s8_read_device_error(unsigned int* code);
 // One CTA whose bounded mbarrier wait runs out (nothing arrives): records a
 // timeout in the GEMM translation unit's device error word and returns.
 cudaError_t launch_wait_timeout_probe(cudaStream_t st);
