@@ -213,14 +213,13 @@ def test_workspace_size(cdll):
 
 def test_few_token_routing():
     """The GEMV takes up to 4 tokens (their codes within 128 KB); the Linear
-    on int8 codes is preferred up to 32 tokens, up to 96 with at least 2^24
-    weights and up to 128 with at least 2^25."""
+    on int8 codes is preferred up to 96 tokens, and up to 128 with at least
+    2^25 weights."""
     import w8a8_int8_linear_gb300 as w
     assert w.gemv_takes(4, 5120) and not w.gemv_takes(5, 5120) and not w.gemv_takes(4, 32784)
     assert w.gemv_takes(1, 131072) and not w.gemv_takes(0, 16)
-    assert w.codes_preferred(1, 3072, 5120) and w.codes_preferred(32, 3072, 5120)
-    assert not w.codes_preferred(33, 3072, 5120) and not w.codes_preferred(77, 3072, 5120)
-    assert w.codes_preferred(77, 5120, 5120) and not w.codes_preferred(97, 5120, 5120)
+    assert w.codes_preferred(1, 3072, 5120) and w.codes_preferred(77, 3072, 5120)
+    assert w.codes_preferred(96, 5120, 5120) and not w.codes_preferred(97, 5120, 5120)
     assert not w.codes_preferred(128, 5120, 5120) and w.codes_preferred(128, 13824, 5120)
     assert not w.codes_preferred(129, 13824, 5120) and not w.codes_preferred(0, 13824, 5120)
 

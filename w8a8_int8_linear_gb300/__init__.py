@@ -188,14 +188,12 @@ def codes_preferred(M, N, K):
     """Whether a post-scale Linear of M tokens is faster on the int8 weight
     codes (linear_postscale_codes: the GEMV, or the int8-operand kernel that
     reads each weight byte once) than on the packed bf16 image.  Measured in
-    steady state on GB300 (K = 5120): the codes win up to 32 tokens at any N,
-    up to 96 tokens once the weights hold 2^24 values, and up to 128 tokens
-    once they hold 2^25; the image wins beyond, where its tensor-core tiles
-    have enough tokens to amortize the 2-byte weight read."""
+    steady state on GB300 (K = 5120, N = 3072 / 5120 / 13824): the codes win
+    up to 96 tokens at every N, and up to 128 once the weights hold 2^25
+    values; beyond 128 tokens the image path runs."""
     if M < 1 or M > INT8_OPERAND_MAX_TOKENS:
         return False
-    weights = N * K
-    return gemv_takes(M, K) or M <= 32 or (M <= 96 and weights >= 1 << 24) or weights >= 1 << 25
+    return gemv_takes(M, K) or M <= 96 or N * K >= 1 << 25
 
 
 def _postscale_workspace(ws, M, N, K, device):
