@@ -125,10 +125,12 @@ def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
-# Few tokens (M <= 256): the weights take the 256-row side of the MMA and the
-# tokens its narrow side (32 / 64 / 128 / 256), and Y is written transposed.
-# With few 256-row weight tiles, K is split and the int32 partials summed in
-# a second kernel (S = number of splits).
+# Few tokens on int8 codes (gemm_postscale): 5..128 tokens run the
+# int8-operand kernel (gemm_s8.cu: 128-row weight tiles, 16..128-token tiles,
+# K split with exact int32 atomics when the weight tiles are few), 129..256
+# the swapped tensor-core kernel on images (weights on the 256-row side,
+# tokens on the narrow side, Y written transposed, K split into int32
+# partials summed by a second kernel).
 @pytest.mark.parametrize("M,N,K,bias", [
     (1, 4096, 4096, True),     # one token: 32-token tiles, S = 4
     (16, 24, 128, False),      # fewer output columns than one store box, S = 1
@@ -143,6 +145,22 @@ def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
     (3, 10000, 256, False),    # 40 weight tiles, no split, ragged last tile
 ])
 def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
+    check_postscale(w8a8, oracle, M, N, K, bias)
+
+
+# The int8-operand kernel at its boundaries: every token tile (16, 32, 64, 96,
+# 128), both sides of the split rule (at most 76 weight tiles and 4 stages),
+# a last 128-K stage of 16 K (zero-filled past K), and a last weight tile of
+# one row.
+@pytest.mark.parametrize("M,N,K,bias", [
+    (5, 300, 5120, True),      # 16-token tile, 3 weight tiles: K split 8 ways
+    (17, 1000, 1040, False),   # 32-token tile, 9 stages (the last 16 K): split 3 ways
+    (96, 9728, 640, True),     # 96-token tile, 76 weight tiles: split 2 ways
+    (97, 9856, 512, False),    # 128-token tile, 77 weight tiles: no split
+    (64, 129, 16400, True),    # a last weight tile of one row, 129 stages, split 8 ways
+    (128, 2048, 384, False),   # 3 stages: too few to split
+])
+def test_gemm_postscale_int8_operands(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
@@ -209,7 +227,7 @@ def check_postscale(w8a8, oracle, M, N, K, bias):
     assert w8a8.get_device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("M", [130, 520])  # swapped operands / the regular tiles
+@pytest.mark.parametrize("M", [16, 77, 130, 520])  # int8-operand kernel (K split 8 ways) / swapped / regular
 def test_gemm_exactness_adversary(w8a8, oracle, M):
     """All-+-127 operands at K = 13824: per-chunk partial sums reach
     127*127*1024 and the total 2.2e8, far past fp32's 2^24 integer range."""
@@ -362,6 +380,7 @@ def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
                                         (3, 520, 1040, False), (8, 4096, 4096, True),
                                         (5, 1000, 16, True), (8, 520, 16384, False), (1, 300, 131072, True),
                                         (2, 300, 131072, False), (9, 600, 2048, True), (77, 3072, 5120, False),
+                                        (6, 100, 32768, True),
                                         (300, 520, 1040, True)])
 def test_linear_postscale_codes(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=45 + M, outliers=0.01, oscale=20.0)
