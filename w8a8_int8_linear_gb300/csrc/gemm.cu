@@ -1086,7 +1086,7 @@ cudaError_t launch_one(const void* Ab, const void* Bb, PFN_cuTensorMapEncodeTile
 // waves x (BN + 16), i.e. whole waves of CTA pairs times the per-tile MMA
 // time plus a fixed per-tile cost.
 int choose_bn(int64_t M, int64_t N, int clusters) {
-    const int cand[3] = {256, 224, 192};
+    const int cand[4] = {256, 224, 192, 160};
     const int64_t mt = (M + TILE_M - 1) / TILE_M;
     int best = 256;
     int64_t best_cost = -1;
@@ -1108,6 +1108,7 @@ cudaError_t launch_bn(int bn, const void* Ab, const void* Bb, PFN_cuTensorMapEnc
     switch (bn) {
         case 224: return launch_one<EPI, 224, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
         case 192: return launch_one<EPI, 192, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
+        case 160: return launch_one<EPI, 160, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
         default: return launch_one<EPI, 256, false>(Ab, Bb, encode, p, num_sms, st, detail, n);
     }
 }
