@@ -227,6 +227,25 @@ def check_postscale(w8a8, oracle, M, N, K, bias):
     assert w8a8.get_device_error() == (0, 0)
 
 
+def test_int8_operands_exactness_at_max_k(w8a8, oracle):
+    """The int8-operand kernel at the largest K (131072: 1024 stages, K split
+    8 ways into units of 16 exact fp32 chunks each) with all-+-127 codes:
+    |acc| reaches 127*127*131072 = 2,114,060,288, just inside int32, and the
+    split sums add up exactly; a ragged last weight tile (136 rows)."""
+    M, N, K = 16, 136, 131072
+    g = torch.Generator().manual_seed(21)
+    Xq = ((torch.randint(0, 2, (M, K), generator=g) * 2 - 1) * 127).to(torch.int8)
+    Wq = ((torch.randint(0, 2, (N, K), generator=g) * 2 - 1) * 127).to(torch.int8)
+    Xq[0] = 127
+    Wq[0] = 127
+    Wq[135] = -127
+    ref = oracle.gemm_s32(Xq.numpy(), Wq.numpy())
+    acc = w8a8.gemm_postscale_s32(Xq.to(DEV), Wq.to(DEV)).cpu().numpy()
+    assert acc[0, 0] == 16129 * K and acc[0, 135] == -16129 * K
+    assert np.array_equal(acc, ref)
+    assert w8a8.get_device_error() == (0, 0)
+
+
 @pytest.mark.parametrize("M", [16, 77, 130, 520])  # int8-operand kernel (K split 8 ways) / swapped / regular
 def test_gemm_exactness_adversary(w8a8, oracle, M):
     """All-+-127 operands at K = 13824: per-chunk partial sums reach
