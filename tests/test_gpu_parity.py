@@ -192,6 +192,18 @@ def test_gemm_postscale_gemv(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
+# The GEMV on long weight streams (N * K >= 2^22): several row groups per
+# warp, an odd row count, K ending in a partial 512-byte slice.
+@pytest.mark.parametrize("M,N,K,bias", [
+    (1, 8192, 4096, True),
+    (2, 4096, 4096, False),
+    (3, 1031, 16384, True),
+    (4, 2000, 2064, False),
+])
+def test_gemm_postscale_gemv_long(w8a8, oracle, M, N, K, bias):
+    check_postscale(w8a8, oracle, M, N, K, bias)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 24, 131072), (4, 40, 32768)])
 def test_gemv_exactness_at_max_k(w8a8, oracle, M, N, K):
     """All-+-127 codes at the largest K the GEMV takes for this M: at one
@@ -399,7 +411,7 @@ def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
                                         (3, 520, 1040, False), (8, 4096, 4096, True),
                                         (5, 1000, 16, True), (8, 520, 16384, False), (1, 300, 131072, True),
                                         (2, 300, 131072, False), (9, 600, 2048, True), (77, 3072, 5120, False),
-                                        (6, 100, 32768, True),
+                                        (6, 100, 32768, True), (2, 2048, 4112, True), (1, 4096, 2048, False),
                                         (300, 520, 1040, True)])
 def test_linear_postscale_codes(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=45 + M, outliers=0.01, oscale=20.0)
