@@ -942,7 +942,8 @@ def report_decode(args):
     its own weight copy, with the C copies together larger than L2, replayed
     back to back; per-call time is the replay time / C.  Columns: the fused
     Linear on the packed image (swapped split-K tensor-core path), the fused
-    Linear on the int8 codes (a GEMV up to 8 tokens), the GEMM on int8 codes
+    Linear on the int8 codes (a GEMV up to 4 tokens, the int8-operand
+    tensor-core kernel up to 128), the GEMM on int8 codes
     quantized beforehand, and torch's bf16 matmul on C bf16 weights."""
     import torch
     import w8a8_int8_linear_gb300 as w
@@ -996,7 +997,8 @@ def report_decode(args):
             wsg = torch.empty(max(w.workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
             t_g8 = graph_time([lambda P=P: w.gemm_postscale(Xq, sxq, P[2], P[1], b, out=Y, workspace=wsg)
                                for P in packs])
-            # the fused Linear on the int8 codes (quantization + GEMV up to 8 tokens)
+            # the fused Linear on the int8 codes (quantization + GEMV up to 4 tokens, then the
+            # int8-operand kernel)
             wsc = torch.empty(max(w.linear_codes_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
             t_codes = graph_time([lambda P=P: w.linear_postscale_codes(X, P[2], P[1], b, out=Y, workspace=wsc,
                                                                        sx_out=sx) for P in packs])

@@ -80,7 +80,7 @@ def test_argument_checks_before_device(cdll):
     assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, null, 1 << 20, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, fake, 10, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, P(0x1010), 1 << 20, null) == 7
-    # 9..128 tokens stream the int8 codes: the fp16 image of Xq, plus int32
+    # 5..128 tokens stream the int8 codes: the fp16 image of Xq, plus int32
     # sums [M][N] and one counter per 32 weight rows where K may be split
     # (77 x 3072: 24 weight tiles; 77 x 13824 has 108, too many to split)
     s = s8_need(77, 3072, 5120)
@@ -170,7 +170,7 @@ def _a256(v):
 
 
 def s8_need(M, N, K):
-    """Workspace of the GEMM on int8 operands (9..128 tokens): the fp16 image
+    """Workspace of the GEMM on int8 operands (5..128 tokens): the fp16 image
     of Xq, and where K may be split (at most 76 tiles of 128 weight rows, at
     least 4 stages of 128 K) int32 sums [M][N] and 4 counters per tile."""
     tiles = -(-N // 128)

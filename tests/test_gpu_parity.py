@@ -318,7 +318,7 @@ def test_gemm_rejects_bad_arguments(w8a8):
         w8a8.gemm_postscale(torch.zeros((200, 32), dtype=torch.int8, device=DEV), torch.ones(200, device=DEV),
                             torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
                             workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
-    # 9..128 tokens stream the int8 codes and need only the fp16 image of Xq
+    # 5..128 tokens stream the int8 codes and need only the fp16 image of Xq
     # (K too short to split): 16 x 32 x 2 bytes, rounded up to 256
     args = (torch.ones((16, 32), dtype=torch.int8, device=DEV), torch.ones(16, device=DEV),
             torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV))
