@@ -121,11 +121,11 @@ W8A8_API w8a8_status w8a8_quantize_act(const void* X, int64_t M, int64_t K, w8a8
  * partial sums of the K splits.  The same size serves both scale modes.
  * The post-scale entry points (w8a8_gemm_postscale, _s32, _noalloc) need less
  * for few tokens and accept it: with M <= 4 and M * K <= 131072 the GEMM is a
- * GEMV on the CUDA cores that needs no workspace; otherwise, with M <= 128,
+ * GEMV on the CUDA cores that needs no workspace; otherwise, with M <= 288,
  * it streams the int8 weight codes itself and needs the fp16 image of Xq
  * (M * K * 2 bytes, rounded up to 256) and, when N <= 76 * 128 and K > 384
  * (shapes whose K it may split), int32 sums (M * N * 4 bytes) and counters
- * (16 bytes per 128 rows of N), each rounded up to 256.
+ * (32 bytes per 128 rows of N), each rounded up to 256.
  */
 W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -140,7 +140,7 @@ W8A8_API size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  *   work completes on `stream`.  Few tokens need less (see
  *   w8a8_gemm_workspace_size): nothing with M <= 4 and M * K <= 131072
  *   (workspace may be NULL and workspace_bytes 0), the fp16 image of Xq plus,
- *   for shapes whose K may be split, int32 sums and counters with M <= 128;
+ *   for shapes whose K may be split, int32 sums and counters with M <= 288;
  *   this also holds for w8a8_gemm_postscale_s32.
  */
 W8A8_API w8a8_status w8a8_gemm_postscale(const int8_t* Xq, const float* sx, const int8_t* Wq, const float* sw,
@@ -193,7 +193,7 @@ W8A8_API w8a8_status w8a8_linear_postscale(const void* X, const void* Wimg, cons
  * M * K <= 131072 (one kernel, no workspace); otherwise room for the int8
  * codes of X (M * K bytes, rounded up to 256; unused when the caller passes
  * Xq) plus what w8a8_gemm_postscale needs for the shape (nothing for the
- * GEMV, M <= 4; the int8 path's scratch with M <= 128; else
+ * GEMV, M <= 4; the int8 path's scratch with M <= 288; else
  * w8a8_gemm_workspace_size(M,N,K)). */
 W8A8_API size_t w8a8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -204,7 +204,7 @@ W8A8_API size_t w8a8_linear_codes_workspace_size(int64_t M, int64_t N, int64_t K
  * tokens (decoding): with M <= 2 and M * K <= 131072 it is one kernel, a
  * GEMV on the CUDA cores in which every CTA quantizes X into its shared
  * memory while its first weight loads are in flight; up to 4 tokens the
- * quantization kernel and the GEMV; up to 128 tokens the quantization kernel
+ * quantization kernel and the GEMV; up to 288 tokens the quantization kernel
  * and the int8-operand tensor-core GEMM.  Any M is accepted; for many
  * tokens w8a8_linear_postscale on a packed image is faster.
  * Results are identical to w8a8_quantize_act (PER_ROW) + w8a8_gemm_postscale
@@ -313,7 +313,7 @@ W8A8_API w8a8_status w8a8_gemm_postscale_images(const void* Ximg, const float* s
  * array inside the library, so the shape's scratch need must fit in it, else
  * W8A8_ERR_WORKSPACE and nothing is launched.  The need is that of
  * w8a8_gemm_postscale: nothing with M <= 4 and M * K <= 131072 (the
- * few-token GEMV), the fp16 image of Xq plus any K-split sums with M <= 128
+ * few-token GEMV), the fp16 image of Xq plus any K-split sums with M <= 288
  * (a few MB: for example M = 77, N = 13824, K = 5120 needs 788 KB), else
  * w8a8_gemm_workspace_size(M,N,K) (for example M = N = K = 4096 fits
  * exactly).

@@ -76,18 +76,22 @@ def test_argument_checks_before_device(cdll):
     assert g(null, null, null, null, null, null, 4, 0, 16, null, 0, null) == 0
     assert g(fake, null, fake, fake, null, fake, 4, 4, 16, fake, 1 << 20, null) == 1
     assert g(fake, fake, fake, fake, odd, fake, 4, 4, 16, fake, 1 << 20, null) == 2
-    # (more than 128 tokens: the bf16-image path, which needs the workspace)
-    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, null, 1 << 20, null) == 7
-    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, fake, 10, null) == 7
-    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, P(0x1010), 1 << 20, null) == 7
-    # 5..128 tokens stream the int8 codes: the fp16 image of Xq, plus int32
-    # sums [M][N] and one counter per 32 weight rows where K may be split
+    # (more than 288 tokens: the bf16-image path, which needs the workspace)
+    assert g(fake, fake, fake, fake, null, fake, 300, 4, 16, null, 1 << 20, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 300, 4, 16, fake, 10, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 300, 4, 16, P(0x1010), 1 << 20, null) == 7
+    # 5..288 tokens stream the int8 codes: the fp16 image of Xq, plus int32
+    # sums [M][N] and counters (8 per 128 weight rows) where K may be split
     # (77 x 3072: 24 weight tiles; 77 x 13824 has 108, too many to split)
     s = s8_need(77, 3072, 5120)
     assert g(fake, fake, fake, fake, null, fake, 77, 3072, 5120, null, 0, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 77, 3072, 5120, fake, s - 256, null) == 7
     assert g(fake, fake, fake, fake, null, fake, 77, 13824, 5120, fake, s8_need(77, 13824, 5120) - 256, null) == 7
     assert s8_need(77, 13824, 5120) == _a256(77 * 5120 * 2)
+    s = s8_need(257, 3072, 5120)
+    assert s == _a256(257 * 5120 * 2) + _a256(257 * 3072 * 4) + _a256(24 * 32)
+    assert g(fake, fake, fake, fake, null, fake, 257, 3072, 5120, fake, s - 256, null) == 7
+    assert g(fake, fake, fake, fake, null, fake, 200, 4, 16, null, 1 << 20, null) == 7
     # blockwise needs its workspace even for one token
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 1, 4, 128, null, 0, null) == 7
     assert L.w8a8_gemm_blockwise(fake, fake, fake, fake, null, fake, 4, 4, 64, fake, 1 << 20, null) == 3
@@ -170,13 +174,13 @@ def _a256(v):
 
 
 def s8_need(M, N, K):
-    """Workspace of the GEMM on int8 operands (5..128 tokens): the fp16 image
-    of Xq, and where K may be split (at most 76 tiles of 128 weight rows, at
-    least 4 stages of 128 K) int32 sums [M][N] and 4 counters per tile."""
+    """Workspace of the GEMM on int8 operands (5..288 tokens): the fp16 image
+    of Xq, and where K may be split (at most 76 tiles of 128 weight rows, K
+    over 384) int32 sums [M][N] and 8 int32 counters per tile."""
     tiles = -(-N // 128)
     b = _a256(M * K * 2)
     if tiles <= 76 and -(-K // 128) >= 4:
-        b += _a256(M * N * 4) + _a256(tiles * 16)
+        b += _a256(M * N * 4) + _a256(tiles * 32)
     return b
 
 
@@ -205,23 +209,27 @@ def test_workspace_size(cdll):
     assert L.w8a8_linear_codes_workspace_size(8, 64, 16400) == _a256(8 * 16400) + s8_need(8, 64, 16400)
     assert L.w8a8_linear_codes_workspace_size(16, 4096, 4096) == 16 * 4096 + s8_need(16, 4096, 4096)
     assert L.w8a8_linear_codes_workspace_size(77, 13824, 5120) == _a256(77 * 5120) + s8_need(77, 13824, 5120)
-    assert L.w8a8_linear_codes_workspace_size(200, 64, 256) == 200 * 256 + L.w8a8_gemm_workspace_size(200, 64, 256)
+    assert L.w8a8_linear_codes_workspace_size(200, 64, 256) == 200 * 256 + s8_need(200, 64, 256)
+    assert L.w8a8_linear_codes_workspace_size(288, 3072, 5120) == 288 * 5120 + s8_need(288, 3072, 5120)
+    assert L.w8a8_linear_codes_workspace_size(300, 64, 256) == 300 * 256 + L.w8a8_gemm_workspace_size(300, 64, 256)
     # the public size covers every path, the int8 path's need included
-    for M, N, K in [(128, 4096, 16), (128, 4096, 512), (9, 9728, 512), (128, 128, 131072)]:
+    for M, N, K in [(128, 4096, 16), (128, 4096, 512), (9, 9728, 512), (128, 128, 131072), (288, 64, 131072),
+                    (257, 3072, 5120), (129, 9856, 400)]:
         assert L.w8a8_gemm_workspace_size(M, N, K) >= s8_need(M, N, K)
 
 
 def test_few_token_routing():
     """The GEMV takes up to 4 tokens (their codes within 128 KB); the Linear
-    on int8 codes is preferred up to 96 tokens, and up to 128 with at least
+    on int8 codes is preferred up to 256 tokens, and up to 288 with at least
     2^25 weights."""
     import w8a8_int8_linear_gb300 as w
     assert w.gemv_takes(4, 5120) and not w.gemv_takes(5, 5120) and not w.gemv_takes(4, 32784)
     assert w.gemv_takes(1, 131072) and not w.gemv_takes(0, 16)
     assert w.codes_preferred(1, 3072, 5120) and w.codes_preferred(77, 3072, 5120)
-    assert w.codes_preferred(96, 5120, 5120) and not w.codes_preferred(97, 5120, 5120)
-    assert not w.codes_preferred(128, 5120, 5120) and w.codes_preferred(128, 13824, 5120)
-    assert not w.codes_preferred(129, 13824, 5120) and not w.codes_preferred(0, 13824, 5120)
+    assert w.codes_preferred(128, 5120, 5120) and w.codes_preferred(256, 3072, 5120)
+    assert not w.codes_preferred(257, 5120, 5120) and w.codes_preferred(257, 13824, 5120)
+    assert w.codes_preferred(288, 15432, 5120) and not w.codes_preferred(289, 15432, 5120)
+    assert not w.codes_preferred(0, 13824, 5120)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -125,12 +125,12 @@ def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
 
 
-# Few tokens on int8 codes (gemm_postscale): 5..128 tokens run the
-# int8-operand kernel (gemm_s8.cu: 128-row weight tiles, 16..128-token tiles,
-# K split with exact int32 atomics when the weight tiles are few), 129..256
-# the swapped tensor-core kernel on images (weights on the 256-row side,
-# tokens on the narrow side, Y written transposed, K split into int32
-# partials summed by a second kernel).
+# Few tokens, both routes.  The GEMM on int8 codes (gemm_postscale) runs the
+# GEMV or the int8-operand kernels (gemm_s8.cu).  The fused Linear on a
+# packed bf16 image (linear_postscale) runs, up to 256 tokens, the swapped
+# tensor-core kernel on images: weights on the 256-row side, tokens on the
+# narrow side, Y written transposed, K split into int32 partials summed by a
+# second kernel.  The split counts S below are those of the swapped kernel.
 @pytest.mark.parametrize("M,N,K,bias", [
     (1, 4096, 4096, True),     # one token: 32-token tiles, S = 4
     (16, 24, 128, False),      # fewer output columns than one store box, S = 1
@@ -146,12 +146,14 @@ def test_gemm_postscale(w8a8, oracle, M, N, K, bias):
 ])
 def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
+    check_linear_image(w8a8, oracle, M, N, K, bias)
 
 
-# The int8-operand kernel at its boundaries: every token tile (16, 32, 64, 96,
-# 128), both sides of the split rule (at most 76 weight tiles and 4 stages),
-# a last 128-K stage of 16 K (zero-filled past K), and a last weight tile of
-# one row.
+# The int8-operand kernels at their boundaries: every token tile (16, 32, 64,
+# 96, 128 on the narrow kernel; 160, 192, 224, 256, 288 on the wide one, whose
+# tile is two halves), both sides of the split rule (at most 76 weight tiles
+# and 256 K per split), a last stage of 16 K (zero-filled past K), and a last
+# weight tile of one row.
 @pytest.mark.parametrize("M,N,K,bias", [
     (5, 300, 5120, True),      # 16-token tile, 3 weight tiles: K split 8 ways
     (17, 1000, 1040, False),   # 32-token tile, 9 stages (the last 16 K): split 3 ways
@@ -159,6 +161,13 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     (97, 9856, 512, False),    # 128-token tile, 77 weight tiles: no split
     (64, 129, 16400, True),    # a last weight tile of one row, 129 stages, split 8 ways
     (128, 2048, 384, False),   # 3 stages: too few to split
+    (129, 300, 5120, True),    # 160-token tile (half 1 mostly zero rows): split 8 ways
+    (160, 1000, 1040, False),  # 160 exactly, 17 stages of 64 K (the last 16 K): split 4 ways
+    (193, 9728, 640, True),    # 224-token tile, 76 weight tiles, one SM each: no split
+    (250, 2048, 384, False),   # 256-token tile, 6 stages: too few to split
+    (257, 9856, 2048, False),  # 288-token tile, 77 weight tiles, two 1024-K chunks: no split
+    (288, 129, 16400, True),   # 288 exactly, a last weight tile of one row, 257 stages: split 8 ways
+    (200, 3072, 5120, True),   # 224-token tile at a model shape: 24 tiles, split 6 ways
 ])
 def test_gemm_postscale_int8_operands(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
@@ -258,7 +267,7 @@ def test_int8_operands_exactness_at_max_k(w8a8, oracle):
     assert w8a8.get_device_error() == (0, 0)
 
 
-@pytest.mark.parametrize("M", [16, 77, 130, 520])  # int8-operand kernel (K split 8 ways) / swapped / regular
+@pytest.mark.parametrize("M", [16, 77, 130, 288, 520])  # int8-operand kernels (K split 8 ways) / regular
 def test_gemm_exactness_adversary(w8a8, oracle, M):
     """All-+-127 operands at K = 13824: per-chunk partial sums reach
     127*127*1024 and the total 2.2e8, far past fp32's 2^24 integer range."""
@@ -313,12 +322,12 @@ def test_gemm_rejects_bad_arguments(w8a8):
     Xq = torch.zeros((4, 33), dtype=torch.int8, device=DEV)[:, 1:]
     with pytest.raises(ValueError):
         w8a8.gemm_postscale(Xq, torch.ones(4, device=DEV), Wq, torch.ones(4, device=DEV))
-    # more than 128 tokens: the bf16-image path, which needs the whole workspace
+    # more than 288 tokens: the bf16-image path, which needs the whole workspace
     with pytest.raises(w8a8.W8A8Error, match="WORKSPACE"):
-        w8a8.gemm_postscale(torch.zeros((200, 32), dtype=torch.int8, device=DEV), torch.ones(200, device=DEV),
+        w8a8.gemm_postscale(torch.zeros((300, 32), dtype=torch.int8, device=DEV), torch.ones(300, device=DEV),
                             torch.zeros((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV),
                             workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
-    # 5..128 tokens stream the int8 codes and need only the fp16 image of Xq
+    # 5..288 tokens stream the int8 codes and need only the fp16 image of Xq
     # (K too short to split): 16 x 32 x 2 bytes, rounded up to 256
     args = (torch.ones((16, 32), dtype=torch.int8, device=DEV), torch.ones(16, device=DEV),
             torch.ones((4, 32), dtype=torch.int8, device=DEV), torch.ones(4, device=DEV))
@@ -385,6 +394,11 @@ def test_pack_weight_is_exact_image(w8a8):
                                         (77, 3072, 5120, True), (5, 4096, 4096, False), (2500, 256, 5120, True),
                                         (2600, 136, 8192, False)])
 def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
+    check_linear_image(w8a8, oracle, M, N, K, bias)
+
+
+def check_linear_image(w8a8, oracle, M, N, K, bias):
+    """The fused Linear on a packed weight image against the oracle."""
     X = rand_bf16((M, K), seed=40 + M, outliers=0.01, oscale=20.0)
     W = rand_bf16((N, K), seed=41 + N, scale=0.02)
     b = rand_bf16((N,), seed=42, scale=0.01) if bias else None
@@ -405,14 +419,15 @@ def test_linear_postscale_fused(w8a8, oracle, M, N, K, bias):
 # The fused Linear on int8 weight codes: one GEMV kernel that quantizes X in
 # every CTA for one or two tokens (M * K <= 131072); the quantization kernel
 # and then the GEMV (weights read before its dependency wait) up to 4 tokens;
-# else the quantization kernel and the int8-operand tensor-core kernel (up to
-# 128 tokens) or operand images.
+# else the quantization kernel and the int8-operand tensor-core kernels (up
+# to 288 tokens) or operand images.
 @pytest.mark.parametrize("M,N,K,bias", [(1, 3072, 5120, True), (2, 1000, 4096, False), (2, 7, 16, True),
                                         (3, 520, 1040, False), (8, 4096, 4096, True),
                                         (5, 1000, 16, True), (8, 520, 16384, False), (1, 300, 131072, True),
                                         (2, 300, 131072, False), (9, 600, 2048, True), (77, 3072, 5120, False),
                                         (6, 100, 32768, True), (2, 2048, 4112, True), (1, 4096, 2048, False),
-                                        (300, 520, 1040, True)])
+                                        (257, 3072, 5120, True), (140, 13824, 1024, False),
+                                        (288, 600, 32768, True), (300, 520, 1040, True)])
 def test_linear_postscale_codes(w8a8, oracle, M, N, K, bias):
     X = rand_bf16((M, K), seed=45 + M, outliers=0.01, oscale=20.0)
     W = rand_bf16((N, K), seed=46 + N, scale=0.02)

@@ -75,14 +75,15 @@ def test_noalloc_repeat_same_shape_and_limit(w8a8):
 
 def test_noalloc_few_token_paths(w8a8):
     """The two few-token routes use the scratch differently: the GEMV (M <= 4)
-    needs none, the int8-operand GEMM (5..128 tokens) the fp16 image of the
+    needs none, the int8-operand GEMM (5..288 tokens) the fp16 image of the
     tokens and, where K is split (77 x 3072), int32 sums and counters that
     its first kernel zeroes.  77 x 13824 x 5120 would need ~142 MB as bf16
     images but fits through the int8 route; two calls in a row each, against
     the workspace entry point."""
     L = w8a8.lib()
     for (M, N, K, seed) in [(4, 3072, 5120, 4), (77, 13824, 5120, 5), (77, 13824, 5120, 6), (77, 3072, 5120, 7),
-                            (77, 3072, 5120, 8)]:
+                            (77, 3072, 5120, 8), (257, 13824, 5120, 9), (200, 3072, 5120, 10),
+                            (200, 3072, 5120, 11)]:
         X, W, b = _inputs(M, N, K, seed, True)
         Xq, sx = w8a8.quantize_act(X)
         Wq, sw = w8a8.quantize_weight(W)

@@ -176,8 +176,8 @@ def _workspace(ws, M, N, K, device):
 GEMV_MAX_TOKENS = 4
 GEMV_MAX_CODE_BYTES = 131072
 # Up to this many tokens the post-scale GEMM on int8 codes streams the codes
-# itself (the int8-operand tensor-core kernel) instead of bf16 images.
-INT8_OPERAND_MAX_TOKENS = 128
+# itself (the int8-operand tensor-core kernels) instead of bf16 images.
+INT8_OPERAND_MAX_TOKENS = 288
 
 
 def gemv_takes(M, K):
@@ -186,14 +186,14 @@ def gemv_takes(M, K):
 
 def codes_preferred(M, N, K):
     """Whether a post-scale Linear of M tokens is faster on the int8 weight
-    codes (linear_postscale_codes: the GEMV, or the int8-operand kernel that
-    reads each weight byte once) than on the packed bf16 image.  Measured in
-    steady state on GB300 (K = 5120, N = 3072 / 5120 / 13824): the codes win
-    up to 96 tokens at every N, and up to 128 once the weights hold 2^25
-    values; beyond 128 tokens the image path runs."""
+    codes (linear_postscale_codes: the GEMV, or the int8-operand kernels that
+    read each weight byte once) than on the packed bf16 image.  Measured in
+    steady state on GB300 (K = 5120, N = 3072 / 5120 / 13824 / 15432): the
+    codes are at least as fast up to 256 tokens at every N, and up to 288
+    once the weights hold 2^25 values; beyond that the image path runs."""
     if M < 1 or M > INT8_OPERAND_MAX_TOKENS:
         return False
-    return gemv_takes(M, K) or M <= 96 or N * K >= 1 << 25
+    return M <= 256 or N * K >= 1 << 25
 
 
 def _postscale_workspace(ws, M, N, K, device):

@@ -114,7 +114,7 @@ w8a8_status check_k(int64_t K, bool block) {
 
 // Workspace bytes the post-scale GEMM (int8 codes in) uses for this shape:
 // none for the few-token GEMV; when the GEMM streams the int8 codes itself
-// (M <= 128), the fp16 image of Xq and, where K may be split, int32 sums and
+// (M <= 288), the fp16 image of Xq and, where K may be split, int32 sums and
 // counters; else the bf16 images of Xq and Wq plus the partial sums of the
 // K splits.  M, N, K > 0.
 size_t postscale_gemm_need(int64_t M, int64_t N, int64_t K) {

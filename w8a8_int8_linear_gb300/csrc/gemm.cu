@@ -48,9 +48,9 @@
 //   - FFN up-projection: the epilogue applies GELU and the 1x128
 //     quantization of the down-projection's input, staged through shared
 //     memory over the next tile's chunk folds (stage_y, gelu_slice);
-//   - few tokens on int8 operands (M <= 128): a single-CTA kernel that
-//     streams the int8 weight codes, widens them into tensor memory and
-//     multiplies them with an fp16 image of the tokens (gemm_s8.cu).
+//   - few tokens on int8 operands (M <= 288): single-CTA kernels that
+//     stream the int8 weight codes, widen them into tensor memory and
+//     multiply them with an fp16 image of the tokens (gemm_s8.cu).
 // Every kernel triggers its dependents' launch at its start and waits on
 // its own prerequisite grid after its prologue (programmatic dependent
 // launch); weights packed before the previous kernel started may be read
@@ -104,7 +104,7 @@ constexpr int GROUP_M_POSTSCALE = 16;
 constexpr int GROUP_M_BLOCKWISE = 8;
 constexpr int SCALE_PREFETCH = 4;           // blockwise: per-block scales loaded this many chunks ahead
 constexpr int kSwapMaxTokens = 256;         // post-scale GEMMs with M <= this swap operands
-constexpr int kInt8MaxTokens = 128;         // ... and with M <= this can stream int8 operands
+constexpr int kInt8MaxTokens = 288;         // post-scale GEMMs with M <= this can stream int8 operands
 constexpr int kSplitTargetUnits = 72;       // split K until about this many CTA-pair work units exist
 constexpr int kSplitMinStages = 4;          // at least 256 K per split
 constexpr int kSplitMax = 8;

@@ -1,8 +1,10 @@
-// Few-token post-scale W8A8 GEMM on the int8 codes themselves (5..128
+// Few-token post-scale W8A8 GEMM on the int8 codes themselves (5..288
 // tokens): the weight codes stream once from HBM and are widened into tensor
 // memory, the tokens arrive as an fp16 image of their codes, and the exact
 // integer product runs on the fp16 tcgen05 pipe.  launch_gemm (gemm.cu)
-// routes int8-operand calls here.
+// routes int8-operand calls here: up to 96 tokens to gemm_s8_kernel, beyond
+// that to gemm_s8w_kernel (whose 160-token tile also beats a 128-token tile
+// of the first kernel from 97 tokens on).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -63,7 +65,7 @@ struct S8Params {
 // none, and the tokens, widened once by s8_prep_kernel, arrive by TMA.
 // ---------------------------------------------------------------- few tokens on int8 weight codes
 //
-// gemm_s8_kernel: Y[t][n] for at most 128 tokens, reading each int8 weight
+// gemm_s8_kernel: Y[t][n] for at most 96 tokens, reading each int8 weight
 // code once.  The kernel's rows are weight rows n (128 per tile, one CTA per
 // tile and K split), its columns the tokens (BN >= tokens: one column tile).
 // Each 128-K stage:
@@ -536,31 +538,468 @@ __global__ void __launch_bounds__(256) s8_prep_kernel(const uint4* __restrict__ 
     for (int64_t i = i0; i < nz16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// ---------------------------------------------------------------- 97..288 tokens on int8 weight codes
+//
+// gemm_s8w_kernel: the same product for 97..288 tokens.  Two accumulator
+// buffers of that width no longer fit in tensor memory beside the widened
+// weights, so the token tile has one accumulator of BN columns, computed as
+// two halves of HB = BN / 2 tokens (one MMA of N = HB each), and the MMAs
+// wait while the epilogue folds a finished 1024-K chunk into int32.  The
+// token image of a 128-K stage would take 72 KB at BN = 288, so stages are
+// 64 K wide: the int8 weight tile [128 rows x 64 bytes] arrives with the
+// 64-byte swizzle and the token image [BN rows x 64 K] as two boxes of HB
+// rows with the 128-byte swizzle.
+// Roles (512 threads):
+//   warp 0      producer;  warp 1  TMEM allocation and the MMAs;  warps 2-3 idle;
+//   warps 4-7   converters, one weight row per thread (32 columns of fp16 pairs);
+//   warps 8-15  epilogue: warp 8 + 4h + q holds tensor-memory lane quarter q
+//               of token half h (HB int32 sums per thread).
+constexpr int S8W_BK = 64;                      // K per stage (bytes of an int8 weight row)
+constexpr int S8W_CHUNK_STAGES = 16;            // 1024 K per exact fp32 chunk
+constexpr uint32_t S8W_A_BYTES = BM * S8W_BK;   // 8 KB
+constexpr int S8W_THREADS = 512;
+constexpr int S8W_EPI_WARP0 = 8;
+// Register split: warpgroup 0 56, converters 72, the two epilogue warpgroups 192.
+static_assert(128 * 56 + 128 * 72 + 256 * 192 <= 65536, "wide int8 kernel register split exceeds the launch budget");
+
+template <int BN_, int BUFS_>
+struct CfgS8W {
+    static constexpr int BN = BN_;
+    static constexpr int BUFS = BUFS_;                   // accumulator buffers
+    static_assert(BUFS == 1 || BUFS == 2, "accumulator buffers");
+    static constexpr int HB = BN / 2;                    // tokens per half (N of one MMA)
+    static_assert(BN % 32 == 0 && HB >= 80 && HB <= 144, "wide token tile");
+    static constexpr uint32_t B_HALF_BYTES = HB * 128;   // HB rows x 64 fp16, a multiple of the 1024-byte swizzle atom
+    static constexpr uint32_t SLOT = S8W_A_BYTES + 2 * B_HALF_BYTES;
+    static constexpr uint32_t A_TMEM0 = BUFS * BN;       // after the accumulators
+    static constexpr uint32_t SX_BYTES = 2048;           // the tile's token scales
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - SX_BYTES - BAR_BYTES;
+    static constexpr int S_SMEM = int(RING_BUDGET / SLOT);
+    static constexpr int S_TMEM = int((TMEM_COLS - A_TMEM0) / 32);
+    static constexpr int S = S_SMEM < S_TMEM ? S_SMEM : S_TMEM;
+    static_assert(S >= 4 && A_TMEM0 + 32 * S <= TMEM_COLS, "ring");
+    static_assert(3 * S + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
+    static_assert(BN * 4 <= int(SX_BYTES), "scale area");
+    static constexpr size_t SMEM = 1024 + size_t(S) * SLOT + SX_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, HB);
+    static constexpr int LDW = 8;   // tensor-memory loads of 8 columns, double-buffered
+    static constexpr int GROUPS = HB / LDW;
+};
+
+// 32 lanes x 8 consecutive 32-bit columns, and the matching wait.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_regs8(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+
+// Widen weight row r of a 64-K int8 stage (128 rows x 64 bytes, as TMA wrote
+// it with the 64-byte swizzle: 16-byte unit c of row r sits at unit
+// c ^ ((r >> 1) & 3)) into tensor memory at taddr: 32 columns of fp16 pairs.
+// The eight threads of a quarter-warp read eight different bank groups.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void widen_row64_to_tmem(const uint8_t* stage, int r, uint32_t taddr) {
+    const uint8_t* row = stage + r * S8W_BK;
+    const int sw = (r >> 1) & 3;
+    uint4 v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t o[16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            uint4 lo, hi;
+            s8x16_to_f16(v[2 * h + c], lo, hi);
+            o[8 * c + 0] = lo.x;
+            o[8 * c + 1] = lo.y;
+            o[8 * c + 2] = lo.z;
+            o[8 * c + 3] = lo.w;
+            o[8 * c + 4] = hi.x;
+            o[8 * c + 5] = hi.y;
+            o[8 * c + 6] = hi.z;
+            o[8 * c + 7] = hi.w;
+        }
+        tmem_st_32x32b_x16(taddr + 16 * h, o);
+    }
+}
+
+// Output column n for the HB tokens t0 .. t0 + HB - 1 of one half: the
+// post-scale epilogue of s8_store, or the int32 sums.
+template <int EPI, int HB>
+__device__ __forceinline__ void s8w_store(const int32_t (&acc)[HB], const S8Params& p, int n, int t0,
+                                          const float* sxs, float swn, float bn) {
+    if (n >= p.M) return;
+    if constexpr (EPI == kEpiPostscaleS32) {
+        int32_t* out = static_cast<int32_t*>(p.out) + static_cast<int64_t>(t0) * p.M + n;
+#pragma unroll
+        for (int t = 0; t < HB; ++t) {
+            if (t0 + t < p.N) *out = acc[t];
+            out += p.M;
+        }
+    } else {
+        uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(t0) * p.M + n;
+#pragma unroll
+        for (int g = 0; g < HB; g += 16) {
+            if (t0 + g >= p.N) break;
+            float sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = sxs[t0 + g + e];
+            uint32_t y[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sv[e]), swn);
+                float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e + 1]), sv[e + 1]), swn);
+                if (p.bias) {
+                    v0 = __fadd_rn(v0, bn);
+                    v1 = __fadd_rn(v1, bn);
+                }
+                __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+                y[e / 2] = *reinterpret_cast<uint32_t*>(&h);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (t0 + g + e < p.N) *out = static_cast<uint16_t>(y[e / 2] >> (16 * (e & 1)));
+                out += p.M;
+            }
+        }
+    }
+}
+
+enum WaitSiteS8W : int {
+    kSiteS8WProducerEmpty = 21,
+    kSiteS8WConvFull = 22,
+    kSiteS8WMmaFull = 23,
+    kSiteS8WProducerDrain = 24,
+    kSiteS8WMmaAccEmpty = 25,
+    kSiteS8WEpiAccFull = 26,
+    kSiteS8WMmaDrain = 27,
+};
+
+template <int EPI, int BN, int BUFS>
+__global__ void __launch_bounds__(S8W_THREADS, 1)
+    gemm_s8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const S8Params p) {
+    grid_launch_dependents();
+    using C = CfgS8W<BN, BUFS>;
+    constexpr int S = C::S;
+    constexpr int HB = C::HB;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sxs = reinterpret_cast<float*>(ring + S * C::SLOT);
+    uint64_t* full8 = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sxs) + C::SX_BYTES);
+    uint64_t* full16 = full8 + S;
+    uint64_t* empty = full16 + S;
+    uint64_t* acc_full = empty + S;  // per accumulator buffer
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* mma_drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = static_cast<int>(blockIdx.x);
+    const int nctas = static_cast<int>(gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full8[s], 1);   // the producer's arrive + the slot's bytes
+            mbar_init(&full16[s], 4);  // the four converter warps
+            mbar_init(&empty[s], 1);   // the MMA commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 8);  // the eight epilogue warps
+        }
+        mbar_init(mma_drain, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp != 0) grid_dependency_wait();
+    const uint32_t tmem_base = *tmem_slot;
+    if (warp < 4) {
+      regs_dec<56>();
+      if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const bool elected = elect_one_sync();
+        int pre = 0;
+        if (elected && p.a_settled && cta < p.num_tiles) {
+            int mb, ks0, ks1;
+            s8_unit(cta, p, mb, ks0, ks1);
+            pre = min(S, ks1 - ks0);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full8[i], C::SLOT);
+                tma_load_2d(ring + i * C::SLOT, &tmA, &full8[i], (ks0 + i) * S8W_BK, mb * BM);
+            }
+        }
+        grid_dependency_wait();
+        if (elected) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_phase = 0;
+            bool ok = true;
+            for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+                int mb, ks0, ks1;
+                s8_unit(u, p, mb, ks0, ks1);
+                for (int ks = ks0; ks < ks1; ++ks) {
+                    uint8_t* slot = ring + stage * C::SLOT;
+                    if (!(u == cta && ks - ks0 < pre)) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteS8WProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full8[stage], C::SLOT);
+                        tma_load_2d(slot, &tmA, &full8[stage], ks * S8W_BK, mb * BM);
+                    }
+                    tma_load_2d(slot + S8W_A_BYTES, &tmB, &full8[stage], ks * S8W_BK, 0);
+                    tma_load_2d(slot + S8W_A_BYTES + C::B_HALF_BYTES, &tmB, &full8[stage], ks * S8W_BK, HB);
+                    armed |= 1u << stage;
+                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < S; ++s)
+                if (armed & (1u << s)) mbar_wait(&full8[s], (armed_phase >> s) & 1u, kSiteS8WProducerDrain);
+        }
+      } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (elect_one_sync()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int buf = 0;
+            uint32_t buf_phase = 0;
+            bool ok = true;
+            const uint64_t desc0 = smem_desc_kmajor_sw128(smem_u32(ring + S8W_A_BYTES));
+            for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+                int mb, ks0, ks1;
+                s8_unit(u, p, mb, ks0, ks1);
+                const int nchunks = (ks1 - ks0 + S8W_CHUNK_STAGES - 1) / S8W_CHUNK_STAGES;
+                for (int c = 0; ok && c < nchunks; ++c) {
+                    // the epilogue has read this buffer's previous chunk out of it
+                    if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteS8WMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                    const int s0 = ks0 + c * S8W_CHUNK_STAGES;
+                    const int s1 = min(ks1, s0 + S8W_CHUNK_STAGES);
+                    for (int ks = s0; ks < s1; ++ks) {
+                        if (!mbar_wait(&full16[stage], phase, kSiteS8WMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_tmem = tmem_base + C::A_TMEM0 + static_cast<uint32_t>(stage * 32);
+                        const uint64_t db = desc0 + static_cast<uint64_t>((stage * C::SLOT) >> 4);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int k = 0; k < S8W_BK / 16; ++k)
+                                mma_f16_ts(d_tmem + static_cast<uint32_t>(h * HB), a_tmem + k * 8,
+                                           db + static_cast<uint64_t>((h * C::B_HALF_BYTES + k * 32) >> 4), C::IDESC,
+                                           (ks > s0 || k > 0) ? 1u : 0u);
+                        mma_commit(&empty[stage]);
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&acc_full[buf]);
+                    if (++buf == BUFS) {
+                        buf = 0;
+                        buf_phase ^= 1u;
+                    }
+                }
+            }
+            mma_commit(mma_drain);
+            mbar_wait(mma_drain, 0, kSiteS8WMmaDrain);
+        }
+      }
+    } else if (warp < S8W_EPI_WARP0) {
+        regs_dec<72>();
+        // ------------------------------------------------------------ converters (warps 4..7)
+        const int r = ((warp & 3) << 5) | lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::A_TMEM0;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+            int mb, ks0, ks1;
+            s8_unit(u, p, mb, ks0, ks1);
+            for (int ks = ks0; ks < ks1; ++ks) {
+                // the slot's copies landed, so the MMAs that last read this
+                // tensor-memory stage have completed (their commit freed the slot)
+                if (!mbar_wait(&full8[stage], phase, kSiteS8WConvFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                widen_row64_to_tmem(ring + stage * C::SLOT, r, lane_base + static_cast<uint32_t>(stage * 32));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full16[stage]);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        regs_inc<192>();
+        // ------------------------------------------------------------ epilogue (warps 8..15)
+        constexpr int LDW = C::LDW;
+        constexpr int GROUPS = C::GROUPS;
+        const int quarter = warp & 3;
+        const int half = (warp - S8W_EPI_WARP0) >> 2;
+        const int t0 = half * HB;                                         // first token of this half
+        const int et = static_cast<int>(threadIdx.x) - 32 * S8W_EPI_WARP0;  // 0..255
+        for (int i = et; i < BN; i += 256)
+            sxs[i] = (EPI == kEpiPostscaleBf16 && i < p.N) ? __ldg(p.sx + i) : 0.0f;
+        named_bar_sync(1, 256);  // the eight epilogue warps
+        int buf = 0;
+        uint32_t buf_phase = 0;
+        bool ok = true;
+        const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(t0);
+        for (int u = cta; ok && u < p.num_tiles; u += nctas) {
+            int mb, ks0, ks1;
+            s8_unit(u, p, mb, ks0, ks1);
+            const int nchunks = (ks1 - ks0 + S8W_CHUNK_STAGES - 1) / S8W_CHUNK_STAGES;
+            const int n = mb * BM + quarter * 32 + lane;
+            float swn = 0.0f, bn = 0.0f;
+            if (EPI == kEpiPostscaleBf16 && n < p.M) {
+                swn = __ldg(p.sw + n);
+                if (p.bias) bn = __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16);
+            }
+            int32_t acc[HB];
+#pragma unroll
+            for (int e = 0; e < HB; ++e) acc[e] = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                if (!mbar_wait(&acc_full[buf], buf_phase, kSiteS8WEpiAccFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = taddr0 + static_cast<uint32_t>(buf * BN);
+                uint32_t ra[LDW], rb[LDW];
+                tmem_ld_32x32b_x8(taddr, ra);
+                tmem_wait_ld_regs8(ra);
+#pragma unroll
+                for (int j = 0; j < GROUPS; ++j) {
+                    uint32_t(&cur)[LDW] = (j & 1) ? rb : ra;
+                    uint32_t(&nxt)[LDW] = (j & 1) ? ra : rb;
+                    if (j + 1 < GROUPS) tmem_ld_32x32b_x8(taddr + (j + 1) * LDW, nxt);
+#pragma unroll
+                    for (int e = 0; e < LDW; ++e) acc[j * LDW + e] += __float2int_rz(__uint_as_float(cur[e]));
+                    if (j + 1 < GROUPS) tmem_wait_ld_regs8(nxt);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+                if (++buf == BUFS) {
+                    buf = 0;
+                    buf_phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (p.k_split == 1) {
+                s8w_store<EPI, HB>(acc, p, n, t0, sxs, swn, bn);
+            } else {
+                if (n < p.M) {
+                    int32_t* dst = p.partial + static_cast<int64_t>(t0) * p.M + n;
+#pragma unroll
+                    for (int t = 0; t < HB; ++t) {
+                        if (t0 + t < p.N) atomicAdd(dst, acc[t]);
+                        dst += p.M;
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                int arrived = 0;
+                if (lane == 0) arrived = atomicAdd(p.counters + mb * 8 + half * 4 + quarter, 1);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == p.k_split - 1) {
+                    __threadfence();
+                    if (n < p.M) {
+                        const int32_t* src = p.partial + static_cast<int64_t>(t0) * p.M + n;
+#pragma unroll
+                        for (int t = 0; t < HB; ++t) {
+                            if (t0 + t < p.N) acc[t] = __ldcg(src);
+                            src += p.M;
+                        }
+                    }
+                    s8w_store<EPI, HB>(acc, p, n, t0, sxs, swn, bn);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 // Whether each kernel instance (epilogue x token tile) has its shared-memory
-// attribute set, per device.
-bool g_configured[64][10];
+// attribute set, per device: five narrow and five wide token tiles per epilogue.
+bool g_configured[64][20];
 
 // Int8-operand GEMM plan for a weight matrix of N rows and K columns:
-// weight tiles, 128-K stages, and the K split (1: none).  K is split only
-// when the weight tiles alone leave most SMs idle; the split count comes from
-// the SM count, the need for the split buffers only from the shape.
+// weight tiles, stages of stage_k K (128 up to 96 tokens, 64 beyond), and
+// the K split (1: none), each split at least 256 K.  K is split only when the
+// weight tiles alone leave most SMs idle; the split count comes from the SM
+// count, the need for the split buffers only from the shape.
 struct S8Plan {
     int num_m, k_stages, k_split, split_stages;
 };
+
+constexpr int S8_COUNTERS_PER_TILE = 8;  // one per 32-row group (and token half, beyond 96 tokens)
 
 bool s8_split_possible(int64_t N, int64_t K) {
     return (N + BM - 1) / BM <= S8_SPLIT_MAX_TILES && (K + S8_BK - 1) / S8_BK >= 4;
 }
 
-S8Plan s8_plan(int64_t N, int64_t K, int num_sms) {
+S8Plan s8_plan(int64_t N, int64_t K, int num_sms, int stage_k) {
     S8Plan pl;
     pl.num_m = static_cast<int>((N + BM - 1) / BM);
-    pl.k_stages = static_cast<int>((K + S8_BK - 1) / S8_BK);
+    pl.k_stages = static_cast<int>((K + stage_k - 1) / stage_k);
     int s = 1;
     if (s8_split_possible(N, K)) {
         s = num_sms / pl.num_m;
         if (s > S8_SPLIT_MAX) s = S8_SPLIT_MAX;
-        if (s > pl.k_stages / 2) s = pl.k_stages / 2;
+        if (s > pl.k_stages / (256 / stage_k)) s = pl.k_stages / (256 / stage_k);
         if (s < 2) s = 1;
     }
     pl.split_stages = (pl.k_stages + s - 1) / s;  // no split is left empty
@@ -570,18 +1009,18 @@ S8Plan s8_plan(int64_t N, int64_t K, int num_sms) {
 
 size_t s8_align(size_t v) { return (v + 255) & ~size_t(255); }
 
-template <int EPI, int BN>
-cudaError_t launch_s8_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S8Params& p, int ctas,
-                         cudaStream_t st) {
-    using C = CfgS8<BN>;
+// One launch of kernel k (instance id of g_configured) with SMEM bytes of
+// dynamic shared memory, THREADS threads and one CTA per work unit (at most
+// one per SM), after the tokens' image is written.
+template <typename Kernel>
+cudaError_t launch_s8_kernel(Kernel k, int id, size_t smem, int threads, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, const S8Params& p, int ctas, cudaStream_t st) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    constexpr int id = (EPI == kEpiPostscaleS32 ? 5 : 0) + (BN == 16 ? 0 : BN == 32 ? 1 : BN == 64 ? 2 : BN == 96 ? 3 : 4);
     if (!g_configured[dev][id]) {
-        e = cudaFuncSetAttribute(gemm_s8_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(C::SMEM));
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         g_configured[dev][id] = true;
     }
@@ -590,36 +1029,71 @@ cudaError_t launch_s8_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(S8_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_s8_kernel<EPI, BN>, tmA, tmB, p);
+    return cudaLaunchKernelEx(&cfg, k, tmA, tmB, p);
 }
 
-// The GEMM on int8 operands (M <= 128 tokens): s8_prep_kernel, then
-// gemm_s8_kernel with one CTA per work unit (at most one per SM).  a.partial
-// is the scratch of s8_workspace_bytes(M, N, K): the tokens' fp16 image, then
-// (when K may be split) the int32 sums [M][N] and the arrival counters.
+template <int EPI, int BN>
+cudaError_t launch_s8_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S8Params& p, int ctas,
+                         cudaStream_t st) {
+    constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + (BN == 16 ? 0 : BN == 32 ? 1 : BN == 64 ? 2 : BN == 96 ? 3 : 4);
+    return launch_s8_kernel(gemm_s8_kernel<EPI, BN>, id, CfgS8<BN>::SMEM, S8_THREADS, tmA, tmB, p, ctas, st);
+}
+
+// The 160-token tile double-buffers its accumulator (2 x 160 columns beside
+// six 64-K stages in tensor memory): the MMAs of the next chunk run while the
+// epilogue folds the last.  Wider tiles have one accumulator and wait for
+// the fold (at 192 tokens two accumulators would leave four stages, which
+// measured slower than six stages and the wait).
+template <int EPI, int BN>
+cudaError_t launch_s8w_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S8Params& p, int ctas,
+                          cudaStream_t st) {
+    constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + 5 + (BN - 160) / 32;
+    static_assert(BN >= 160 && BN <= 288 && BN % 32 == 0, "wide token tile");
+    constexpr int BUFS = BN == 160 ? 2 : 1;
+    using C = CfgS8W<BN, BUFS>;
+    return launch_s8_kernel(gemm_s8w_kernel<EPI, BN, BUFS>, id, C::SMEM, S8W_THREADS, tmA, tmB, p, ctas, st);
+}
+
+constexpr int S8_NARROW_MAX_TOKENS = 96;  // gemm_s8_kernel up to this many tokens, gemm_s8w_kernel beyond
+
+// Token tile of the int8-operand GEMM for T tokens: the narrowest that holds
+// them (16 .. 96 on the narrow kernel, 160 .. 288 on the wide one).
+int s8_token_tile(int64_t T) {
+    if (T <= S8_NARROW_MAX_TOKENS) return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 96;
+    return static_cast<int>((T + 31) / 32 * 32) < 160 ? 160 : static_cast<int>((T + 31) / 32 * 32);
+}
+
+// The GEMM on int8 operands (M <= 288 tokens): s8_prep_kernel, then
+// gemm_s8_kernel (up to 96 tokens) or gemm_s8w_kernel with one CTA per work
+// unit (at most one per SM).  a.partial is the scratch of
+// s8_workspace_bytes(M, N, K): the tokens' fp16 image, then (when K may be
+// split) the int32 sums [M][N] and the arrival counters.
 template <int EPI>
 cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num_sms,
                       PFN_cuTensorMapEncodeTiled_v12000 encode, cudaStream_t st, char* detail, size_t n) {
     const int64_t T = a.M, N = a.N, K = a.K;
-    const S8Plan pl = s8_plan(N, K, num_sms);
+    const bool wide = T > S8_NARROW_MAX_TOKENS;
+    const int stage_k = wide ? S8W_BK : S8_BK;
+    const S8Plan pl = s8_plan(N, K, num_sms, stage_k);
     uint8_t* ws = reinterpret_cast<uint8_t*>(a.partial);
     const size_t img_bytes = s8_align(static_cast<size_t>(T) * K * 2);
     const size_t sum_bytes = s8_align(static_cast<size_t>(T) * N * 4);
-    const size_t cnt_bytes = s8_align(static_cast<size_t>(pl.num_m) * 16);
+    const size_t cnt_bytes = s8_align(static_cast<size_t>(pl.num_m) * S8_COUNTERS_PER_TILE * 4);
 
     CUtensorMap tmA, tmB;
     {
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-        cuuint32_t box[2] = {static_cast<cuuint32_t>(S8_BK), static_cast<cuuint32_t>(BM)};
+        cuuint32_t box[2] = {static_cast<cuuint32_t>(stage_k), static_cast<cuuint32_t>(BM)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            wide ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) {
             snprintf(detail, n, "cuTensorMapEncodeTiled(weight codes: %lld x %lld) returned %d", (long long)N,
@@ -627,11 +1101,12 @@ cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num
             return cudaErrorInvalidValue;
         }
     }
-    const int bn = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 96 ? 96 : 128;
+    const int bn = s8_token_tile(T);
     {
+        // the narrow kernel loads all bn token rows per box, the wide one each half
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(bn)};
+        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(wide ? bn / 2 : bn)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -688,7 +1163,14 @@ cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num
         case 32: return launch_s8_bn<EPI, 32>(tmA, tmB, p, ctas, st);
         case 64: return launch_s8_bn<EPI, 64>(tmA, tmB, p, ctas, st);
         case 96: return launch_s8_bn<EPI, 96>(tmA, tmB, p, ctas, st);
-        default: return launch_s8_bn<EPI, 128>(tmA, tmB, p, ctas, st);
+        case 160: return launch_s8w_bn<EPI, 160>(tmA, tmB, p, ctas, st);
+        case 192: return launch_s8w_bn<EPI, 192>(tmA, tmB, p, ctas, st);
+        case 224: return launch_s8w_bn<EPI, 224>(tmA, tmB, p, ctas, st);
+        case 256: return launch_s8w_bn<EPI, 256>(tmA, tmB, p, ctas, st);
+        case 288: return launch_s8w_bn<EPI, 288>(tmA, tmB, p, ctas, st);
+        default:
+            snprintf(detail, n, "int8-operand GEMM: %lld tokens exceed the widest token tile", (long long)T);
+            return cudaErrorInvalidValue;
     }
 }
 
@@ -696,16 +1178,18 @@ cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num
 }  // namespace
 
 void s8_scratch_zero(int64_t M, int64_t N, int64_t K, int num_sms, size_t* offset, size_t* bytes) {
-    const S8Plan pl = s8_plan(N, K, num_sms);
+    const S8Plan pl = s8_plan(N, K, num_sms, M > S8_NARROW_MAX_TOKENS ? S8W_BK : S8_BK);
     *offset = s8_align(static_cast<size_t>(M) * K * 2);
-    *bytes = pl.k_split > 1 ? s8_align(static_cast<size_t>(M) * N * 4) + s8_align(static_cast<size_t>(pl.num_m) * 16)
+    *bytes = pl.k_split > 1 ? s8_align(static_cast<size_t>(M) * N * 4) +
+                                  s8_align(static_cast<size_t>(pl.num_m) * S8_COUNTERS_PER_TILE * 4)
                             : 0;
 }
 
 size_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     size_t b = s8_align(static_cast<size_t>(M) * K * 2);
     if (s8_split_possible(N, K))
-        b += s8_align(static_cast<size_t>(M) * N * 4) + s8_align(static_cast<size_t>((N + BM - 1) / BM) * 16);
+        b += s8_align(static_cast<size_t>(M) * N * 4) +
+             s8_align(static_cast<size_t>((N + BM - 1) / BM) * S8_COUNTERS_PER_TILE * 4);
     return b;
 }
 

@@ -7,7 +7,7 @@ initialization, activations quantized dynamically before every Linear.  This
 module does exactly that through the library: the weight is quantized and its
 exact bf16 image packed once (`from_linear` / `__init__`), and every forward
 is one fused call (per-token or 1x128 quantization plus the INT8 GEMM).  With
-few tokens (decoding, and up to 128 tokens where that is faster:
+few tokens (decoding, and up to 288 tokens where that is faster:
 `codes_preferred`) a post-scale forward runs against the int8 codes instead of
 the image, reading each weight byte once.  It keeps no
 bf16 copy of the original weight and has no fallback path: every shape runs
