@@ -540,51 +540,59 @@ __global__ void __launch_bounds__(256) s8_prep_kernel(const uint4* __restrict__ 
 
 // ---------------------------------------------------------------- 97..288 tokens on int8 weight codes
 //
-// gemm_s8w_kernel: the same product for 97..288 tokens.  Two accumulator
-// buffers of that width no longer fit in tensor memory beside the widened
-// weights, so the token tile has one accumulator of BN columns, computed as
-// two halves of HB = BN / 2 tokens (one MMA of N = HB each), and the MMAs
-// wait while the epilogue folds a finished 1024-K chunk into int32.  The
-// token image of a 128-K stage would take 72 KB at BN = 288, so stages are
-// 64 K wide: the int8 weight tile [128 rows x 64 bytes] arrives with the
-// 64-byte swizzle and the token image [BN rows x 64 K] as two boxes of HB
-// rows with the 128-byte swizzle.
+// gemm_s8w_kernel: the same product for 97..288 tokens.  Two accumulators of
+// the whole token tile no longer fit in tensor memory beside the widened
+// weights, and one alone would stop the MMAs at every 1024-K chunk while the
+// epilogue folds it into int32.  So the tile is cut into P token parts of W
+// columns (P = 3 at 288 tokens, else 2; one MMA of N = W per part) that share
+// P + 1 accumulator regions of W columns: the parts' chunks end at staggered
+// stages (s8w_chunk_start), and at the end of a chunk a part moves on into the
+// free region while the epilogue folds the one it leaves.  The MMAs never
+// wait for a fold as long as it ends within the 5..8 stages before the next
+// part's chunk ends.  The token image of a 128-K stage would take 72 KB at
+// BN = 288, so stages are 64 K wide: the int8 weight tile [128 rows x 64
+// bytes] arrives with the 64-byte swizzle and the token image [BN rows x 64
+// K] as P boxes of W rows with the 128-byte swizzle.
 // Roles (512 threads):
 //   warp 0      producer;  warp 1  TMEM allocation and the MMAs;  warps 2-3 idle;
 //   warps 4-7   converters, one weight row per thread (32 columns of fp16 pairs);
-//   warps 8-15  epilogue: warp 8 + 4h + q holds tensor-memory lane quarter q
-//               of token half h (HB int32 sums per thread).
+//   warps 8-15  epilogue: warp 8 + 4c + q holds tensor-memory lane quarter q
+//               and column half c of every part (BN / 2 int32 sums per thread),
+//               and all eight fold each region the MMAs leave.
 constexpr int S8W_BK = 64;                      // K per stage (bytes of an int8 weight row)
 constexpr int S8W_CHUNK_STAGES = 16;            // 1024 K per exact fp32 chunk
 constexpr uint32_t S8W_A_BYTES = BM * S8W_BK;   // 8 KB
 constexpr int S8W_THREADS = 512;
 constexpr int S8W_EPI_WARP0 = 8;
-// Register split: warpgroup 0 56, converters 72, the two epilogue warpgroups 192.
-static_assert(128 * 56 + 128 * 72 + 256 * 192 <= 65536, "wide int8 kernel register split exceeds the launch budget");
+// Register split: warpgroup 0 64 (the MMA issuer's region bookkeeping), converters 64, the two
+// epilogue warpgroups 192 (up to 144 int32 sums per thread).
+static_assert(128 * 64 + 128 * 64 + 256 * 192 <= 65536, "wide int8 kernel register split exceeds the launch budget");
 
-template <int BN_, int BUFS_>
+// Token parts of a wide token tile of bn columns.
+__host__ __device__ constexpr int s8w_parts(int bn) { return bn > 256 ? 3 : 2; }
+
+template <int BN_>
 struct CfgS8W {
     static constexpr int BN = BN_;
-    static constexpr int BUFS = BUFS_;                   // accumulator buffers
-    static_assert(BUFS == 1 || BUFS == 2, "accumulator buffers");
-    static constexpr int HB = BN / 2;                    // tokens per half (N of one MMA)
-    static_assert(BN % 32 == 0 && HB >= 80 && HB <= 144, "wide token tile");
-    static constexpr uint32_t B_HALF_BYTES = HB * 128;   // HB rows x 64 fp16, a multiple of the 1024-byte swizzle atom
-    static constexpr uint32_t SLOT = S8W_A_BYTES + 2 * B_HALF_BYTES;
-    static constexpr uint32_t A_TMEM0 = BUFS * BN;       // after the accumulators
-    static constexpr uint32_t SX_BYTES = 2048;           // the tile's token scales
+    static constexpr int P = s8w_parts(BN);             // token parts
+    static constexpr int W = BN / P;                    // tokens per part: N of its MMA, columns of a region
+    static constexpr int REGIONS = P + 1;
+    static constexpr int HALF = W / 2;                  // columns of a region per epilogue warp
+    static_assert(BN % (16 * P) == 0 && W >= 64 && W <= 128 && HALF % 8 == 0, "wide token tile");
+    static constexpr uint32_t B_PART_BYTES = W * 128;   // W rows x 64 fp16, a multiple of the 1024-byte swizzle atom
+    static constexpr uint32_t SLOT = S8W_A_BYTES + P * B_PART_BYTES;
+    static constexpr uint32_t A_TMEM0 = REGIONS * W;    // after the accumulator regions
+    static constexpr uint32_t SX_BYTES = 2048;          // the tile's token scales
     static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t RING_BUDGET = MAX_DYN_SMEM - 1024 - SX_BYTES - BAR_BYTES;
     static constexpr int S_SMEM = int(RING_BUDGET / SLOT);
     static constexpr int S_TMEM = int((TMEM_COLS - A_TMEM0) / 32);
     static constexpr int S = S_SMEM < S_TMEM ? S_SMEM : S_TMEM;
     static_assert(S >= 4 && A_TMEM0 + 32 * S <= TMEM_COLS, "ring");
-    static_assert(3 * S + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
+    static_assert(3 * S + 2 * REGIONS + 1 <= int(BAR_BYTES / 8) - 1, "barrier area");
     static_assert(BN * 4 <= int(SX_BYTES), "scale area");
     static constexpr size_t SMEM = 1024 + size_t(S) * SLOT + SX_BYTES + BAR_BYTES;
-    static constexpr uint32_t IDESC = idesc_f16_f32(BM, HB);
-    static constexpr int LDW = 8;   // tensor-memory loads of 8 columns, double-buffered
-    static constexpr int GROUPS = HB / LDW;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, W);
 };
 
 // 32 lanes x 8 consecutive 32-bit columns, and the matching wait.
@@ -640,30 +648,32 @@ __device__ __forceinline__ void widen_row64_to_tmem(const uint8_t* stage, int r,
     }
 }
 
-// Output column n for the HB tokens t0 .. t0 + HB - 1 of one half: the
-// post-scale epilogue of s8_store, or the int32 sums.
-template <int EPI, int HB>
-__device__ __forceinline__ void s8w_store(const int32_t (&acc)[HB], const S8Params& p, int n, int t0,
+// Output column n for the tokens t0 .. t0 + CNT - 1 (a part's columns held
+// by one epilogue warp): the post-scale epilogue of s8_store, 8 tokens at a
+// time, or the int32 sums.
+template <int EPI, int CNT>
+__device__ __forceinline__ void s8w_store(const int32_t (&acc)[CNT], const S8Params& p, int n, int t0,
                                           const float* sxs, float swn, float bn) {
+    static_assert(CNT % 8 == 0, "token groups");
     if (n >= p.M) return;
     if constexpr (EPI == kEpiPostscaleS32) {
         int32_t* out = static_cast<int32_t*>(p.out) + static_cast<int64_t>(t0) * p.M + n;
 #pragma unroll
-        for (int t = 0; t < HB; ++t) {
+        for (int t = 0; t < CNT; ++t) {
             if (t0 + t < p.N) *out = acc[t];
             out += p.M;
         }
     } else {
         uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(t0) * p.M + n;
 #pragma unroll
-        for (int g = 0; g < HB; g += 16) {
+        for (int g = 0; g < CNT; g += 8) {
             if (t0 + g >= p.N) break;
-            float sv[16];
+            float sv[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sv[e] = sxs[t0 + g + e];
-            uint32_t y[8];
+            for (int e = 0; e < 8; ++e) sv[e] = sxs[t0 + g + e];
+            uint32_t y[4];
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
+            for (int e = 0; e < 8; e += 2) {
                 float v0 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e]), sv[e]), swn);
                 float v1 = __fmul_rn(__fmul_rn(__int2float_rn(acc[g + e + 1]), sv[e + 1]), swn);
                 if (p.bias) {
@@ -674,12 +684,30 @@ __device__ __forceinline__ void s8w_store(const int32_t (&acc)[HB], const S8Para
                 y[e / 2] = *reinterpret_cast<uint32_t*>(&h);
             }
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
+            for (int e = 0; e < 8; ++e) {
                 if (t0 + g + e < p.N) *out = static_cast<uint16_t>(y[e / 2] >> (16 * (e & 1)));
                 out += p.M;
             }
         }
     }
+}
+
+// Local stages of a work unit (of n) at which token part q of P starts an
+// exact 1024-K chunk: stage 0, and every stage j with (j + q * (16 / P)) a
+// multiple of 16 -- so part 0 at 16, 32, ...; with two parts part 1 at 8,
+// 24, ...; with three parts part 1 at 11, 27, ... and part 2 at 6, 22, ...
+// No two parts start a chunk at the same stage after stage 0.
+template <int P>
+__device__ __forceinline__ bool s8w_chunk_start(int q, int j) {
+    return j == 0 || (j + q * (S8W_CHUNK_STAGES / P)) % S8W_CHUNK_STAGES == 0;
+}
+// The part whose chunk starts at local stage j > 0, or -1.
+template <int P>
+__device__ __forceinline__ int s8w_part_starting(int j) {
+#pragma unroll
+    for (int q = 0; q < P; ++q)
+        if ((j + q * (S8W_CHUNK_STAGES / P)) % S8W_CHUNK_STAGES == 0) return q;
+    return -1;
 }
 
 enum WaitSiteS8W : int {
@@ -692,23 +720,52 @@ enum WaitSiteS8W : int {
     kSiteS8WMmaDrain = 27,
 };
 
-template <int EPI, int BN, int BUFS>
+// Fold a region's chunk into one warp's int32 sums: HALF columns from taddr,
+// 8 at a time, the next load in flight while the last is converted.
+template <int HALF>
+__device__ __forceinline__ void s8w_fold(int32_t (&acc)[HALF], uint32_t taddr) {
+    constexpr int G = HALF / 8;
+    uint32_t ra[8], rb[8];
+    tmem_ld_32x32b_x8(taddr, ra);
+    tmem_wait_ld_regs8(ra);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        uint32_t(&cur)[8] = (j & 1) ? rb : ra;
+        uint32_t(&nxt)[8] = (j & 1) ? ra : rb;
+        if (j + 1 < G) tmem_ld_32x32b_x8(taddr + (j + 1) * 8, nxt);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j * 8 + e] += __float2int_rz(__uint_as_float(cur[e]));
+        if (j + 1 < G) tmem_wait_ld_regs8(nxt);
+    }
+}
+
+// Region of token part q in a packed table (two bits per part), and the table
+// after part q moves into region r.
+__device__ __forceinline__ int s8w_region(uint32_t table, int q) { return static_cast<int>((table >> (2 * q)) & 3u); }
+__device__ __forceinline__ uint32_t s8w_move(uint32_t table, int q, int r) {
+    return (table & ~(3u << (2 * q))) | (static_cast<uint32_t>(r) << (2 * q));
+}
+
+template <int EPI, int BN>
 __global__ void __launch_bounds__(S8W_THREADS, 1)
     gemm_s8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const S8Params p) {
     grid_launch_dependents();
-    using C = CfgS8W<BN, BUFS>;
+    using C = CfgS8W<BN>;
     constexpr int S = C::S;
-    constexpr int HB = C::HB;
+    constexpr int P = C::P;
+    constexpr int W = C::W;
+    constexpr int HALF = C::HALF;
+    constexpr uint32_t TABLE0 = P == 3 ? 0x24u : 0x4u;  // part q starts in region q; region P is free
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sxs = reinterpret_cast<float*>(ring + S * C::SLOT);
     uint64_t* full8 = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sxs) + C::SX_BYTES);
     uint64_t* full16 = full8 + S;
     uint64_t* empty = full16 + S;
-    uint64_t* acc_full = empty + S;  // per accumulator buffer
-    uint64_t* acc_empty = acc_full + 2;
-    uint64_t* mma_drain = acc_empty + 2;
+    uint64_t* acc_full = empty + S;  // per accumulator region
+    uint64_t* acc_empty = acc_full + C::REGIONS;
+    uint64_t* mma_drain = acc_empty + C::REGIONS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -722,9 +779,9 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
             mbar_init(&full16[s], 4);  // the four converter warps
             mbar_init(&empty[s], 1);   // the MMA commit
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 8);  // the eight epilogue warps
+        for (int r = 0; r < C::REGIONS; ++r) {
+            mbar_init(&acc_full[r], 1);   // the MMA commit at the end of a part's chunk
+            mbar_init(&acc_empty[r], 8);  // the eight epilogue warps, after the fold
         }
         mbar_init(mma_drain, 1);
         fence_mbarrier_init();
@@ -743,7 +800,7 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
     if (warp != 0) grid_dependency_wait();
     const uint32_t tmem_base = *tmem_slot;
     if (warp < 4) {
-      regs_dec<56>();
+      regs_dec<64>();
       if (warp == 0) {
         // ------------------------------------------------------------ producer
         const bool elected = elect_one_sync();
@@ -776,8 +833,10 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
                         mbar_arrive_expect_tx(&full8[stage], C::SLOT);
                         tma_load_2d(slot, &tmA, &full8[stage], ks * S8W_BK, mb * BM);
                     }
-                    tma_load_2d(slot + S8W_A_BYTES, &tmB, &full8[stage], ks * S8W_BK, 0);
-                    tma_load_2d(slot + S8W_A_BYTES + C::B_HALF_BYTES, &tmB, &full8[stage], ks * S8W_BK, HB);
+#pragma unroll
+                    for (int q = 0; q < P; ++q)
+                        tma_load_2d(slot + S8W_A_BYTES + q * C::B_PART_BYTES, &tmB, &full8[stage], ks * S8W_BK,
+                                    q * W);
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -794,51 +853,70 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
         if (elect_one_sync()) {
             int stage = 0;
             uint32_t phase = 0;
-            int buf = 0;
-            uint32_t buf_phase = 0;
+            uint32_t table = TABLE0;  // region of each part
+            int free_r = P;           // the region no part uses
+            uint32_t used = 0;        // bit r: parity of the chunks committed to region r
             bool ok = true;
             const uint64_t desc0 = smem_desc_kmajor_sw128(smem_u32(ring + S8W_A_BYTES));
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
                 int mb, ks0, ks1;
                 s8_unit(u, p, mb, ks0, ks1);
-                const int nchunks = (ks1 - ks0 + S8W_CHUNK_STAGES - 1) / S8W_CHUNK_STAGES;
-                for (int c = 0; ok && c < nchunks; ++c) {
-                    // the epilogue has read this buffer's previous chunk out of it
-                    if (!mbar_wait(&acc_empty[buf], buf_phase ^ 1u, kSiteS8WMmaAccEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                    const int s0 = ks0 + c * S8W_CHUNK_STAGES;
-                    const int s1 = min(ks1, s0 + S8W_CHUNK_STAGES);
-                    for (int ks = s0; ks < s1; ++ks) {
-                        if (!mbar_wait(&full16[stage], phase, kSiteS8WMmaFull)) {
+                const int n = ks1 - ks0;
+                // every region a part starts in has been folded (the previous unit's last chunks)
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    const int r = s8w_region(table, q);
+                    ok = ok && mbar_wait(&acc_empty[r], ((used >> r) & 1u) ^ 1u, kSiteS8WMmaAccEmpty);
+                }
+                if (!ok) break;
+                tc_fence_after();
+                for (int j = 0; j < n; ++j) {
+                    const int qs = j > 0 ? s8w_part_starting<P>(j) : -1;
+                    if (qs >= 0) {
+                        // part qs's chunk is complete: the epilogue folds its region while
+                        // the part goes on in the free one, once that one's last fold is done
+                        const int old = s8w_region(table, qs);
+                        mma_commit(&acc_full[old]);
+                        used ^= 1u << old;
+                        table = s8w_move(table, qs, free_r);
+                        const int r = free_r;
+                        free_r = old;
+                        if (!mbar_wait(&acc_empty[r], ((used >> r) & 1u) ^ 1u, kSiteS8WMmaAccEmpty)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_tmem = tmem_base + C::A_TMEM0 + static_cast<uint32_t>(stage * 32);
-                        const uint64_t db = desc0 + static_cast<uint64_t>((stage * C::SLOT) >> 4);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int k = 0; k < S8W_BK / 16; ++k)
-                                mma_f16_ts(d_tmem + static_cast<uint32_t>(h * HB), a_tmem + k * 8,
-                                           db + static_cast<uint64_t>((h * C::B_HALF_BYTES + k * 32) >> 4), C::IDESC,
-                                           (ks > s0 || k > 0) ? 1u : 0u);
-                        mma_commit(&empty[stage]);
-                        if (++stage == S) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
                     }
-                    if (!ok) break;
-                    mma_commit(&acc_full[buf]);
-                    if (++buf == BUFS) {
-                        buf = 0;
-                        buf_phase ^= 1u;
+                    if (!mbar_wait(&full16[stage], phase, kSiteS8WMmaFull)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem_base + C::A_TMEM0 + static_cast<uint32_t>(stage * 32);
+                    const uint64_t db = desc0 + static_cast<uint64_t>((stage * C::SLOT) >> 4);
+#pragma unroll
+                    for (int q = 0; q < P; ++q) {
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(s8w_region(table, q) * W);
+                        const uint32_t first = s8w_chunk_start<P>(q, j) ? 0u : 1u;
+#pragma unroll
+                        for (int k = 0; k < S8W_BK / 16; ++k)
+                            mma_f16_ts(d, a_tmem + k * 8,
+                                       db + static_cast<uint64_t>((q * C::B_PART_BYTES + k * 32) >> 4), C::IDESC,
+                                       k > 0 ? 1u : first);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                // the parts' last chunks of the unit
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    const int r = s8w_region(table, q);
+                    mma_commit(&acc_full[r]);
+                    used ^= 1u << r;
                 }
             }
             mma_commit(mma_drain);
@@ -846,7 +924,7 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
         }
       }
     } else if (warp < S8W_EPI_WARP0) {
-        regs_dec<72>();
+        regs_dec<64>();
         // ------------------------------------------------------------ converters (warps 4..7)
         const int r = ((warp & 3) << 5) | lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::A_TMEM0;
@@ -878,87 +956,95 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
     } else {
         regs_inc<192>();
         // ------------------------------------------------------------ epilogue (warps 8..15)
-        constexpr int LDW = C::LDW;
-        constexpr int GROUPS = C::GROUPS;
         const int quarter = warp & 3;
-        const int half = (warp - S8W_EPI_WARP0) >> 2;
-        const int t0 = half * HB;                                         // first token of this half
+        const int ch = (warp - S8W_EPI_WARP0) >> 2;                       // column half of every part
         const int et = static_cast<int>(threadIdx.x) - 32 * S8W_EPI_WARP0;  // 0..255
         for (int i = et; i < BN; i += 256)
             sxs[i] = (EPI == kEpiPostscaleBf16 && i < p.N) ? __ldg(p.sx + i) : 0.0f;
         named_bar_sync(1, 256);  // the eight epilogue warps
-        int buf = 0;
-        uint32_t buf_phase = 0;
+        uint32_t table = TABLE0;  // the MMA issuer's region table, replayed
+        int free_r = P;
+        uint32_t folded = 0;      // bit r: parity of the folds of region r
         bool ok = true;
-        const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(t0);
+        const uint32_t lane_base =
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(ch * HALF);
         for (int u = cta; ok && u < p.num_tiles; u += nctas) {
             int mb, ks0, ks1;
             s8_unit(u, p, mb, ks0, ks1);
-            const int nchunks = (ks1 - ks0 + S8W_CHUNK_STAGES - 1) / S8W_CHUNK_STAGES;
-            const int n = mb * BM + quarter * 32 + lane;
+            const int n_st = ks1 - ks0;
+            const int n = mb * BM + quarter * 32 + lane;  // output column (weight row)
             float swn = 0.0f, bn = 0.0f;
             if (EPI == kEpiPostscaleBf16 && n < p.M) {
                 swn = __ldg(p.sw + n);
                 if (p.bias) bn = __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16);
             }
-            int32_t acc[HB];
+            int32_t acc[P][HALF];
 #pragma unroll
-            for (int e = 0; e < HB; ++e) acc[e] = 0;
-            for (int c = 0; c < nchunks; ++c) {
-                if (!mbar_wait(&acc_full[buf], buf_phase, kSiteS8WEpiAccFull)) {
-                    ok = false;
-                    break;
-                }
+            for (int q = 0; q < P; ++q)
+#pragma unroll
+                for (int e = 0; e < HALF; ++e) acc[q][e] = 0;
+            // fold part q's chunk from region r into the part's sums
+            auto fold = [&](int q, int r) -> bool {
+                if (!mbar_wait(&acc_full[r], (folded >> r) & 1u, kSiteS8WEpiAccFull)) return false;
+                folded ^= 1u << r;
                 tc_fence_after();
-                const uint32_t taddr = taddr0 + static_cast<uint32_t>(buf * BN);
-                uint32_t ra[LDW], rb[LDW];
-                tmem_ld_32x32b_x8(taddr, ra);
-                tmem_wait_ld_regs8(ra);
+                const uint32_t taddr = lane_base + static_cast<uint32_t>(r * W);
 #pragma unroll
-                for (int j = 0; j < GROUPS; ++j) {
-                    uint32_t(&cur)[LDW] = (j & 1) ? rb : ra;
-                    uint32_t(&nxt)[LDW] = (j & 1) ? ra : rb;
-                    if (j + 1 < GROUPS) tmem_ld_32x32b_x8(taddr + (j + 1) * LDW, nxt);
-#pragma unroll
-                    for (int e = 0; e < LDW; ++e) acc[j * LDW + e] += __float2int_rz(__uint_as_float(cur[e]));
-                    if (j + 1 < GROUPS) tmem_wait_ld_regs8(nxt);
-                }
+                for (int qq = 0; qq < P; ++qq)
+                    if (qq == q) s8w_fold<HALF>(acc[qq], taddr);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
-                if (++buf == BUFS) {
-                    buf = 0;
-                    buf_phase ^= 1u;
-                }
+                if (lane == 0) mbar_arrive(&acc_empty[r]);
+                return true;
+            };
+            for (int j = 1; ok && j < n_st; ++j) {
+                const int qs = s8w_part_starting<P>(j);
+                if (qs < 0) continue;
+                const int old = s8w_region(table, qs);
+                ok = fold(qs, old);
+                table = s8w_move(table, qs, free_r);
+                free_r = old;
             }
+#pragma unroll
+            for (int q = 0; q < P; ++q) ok = ok && fold(q, s8w_region(table, q));
             if (!ok) break;
             if (p.k_split == 1) {
-                s8w_store<EPI, HB>(acc, p, n, t0, sxs, swn, bn);
-            } else {
-                if (n < p.M) {
-                    int32_t* dst = p.partial + static_cast<int64_t>(t0) * p.M + n;
 #pragma unroll
-                    for (int t = 0; t < HB; ++t) {
-                        if (t0 + t < p.N) atomicAdd(dst, acc[t]);
-                        dst += p.M;
+                for (int q = 0; q < P; ++q) s8w_store<EPI, HALF>(acc[q], p, n, q * W + ch * HALF, sxs, swn, bn);
+            } else {
+                // add this unit's sums; the warp completing the (row group, column half) writes it
+                if (n < p.M) {
+#pragma unroll
+                    for (int q = 0; q < P; ++q) {
+                        const int t0 = q * W + ch * HALF;
+                        int32_t* dst = p.partial + static_cast<int64_t>(t0) * p.M + n;
+#pragma unroll
+                        for (int t = 0; t < HALF; ++t) {
+                            if (t0 + t < p.N) atomicAdd(dst, acc[q][t]);
+                            dst += p.M;
+                        }
                     }
                 }
                 __threadfence();
                 __syncwarp();
                 int arrived = 0;
-                if (lane == 0) arrived = atomicAdd(p.counters + mb * 8 + half * 4 + quarter, 1);
+                if (lane == 0) arrived = atomicAdd(p.counters + mb * 8 + ch * 4 + quarter, 1);
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == p.k_split - 1) {
                     __threadfence();
-                    if (n < p.M) {
-                        const int32_t* src = p.partial + static_cast<int64_t>(t0) * p.M + n;
 #pragma unroll
-                        for (int t = 0; t < HB; ++t) {
-                            if (t0 + t < p.N) acc[t] = __ldcg(src);
-                            src += p.M;
+                    for (int q = 0; q < P; ++q) {
+                        const int t0 = q * W + ch * HALF;
+                        if (n < p.M) {
+                            const int32_t* src = p.partial + static_cast<int64_t>(t0) * p.M + n;
+#pragma unroll
+                            for (int t = 0; t < HALF; ++t) {
+                                if (t0 + t < p.N) acc[q][t] = __ldcg(src);
+                                src += p.M;
+                            }
                         }
+                        s8w_store<EPI, HALF>(acc[q], p, n, t0, sxs, swn, bn);
                     }
-                    s8w_store<EPI, HB>(acc, p, n, t0, sxs, swn, bn);
                 }
             }
         }
@@ -971,6 +1057,7 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
+
 
 // Whether each kernel instance (epilogue x token tile) has its shared-memory
 // attribute set, per device: five narrow and five wide token tiles per epilogue.
@@ -1044,19 +1131,12 @@ cudaError_t launch_s8_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S
     return launch_s8_kernel(gemm_s8_kernel<EPI, BN>, id, CfgS8<BN>::SMEM, S8_THREADS, tmA, tmB, p, ctas, st);
 }
 
-// The 160-token tile double-buffers its accumulator (2 x 160 columns beside
-// six 64-K stages in tensor memory): the MMAs of the next chunk run while the
-// epilogue folds the last.  Wider tiles have one accumulator and wait for
-// the fold (at 192 tokens two accumulators would leave four stages, which
-// measured slower than six stages and the wait).
 template <int EPI, int BN>
 cudaError_t launch_s8w_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S8Params& p, int ctas,
                           cudaStream_t st) {
     constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + 5 + (BN - 160) / 32;
     static_assert(BN >= 160 && BN <= 288 && BN % 32 == 0, "wide token tile");
-    constexpr int BUFS = BN == 160 ? 2 : 1;
-    using C = CfgS8W<BN, BUFS>;
-    return launch_s8_kernel(gemm_s8w_kernel<EPI, BN, BUFS>, id, C::SMEM, S8W_THREADS, tmA, tmB, p, ctas, st);
+    return launch_s8_kernel(gemm_s8w_kernel<EPI, BN>, id, CfgS8W<BN>::SMEM, S8W_THREADS, tmA, tmB, p, ctas, st);
 }
 
 constexpr int S8_NARROW_MAX_TOKENS = 96;  // gemm_s8_kernel up to this many tokens, gemm_s8w_kernel beyond
@@ -1103,10 +1183,10 @@ cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num
     }
     const int bn = s8_token_tile(T);
     {
-        // the narrow kernel loads all bn token rows per box, the wide one each half
+        // the narrow kernel loads all bn token rows per box, the wide one each part
         cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
         cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(wide ? bn / 2 : bn)};
+        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(wide ? bn / s8w_parts(bn) : bn)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
