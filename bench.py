@@ -1024,6 +1024,8 @@ PROFILE_CASES = {
     "linear_codes_decode_1x13824x5120": ("linear_codes", 1, 13824, 5120),
     "linear_codes_77x13824x5120": ("linear_codes", 77, 13824, 5120),
     "linear_codes_77x3072x5120": ("linear_codes", 77, 3072, 5120),
+    "linear_codes_257x13824x5120": ("linear_codes", 257, 13824, 5120),
+    "linear_codes_160x15432x5120": ("linear_codes", 160, 15432, 5120),
 }
 
 
