@@ -150,17 +150,18 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
 
 
 # The int8-operand kernels at their boundaries: every token tile (16, 32, 64,
-# 96, 128 on the narrow kernel; 160, 192, 224, 256, 288 on the wide one, whose
-# tile is two halves), both sides of the split rule (at most 76 weight tiles
-# and 256 K per split), a last stage of 16 K (zero-filled past K), and a last
-# weight tile of one row.
+# 96 on the narrow kernel; 128, 160, 192, 224, 256 in two token parts and 288
+# in three on the wide one), both sides of the split rule (at most 76 weight
+# tiles and 256 K per split), a last stage of 16 K (zero-filled past K), and
+# a last weight tile of one row.
 @pytest.mark.parametrize("M,N,K,bias", [
     (5, 300, 5120, True),      # 16-token tile, 3 weight tiles: K split 8 ways
     (17, 1000, 1040, False),   # 32-token tile, 9 stages (the last 16 K): split 3 ways
     (96, 9728, 640, True),     # 96-token tile, 76 weight tiles: split 2 ways
-    (97, 9856, 512, False),    # 128-token tile, 77 weight tiles: no split
+    (97, 9856, 512, False),    # wide 128-token tile, 77 weight tiles: no split
     (64, 129, 16400, True),    # a last weight tile of one row, 129 stages, split 8 ways
-    (128, 2048, 384, False),   # 3 stages: too few to split
+    (128, 2048, 384, False),   # 6 stages of 64 K: too few to split
+    (120, 700, 4096, True),    # wide 128-token tile, 6 weight tiles: split 8 ways
     (129, 300, 5120, True),    # 160-token tile (half 1 mostly zero rows): split 8 ways
     (160, 1000, 1040, False),  # 160 exactly, 17 stages of 64 K (the last 16 K): split 4 ways
     (193, 9728, 640, True),    # 224-token tile, 76 weight tiles, one SM each: no split
@@ -171,6 +172,29 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
 ])
 def test_gemm_postscale_int8_operands(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
+
+
+@pytest.mark.parametrize("M", [77, 200])
+def test_int8_operands_repeatable_after_fresh_quantization(w8a8, M):
+    """The int8-operand kernels right after the quantization kernels that
+    produce their operands, on fresh inputs every time: two GEMMs on the same
+    codes must agree bit for bit, 150 times over.  The narrow kernel's two
+    converter warpgroups take alternate stages of an odd-length ring; with one
+    full barrier per slot, a group could pass its wait while the other
+    group's earlier copy into the slot was still landing (copies complete out
+    of order), and convert a half-written stage -- a wrong tile, or a stall,
+    a few times in a few hundred launches."""
+    N, K = 13824, 5120
+    g = torch.Generator(device=DEV).manual_seed(7)
+    for _ in range(150):
+        X = torch.randn((M, K), generator=g, device=DEV).to(torch.bfloat16)
+        W = (0.02 * torch.randn((N, K), generator=g, device=DEV)).to(torch.bfloat16)
+        Xq, sx = w8a8.quantize_act(X)
+        Wq, sw = w8a8.quantize_weight(W)
+        Y1 = w8a8.gemm_postscale(Xq, sx, Wq, sw)
+        Y2 = w8a8.gemm_postscale(Xq, sx, Wq, sw)
+        assert torch.equal(Y1, Y2)
+    assert w8a8.get_device_error() == (0, 0)
 
 
 # At most 4 tokens (M * K <= 131072): a CUDA-core GEMV on the int8 codes

@@ -107,7 +107,7 @@ struct CfgS8 {
     static constexpr int S_TMEM = int((TMEM_COLS - A_TMEM0) / 64);
     static constexpr int S = S_SMEM < S_TMEM ? S_SMEM : S_TMEM;
     static_assert(S >= 3 && A_TMEM0 + 64 * S <= TMEM_COLS, "ring");
-    static_assert(3 * S + 5 <= int(BAR_BYTES / 8) - 1, "barrier area");
+    static_assert(4 * S + 5 <= int(BAR_BYTES / 8) - 1 && 2 * S <= 32, "barrier area, barrier bitmasks");
     static constexpr size_t SMEM = 1024 + size_t(S) * SLOT + SX_BYTES + BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
     static constexpr int LDW = 16;  // tensor-memory loads of 16 columns: the 128 int32 sums stay in registers
@@ -246,8 +246,15 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sxs = reinterpret_cast<float*>(ring + S * C::SLOT);
+    // full8[g * S + s]: the copies of slot s for a stage of converter group g.
+    // The groups take alternate stages and S may be odd, so a slot serves
+    // both groups in turn; with one barrier per slot a group would wait on
+    // only every other phase of it, and a parity wait cannot tell the other
+    // group's earlier phase still in flight (copies land out of order) from
+    // its own phase complete.  One barrier per slot and group lets every
+    // waiter see every phase of the barriers it waits on.
     uint64_t* full8 = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sxs) + C::SX_BYTES);
-    uint64_t* full16 = full8 + S;
+    uint64_t* full16 = full8 + 2 * S;
     uint64_t* empty = full16 + S;
     uint64_t* acc_full = empty + S;
     uint64_t* acc_empty = acc_full + 2;
@@ -261,9 +268,10 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full8[s], 1);   // the producer's arrive + the slot's bytes
-            mbar_init(&full16[s], 4);  // the four converter warps of the stage's group
-            mbar_init(&empty[s], 1);   // the MMA commit
+            mbar_init(&full8[s], 1);       // the producer's arrive + the slot's bytes (group 0)
+            mbar_init(&full8[S + s], 1);   // (group 1)
+            mbar_init(&full16[s], 4);      // the four converter warps of the stage's group
+            mbar_init(&empty[s], 1);       // the MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -298,33 +306,38 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             s8_unit(cta, p, mb, ks0, ks1);
             pre = min(S, ks1 - ks0);
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full8[i], C::SLOT);
-                tma_load_2d(ring + i * C::SLOT, &tmA, &full8[i], (ks0 + i) * S8_BK, mb * BM);
+                uint64_t* bar = &full8[(i % S8_CONV_GROUPS) * S + i];
+                mbar_arrive_expect_tx(bar, C::SLOT);
+                tma_load_2d(ring + i * C::SLOT, &tmA, bar, (ks0 + i) * S8_BK, mb * BM);
             }
         }
         grid_dependency_wait();
         if (elected) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t armed = 0, armed_phase = 0;
+            int g_stage = 0;                        // stage count of this CTA (all its units)
+            uint32_t uses = 0;                      // bit b: parity of the uses of full8[b] so far
+            uint32_t armed = 0, armed_phase = 0;    // per full8 barrier: used, and its last use's parity
             bool ok = true;
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
                 int mb, ks0, ks1;
                 s8_unit(u, p, mb, ks0, ks1);
-                for (int ks = ks0; ks < ks1; ++ks) {
+                for (int ks = ks0; ks < ks1; ++ks, ++g_stage) {
                     uint8_t* slot = ring + stage * C::SLOT;
+                    const int b = (g_stage % S8_CONV_GROUPS) * S + stage;
                     if (!(u == cta && ks - ks0 < pre)) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteS8ProducerEmpty)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full8[stage], C::SLOT);
-                        tma_load_2d(slot, &tmA, &full8[stage], ks * S8_BK, mb * BM);
+                        mbar_arrive_expect_tx(&full8[b], C::SLOT);
+                        tma_load_2d(slot, &tmA, &full8[b], ks * S8_BK, mb * BM);
                     }
-                    tma_load_2d(slot + S8_A_BYTES, &tmB, &full8[stage], ks * S8_BK, 0);
-                    tma_load_2d(slot + S8_A_BYTES + C::B_BOX_BYTES, &tmB, &full8[stage], ks * S8_BK + 64, 0);
-                    armed |= 1u << stage;
-                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                    tma_load_2d(slot + S8_A_BYTES, &tmB, &full8[b], ks * S8_BK, 0);
+                    tma_load_2d(slot + S8_A_BYTES + C::B_BOX_BYTES, &tmB, &full8[b], ks * S8_BK + 64, 0);
+                    armed |= 1u << b;
+                    armed_phase = (armed_phase & ~(1u << b)) | (((uses >> b) & 1u) << b);
+                    uses ^= 1u << b;
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -332,8 +345,8 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                 }
             }
             // Every copy issued has landed before this CTA's shared memory is released.
-            for (int s = 0; s < S; ++s)
-                if (armed & (1u << s)) mbar_wait(&full8[s], (armed_phase >> s) & 1u, kSiteS8ProducerDrain);
+            for (int b = 0; b < S8_CONV_GROUPS * S; ++b)
+                if (armed & (1u << b)) mbar_wait(&full8[b], (armed_phase >> b) & 1u, kSiteS8ProducerDrain);
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -397,8 +410,8 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
         const int r = ((warp & 3) << 5) | lane;  // weight row of the tile = tensor-memory lane
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::A_TMEM0;
         int stage = 0;
-        uint32_t phase = 0;
         int g_stage = 0;                       // stage count of this CTA (all its units)
+        uint32_t uses = 0;                     // bit s: parity of this group's uses of full8[group * S + s]
         bool ok = true;
         for (int u = cta; ok && u < p.num_tiles; u += nctas) {
             int mb, ks0, ks1;
@@ -407,10 +420,11 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                 if (g_stage % S8_CONV_GROUPS == group) {
                     // the slot's copies landed, so the MMAs that last read this
                     // tensor-memory stage have completed (their commit freed the slot)
-                    if (!mbar_wait(&full8[stage], phase, kSiteS8ConvFull)) {
+                    if (!mbar_wait(&full8[group * S + stage], (uses >> stage) & 1u, kSiteS8ConvFull)) {
                         ok = false;
                         break;
                     }
+                    uses ^= 1u << stage;
                     tc_fence_after();
                     widen_row_to_tmem(ring + stage * C::SLOT, r, lane_base + static_cast<uint32_t>(stage * 64));
                     tmem_wait_st();
@@ -418,10 +432,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&full16[stage]);
                 }
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                if (++stage == S) stage = 0;
             }
         }
     } else {
@@ -544,12 +555,13 @@ __global__ void __launch_bounds__(256) s8_prep_kernel(const uint4* __restrict__ 
 // the whole token tile no longer fit in tensor memory beside the widened
 // weights, and one alone would stop the MMAs at every 1024-K chunk while the
 // epilogue folds it into int32.  So the tile is cut into P token parts of W
-// columns (P = 3 at 288 tokens, else 2; one MMA of N = W per part) that share
-// P + 1 accumulator regions of W columns: the parts' chunks end at staggered
-// stages (s8w_chunk_start), and at the end of a chunk a part moves on into the
-// free region while the epilogue folds the one it leaves.  The MMAs never
-// wait for a fold as long as it ends within the 5..8 stages before the next
-// part's chunk ends.  The token image of a 128-K stage would take 72 KB at
+// columns (P = 3 at 288 tokens, else 2; one MMA of N = W per part) that
+// share P + 1 accumulator regions of W columns: the parts' chunks end at
+// staggered stages (s8w_chunk_start), and at the end of a chunk a part moves
+// on into the free region while the epilogue folds the one it leaves.  The
+// MMAs never wait for a fold as long as it ends within the 16 / P stages
+// before the next part's chunk ends.  (Smaller parts cost more than they
+// save: a tcgen05.mma of N <= ~112 takes about as long as one of N = 112.)  The token image of a 128-K stage would take 72 KB at
 // BN = 288, so stages are 64 K wide: the int8 weight tile [128 rows x 64
 // bytes] arrives with the 64-byte swizzle and the token image [BN rows x 64
 // K] as P boxes of W rows with the 128-byte swizzle.
@@ -578,7 +590,7 @@ struct CfgS8W {
     static constexpr int W = BN / P;                    // tokens per part: N of its MMA, columns of a region
     static constexpr int REGIONS = P + 1;
     static constexpr int HALF = W / 2;                  // columns of a region per epilogue warp
-    static_assert(BN % (16 * P) == 0 && W >= 64 && W <= 128 && HALF % 8 == 0, "wide token tile");
+    static_assert(BN % (16 * P) == 0 && W >= 64 && W <= 128 && HALF % 8 == 0 && P <= 4, "wide token tile");
     static constexpr uint32_t B_PART_BYTES = W * 128;   // W rows x 64 fp16, a multiple of the 1024-byte swizzle atom
     static constexpr uint32_t SLOT = S8W_A_BYTES + P * B_PART_BYTES;
     static constexpr uint32_t A_TMEM0 = REGIONS * W;    // after the accumulator regions
@@ -739,11 +751,18 @@ __device__ __forceinline__ void s8w_fold(int32_t (&acc)[HALF], uint32_t taddr) {
     }
 }
 
-// Region of token part q in a packed table (two bits per part), and the table
-// after part q moves into region r.
-__device__ __forceinline__ int s8w_region(uint32_t table, int q) { return static_cast<int>((table >> (2 * q)) & 3u); }
+// Region of token part q in a packed table (four bits per part), and the
+// table after part q moves into region r.
+__device__ __forceinline__ int s8w_region(uint32_t table, int q) { return static_cast<int>((table >> (4 * q)) & 15u); }
 __device__ __forceinline__ uint32_t s8w_move(uint32_t table, int q, int r) {
-    return (table & ~(3u << (2 * q))) | (static_cast<uint32_t>(r) << (2 * q));
+    return (table & ~(15u << (4 * q))) | (static_cast<uint32_t>(r) << (4 * q));
+}
+// The starting table: part q in region q (region P is free).
+template <int P>
+__host__ __device__ constexpr uint32_t s8w_table0() {
+    uint32_t t = 0;
+    for (int q = 0; q < P; ++q) t |= static_cast<uint32_t>(q) << (4 * q);
+    return t;
 }
 
 template <int EPI, int BN>
@@ -756,7 +775,7 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
     constexpr int P = C::P;
     constexpr int W = C::W;
     constexpr int HALF = C::HALF;
-    constexpr uint32_t TABLE0 = P == 3 ? 0x24u : 0x4u;  // part q starts in region q; region P is free
+    constexpr uint32_t TABLE0 = s8w_table0<P>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sxs = reinterpret_cast<float*>(ring + S * C::SLOT);
@@ -1060,7 +1079,7 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
 
 
 // Whether each kernel instance (epilogue x token tile) has its shared-memory
-// attribute set, per device: five narrow and five wide token tiles per epilogue.
+// attribute set, per device: four narrow and six wide token tiles per epilogue.
 bool g_configured[64][20];
 
 // Int8-operand GEMM plan for a weight matrix of N rows and K columns:
@@ -1127,25 +1146,26 @@ cudaError_t launch_s8_kernel(Kernel k, int id, size_t smem, int threads, const C
 template <int EPI, int BN>
 cudaError_t launch_s8_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S8Params& p, int ctas,
                          cudaStream_t st) {
-    constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + (BN == 16 ? 0 : BN == 32 ? 1 : BN == 64 ? 2 : BN == 96 ? 3 : 4);
+    constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + (BN == 16 ? 0 : BN == 32 ? 1 : BN == 64 ? 2 : 3);
+    static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 96, "narrow token tile");
     return launch_s8_kernel(gemm_s8_kernel<EPI, BN>, id, CfgS8<BN>::SMEM, S8_THREADS, tmA, tmB, p, ctas, st);
 }
 
 template <int EPI, int BN>
 cudaError_t launch_s8w_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const S8Params& p, int ctas,
                           cudaStream_t st) {
-    constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + 5 + (BN - 160) / 32;
-    static_assert(BN >= 160 && BN <= 288 && BN % 32 == 0, "wide token tile");
+    constexpr int id = (EPI == kEpiPostscaleS32 ? 10 : 0) + 4 + (BN - 128) / 32;
+    static_assert(BN >= 128 && BN <= 288 && BN % 32 == 0, "wide token tile");
     return launch_s8_kernel(gemm_s8w_kernel<EPI, BN>, id, CfgS8W<BN>::SMEM, S8W_THREADS, tmA, tmB, p, ctas, st);
 }
 
 constexpr int S8_NARROW_MAX_TOKENS = 96;  // gemm_s8_kernel up to this many tokens, gemm_s8w_kernel beyond
 
 // Token tile of the int8-operand GEMM for T tokens: the narrowest that holds
-// them (16 .. 96 on the narrow kernel, 160 .. 288 on the wide one).
+// them (16 .. 96 on the narrow kernel, 128 .. 288 in steps of 32 on the wide one).
 int s8_token_tile(int64_t T) {
     if (T <= S8_NARROW_MAX_TOKENS) return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 96;
-    return static_cast<int>((T + 31) / 32 * 32) < 160 ? 160 : static_cast<int>((T + 31) / 32 * 32);
+    return static_cast<int>((T + 31) / 32 * 32);
 }
 
 // The GEMM on int8 operands (M <= 288 tokens): s8_prep_kernel, then
@@ -1243,6 +1263,7 @@ cudaError_t launch_s8(const void* Xq, const void* Wq, const GemmArgs& a, int num
         case 32: return launch_s8_bn<EPI, 32>(tmA, tmB, p, ctas, st);
         case 64: return launch_s8_bn<EPI, 64>(tmA, tmB, p, ctas, st);
         case 96: return launch_s8_bn<EPI, 96>(tmA, tmB, p, ctas, st);
+        case 128: return launch_s8w_bn<EPI, 128>(tmA, tmB, p, ctas, st);
         case 160: return launch_s8w_bn<EPI, 160>(tmA, tmB, p, ctas, st);
         case 192: return launch_s8w_bn<EPI, 192>(tmA, tmB, p, ctas, st);
         case 224: return launch_s8w_bn<EPI, 224>(tmA, tmB, p, ctas, st);
