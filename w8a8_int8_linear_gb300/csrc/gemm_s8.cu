@@ -90,6 +90,7 @@ constexpr int S8_CHUNK_STAGES = 8;           // 1024 K per exact fp32 chunk
 constexpr uint32_t S8_A_BYTES = BM * S8_BK;  // 16 KB
 constexpr int S8_SPLIT_MAX_TILES = 76;       // K splits only when the weight rows make at most this many tiles
 constexpr int S8_SPLIT_MAX = 8;
+constexpr int S8_PREFETCH = 8;               // weight stages asked into L2 ahead of their load (1024 K)
 
 template <int BN_>
 struct CfgS8 {
@@ -131,6 +132,16 @@ __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& lo, uint4& h
     }
     lo = make_uint4(o[0], o[1], o[2], o[3]);
     hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Bring a 2-D tile of the tensor into L2 ahead of its load (no shared-memory
+// destination, nothing to wait for): the weight stream of these kernels is
+// latency-bound with a ring of a few stages, and loads that hit L2 keep it full.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // Widen weight row r of an int8 stage (128 rows x 128 bytes, as TMA wrote it
@@ -310,6 +321,8 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
                 mbar_arrive_expect_tx(bar, C::SLOT);
                 tma_load_2d(ring + i * C::SLOT, &tmA, bar, (ks0 + i) * S8_BK, mb * BM);
             }
+            for (int i = pre; i < min(S8_PREFETCH, ks1 - ks0); ++i)
+                tma_prefetch_l2_2d(&tmA, (ks0 + i) * S8_BK, mb * BM);
         }
         grid_dependency_wait();
         if (elected) {
@@ -322,9 +335,13 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
                 int mb, ks0, ks1;
                 s8_unit(u, p, mb, ks0, ks1);
+                if (!(u == cta && pre > 0))
+                    for (int i = S; i < min(S8_PREFETCH, ks1 - ks0); ++i)
+                        tma_prefetch_l2_2d(&tmA, (ks0 + i) * S8_BK, mb * BM);
                 for (int ks = ks0; ks < ks1; ++ks, ++g_stage) {
                     uint8_t* slot = ring + stage * C::SLOT;
                     const int b = (g_stage % S8_CONV_GROUPS) * S + stage;
+                    if (ks + S8_PREFETCH < ks1) tma_prefetch_l2_2d(&tmA, (ks + S8_PREFETCH) * S8_BK, mb * BM);
                     if (!(u == cta && ks - ks0 < pre)) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteS8ProducerEmpty)) {
                             ok = false;
@@ -573,6 +590,7 @@ __global__ void __launch_bounds__(256) s8_prep_kernel(const uint4* __restrict__ 
 //               and all eight fold each region the MMAs leave.
 constexpr int S8W_BK = 64;                      // K per stage (bytes of an int8 weight row)
 constexpr int S8W_CHUNK_STAGES = 16;            // 1024 K per exact fp32 chunk
+constexpr int S8W_PREFETCH = 16;                // weight stages asked into L2 ahead of their load (1024 K)
 constexpr uint32_t S8W_A_BYTES = BM * S8W_BK;   // 8 KB
 constexpr int S8W_THREADS = 512;
 constexpr int S8W_EPI_WARP0 = 8;
@@ -832,6 +850,8 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
                 mbar_arrive_expect_tx(&full8[i], C::SLOT);
                 tma_load_2d(ring + i * C::SLOT, &tmA, &full8[i], (ks0 + i) * S8W_BK, mb * BM);
             }
+            for (int i = pre; i < min(S8W_PREFETCH, ks1 - ks0); ++i)
+                tma_prefetch_l2_2d(&tmA, (ks0 + i) * S8W_BK, mb * BM);
         }
         grid_dependency_wait();
         if (elected) {
@@ -842,8 +862,12 @@ __global__ void __launch_bounds__(S8W_THREADS, 1)
             for (int u = cta; ok && u < p.num_tiles; u += nctas) {
                 int mb, ks0, ks1;
                 s8_unit(u, p, mb, ks0, ks1);
+                if (!(u == cta && pre > 0))
+                    for (int i = S; i < min(S8W_PREFETCH, ks1 - ks0); ++i)
+                        tma_prefetch_l2_2d(&tmA, (ks0 + i) * S8W_BK, mb * BM);
                 for (int ks = ks0; ks < ks1; ++ks) {
                     uint8_t* slot = ring + stage * C::SLOT;
+                    if (ks + S8W_PREFETCH < ks1) tma_prefetch_l2_2d(&tmA, (ks + S8W_PREFETCH) * S8W_BK, mb * BM);
                     if (!(u == cta && ks - ks0 < pre)) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, kSiteS8WProducerEmpty)) {
                             ok = false;
