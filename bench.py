@@ -943,7 +943,7 @@ def report_decode(args):
     back to back; per-call time is the replay time / C.  Columns: the fused
     Linear on the packed image (swapped split-K tensor-core path), the fused
     Linear on the int8 codes (a GEMV up to 4 tokens, the int8-operand
-    tensor-core kernel up to 128), the GEMM on int8 codes
+    tensor-core kernels up to 288), the GEMM on int8 codes
     quantized beforehand, and torch's bf16 matmul on C bf16 weights."""
     import torch
     import w8a8_int8_linear_gb300 as w
@@ -984,7 +984,7 @@ def report_decode(args):
             Wq, sw = w.quantize_weight(W)
             packs.append((w.pack_weight(Wq), sw, Wq))
         b = (0.01 * torch.randn((N,), generator=gen, device=dev)).to(torch.bfloat16)
-        for M in (1, 2, 4, 8, 16, 77, 128, 256):
+        for M in (1, 2, 4, 8, 16, 77, 128, 160, 192, 256, 257):
             X = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
             Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             sx = torch.empty((M,), dtype=torch.float32, device=dev)
