@@ -169,6 +169,9 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     (257, 9856, 2048, False),  # 288-token tile, 77 weight tiles, two 1024-K chunks: no split
     (288, 129, 16400, True),   # 288 exactly, a last weight tile of one row, 257 stages: split 8 ways
     (200, 3072, 5120, True),   # 224-token tile at a model shape: 24 tiles, split 6 ways
+    (77, 19200, 1024, True),   # 150 weight tiles: some CTAs take two units (narrow kernel)
+    (200, 19200, 1040, False), # the same on the wide kernel: the region table carries over units
+    (288, 20000, 2048, True),  # three token parts over two units, two chunks per unit
 ])
 def test_gemm_postscale_int8_operands(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
