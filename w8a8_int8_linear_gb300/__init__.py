@@ -348,8 +348,8 @@ def linear_postscale_codes(X, Wq, sw, bias=None, out=None, workspace=None, sx_ou
     """Fused W8A8 Linear, post-scale, against the int8 weight codes (no
     image): per-token quantization of X, then the post-scale GEMM on the
     codes, which reads each weight code once (one or two tokens: one GEMV
-    kernel that quantizes X itself; up to 4: the GEMV; up to 128: the
-    int8-operand tensor-core kernel).  Returns (Y, sx, Xq or None);
+    kernel that quantizes X itself; up to 4: the GEMV; up to 288: the
+    int8-operand tensor-core kernels).  Returns (Y, sx, Xq or None);
     codes=True also returns Xq."""
     _need(X, torch.bfloat16, "X", 2)
     _need(Wq, torch.int8, "Wq", 2)
