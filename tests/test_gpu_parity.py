@@ -172,6 +172,9 @@ def test_gemm_postscale_few_tokens(w8a8, oracle, M, N, K, bias):
     (77, 19200, 1024, True),   # 150 weight tiles: some CTAs take two units (narrow kernel)
     (200, 19200, 1040, False), # the same on the wide kernel: the region table carries over units
     (288, 20000, 2048, True),  # three token parts over two units, two chunks per unit
+    (130, 64, 16, True),       # wide kernel, K shorter than one 64-K stage (zero-filled past K)
+    (97, 1, 48, False),        # one weight row: the tile's other 127 rows past N
+    (6, 1, 4096, True),        # the same on the narrow kernel, K split 8 ways
 ])
 def test_gemm_postscale_int8_operands(w8a8, oracle, M, N, K, bias):
     check_postscale(w8a8, oracle, M, N, K, bias)
