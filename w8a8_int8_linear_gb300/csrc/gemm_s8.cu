@@ -84,7 +84,9 @@ struct S8Params {
 // the epilogue folds each chunk into int32.  With K split, each unit adds its
 // int32 sums into a zeroed buffer with integer atomics (exact in any order)
 // and the warp whose arrival completes a 32-row group writes that group's Y.
-// Two converter warpgroups take alternate stages.
+// Two converter warpgroups take alternate stages, each with its own full
+// barrier per slot (see the barrier layout in the kernel).  The producer asks
+// each weight tile into L2 1024 K before its load.
 constexpr int S8_BK = 128;                   // K per stage (bytes of an int8 weight row)
 constexpr int S8_CHUNK_STAGES = 8;           // 1024 K per exact fp32 chunk
 constexpr uint32_t S8_A_BYTES = BM * S8_BK;  // 16 KB
@@ -1115,7 +1117,7 @@ struct S8Plan {
     int num_m, k_stages, k_split, split_stages;
 };
 
-constexpr int S8_COUNTERS_PER_TILE = 8;  // one per 32-row group (and token half, beyond 96 tokens)
+constexpr int S8_COUNTERS_PER_TILE = 8;  // one per 32-row group (and column half, beyond 96 tokens)
 
 bool s8_split_possible(int64_t N, int64_t K) {
     return (N + BM - 1) / BM <= S8_SPLIT_MAX_TILES && (K + S8_BK - 1) / S8_BK >= 4;
