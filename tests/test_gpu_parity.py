@@ -541,10 +541,11 @@ def test_int8linear_module(w8a8, oracle, mode):
     assert d.max() == 0
 
 
-@pytest.mark.parametrize("M", [1, 4, 8])
+@pytest.mark.parametrize("M", [1, 4, 8, 120, 250])
 def test_int8linear_module_decode(w8a8, oracle, M):
-    """With few tokens the post-scale module runs on the int8 codes (the GEMV
-    up to 4 tokens, the int8-operand tensor-core kernel beyond)."""
+    """With few tokens the post-scale module runs on the int8 codes: the GEMV
+    up to 4 tokens, the int8-operand tensor-core kernels beyond (the wide
+    one from 97 tokens; codes_preferred up to 256 at any N)."""
     from w8a8_int8_linear_gb300.module import Int8Linear
     torch.manual_seed(2)
     lin = torch.nn.Linear(1040, 300, bias=True).to(DEV).to(torch.bfloat16)
