@@ -1026,6 +1026,8 @@ PROFILE_CASES = {
     "linear_codes_77x3072x5120": ("linear_codes", 77, 3072, 5120),
     "linear_codes_257x13824x5120": ("linear_codes", 257, 13824, 5120),
     "linear_codes_160x15432x5120": ("linear_codes", 160, 15432, 5120),
+    "gelu_quant_4096x13824x5120": ("gelu_quant", 4096, 13824, 5120),
+    "linear_4096x13824x5120": ("linear", 4096, 13824, 5120),
 }
 
 
@@ -1054,6 +1056,10 @@ def profile_case(name):
             b = (0.5 * torch.randn((N,), generator=g, device=dev)).to(torch.bfloat16)
             Wimg = w.pack_weight(Wq)
             fn = lambda: w.linear_postscale_gelu_quant(X, Wimg, sw, b)
+        elif what == "linear":
+            b = (0.5 * torch.randn((N,), generator=g, device=dev)).to(torch.bfloat16)
+            Wimg = w.pack_weight(Wq)
+            fn = lambda: w.linear_postscale(X, Wimg, sw, b)
         elif what == "linear_codes":
             b = (0.5 * torch.randn((N,), generator=g, device=dev)).to(torch.bfloat16)
             fn = lambda: w.linear_postscale_codes(X, Wq, sw, b)
