@@ -278,12 +278,15 @@ def check_postscale(w8a8, oracle, M, N, K, bias):
     assert w8a8.get_device_error() == (0, 0)
 
 
-def test_int8_operands_exactness_at_max_k(w8a8, oracle):
-    """The int8-operand kernel at the largest K (131072: 1024 stages, K split
-    8 ways into units of 16 exact fp32 chunks each) with all-+-127 codes:
-    |acc| reaches 127*127*131072 = 2,114,060,288, just inside int32, and the
-    split sums add up exactly; a ragged last weight tile (136 rows)."""
-    M, N, K = 16, 136, 131072
+@pytest.mark.parametrize("M", [16, 200])
+def test_int8_operands_exactness_at_max_k(w8a8, oracle, M):
+    """The int8-operand kernels at the largest K (131072, K split 8 ways)
+    with all-+-127 codes: |acc| reaches 127*127*131072 = 2,114,060,288, just
+    inside int32, and the split sums add up exactly; a ragged last weight
+    tile (136 rows).  16 tokens: the narrow kernel (units of 16 exact fp32
+    chunks); 200 tokens: the wide kernel, its token parts rotating through
+    the accumulator regions over 2048 stages of 64 K."""
+    N, K = 136, 131072
     g = torch.Generator().manual_seed(21)
     Xq = ((torch.randint(0, 2, (M, K), generator=g) * 2 - 1) * 127).to(torch.int8)
     Wq = ((torch.randint(0, 2, (N, K), generator=g) * 2 - 1) * 127).to(torch.int8)
