@@ -204,9 +204,10 @@ def test_int8_operands_repeatable_after_fresh_quantization(w8a8, M):
 
 
 # At most 4 tokens (M * K <= 131072): a CUDA-core GEMV on the int8 codes
-# (dp4a), the activation codes staged in each CTA's shared memory.  Warps own
-# balanced ranges of weight-row groups (1 row for up to 2 tokens, 2 rows for
-# 3..4) and walk each row in steps of 4 x 512 bytes, prefetching the next
+# (dp4a), the activation codes staged in each CTA's shared memory by one bulk
+# copy.  Warps own balanced ranges of weight-row groups (1 row for up to 2
+# tokens, and for 3..4 with N <= 4096; else 2 rows) and walk each row in steps
+# of 4 x 512 bytes, prefetching the next
 # step.  The shapes cover every token count, K shorter than one slice, a
 # partial last step, many steps per row, N below one group per warp, odd,
 # and larger than the persistent grid's warp count, the shared-memory limit,
@@ -215,13 +216,15 @@ def test_int8_operands_repeatable_after_fresh_quantization(w8a8, M):
 @pytest.mark.parametrize("M,N,K,bias", [
     (1, 1, 16, True),          # one output, one 16-byte slice
     (2, 3, 48, False),
-    (3, 7, 528, True),         # odd N with 2-row groups, partial step
+    (3, 7, 528, True),         # partial step
     (4, 33, 2064, False),
     (5, 300, 5120, True),
     (6, 1031, 1040, False),
     (7, 64, 16384, True),      # 16 steps per row
     (8, 777, 4112, True),      # the tensor-core kernel's 16-token tile, odd N
     (1, 3072, 5120, False),    # the decode shape
+    (4, 4096, 5120, False),    # the largest N with one row per warp at 4 tokens
+    (3, 4097, 528, True),      # odd N with 2-row groups, partial step
     (4, 9999, 256, False),     # more row groups than the grid's warps
     (4, 300, 32768, True),     # 128 KB of codes: the shared-memory limit
     (4, 100, 32784, False),    # past it: the tensor-core kernel

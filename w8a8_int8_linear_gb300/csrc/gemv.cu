@@ -9,7 +9,7 @@
 // order: |acc| <= 127 * 127 * K < 2^31 for K <= 131072.
 //
 // Work layout: a persistent grid of 8-warp CTAs.  Each CTA first stages the
-// M x K activation codes in shared memory: copied from Xq, or (the fused
+// M x K activation codes in shared memory: one bulk copy from Xq, or (the fused
 // Linear with one or two tokens) quantized from the bf16 rows of X by the CTA
 // itself, with the per-token quantizer's arithmetic, so one kernel does the
 // whole Linear.
@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSiteGemvStage = 40;  // the bounded wait for the staged activation codes
 constexpr size_t kSmemPerSm = 228 * 1024;  // shared memory of one SM, for the CTAs-per-SM estimate
 
 struct GemvParams {
@@ -166,11 +167,26 @@ __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_co
     if (!p.settled && busy) load(g, 0, cur);
     if constexpr (QUANT) {
         stage_quantized<MT>(p, xs4, red, sxs);
+        __syncthreads();
     } else {
-        const int4* src = static_cast<const int4*>(p.x);
-        for (int i = threadIdx.x; i < M * kq; i += kThreads) xs4[i] = __ldg(src + i);
+        // The M x K codes arrive in one bulk copy (Xq is 16-byte aligned and
+        // M * K a multiple of 16), instead of a loop of dependent 16-byte
+        // loads per thread.  Every thread waits on the copy's barrier; a wait
+        // that runs out is recorded and ends the CTA on every thread alike.
+        __shared__ uint64_t staged;
+        if (threadIdx.x == 0) {
+            mbar_init(&staged, 1);
+            fence_mbarrier_init();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(M) * static_cast<uint32_t>(K);
+            mbar_arrive_expect_tx(&staged, bytes);
+            bulk_load(xs4, p.x, bytes, &staged);
+        }
+        const bool ok = mbar_wait(&staged, 0, kSiteGemvStage);
+        if (__syncthreads_or(!ok)) return;
     }
-    __syncthreads();
     if (!busy) return;
 
     int32_t acc[R][MT];
@@ -237,10 +253,9 @@ __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_co
     }
 }
 
-template <int MT, int EPI, bool QUANT>
+template <int MT, int R, int EPI, bool QUANT>
 cudaError_t launch_mt(const GemvParams& p, int num_sms, cudaStream_t st) {
-    constexpr int R = MT <= 2 ? 1 : 2;  // rows sharing each activation read
-    constexpr int U = 4 / R;            // 4 x 16 bytes of weights per lane and step
+    constexpr int U = 4 / R;  // 4 x 16 bytes of weights per lane and step
     // CTAs per SM: 4 (64 registers) unless the staging's scales next to the
     // first weight loads need more
     constexpr int MINB = (QUANT && MT >= 2) ? 3 : 4;
@@ -272,14 +287,22 @@ cudaError_t launch_mt(const GemvParams& p, int num_sms, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Rows sharing each activation read: one for one or two tokens, and for 3..4
+// while N <= kOneRowMaxN (one row per warp is then within a wave of warps
+// and the GEMV is bound by load latency: more warps, fewer steps each; at
+// N = 3072 the GEMM went from 8.8 to 7.1 us); else two, which halves the
+// shared-memory reads per weight byte (faster from N = 5120 on).
+constexpr int kOneRowMaxN = 4096;
+
 template <int EPI, bool QUANT>
 cudaError_t launch_tokens(const GemvParams& p, int num_sms, cudaStream_t st) {
-    if (p.M <= 1) return launch_mt<1, EPI, QUANT>(p, num_sms, st);
+    if (p.M <= 1) return launch_mt<1, 1, EPI, QUANT>(p, num_sms, st);
     if constexpr (QUANT) {
-        return launch_mt<2, EPI, QUANT>(p, num_sms, st);
+        return launch_mt<2, 1, EPI, QUANT>(p, num_sms, st);
     } else {
-        if (p.M <= 2) return launch_mt<2, EPI, QUANT>(p, num_sms, st);
-        return launch_mt<4, EPI, QUANT>(p, num_sms, st);
+        if (p.M <= 2) return launch_mt<2, 1, EPI, QUANT>(p, num_sms, st);
+        return p.N <= kOneRowMaxN ? launch_mt<4, 1, EPI, QUANT>(p, num_sms, st)
+                                  : launch_mt<4, 2, EPI, QUANT>(p, num_sms, st);
     }
 }
 
