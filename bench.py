@@ -1020,6 +1020,7 @@ PROFILE_CASES = {
     "quant_block_32768x13824": ("quant_block", 32768, 0, 13824),
     "gelu_quant_4096x4096x2048": ("gelu_quant", 4096, 4096, 2048),
     "norm_layer_8192x5120": ("norm_layer", 8192, 0, 5120),
+    "norm_rms_8192x5120": ("norm_rms", 8192, 0, 5120),
     "gemm_int8_decode_1x13824x5120": ("gemm_int8", 1, 13824, 5120),
     "linear_codes_decode_1x13824x5120": ("linear_codes", 1, 13824, 5120),
     "linear_codes_77x13824x5120": ("linear_codes", 77, 13824, 5120),
@@ -1045,10 +1046,13 @@ def profile_case(name):
         Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
         sx = torch.empty((M,) if mode == w.PER_ROW else (M, K // 128), dtype=torch.float32, device=dev)
         fn = lambda: w.quantize_act(X, mode, out=(Xq, sx))
-    elif what == "norm_layer":
+    elif what in ("norm_layer", "norm_rms"):
         gamma = (1 + 0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
         beta = (0.1 * torch.randn((K,), generator=g, device=dev)).to(torch.bfloat16)
-        fn = lambda: w.norm_quant(X, gamma, beta, 1e-5, w.LAYER_NORM)
+        if what == "norm_layer":
+            fn = lambda: w.norm_quant(X, gamma, beta, 1e-5, w.LAYER_NORM)
+        else:
+            fn = lambda: w.norm_quant(X, gamma, None, 1e-6, w.RMS_NORM)
     else:
         W = (0.05 * torch.randn((N, K), generator=g, device=dev)).to(torch.bfloat16)
         Wq, sw = w.quantize_weight(W)

@@ -720,6 +720,35 @@ def test_norm_quant(w8a8, oracle, layer, M, K):
         assert np.array_equal(Xq.cpu().numpy(), Xqf)
         assert np.array_equal(sx.cpu().numpy().view(np.uint32), sxf.view(np.uint32))
         assert torch.equal(Ximg.float().cpu(), Xq.float().cpu())
+        # only the code image and the scales (the specialized kernels for
+        # gamma with or without beta, rows up to 8192 elements)
+        Ximg1, sx1, none_q, none_y = w8a8.norm_quant(X.to(DEV), None if gg is None else gg.to(DEV),
+                                                     None if bb is None else bb.to(DEV), 1e-5, kind)
+        assert none_q is None and none_y is None
+        assert np.array_equal(Ximg1.float().cpu().numpy(), Xqf.astype(np.float32))
+        assert np.array_equal(sx1.cpu().numpy().view(np.uint32), sxf.view(np.uint32))
+    assert w8a8.get_device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("layer", [False, True])
+@pytest.mark.parametrize("M,K", [(2000, 5120), (10000, 264), (5000, 1040)])
+def test_norm_quant_many_rows(w8a8, oracle, layer, M, K):
+    """Thousands of rows through the specialized kernels (gamma, beta for
+    LayerNorm, code image only), rows of 33 and 130 chunks (padding chunk
+    slots) and 640: codes and scales bit for bit against the fixed-order
+    statement, an all-zero and a constant row included."""
+    X = rand_bf16((M, K), seed=80 + K, scale=2.0, outliers=0.01, oscale=30.0)
+    if layer:
+        X = (X.float() - 0.5).to(torch.bfloat16)
+    X[7] = 0.0
+    X[M - 1] = -3.0
+    g = (rand_bf16((K,), seed=81, scale=0.2) + 1.0).to(torch.bfloat16)
+    b = rand_bf16((K,), seed=82, scale=0.2) if layer else None
+    kind = oracle.LAYER_NORM if layer else oracle.RMS_NORM
+    _, Xqf, sxf = oracle.norm_quant_fixed_order(bits(X), bits(g), None if b is None else bits(b), 1e-5, kind)
+    Ximg, sx, _, _ = w8a8.norm_quant(X.to(DEV), g.to(DEV), None if b is None else b.to(DEV), 1e-5, kind)
+    assert np.array_equal(Ximg.float().cpu().numpy(), Xqf.astype(np.float32))
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), sxf.view(np.uint32))
     assert w8a8.get_device_error() == (0, 0)
 
 

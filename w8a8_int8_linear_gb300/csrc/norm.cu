@@ -79,29 +79,21 @@ __device__ __forceinline__ float tree_sum_local(float (&s)[C]) {
     return s[0];
 }
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = bf16_lo(w[i]);
-        f[2 * i + 1] = bf16_hi(w[i]);
-    }
-}
-
 // The normalized bf16 values of one chunk, packed.  d = x - mu, d * r and
 // (d * r) * gamma run two values at a time on the packed fp32 pipe (a
 // subtraction feeding a multiplication and products feeding products, which
 // are never contracted); the beta addition is scalar with explicit rounding.
+// layer / use_gamma / add_beta are compile-time constants in the specialized
+// kernels, so the unrolled chunk code carries no branches on them.
 __device__ __forceinline__ uint4 normalize_chunk(const uint4& v, const uint4* __restrict__ gamma,
-                                                 const uint4* __restrict__ beta, int layer, int c, float mu,
-                                                 float r) {
+                                                 const uint4* __restrict__ beta, bool layer, bool use_gamma,
+                                                 bool add_beta, int c, float mu, float r) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t gw[4] = {0, 0, 0, 0}, bw[4] = {0, 0, 0, 0};
-    if (gamma) {
+    if (use_gamma) {
         const uint4 t = __ldg(gamma + c);
         gw[0] = t.x; gw[1] = t.y; gw[2] = t.z; gw[3] = t.w;
     }
-    const bool add_beta = layer && beta;
     if (add_beta) {
         const uint4 t = __ldg(beta + c);
         bw[0] = t.x; bw[1] = t.y; bw[2] = t.z; bw[3] = t.w;
@@ -115,7 +107,7 @@ __device__ __forceinline__ uint4 normalize_chunk(const uint4& v, const uint4* __
         if (layer) d = f2_sub(d, mu2);
         float y0, y1;
         uint64_t t = f2_mul(d, r2);
-        if (gamma) t = f2_mul(t, f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i])));
+        if (use_gamma) t = f2_mul(t, f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i])));
         f2_unpack(t, y0, y1);
         if (add_beta) {
             y0 = __fadd_rn(y0, bf16_lo(bw[i]));
@@ -127,25 +119,22 @@ __device__ __forceinline__ uint4 normalize_chunk(const uint4& v, const uint4* __
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// One CTA per row; thread t owns chunks [tC, (t+1)C).  The row stays in
-// registers as bf16, and so do its normalized values between the absmax and
-// the quantization.
-template <int C, int TMAX, int MINB>
-__global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __restrict__ X,
-                                                                const uint4* __restrict__ gamma,
-                                                                const uint4* __restrict__ beta, float eps,
-                                                                int layer, int K, int tree, uint4* __restrict__ Y,
-                                                                uint2* __restrict__ Xq, uint4* __restrict__ img,
-                                                                float* __restrict__ sx) {
-    grid_launch_dependents();
-    __shared__ float red[3][32];
-    const int64_t row = blockIdx.x;
+// Kernel forms: the generic one tests every option at run time; the two
+// common ones (gamma, and for LayerNorm beta; only the code image and the
+// scales written) have them fixed at compile time.
+enum NormForm : int { kNormGeneric = 0, kNormRmsImage = 1, kNormLayerImage = 2 };
+
+// One row's statistics, normalization and scale.  v holds this thread's
+// chunks [c0, c0 + C) of the row as bf16 on entry and their normalized
+// values y on exit.  Every chunk slot is normalized without a branch; a slot
+// past the row (zeros, gamma and beta read at chunk 0) is left out of the
+// absmax by a select.  Each reduction has its own slot of `red`, so one
+// barrier per reduction suffices, also from one row to the next.
+template <int C>
+__device__ __forceinline__ RowScale norm_row(uint4 (&v)[C], const uint4* __restrict__ gamma,
+                                             const uint4* __restrict__ beta, float eps, bool layer, bool use_gamma,
+                                             bool add_beta, int K, int c0, int tree, float (*red)[32]) {
     const int chunks = K >> 3;
-    const uint4* x = X + row * chunks;
-    const int c0 = threadIdx.x * C;
-    uint4 v[C];
-#pragma unroll
-    for (int i = 0; i < C; ++i) v[i] = (c0 + i < chunks) ? __ldg(x + c0 + i) : make_uint4(0, 0, 0, 0);
     const float Kf = static_cast<float>(K);
     float mu = 0.0f;
     if (layer) {
@@ -190,22 +179,74 @@ __global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __r
 #pragma unroll
     for (int i = 0; i < C; ++i) {
         const int c = c0 + i;
-        if (c < chunks) {
-            v[i] = normalize_chunk(v[i], gamma, beta, layer, c, mu, r);  // v now holds y
-            amax = fmaxf(amax, chunk_absmax(v[i]));
-        }
+        const bool in = c < chunks;
+        v[i] = normalize_chunk(v[i], gamma, beta, layer, use_gamma, add_beta, in ? c : 0, mu, r);  // v holds y
+        const float ca = chunk_absmax(v[i]);
+        amax = in ? fmaxf(amax, ca) : amax;
     }
-    amax = block_absmax(amax, red[2]);
-    const RowScale sc = make_scale_div(amax);
-    if (threadIdx.x == 0) sx[row] = sc.s;
+    return make_scale_div(block_absmax(amax, red[2]));
+}
+
+// The code image of this thread's chunks (the specialized forms).  The row's
+// path (exact for a subnormal scale) is chosen once, not per chunk.
+template <int C>
+__device__ __forceinline__ void store_image(const uint4 (&v)[C], const RowScale& sc, uint4* __restrict__ img_row,
+                                            int c0, int chunks) {
+    auto store = [&](const RowScale& scl) {
 #pragma unroll
-    for (int i = 0; i < C; ++i) {
-        const int c = c0 + i;
-        if (c >= chunks) continue;
-        const int64_t o = row * chunks + c;
-        if (Y) Y[o] = v[i];
-        if (img) img[o] = quant_chunk_img(v[i], sc);
-        if (Xq) __stcs(Xq + o, quant_chunk(v[i], sc));
+        for (int i = 0; i < C; ++i) {
+            const int c = c0 + i;
+            const uint4 q = quant_chunk_img(v[i], scl);
+            if (c < chunks) img_row[c] = q;
+        }
+    };
+    RowScale fixed = sc;
+    if (sc.exact) {
+        fixed.exact = true;
+        store(fixed);
+    } else {
+        fixed.exact = false;
+        store(fixed);
+    }
+}
+
+// One CTA per row; thread t owns chunks [tC, (t+1)C).  The row stays in
+// registers as bf16, and so do its normalized values between the absmax and
+// the quantization.
+template <int C, int TMAX, int MINB, int FORM>
+__global__ void __launch_bounds__(TMAX, MINB) norm_quant_kernel(const uint4* __restrict__ X,
+                                                                const uint4* __restrict__ gamma,
+                                                                const uint4* __restrict__ beta, float eps,
+                                                                int layer_arg, int K, int tree,
+                                                                uint4* __restrict__ Y, uint2* __restrict__ Xq,
+                                                                uint4* __restrict__ img, float* __restrict__ sx) {
+    grid_launch_dependents();
+    constexpr bool kFixed = FORM != kNormGeneric;
+    const bool layer = kFixed ? FORM == kNormLayerImage : layer_arg != 0;
+    const bool use_gamma = kFixed ? true : gamma != nullptr;
+    const bool add_beta = kFixed ? FORM == kNormLayerImage : (layer && beta != nullptr);
+    __shared__ float red[3][32];
+    const int64_t row = blockIdx.x;
+    const int chunks = K >> 3;
+    const uint4* x = X + row * chunks;
+    const int c0 = threadIdx.x * C;
+    uint4 v[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) v[i] = (c0 + i < chunks) ? __ldg(x + c0 + i) : make_uint4(0, 0, 0, 0);
+    const RowScale sc = norm_row<C>(v, gamma, beta, eps, layer, use_gamma, add_beta, K, c0, tree, red);
+    if (threadIdx.x == 0) sx[row] = sc.s;
+    if constexpr (kFixed) {
+        store_image<C>(v, sc, img + row * chunks, c0, chunks);
+    } else {
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const int c = c0 + i;
+            if (c >= chunks) continue;
+            const int64_t o = row * chunks + c;
+            if (Y) Y[o] = v[i];
+            if (img) img[o] = quant_chunk_img(v[i], sc);
+            if (Xq) __stcs(Xq + o, quant_chunk(v[i], sc));
+        }
     }
 }
 
@@ -227,14 +268,27 @@ cudaError_t launch_norm_quant(const void* X, const void* gamma, const void* beta
     // launched, the tree still spans P / C threads.
     const int k = static_cast<int>(K);
     auto warps_for = [&](int C) { return ((chunks + C - 1) / C + 31) / 32; };
+    // the specialized forms (rows of 257..8192 elements): gamma (and beta
+    // exactly for LayerNorm), only the code image and the scales written;
+    // held to 64 registers (4 CTAs of 256 threads, 6 rows of 5120 per SM)
+    const bool image_only = im && !y && !q && g;
+    const int form = (image_only && !layer && !b) ? kNormRmsImage
+                     : (image_only && layer && b) ? kNormLayerImage
+                                                  : kNormGeneric;
+    auto launch = [&](auto kern, int threads, int tree) {
+        kern<<<grid, threads, 0, st>>>(x, g, b, eps, layer, k, tree, y, q, im, sx);
+    };
     if (P <= 32) {
-        norm_quant_kernel<1, 32, 16><<<grid, 32, 0, st>>>(x, g, b, eps, layer, k, P, y, q, im, sx);
+        launch(norm_quant_kernel<1, 32, 16, kNormGeneric>, 32, P);
     } else if (P <= 1024) {
-        norm_quant_kernel<4, 256, 3><<<grid, 32 * warps_for(4), 0, st>>>(x, g, b, eps, layer, k, P / 4, y, q, im,
-                                                                          sx);
+        const int t = 32 * warps_for(4);
+        if (form == kNormRmsImage) launch(norm_quant_kernel<4, 256, 4, kNormRmsImage>, t, P / 4);
+        else if (form == kNormLayerImage) launch(norm_quant_kernel<4, 256, 4, kNormLayerImage>, t, P / 4);
+        else launch(norm_quant_kernel<4, 256, 3, kNormGeneric>, t, P / 4);
     } else {
-        norm_quant_kernel<8, 256, 1><<<grid, 32 * warps_for(8), 0, st>>>(x, g, b, eps, layer, k, P / 8, y, q, im,
-                                                                          sx);
+        // rows over 8192 elements: the specialized forms would need 124-130
+        // registers here (85 generic), one CTA per SM instead of three
+        launch(norm_quant_kernel<8, 256, 1, kNormGeneric>, 32 * warps_for(8), P / 8);
     }
     return cudaGetLastError();
 }
