@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_co
         // The M x K codes arrive in one bulk copy (Xq is 16-byte aligned and
         // M * K a multiple of 16), instead of a loop of dependent 16-byte
         // loads per thread.  Every thread waits on the copy's barrier; a wait
-        // that runs out is recorded and ends the CTA on every thread alike.
+        // that runs out (2 s) is recorded as 0x100 + kSiteGemvStage and ends
+        // the CTA on every thread alike.
         __shared__ uint64_t staged;
         if (threadIdx.x == 0) {
             mbar_init(&staged, 1);
@@ -185,7 +186,12 @@ __global__ void __launch_bounds__(kThreads, MINB) gemv_s8_kernel(const __grid_co
             bulk_load(xs4, p.x, bytes, &staged);
         }
         const bool ok = mbar_wait(&staged, 0, kSiteGemvStage);
-        if (__syncthreads_or(!ok)) return;
+        if (__syncthreads_or(!ok)) {
+            // the copy may still be on its way: one more bounded wait for it
+            // before this CTA's shared memory is released
+            if (threadIdx.x == 0) mbar_wait(&staged, 0, kSiteGemvStage);
+            return;
+        }
     }
     if (!busy) return;
 
