@@ -704,6 +704,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
+            // Shared-memory descriptors of stage 0; a stage's descriptors differ
+            // only in the start address field (bits 0-13, address >> 4), which
+            // stays below 2^14 for any stage, so each stage's low words are a
+            // running sum and each K step adds 32 bytes (2) to them.
+            const uint64_t dA0 = smem_desc_kmajor_sw128(smem_u32(sA));
+            const uint64_t dB0 = smem_desc_kmajor_sw128(smem_u32(sB));
+            const uint32_t hiA = static_cast<uint32_t>(dA0 >> 32), hiB = static_cast<uint32_t>(dB0 >> 32);
+            uint32_t loA = static_cast<uint32_t>(dA0), loB = static_cast<uint32_t>(dB0);
             for (int u = cluster; ok && u < p.num_tiles; u += nclusters) {
                 const Unit w = unit_coords(u, p);
                 const int nchunks = (w.ks1 - w.ks0 + p.chunk_stages - 1) / p.chunk_stages;
@@ -722,18 +730,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t da = smem_desc_kmajor_sw128(a_addr + k * 32);
-                            const uint64_t db = smem_desc_kmajor_sw128(b_addr + k * 32);
+                            const uint64_t da = (static_cast<uint64_t>(hiA) << 32) | (loA + 2u * k);
+                            const uint64_t db = (static_cast<uint64_t>(hiB) << 32) | (loB + 2u * k);
                             mma_bf16_ss_pair(d_tmem, da, db, C::IDESC, (ks > s0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit_pair_multicast(&empty[stage], 0x3);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
+                            loA = static_cast<uint32_t>(dA0);
+                            loB = static_cast<uint32_t>(dB0);
+                        } else {
+                            loA += A_BYTES >> 4;
+                            loB += C::B_BYTES >> 4;
                         }
                     }
                     if (!ok) break;
