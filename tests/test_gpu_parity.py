@@ -685,8 +685,8 @@ def test_ffn_up_gelu_quant_rejects_bad_arguments(w8a8):
 
 # ----------------------------------------------------------------- normalization fused with quantization
 @pytest.mark.parametrize("layer", [False, True])
-@pytest.mark.parametrize("M,K", [(1, 8), (7, 128), (33, 264), (300, 4096), (64, 5120), (5, 13824), (3, 16384),
-                                 (1000, 1040)])
+@pytest.mark.parametrize("M,K", [(1, 8), (7, 128), (33, 264), (300, 4096), (64, 5120), (9, 8192), (11, 8200),
+                                 (5, 13824), (3, 16384), (1000, 1040)])
 def test_norm_quant(w8a8, oracle, layer, M, K):
     """Against the plain definition (fp64 statistics and normalization): the
     normalized bf16 row within 1 ulp, except where the exact value comes out
