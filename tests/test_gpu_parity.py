@@ -706,14 +706,17 @@ def test_norm_quant(w8a8, oracle, layer, M, K):
     g = g.to(torch.bfloat16)
     b = rand_bf16((K,), seed=62, scale=0.2) if layer else None
     kind = oracle.LAYER_NORM if layer else oracle.RMS_NORM
-    for gg, bb in ((g, b), (None, None)):
+    # also LayerNorm without beta, and RMSNorm given a beta (which it does not
+    # use): the generic kernel for image-only calls
+    other = (g, None) if layer else (g, rand_bf16((K,), seed=63, scale=0.2))
+    for gg, bb in ((g, b), (None, None), other):
         args = (bits(X), None if gg is None else bits(gg), None if bb is None else bits(bb), 1e-5, kind)
         Yo, Xqo, sxo = oracle.norm_quant(*args)
         Yf, Xqf, sxf = oracle.norm_quant_fixed_order(*args)
         Ximg, sx, Xq, Y = w8a8.norm_quant(X.to(DEV), None if gg is None else gg.to(DEV),
                                           None if bb is None else bb.to(DEV), 1e-5, kind, codes=True, y=True)
-        bound = norm_error_bound(bits(X), None if gg is None else bits(gg), None if bb is None else bits(bb), 1e-5,
-                                 layer)
+        bound = norm_error_bound(bits(X), None if gg is None else bits(gg),
+                                 None if (bb is None or not layer) else bits(bb), 1e-5, layer)
         assert_quant_follows_plain(oracle, bits(Y), Yo, Xq.cpu().numpy(), sx.cpu().numpy(), Xqo, sxo, K,
                                    err_bound=bound, max_frac_beyond_ulp=1e-5)
         assert np.array_equal(bits(Y), Yf)
