@@ -1022,6 +1022,7 @@ PROFILE_CASES = {
     "norm_layer_8192x5120": ("norm_layer", 8192, 0, 5120),
     "norm_rms_8192x5120": ("norm_rms", 8192, 0, 5120),
     "gemm_int8_decode_1x13824x5120": ("gemm_int8", 1, 13824, 5120),
+    "gemm_int8_4x3072x5120": ("gemm_int8", 4, 3072, 5120),
     "linear_codes_decode_1x13824x5120": ("linear_codes", 1, 13824, 5120),
     "linear_codes_77x13824x5120": ("linear_codes", 77, 13824, 5120),
     "linear_codes_77x3072x5120": ("linear_codes", 77, 3072, 5120),
